@@ -1,0 +1,390 @@
+"""Benchmark of the FS-L attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload fsl_64k]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-e2e]
+
+One step = one ``fs_attention_fwd`` over the whole workload (cell summaries,
+pruning, selection, readout, window + mix), inputs resident in HBM.  With
+``--gpus N`` (under torchrun) every rank runs its own replica of the workload
+on its GPU (the op shards over independent (batch, head) slices, so there is
+no data-path collective): weak scaling, value = tokens of all ranks / max
+rank time.  Prints one JSON line on rank 0.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only) and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from long_context_lm_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "FS-L attn fwd tokens/s at 16k/64k/256k (H=16,d=64,bf16); % of roofline"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def window_flops(BH, N, w, d=64):
+    """Algorithmic flops of the window branch: QK^T and PV over the exact
+    number of keys each query attends to (4*d per query-key pair)."""
+    n = np.arange(N, dtype=np.float64)
+    return float(BH * 4 * d * np.minimum(n + 1, w).sum())
+
+
+def stage_work(wl, distinct_cells, sel_counts):
+    """Algorithmic bytes / flops per launch of each stage (one step)."""
+    B, H, N, d = wl.batch, wl.heads, wl.seq_len, wl.head_dim
+    BH, C, nblk = B * H, N // 32, N // 128
+    p = wl.params
+    K, cap = p["K"], p["P"] + p["W"]
+    tok = BH * N
+    work = {}
+    # K1: read k (bf16), write kbar (fp32) and amax
+    work["cell_summary"] = dict(bound="hbm", bytes=tok * d * 2 + BH * C * (d * 4 + 4))
+    # K2: read amax (per chunk sort + per block), write pools
+    work["prune"] = dict(bound="latency", bytes=BH * C * 4 * 2 + BH * nblk * (cap + 1) * 4)
+    # K3: q (bf16), pool ids, mean keys of pool cells once per block (fp32), sel out
+    work["select"] = dict(bound="alu", bytes=tok * d * 2 + BH * nblk * cap * (d * 4 + 8) + tok * K * 4,
+                          flops=2.0 * d * float(sel_counts["cands"]))
+    # K4: q, sel, o_long out (fp32) + k/v of every distinct selected cell once
+    work["readout"] = dict(bound="hbm", bytes=tok * d * 2 + tok * K * 4 + tok * d * 4
+                           + distinct_cells * 32 * d * 2 * 2,
+                           flops=4.0 * d * float(sel_counts["tokens_read"]))
+    # K5: q, k, v (bf16), o_long in (fp32), out (fp32); flops of the window
+    work["window"] = dict(bound="tensor", bytes=tok * d * (2 * 3 + 4 + 4),
+                          flops=window_flops(BH, N, p["w"], d))
+    return work
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    from long_context_lm_gb300 import fs
+    from long_context_lm_gb300.fs import FS_N_STAGES, STAGE_NAMES
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl.batch, wl.heads, wl.seq_len, wl.head_dim, wl.seed, wl.sigma_ln, wl.dtype,
+                      wl.needles, wl.n_needles, wl.params)
+    B, H, N, d = inp.q.shape
+    params = fs.fs_default_params(**wl.params)
+    code = fs.FS_FP32 if inp.q.dtype == torch.float32 else fs.FS_BF16
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    lam, sigma, mix = inp.lam.to(dev), inp.sigma.to(dev), inp.mix.to(dev)
+    ws = torch.empty(fs.fs_workspace_bytes(B, H, N, d, params, code), device=dev, dtype=torch.uint8)
+    out = torch.empty((B, H, N, d), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+
+    # warm-up (also builds the selection statistics used for the byte counts)
+    for _ in range(args.warmup):
+        fs.fs_attention_fwd(q, k, v, lam, sigma, mix, params, out=out, ws=ws)
+    torch.cuda.synchronize()
+    view = fs.fs_workspace_view(ws, B, H, N, d, params, code)
+    sel = view["sel"].reshape(B * H, -1)
+    distinct = sum(int(torch.unique(sel[i][sel[i] >= 0]).numel()) for i in range(B * H))
+    nsel = int((view["sel"] >= 0).sum().item())
+    if params.mode == fs.FS_MODE_FSL:
+        cands = int(view["pool_count"].sum().item()) * 128
+    else:
+        A = torch.arange(N // 128, dtype=torch.float64) * 4
+        cands = float(A.sum().item()) * 128 * B * H
+    counts = dict(cands=cands, tokens_read=nsel * 32)
+    work = stage_work(wl, distinct, counts)
+
+    # timed region: K steps, per-stage CUDA events on the launch stream
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(FS_N_STAGES + 1)]
+              for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            fs.fs_attention_fwd_traced(q, k, v, lam, sigma, mix, events[i], params, out=out, ws=ws)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = t0.elapsed_time(t1)
+    stage_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
+                for j, name in enumerate(STAGE_NAMES)}
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = B * N * world
+    value = tokens / (ms / 1e3)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+        hout = torch.empty((B, H, N, d), dtype=torch.float32).pin_memory()
+        e2e_steps = max(2, min(args.steps, 5))
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            fs.fs_attention_fwd(q, k, v, lam, sigma, mix, params, out=out, ws=ws)
+            hout.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        e2e = {"value": B * N * world / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * 4,
+               "ms_per_step": e2e_ms}
+
+    pk = peaks()
+    kernels = {}
+    for name in STAGE_NAMES:
+        wk = work[name]
+        t_s = stage_ms[name] / 1e3
+        entry = {"ms": stage_ms[name], "share": stage_ms[name] / sum(stage_ms.values())}
+        entry["GB/s"] = wk["bytes"] / t_s / 1e9
+        entry["hbm_frac"] = entry["GB/s"] / pk["hbm"]
+        if "flops" in wk:
+            entry["TFLOP/s"] = wk["flops"] / t_s / 1e12
+            entry["tensor_frac"] = entry["TFLOP/s"] / pk["bf16"]
+        entry["bound"] = wk["bound"]
+        kernels[name] = entry
+    dom = max(STAGE_NAMES, key=lambda n: stage_ms[n])
+    wk = work[dom]
+    if wk["bound"] == "tensor":
+        ach = wk["flops"] / (stage_ms[dom] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16"], "traffic": None,
+                "peak_source": pk["source"] + " (bf16 burst)"}
+    else:
+        ach = wk["bytes"] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": ach / pk["hbm"], "traffic": None, "peak_source": pk["source"]}
+    # our kernels per step: cells 1, prune (sort, scan when >1 chunk, emit),
+    # select 1, readout 1, RoPE tables 1, window 1 (+3 roundings for fp32)
+    prune_launches = 0 if params.mode == fs.FS_MODE_FS else 2 + (1 if N // 32 > 64 else 0)
+    launches_per_step = 1 + prune_launches + 1 + 1 + 2 + (3 if code == fs.FS_FP32 else 0)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if code == fs.FS_BF16 else "fp32",
+        "data": "synthetic (seeded; lognormal key norms)",
+        "config": {"workload": wl.name, "batch": B, "heads": H, "seq_len": N, "head_dim": d,
+                   "w": params.w, "s": params.s, "K": params.K, "P": params.P, "W": params.W,
+                   "Bq": params.Bq, "mode": "FS-L" if params.mode == 0 else "FS",
+                   "parallelism": f"replica x{world} (independent (batch, head) slices)",
+                   "l2": "inputs larger than L2 (%.0f MB vs 129 MB)" % (in_bytes / 2**20)},
+        "roofline": roof, "kernels": kernels, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    return res
+
+
+# ---------------------------------------------------------------------------
+# oracle on host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, budget_s=10.0, seed=123):
+    """Time the fp64 oracle on host cores on a bounded sample of the workload:
+    whole head slices' setup plus a random set of query rows per head.
+    Returns (tokens_per_s, cores, description)."""
+    from oracle import oracle as O
+    from long_context_lm_gb300.inputs import bf16_values
+
+    O.build()
+    inp = make_inputs(1, 1, wl.seq_len, wl.head_dim, wl.seed, wl.sigma_ln, wl.dtype,
+                      "none", 0, wl.params)
+    q, k, v = [bf16_values(t).reshape(1, wl.seq_len, wl.head_dim).numpy() for t in (inp.q, inp.k, inp.v)]
+    rng = np.random.default_rng(seed)
+    cores = O.max_threads()
+    nrows = 256
+    elapsed, done = 0.0, 0
+    while True:
+        rows = np.sort(rng.choice(wl.seq_len, size=nrows, replace=False))
+        t = time.perf_counter()
+        O.forward(q, k, v, 1, inp.lam.numpy()[:1], inp.sigma.numpy()[:1], inp.mix.numpy()[:1],
+                  rows=rows, params=wl.params, want_branches=False)
+        dt = time.perf_counter() - t
+        elapsed += dt
+        done += nrows
+        if elapsed >= budget_s or nrows >= wl.seq_len:
+            break
+        nrows = int(min(wl.seq_len, max(nrows * 2, nrows * (budget_s - elapsed) / max(dt, 1e-3) / 2)))
+    # one token = one position across all H heads
+    tok_per_s = done / elapsed / wl.heads
+    desc = (f"{done} query rows of one head of {wl.name} (N={wl.seq_len}); per-call head setup "
+            f"(cells, pools of the sampled blocks, rotated keys) included; tokens = rows / H")
+    return tok_per_s, cores, desc, elapsed
+
+
+def run_reference(args):
+    wl = WORKLOADS[args.workload]
+    per_step = []
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    cores = desc = None
+    for i in range(args.warmup + args.steps):
+        v, cores, desc, el = oracle_sample(wl, budget_s=budget, seed=1000 + i)
+        if i >= args.warmup:
+            per_step.append(v)
+    value = statistics.mean(per_step)
+    ms = wl.batch * wl.seq_len / value * 1e3
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; lognormal key norms)",
+        "impl": "reference",
+        "config": {"workload": wl.name, "batch": wl.batch, "heads": wl.heads, "seq_len": wl.seq_len,
+                   "head_dim": wl.head_dim, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="fsl_64k", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--extra-lengths", default="fsl_16k_b2,fsl_256k",
+                    help="other workloads timed briefly for the per-length figures ('' = none)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if args.extra_lengths:
+        per_len = {args.workload: res["value"]}
+        for name in [n for n in args.extra_lengths.split(",") if n and n != args.workload]:
+            sub = argparse.Namespace(**vars(args))
+            sub.workload, sub.steps, sub.warmup, sub.no_e2e = name, 5, 3, True
+            r = run_ours(sub, rank, world, local_rank)
+            per_len[name] = r["value"]
+            res.setdefault("other_lengths", {})[name] = {
+                "value": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
+                "kernels": {k_: {"ms": v_["ms"], "share": v_["share"]} for k_, v_ in r["kernels"].items()}}
+        res["tokens_per_s_by_length"] = per_len
+    if rank == 0 and not args.no_cpu_baseline:
+        wl = WORKLOADS[args.workload]
+        v, cores, desc, el = oracle_sample(wl, budget_s=10.0)
+        res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc, "seconds": el}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

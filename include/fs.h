@@ -1,0 +1,192 @@
+/*
+ * fs.h -- C ABI of the GB300 (sm_103a) FreeSolo FS-L attention forward.
+ *
+ * Method: "FreeSolo: Linear-time Sparse Attention with Zero-Shot Length
+ * Extrapolation", as summarised on paper.rainbus.top (sections 核心方法 and
+ * 方法步骤详情 ②-⑥) and ai.info (section "Methodology in Plain English").
+ * Every head has a w-token sliding-window RoPE branch and a long-range NoPE
+ * branch that reads the tokens of K selected s-token key cells; the two are
+ * added with a per-head weight.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are DEVICE pointers to contiguous row-major arrays owned by the
+ *    caller.  q, k, v are [batch, H, N, d]; per-head parameter arrays are
+ *    [H] float32 device arrays.
+ *  - The library never allocates or frees memory.  Scratch comes from a
+ *    caller-provided device workspace sized by fs_workspace_bytes().
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work on it and return without
+ *    synchronising; a returned FS_OK means the arguments were valid and the
+ *    launches were accepted.
+ *  - Arguments are validated before anything is launched: a NULL pointer, a
+ *    non-positive size, N not a multiple of Bq or Bq not a multiple of s
+ *    give FS_ERR_INVALID_ARG; shapes the kernels are not built for (d != 64,
+ *    s != 32, Bq != 128, P > 64, K > 8, w outside [1, 8192]) give
+ *    FS_ERR_UNSUPPORTED.  A CUDA launch error gives FS_ERR_CUDA.  No call
+ *    throws across the ABI.
+ *  - Cell c covers tokens [c*s, (c+1)*s); C = N/s.  Query block beta covers
+ *    queries [beta*Bq, (beta+1)*Bq); a cell is available to the block iff it
+ *    ends at or before beta*Bq.
+ */
+#ifndef FS_H_
+#define FS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FS_OK = 0,
+  FS_ERR_INVALID_ARG = 1,
+  FS_ERR_UNSUPPORTED = 2,
+  FS_ERR_CUDA = 3,
+  FS_ERR_TIMEOUT = 4
+} fs_status;
+
+typedef enum { FS_BF16 = 0, FS_FP32 = 1 } fs_dtype;
+
+/* FS-L prunes the prefix to P + W cells per block; FS scores the whole
+ * available prefix (quadratic).  paper.rainbus.top summary, 核心方法. */
+typedef enum { FS_MODE_FSL = 0, FS_MODE_FS = 1 } fs_mode;
+
+/* Method parameters.  Page values: w=512, s=32, K=4, P=64, W=8, Bq=128
+ * (paper.rainbus.top summary, 核心方法); rope_base=10000 and rms_eps=1e-6 are
+ * readings (the pages give neither). */
+typedef struct {
+  int w;           /* window keys, self included: [n-w+1, n]           */
+  int s;           /* tokens per cell                                    */
+  int K;           /* cells read per query                               */
+  int P;           /* FS-L: older cells kept by largest max key norm     */
+  int W;           /* FS-L: most recent available cells always kept      */
+  int Bq;          /* query block sharing one availability set           */
+  float rope_base; /* theta_i = rope_base^(-2i/d), half-split pairing    */
+  float rms_eps;   /* RMSNorm epsilon of the long-branch output          */
+  int mode;        /* fs_mode                                            */
+} fs_params;
+
+/* Fills the page values above. */
+void fs_default_params(fs_params *p);
+
+/* Human-readable name of a status code (static string). */
+const char *fs_status_string(int status);
+
+/* Device workspace bytes fs_attention_fwd needs for this shape (includes the
+ * bf16 staging copies of q, k, v when dtype is FS_FP32).  0 on bad args. */
+size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p,
+                          int dtype);
+
+/* Workspace bytes fs_prune_cells needs (per-chunk running lists). */
+size_t fs_prune_workspace_bytes(int batch, int H, int N, const fs_params *p);
+
+/* Cell summaries (paper.rainbus.top summary, 方法步骤详情 ③; ai.info,
+ * "Key Contributions" 2): for every cell of every (batch, head)
+ *   kbar[c] = (1/s) * sum of the cell's s unrotated keys      [batch,H,C,d] f32
+ *   amax[c] = max over the cell's tokens of ||k_t||_2          [batch,H,C]   f32
+ * k is bf16 (dtype FS_BF16) or float32 (FS_FP32, rounded to bf16 first). */
+int fs_cell_summarize(const void *k, int dtype, int batch, int H, int N, int d,
+                      int s, float *kbar, float *amax, void *stream);
+
+/* FS-L availability sets (paper.rainbus.top summary, 方法步骤详情 ④; ai.info,
+ * "Methodology in Plain English": 8 recent plus the 64 highest-norm cells,
+ * updated only at query-block boundaries).  For every query block beta with
+ * A = beta*Bq/s available cells, the pool is the min(W, A) newest available
+ * cells plus the top-P older cells ranked by (amax desc, index asc).
+ *   amax        [batch,H,C] f32 (from fs_cell_summarize)
+ *   pool        [batch,H,N/Bq,P+W] int32: recent cells ascending, then the
+ *               kept older cells in rank order; unused slots are -1
+ *   pool_count  [batch,H,N/Bq] int32
+ *   ws          device scratch of fs_prune_workspace_bytes() bytes
+ * Linear in N: per 64-cell chunk sorted lists and a prefix merge.
+ * mode must be FS_MODE_FSL (FS needs no pool). */
+int fs_prune_cells(const float *amax, int batch, int H, int N,
+                   const fs_params *p, int32_t *pool, int32_t *pool_count,
+                   void *ws, size_t ws_bytes, void *stream);
+
+/* Cell scoring and top-K (paper.rainbus.top summary, 核心方法 and
+ * 方法步骤详情 ⑤; 局限与改进 for the erf factor; ai.info "Methodology in
+ * Plain English").  For query n of block beta and candidate c
+ *   u = q_n . kbar_c + lambda_h * amax_c * erf(sigma_h * (n - p_c) / s),
+ *   p_c = c*s + s/2,
+ * q unrotated.  Candidates: the block's pool (FS-L) or every available cell
+ * (FS; pool and pool_count may then be NULL).  Keeps the top min(K, |cands|)
+ * by (u desc, c asc).
+ *   q            [batch,H,N,d] bf16
+ *   lambda,sigma [H] f32
+ *   sel          [batch,H,N,K] int32 ranked, -1 padded
+ *   sel_score    [batch,H,N,K] f32 or NULL */
+int fs_select_cells(const void *q, int dtype, const float *kbar,
+                    const float *amax, const int32_t *pool,
+                    const int32_t *pool_count, const float *lambda,
+                    const float *sigma, int batch, int H, int N, int d,
+                    const fs_params *p, int32_t *sel, float *sel_score,
+                    void *stream);
+
+/* NoPE readout (paper.rainbus.top summary, 方法步骤详情 ⑥ and 前置知识
+ * NoPE): softmax(q_n . k_t / sqrt(d)) over the tokens of query n's selected
+ * cells, unrotated, weighted sum of v, then RMSNorm without gain:
+ *   o_long[n] = o / sqrt(mean(o^2) + rms_eps);  0 when no cell is selected.
+ *   q, k, v   [batch,H,N,d] bf16;  sel [batch,H,N,K] int32 (-1 = none)
+ *   o_long    [batch,H,N,d] f32 */
+int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
+                      const int32_t *sel, int batch, int H, int N, int d,
+                      const fs_params *p, float *o_long, void *stream);
+
+/* Workspace bytes fs_window_attn needs (RoPE angle tables). */
+size_t fs_window_workspace_bytes(int N, const fs_params *p);
+
+/* Sliding-window RoPE branch and branch mix (paper.rainbus.top summary,
+ * 方法步骤详情 ② and ⑥; ai.info, "Methodology in Plain English"):
+ *   o_win[n] = softmax over j in [max(0,n-w+1), n] of (R(n)q_n . R(j)k_j)/sqrt(d)
+ *              applied to v_j, RoPE half-split with base rope_base;
+ *   out[n]   = o_win[n] + mix_h * o_long[n]   (o_long NULL: out = o_win).
+ *   out       [batch,H,N,d] f32
+ *   ws        device scratch of fs_window_workspace_bytes() bytes */
+int fs_window_attn(const void *q, const void *k, const void *v, int dtype,
+                   const float *o_long, const float *mix, int batch, int H,
+                   int N, int d, const fs_params *p, float *out, void *ws,
+                   size_t ws_bytes, void *stream);
+
+/* Whole FS-L (or FS) attention forward: cell summaries, pools, selection,
+ * readout, window and mix, all on `stream`.
+ *   q, k, v   [batch,H,N,d] bf16 or f32 (f32 is rounded to bf16 once)
+ *   lambda, sigma, mix   [H] f32
+ *   out       [batch,H,N,d] f32
+ *   ws        device workspace of at least fs_workspace_bytes() bytes; after
+ *             the call it holds the intermediates (see fs_workspace_view). */
+int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype,
+                     int batch, int H, int N, int d, const fs_params *p,
+                     const float *lambda, const float *sigma, const float *mix,
+                     float *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Number of timed stages of fs_attention_fwd_traced: cell summaries,
+ * pruning, selection, readout, window (RoPE tables + window + mix). */
+#define FS_N_STAGES 5
+
+/* fs_attention_fwd that also records CUDA events between its stages, for
+ * per-kernel timing on the launch stream.  stage_events: NULL, or an array of
+ * FS_N_STAGES + 1 cudaEvent_t (as void*) created by the caller; event i is
+ * recorded before stage i and event FS_N_STAGES after the last stage (the
+ * fp32-to-bf16 rounding of FS_FP32 inputs happens before event 0; the prune
+ * stage is empty in FS mode).  Same arguments and results otherwise. */
+int fs_attention_fwd_traced(const void *q, const void *k, const void *v,
+                            int dtype, int batch, int H, int N, int d,
+                            const fs_params *p, const float *lambda,
+                            const float *sigma, const float *mix, float *out,
+                            void *ws, size_t ws_bytes, void *stream,
+                            void *const *stage_events);
+
+/* Byte offsets of the intermediates inside an fs_attention_fwd workspace,
+ * for inspection: kbar, amax, pool, pool_count, sel, o_long (any may be
+ * NULL).  Returns FS_OK or FS_ERR_INVALID_ARG. */
+int fs_workspace_view(int batch, int H, int N, int d, const fs_params *p,
+                      int dtype, size_t *off_kbar, size_t *off_amax,
+                      size_t *off_pool, size_t *off_pool_count,
+                      size_t *off_sel, size_t *off_o_long);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FS_H_ */

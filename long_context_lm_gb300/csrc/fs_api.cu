@@ -1,0 +1,286 @@
+// fs_api.cu -- the extern "C" entry points declared in include/fs.h:
+// argument validation, workspace carving and stream-ordered launches.
+#include <stdio.h>
+
+#include "fs_common.cuh"
+#include "fs_internal.h"
+
+namespace fs {
+
+__global__ void round_bf16_kernel(const float4 *__restrict__ src, uint2 *__restrict__ dst,
+                                  size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 x = __ldg(src + i);
+    dst[i] = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+  }
+}
+
+cudaError_t launch_round_bf16(const float *src, void *dst, size_t n, cudaStream_t st) {
+  const size_t n4 = n / 4;  // n is a multiple of 64 here
+  const unsigned grid = (unsigned)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
+  round_bf16_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const float4 *>(src),
+                                          static_cast<uint2 *>(dst), n4);
+  return cudaGetLastError();
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int check_params(const fs_params *p) {
+  if (!p) return FS_ERR_INVALID_ARG;
+  if (p->w < 1 || p->s < 1 || p->K < 1 || p->P < 0 || p->W < 0 || p->Bq < 1)
+    return FS_ERR_INVALID_ARG;
+  if (p->Bq % p->s) return FS_ERR_INVALID_ARG;
+  if (!(p->rms_eps >= 0.f) || !(p->rope_base > 0.f)) return FS_ERR_INVALID_ARG;
+  if (p->mode != FS_MODE_FSL && p->mode != FS_MODE_FS) return FS_ERR_INVALID_ARG;
+  if (p->s != kS || p->Bq != kBq || p->P > kMaxP || p->K > kMaxK || p->w > 8192)
+    return FS_ERR_UNSUPPORTED;
+  return FS_OK;
+}
+
+int check_shape(int batch, int H, int N, int d) {
+  if (batch < 1 || H < 1 || N < 1 || d < 1) return FS_ERR_INVALID_ARG;
+  if (N % kBq) return FS_ERR_INVALID_ARG;
+  if (d != kD) return FS_ERR_UNSUPPORTED;
+  if ((long long)batch * H > 65535) return FS_ERR_UNSUPPORTED;
+  if ((long long)N > (1ll << 24)) return FS_ERR_UNSUPPORTED;
+  return FS_OK;
+}
+
+int check_dtype(int dtype) {
+  return (dtype == FS_BF16 || dtype == FS_FP32) ? FS_OK : FS_ERR_INVALID_ARG;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? FS_OK : FS_ERR_CUDA; }
+
+#define FS_TRY(x)                  \
+  do {                             \
+    int _rc = (x);                 \
+    if (_rc != FS_OK) return _rc;  \
+  } while (0)
+
+// Layout of the fs_attention_fwd workspace.
+struct Layout {
+  size_t qb, kb, vb;       // bf16 copies (fp32 inputs only)
+  size_t kbar, amax, pool, pool_count, sel, o_long, rope, prune;
+  size_t total;
+};
+
+Layout make_layout(const Shape &sh, const fs_params &p, int dtype) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  const size_t elems = (size_t)sh.BH() * sh.N * sh.d;
+  const size_t in_bytes = dtype == FS_FP32 ? elems * 2 : 0;
+  L.qb = take(in_bytes);
+  L.kb = take(in_bytes);
+  L.vb = take(in_bytes);
+  L.kbar = take((size_t)sh.BH() * sh.C() * kD * sizeof(float));
+  L.amax = take((size_t)sh.BH() * sh.C() * sizeof(float));
+  L.pool = take((size_t)sh.BH() * sh.nblk() * (p.P + p.W) * sizeof(int32_t));
+  L.pool_count = take((size_t)sh.BH() * sh.nblk() * sizeof(int32_t));
+  L.sel = take((size_t)sh.BH() * sh.N * p.K * sizeof(int32_t));
+  L.o_long = take(elems * sizeof(float));
+  L.rope = take(rope_table_bytes(sh));
+  L.prune = take(prune_workspace_bytes(sh));
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" {
+
+void fs_default_params(fs_params *p) {
+  if (!p) return;
+  p->w = 512;
+  p->s = 32;
+  p->K = 4;
+  p->P = 64;
+  p->W = 8;
+  p->Bq = 128;
+  p->rope_base = 10000.f;
+  p->rms_eps = 1e-6f;
+  p->mode = FS_MODE_FSL;
+}
+
+const char *fs_status_string(int status) {
+  switch (status) {
+    case FS_OK: return "ok";
+    case FS_ERR_INVALID_ARG: return "invalid argument";
+    case FS_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case FS_ERR_CUDA: return "CUDA error";
+    case FS_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p, int dtype) {
+  if (check_params(p) || check_shape(batch, H, N, d) || check_dtype(dtype)) return 0;
+  return make_layout(Shape{batch, H, N, d}, *p, dtype).total;
+}
+
+int fs_workspace_view(int batch, int H, int N, int d, const fs_params *p, int dtype,
+                      size_t *off_kbar, size_t *off_amax, size_t *off_pool,
+                      size_t *off_pool_count, size_t *off_sel, size_t *off_o_long) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  const Layout L = make_layout(Shape{batch, H, N, d}, *p, dtype);
+  if (off_kbar) *off_kbar = L.kbar;
+  if (off_amax) *off_amax = L.amax;
+  if (off_pool) *off_pool = L.pool;
+  if (off_pool_count) *off_pool_count = L.pool_count;
+  if (off_sel) *off_sel = L.sel;
+  if (off_o_long) *off_o_long = L.o_long;
+  return FS_OK;
+}
+
+size_t fs_prune_workspace_bytes(int batch, int H, int N, const fs_params *p) {
+  if (check_params(p) || check_shape(batch, H, N, kD)) return 0;
+  return prune_workspace_bytes(Shape{batch, H, N, kD});
+}
+
+size_t fs_window_workspace_bytes(int N, const fs_params *p) {
+  if (check_params(p) || check_shape(1, 1, N, kD)) return 0;
+  return rope_table_bytes(Shape{1, 1, N, kD});
+}
+
+int fs_cell_summarize(const void *k, int dtype, int batch, int H, int N, int d, int s,
+                      float *kbar, float *amax, void *stream) {
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (!k || !kbar || !amax || s < 1) return FS_ERR_INVALID_ARG;
+  if (N % s) return FS_ERR_INVALID_ARG;
+  if (s != kS) return FS_ERR_UNSUPPORTED;
+  return status_of(launch_cell_summary(k, dtype == FS_FP32, Shape{batch, H, N, d}, kbar, amax,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int fs_prune_cells(const float *amax, int batch, int H, int N, const fs_params *p,
+                   int32_t *pool, int32_t *pool_count, void *ws, size_t ws_bytes,
+                   void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, kD));
+  if (!amax || !pool || !pool_count || !ws) return FS_ERR_INVALID_ARG;
+  if (p->mode != FS_MODE_FSL) return FS_ERR_INVALID_ARG;
+  const Shape sh{batch, H, N, kD};
+  if (ws_bytes < prune_workspace_bytes(sh)) return FS_ERR_INVALID_ARG;
+  return status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, ws,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int fs_select_cells(const void *q, int dtype, const float *kbar, const float *amax,
+                    const int32_t *pool, const int32_t *pool_count, const float *lambda,
+                    const float *sigma, int batch, int H, int N, int d, const fs_params *p,
+                    int32_t *sel, float *sel_score, void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+  if (!q || !kbar || !amax || !lambda || !sigma || !sel) return FS_ERR_INVALID_ARG;
+  const bool fs_mode = p->mode == FS_MODE_FS;
+  if (!fs_mode && (!pool || !pool_count)) return FS_ERR_INVALID_ARG;
+  return status_of(launch_select(q, kbar, amax, pool, pool_count, lambda, sigma,
+                                 Shape{batch, H, N, d}, p->K, p->P + p->W, fs_mode, sel,
+                                 sel_score, static_cast<cudaStream_t>(stream)));
+}
+
+int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
+                      const int32_t *sel, int batch, int H, int N, int d, const fs_params *p,
+                      float *o_long, void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !sel || !o_long) return FS_ERR_INVALID_ARG;
+  return status_of(launch_readout(q, k, v, sel, Shape{batch, H, N, d}, p->K, p->rms_eps, o_long,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const float *o_long,
+                   const float *mix, int batch, int H, int N, int d, const fs_params *p,
+                   float *out, void *ws, size_t ws_bytes, void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !out || !ws || (o_long && !mix)) return FS_ERR_INVALID_ARG;
+  const Shape sh{batch, H, N, d};
+  if (ws_bytes < rope_table_bytes(sh)) return FS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float2 *tables = static_cast<float2 *>(ws);
+  FS_TRY(status_of(launch_rope_tables(sh, p->rope_base, tables, st)));
+  return status_of(launch_window(q, k, v, o_long, mix, tables, sh, p->w, out, st));
+}
+
+int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype, int batch, int H,
+                     int N, int d, const fs_params *p, const float *lambda, const float *sigma,
+                     const float *mix, float *out, void *ws, size_t ws_bytes, void *stream) {
+  return fs_attention_fwd_traced(q, k, v, dtype, batch, H, N, d, p, lambda, sigma, mix, out, ws,
+                                 ws_bytes, stream, nullptr);
+}
+
+int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dtype, int batch,
+                            int H, int N, int d, const fs_params *p, const float *lambda,
+                            const float *sigma, const float *mix, float *out, void *ws,
+                            size_t ws_bytes, void *stream, void *const *stage_events) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (!q || !k || !v || !lambda || !sigma || !mix || !out || !ws) return FS_ERR_INVALID_ARG;
+  const Shape sh{batch, H, N, d};
+  const Layout L = make_layout(sh, *p, dtype);
+  if (ws_bytes < L.total) return FS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *base = static_cast<char *>(ws);
+  const void *qb = q, *kb = k, *vb = v;
+  if (dtype == FS_FP32) {
+    const size_t elems = (size_t)sh.BH() * N * d;
+    FS_TRY(status_of(launch_round_bf16(static_cast<const float *>(q), base + L.qb, elems, st)));
+    FS_TRY(status_of(launch_round_bf16(static_cast<const float *>(k), base + L.kb, elems, st)));
+    FS_TRY(status_of(launch_round_bf16(static_cast<const float *>(v), base + L.vb, elems, st)));
+    qb = base + L.qb;
+    kb = base + L.kb;
+    vb = base + L.vb;
+  }
+  float *kbar = reinterpret_cast<float *>(base + L.kbar);
+  float *amax = reinterpret_cast<float *>(base + L.amax);
+  int32_t *pool = reinterpret_cast<int32_t *>(base + L.pool);
+  int32_t *pool_count = reinterpret_cast<int32_t *>(base + L.pool_count);
+  int32_t *sel = reinterpret_cast<int32_t *>(base + L.sel);
+  float *o_long = reinterpret_cast<float *>(base + L.o_long);
+  float2 *rope = reinterpret_cast<float2 *>(base + L.rope);
+  const bool fs_mode = p->mode == FS_MODE_FS;
+
+  auto mark = [&](int i) -> int {
+    if (!stage_events || !stage_events[i]) return FS_OK;
+    return status_of(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st));
+  };
+  FS_TRY(mark(0));
+  FS_TRY(status_of(launch_cell_summary(kb, false, sh, kbar, amax, st)));
+  FS_TRY(mark(1));
+  if (!fs_mode)
+    FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));
+  FS_TRY(mark(2));
+  FS_TRY(status_of(launch_select(qb, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
+                                 p->P + p->W, fs_mode, sel, nullptr, st)));
+  FS_TRY(mark(3));
+  FS_TRY(status_of(launch_readout(qb, kb, vb, sel, sh, p->K, p->rms_eps, o_long, st)));
+  FS_TRY(mark(4));
+  FS_TRY(status_of(launch_rope_tables(sh, p->rope_base, rope, st)));
+  FS_TRY(status_of(launch_window(qb, kb, vb, o_long, mix, rope, sh, p->w, out, st)));
+  return mark(5);
+}
+
+}  // extern "C"

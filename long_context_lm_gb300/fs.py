@@ -1,0 +1,322 @@
+"""Thin Python binding of the C-ABI library ``libfs.so`` (``include/fs.h``).
+
+Only argument marshalling happens here: tensors are checked for device,
+dtype, shape and contiguity, their device pointers and the current CUDA
+stream are handed to the library, and a non-zero status raises ``FSError``.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU fallback, and a missing or unbuildable library raises.
+
+Function names match the C entry points.  Tensors follow the C layouts:
+q, k, v ``[batch, H, N, d]`` (bf16, or fp32 for ``fs_attention_fwd`` /
+``fs_cell_summarize``); per-head ``lam``, ``sigma``, ``mix`` ``[H]`` fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT = range(5)
+FS_BF16, FS_FP32 = 0, 1
+FS_MODE_FSL, FS_MODE_FS = 0, 1
+
+SYMBOLS = ["fs_default_params", "fs_status_string", "fs_workspace_bytes",
+           "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
+           "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
+           "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view"]
+FS_N_STAGES = 5
+STAGE_NAMES = ["cell_summary", "prune", "select", "readout", "window"]
+
+
+class fs_params(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_int), ("s", ctypes.c_int), ("K", ctypes.c_int),
+                ("P", ctypes.c_int), ("W", ctypes.c_int), ("Bq", ctypes.c_int),
+                ("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("mode", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class FSError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_stale: bool = True):
+    """Load libfs.so (compiling it in-tree first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_stale:
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is missing: build it with "
+                               "`python -m long_context_lm_gb300.build`")
+        L = ctypes.CDLL(_build.LIB)
+        P, I, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        PP = ctypes.POINTER(fs_params)
+        L.fs_default_params.argtypes = [PP]
+        L.fs_default_params.restype = None
+        L.fs_status_string.argtypes = [I]
+        L.fs_status_string.restype = ctypes.c_char_p
+        L.fs_workspace_bytes.argtypes = [I, I, I, I, PP, I]
+        L.fs_workspace_bytes.restype = Z
+        L.fs_prune_workspace_bytes.argtypes = [I, I, I, PP]
+        L.fs_prune_workspace_bytes.restype = Z
+        L.fs_window_workspace_bytes.argtypes = [I, PP]
+        L.fs_window_workspace_bytes.restype = Z
+        L.fs_cell_summarize.argtypes = [P, I, I, I, I, I, I, P, P, P]
+        L.fs_prune_cells.argtypes = [P, I, I, I, PP, P, P, P, Z, P]
+        L.fs_select_cells.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, PP, P, P, P]
+        L.fs_sparse_readout.argtypes = [P, P, P, I, P, I, I, I, I, PP, P, P]
+        L.fs_window_attn.argtypes = [P, P, P, I, P, P, I, I, I, I, PP, P, P, Z, P]
+        L.fs_attention_fwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, Z, P]
+        L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
+        L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 6
+        for name in SYMBOLS:
+            if name not in ("fs_default_params", "fs_status_string", "fs_workspace_bytes",
+                            "fs_prune_workspace_bytes", "fs_window_workspace_bytes"):
+                getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().fs_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != FS_OK:
+        raise FSError(status, where)
+
+
+def fs_default_params(**overrides) -> fs_params:
+    p = fs_params()
+    load().fs_default_params(ctypes.byref(p))
+    for k, v in overrides.items():
+        setattr(p, k, v)
+    return p
+
+
+def _params(params):
+    if params is None:
+        return fs_default_params()
+    if isinstance(params, dict):
+        return fs_default_params(**params)
+    return params
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtypes):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _dtype_code(t):
+    return FS_BF16 if t.dtype == torch.bfloat16 else FS_FP32
+
+
+def _qkv_shape(q):
+    if q.dim() != 4:
+        raise ValueError("q/k/v must be [batch, H, N, d]")
+    return tuple(q.shape)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def fs_workspace_bytes(batch, H, N, d, params=None, dtype=FS_BF16) -> int:
+    p = _params(params)
+    return load().fs_workspace_bytes(batch, H, N, d, ctypes.byref(p), dtype)
+
+
+def fs_cell_summarize(k, s=32, kbar=None, amax=None, stream=None):
+    L = load()
+    _dev(k, "k", (torch.bfloat16, torch.float32))
+    B, H, N, d = _qkv_shape(k)
+    C = N // s
+    kbar = kbar if kbar is not None else torch.empty((B, H, C, d), device=k.device, dtype=torch.float32)
+    amax = amax if amax is not None else torch.empty((B, H, C), device=k.device, dtype=torch.float32)
+    _dev(kbar, "kbar", (torch.float32,))
+    _dev(amax, "amax", (torch.float32,))
+    _check(L.fs_cell_summarize(_ptr(k), _dtype_code(k), B, H, N, d, s, _ptr(kbar), _ptr(amax),
+                               _stream(stream)), "fs_cell_summarize")
+    return kbar, amax
+
+
+def fs_prune_cells(amax, N, params=None, stream=None):
+    L = load()
+    p = _params(params)
+    _dev(amax, "amax", (torch.float32,))
+    B, H, C = amax.shape
+    nblk = N // p.Bq
+    pool = torch.empty((B, H, nblk, p.P + p.W), device=amax.device, dtype=torch.int32)
+    count = torch.empty((B, H, nblk), device=amax.device, dtype=torch.int32)
+    wsb = L.fs_prune_workspace_bytes(B, H, N, ctypes.byref(p))
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_prune_workspace_bytes")
+    ws = torch.empty(wsb, device=amax.device, dtype=torch.uint8)
+    _check(L.fs_prune_cells(_ptr(amax), B, H, N, ctypes.byref(p), _ptr(pool), _ptr(count),
+                            _ptr(ws), wsb, _stream(stream)), "fs_prune_cells")
+    return pool, count
+
+
+def fs_select_cells(q, kbar, amax, pool, pool_count, lam, sigma, params=None,
+                    with_scores=False, stream=None):
+    L = load()
+    p = _params(params)
+    _dev(q, "q", (torch.bfloat16,))
+    B, H, N, d = _qkv_shape(q)
+    for t, n in ((kbar, "kbar"), (amax, "amax"), (lam, "lam"), (sigma, "sigma")):
+        _dev(t, n, (torch.float32,))
+    if pool is not None:
+        _dev(pool, "pool", (torch.int32,))
+        _dev(pool_count, "pool_count", (torch.int32,))
+    sel = torch.empty((B, H, N, p.K), device=q.device, dtype=torch.int32)
+    score = torch.empty((B, H, N, p.K), device=q.device, dtype=torch.float32) if with_scores else None
+    _check(L.fs_select_cells(_ptr(q), FS_BF16, _ptr(kbar), _ptr(amax), _ptr(pool),
+                             _ptr(pool_count), _ptr(lam), _ptr(sigma), B, H, N, d,
+                             ctypes.byref(p), _ptr(sel), _ptr(score), _stream(stream)),
+           "fs_select_cells")
+    return (sel, score) if with_scores else sel
+
+
+def fs_sparse_readout(q, k, v, sel, params=None, o_long=None, stream=None):
+    L = load()
+    p = _params(params)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, n, (torch.bfloat16,))
+    _dev(sel, "sel", (torch.int32,))
+    B, H, N, d = _qkv_shape(q)
+    o_long = o_long if o_long is not None else torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
+    _check(L.fs_sparse_readout(_ptr(q), _ptr(k), _ptr(v), FS_BF16, _ptr(sel), B, H, N, d,
+                               ctypes.byref(p), _ptr(o_long), _stream(stream)), "fs_sparse_readout")
+    return o_long
+
+
+def fs_window_attn(q, k, v, o_long=None, mix=None, params=None, out=None, stream=None):
+    L = load()
+    p = _params(params)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, n, (torch.bfloat16,))
+    B, H, N, d = _qkv_shape(q)
+    if o_long is not None:
+        _dev(o_long, "o_long", (torch.float32,))
+        _dev(mix, "mix", (torch.float32,))
+    out = out if out is not None else torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
+    wsb = L.fs_window_workspace_bytes(N, ctypes.byref(p))
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_window_workspace_bytes")
+    ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    _check(L.fs_window_attn(_ptr(q), _ptr(k), _ptr(v), FS_BF16, _ptr(o_long), _ptr(mix), B, H,
+                            N, d, ctypes.byref(p), _ptr(out), _ptr(ws), wsb, _stream(stream)),
+           "fs_window_attn")
+    return out
+
+
+def fs_attention_fwd(q, k, v, lam, sigma, mix, params=None, out=None, ws=None, stream=None):
+    """Whole FS-L (or FS) forward.  Returns ``out`` [batch, H, N, d] fp32."""
+    L = load()
+    p = _params(params)
+    dt = (torch.bfloat16, torch.float32)
+    _dev(q, "q", dt)
+    _dev(k, "k", (q.dtype,))
+    _dev(v, "v", (q.dtype,))
+    for t, n in ((lam, "lam"), (sigma, "sigma"), (mix, "mix")):
+        _dev(t, n, (torch.float32,))
+    B, H, N, d = _qkv_shape(q)
+    code = _dtype_code(q)
+    wsb = L.fs_workspace_bytes(B, H, N, d, ctypes.byref(p), code)
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_workspace_bytes")
+    if ws is None:
+        ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    elif ws.numel() * ws.element_size() < wsb:
+        raise ValueError(f"workspace too small: {ws.numel()} < {wsb} bytes")
+    out = out if out is not None else torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
+    _dev(out, "out", (torch.float32,))
+    _check(L.fs_attention_fwd(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, d, ctypes.byref(p),
+                              _ptr(lam), _ptr(sigma), _ptr(mix), _ptr(out), _ptr(ws), wsb,
+                              _stream(stream)), "fs_attention_fwd")
+    return out
+
+
+def fs_attention_fwd_traced(q, k, v, lam, sigma, mix, events, params=None, out=None, ws=None,
+                            stream=None):
+    """fs_attention_fwd recording ``events`` (FS_N_STAGES + 1 torch.cuda.Event
+    objects, created with enable_timing) between its stages on the stream."""
+    L = load()
+    p = _params(params)
+    if len(events) != FS_N_STAGES + 1:
+        raise ValueError(f"need {FS_N_STAGES + 1} events")
+    B, H, N, d = _qkv_shape(q)
+    code = _dtype_code(q)
+    wsb = L.fs_workspace_bytes(B, H, N, d, ctypes.byref(p), code)
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_workspace_bytes")
+    if ws is None:
+        ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    elif ws.numel() * ws.element_size() < wsb:
+        raise ValueError("workspace too small")
+    out = out if out is not None else torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event lazily
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(L.fs_attention_fwd_traced(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, d,
+                                     ctypes.byref(p), _ptr(lam), _ptr(sigma), _ptr(mix),
+                                     _ptr(out), _ptr(ws), wsb, _stream(stream), arr),
+           "fs_attention_fwd_traced")
+    return out
+
+
+def fs_workspace_view(ws, batch, H, N, d, params=None, dtype=FS_BF16):
+    """Views of the intermediates an fs_attention_fwd call left in ``ws``:
+    dict with kbar, amax, pool, pool_count, sel, o_long."""
+    L = load()
+    p = _params(params)
+    offs = [ctypes.c_size_t() for _ in range(6)]
+    _check(L.fs_workspace_view(batch, H, N, d, ctypes.byref(p), dtype,
+                               *[ctypes.byref(o) for o in offs]), "fs_workspace_view")
+    C, nblk = N // p.s, N // p.Bq
+    spec = [("kbar", (batch, H, C, d), torch.float32), ("amax", (batch, H, C), torch.float32),
+            ("pool", (batch, H, nblk, p.P + p.W), torch.int32),
+            ("pool_count", (batch, H, nblk), torch.int32),
+            ("sel", (batch, H, N, p.K), torch.int32), ("o_long", (batch, H, N, d), torch.float32)]
+    res = {}
+    for (name, shape, dtype_), off in zip(spec, offs):
+        n = 1
+        for x in shape:
+            n *= x
+        nbytes = n * torch.tensor([], dtype=dtype_).element_size()
+        res[name] = ws[off.value: off.value + nbytes].view(dtype_).view(shape)
+    return res

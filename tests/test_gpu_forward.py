@@ -1,0 +1,83 @@
+"""End-to-end parity of fs_attention_fwd against the fp64 oracle (GPU only):
+small cases on every row, every workload at its full size on sampled rows (in
+the launch configuration the benchmark times), planted needles, edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from long_context_lm_gb300 import fs
+from long_context_lm_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+from parity import compare_forward, oracle_rows, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+PAGE = dict(w=512, s=32, K=4, P=64, W=8, Bq=128, rope_base=10000.0, rms_eps=1e-6, mode=0)
+
+
+def run_fwd(inp, params):
+    d = to_device(inp)
+    B, H, N, dd = inp.q.shape
+    code = fs.FS_FP32 if inp.q.dtype == torch.float32 else fs.FS_BF16
+    ws = torch.empty(fs.fs_workspace_bytes(B, H, N, dd, params, code), device="cuda",
+                     dtype=torch.uint8)
+    out = fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], params,
+                              ws=ws)
+    view = fs.fs_workspace_view(ws, B, H, N, dd, params, code)
+    torch.cuda.synchronize()
+    return (out.cpu().numpy().reshape(B * H, N, dd),
+            view["sel"].cpu().numpy().reshape(B * H, N, -1), view)
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=1, H=2, N=2048, dtype="fp32", seed=0, params=PAGE),             # small fp32 case
+    dict(B=2, H=4, N=4096, dtype="bf16", seed=1, params=PAGE, needles="train", n=4),
+    dict(B=1, H=2, N=3072, dtype="bf16", seed=5, params=dict(PAGE, mode=1)),   # base FS
+    dict(B=1, H=3, N=4096, dtype="bf16", seed=6, params=dict(PAGE, P=8, W=2)),  # heavy pruning
+    dict(B=1, H=2, N=128, dtype="bf16", seed=7, params=PAGE),               # one block
+    dict(B=1, H=2, N=640, dtype="bf16", seed=8, params=dict(PAGE, w=64, K=2)),
+])
+def test_forward_all_rows(case):
+    inp = make_inputs(case["B"], case["H"], case["N"], seed=case["seed"], dtype=case["dtype"],
+                      needles=case.get("needles", "none"), n_needles=case.get("n", 0))
+    params = case["params"]
+    out, sel, _ = run_fwd(inp, params)
+    rows = np.arange(case["N"])
+    stats = compare_forward(inp, params, rows, out, sel)
+    print(case, stats)
+
+
+def test_first_block_has_no_long_branch():
+    inp = make_inputs(1, 2, 256, seed=3)
+    out, sel, view = run_fwd(inp, PAGE)
+    assert np.all(sel[:, :128] == -1)
+    assert torch.all(view["o_long"][:, :, :128] == 0)
+
+
+@pytest.mark.parametrize("name", ["fsl_2k_h2_fp32", "fsl_4k_b8", "fsl_16k_b2", "fsl_64k", "fsl_256k"])
+def test_workload_full_size(name):
+    # The benchmark's workloads at full size; the oracle checks sampled rows
+    # (first/last/random blocks, first/last/random rows in each) plus every
+    # planted needle's query.
+    wl = WORKLOADS[name]
+    inp = workload_inputs(name)
+    out, sel, _ = run_fwd(inp, wl.params)
+    N = wl.seq_len
+    rows = sample_rows(N, n_blocks=24 if N <= 16384 else 16, per_block=16, seed=wl.seed)
+    needle_rows = sorted({j for (_, _, _, j) in inp.needles})
+    rows = np.unique(np.concatenate([rows, np.asarray(needle_rows, dtype=np.int64)]))
+    stats = compare_forward(inp, wl.params, rows, out, sel)
+    H = wl.heads
+    hits = [p // 32 in sel[b * H + h, j].tolist() for (b, h, p, j) in inp.needles]
+    if name == "fsl_256k":  # the boosted needle must be retrieved
+        assert all(hits), inp.needles
+    print(name, stats, "needle hit rate", np.mean(hits) if hits else None)
+
+
+def test_explicit_stream_and_repeat_calls_are_deterministic():
+    inp = make_inputs(1, 2, 4096, seed=11)
+    d = to_device(inp)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], PAGE)
+        b = fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], PAGE)
+    s.synchronize()
+    assert torch.equal(a, b)
