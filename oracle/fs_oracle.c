@@ -408,6 +408,8 @@ int fso_forward(const float *q, const float *k, const float *v, int BH, int H,
                 double *gap_rel, double *pool_gap, int nthreads) {
   if (N % Bq || Bq % s || d > 256 || d % 2 || K < 0 || K > 64) return 1;
   if (rows == NULL) nrows = N;
+  for (int r = 0; rows && r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return 4;
   int C = N / s, nblk = N / Bq;
   int cap = mode == 1 ? C : P + W;
   set_threads(nthreads);

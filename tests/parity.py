@@ -99,8 +99,9 @@ def sample_rows(N, n_blocks=24, per_block=16, seed=0, Bq=128):
     and last row of each chosen block and random rows inside it."""
     rng = np.random.default_rng(seed)
     nblk = N // Bq
-    blocks = sorted(set([0, 1, min(2, nblk - 1), nblk - 1] +
-                        rng.integers(0, nblk, size=max(0, n_blocks - 4)).tolist()))
+    blocks = sorted(b for b in set([0, 1, 2, nblk - 1] +
+                                   rng.integers(0, nblk, size=max(0, n_blocks - 4)).tolist())
+                    if 0 <= b < nblk)
     rows = []
     for b in blocks:
         rows += [b * Bq, b * Bq + Bq - 1]
