@@ -66,7 +66,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -278,46 +278,49 @@ def run_ours(args, rank, world, local_rank):
 # oracle on host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, budget_s=10.0, seed=123):
-    """Time the fp64 oracle on host cores on a bounded sample of the workload:
-    whole head slices' setup plus a random set of query rows per head.
-    Returns (tokens_per_s, cores, description)."""
+def oracle_sample(wl, budget_s=10.0, start=0, inp=None):
+    """Time the fp64 oracle, as it stands, on the host cores on a bounded
+    sample of the workload: whole (batch, head) slices, every query row, one
+    slice after another until the time budget is spent (at least one slice).
+    Returns (tokens_per_s, cores, description, seconds)."""
     from oracle import oracle as O
     from long_context_lm_gb300.inputs import bf16_values
 
     O.build()
-    inp = make_inputs(1, 1, wl.seq_len, wl.head_dim, wl.seed, wl.sigma_ln, wl.dtype,
-                      "none", 0, wl.params)
-    q, k, v = [bf16_values(t).reshape(1, wl.seq_len, wl.head_dim).numpy() for t in (inp.q, inp.k, inp.v)]
-    rng = np.random.default_rng(seed)
+    if inp is None:
+        inp = make_inputs(wl.batch, wl.heads, wl.seq_len, wl.head_dim, wl.seed, wl.sigma_ln,
+                          wl.dtype, wl.needles, wl.n_needles, wl.params)
+    B, H, N, d = inp.q.shape
+    qs, ks, vs = [t.reshape(B * H, N, d) for t in (inp.q, inp.k, inp.v)]
     cores = O.max_threads()
-    nrows = 256
-    elapsed, done = 0.0, 0
-    while True:
-        rows = np.sort(rng.choice(wl.seq_len, size=nrows, replace=False))
+    elapsed, slices = 0.0, 0
+    for i in range(B * H):
+        bh = (start + i) % (B * H)
+        q, k, v = [bf16_values(t[bh:bh + 1]).numpy() for t in (qs, ks, vs)]
+        h = bh % H
         t = time.perf_counter()
-        O.forward(q, k, v, 1, inp.lam.numpy()[:1], inp.sigma.numpy()[:1], inp.mix.numpy()[:1],
-                  rows=rows, params=wl.params, want_branches=False)
-        dt = time.perf_counter() - t
-        elapsed += dt
-        done += nrows
-        if elapsed >= budget_s or nrows >= wl.seq_len:
+        O.forward(q, k, v, 1, inp.lam.numpy()[h:h + 1], inp.sigma.numpy()[h:h + 1],
+                  inp.mix.numpy()[h:h + 1], params=wl.params, want_branches=False)
+        elapsed += time.perf_counter() - t
+        slices += 1
+        if elapsed >= budget_s:
             break
-        nrows = int(min(wl.seq_len, max(nrows * 2, nrows * (budget_s - elapsed) / max(dt, 1e-3) / 2)))
-    # one token = one position across all H heads
-    tok_per_s = done / elapsed / wl.heads
-    desc = (f"{done} query rows of one head of {wl.name} (N={wl.seq_len}); per-call head setup "
-            f"(cells, pools of the sampled blocks, rotated keys) included; tokens = rows / H")
+    # one token = one position of one batch row across all H heads
+    tok_per_s = slices * N / H / elapsed
+    desc = (f"{slices} of {B * H} (batch, head) slices of {wl.name} (N={N}), every query row; "
+            f"tokens counted as rows / H")
     return tok_per_s, cores, desc, elapsed
 
 
 def run_reference(args):
     wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl.batch, wl.heads, wl.seq_len, wl.head_dim, wl.seed, wl.sigma_ln, wl.dtype,
+                      wl.needles, wl.n_needles, wl.params)
     per_step = []
-    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    budget = min(10.0, 120.0 / max(1, args.steps + args.warmup))
     cores = desc = None
     for i in range(args.warmup + args.steps):
-        v, cores, desc, el = oracle_sample(wl, budget_s=budget, seed=1000 + i)
+        v, cores, desc, el = oracle_sample(wl, budget_s=budget, start=i, inp=inp)
         if i >= args.warmup:
             per_step.append(v)
     value = statistics.mean(per_step)
@@ -340,7 +343,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="fsl_64k", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
