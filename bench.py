@@ -350,7 +350,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--extra-lengths", default="fsl_16k_b2,fsl_256k",
-                    help="other workloads timed briefly for the per-length figures ('' = none)")
+                    help="other workloads timed briefly for the per-length figures ('none' = skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -367,7 +367,7 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_ours(args, rank, world, local_rank)
-    if args.extra_lengths:
+    if args.extra_lengths and args.extra_lengths != "none":
         per_len = {args.workload: res["value"]}
         for name in [n for n in args.extra_lengths.split(",") if n and n != args.workload]:
             sub = argparse.Namespace(**vars(args))
