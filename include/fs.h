@@ -178,6 +178,14 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v,
                             void *ws, size_t ws_bytes, void *stream,
                             void *const *stage_events);
 
+/* Every workspace begins with a 256-byte header whose first int is a device
+ * error word, cleared at the start of each call.  Kernels that wait on
+ * mbarriers give up after a bounded number of polls (seconds) and record
+ * FS_ERR_TIMEOUT there instead of hanging.  fs_check_status synchronises
+ * `stream` and returns FS_OK or the recorded status (FS_ERR_CUDA if the copy
+ * or the synchronisation fails). */
+int fs_check_status(const void *ws, void *stream);
+
 /* Byte offsets of the intermediates inside an fs_attention_fwd workspace,
  * for inspection: kbar, amax, pool, pool_count, sel, o_long (any may be
  * NULL).  Returns FS_OK or FS_ERR_INVALID_ARG. */

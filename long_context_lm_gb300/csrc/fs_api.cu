@@ -62,6 +62,10 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? FS_OK : FS_ERR_CUDA; }
     if (_rc != FS_OK) return _rc;  \
   } while (0)
 
+// Every workspace starts with a 256-byte header whose first int is the device
+// error word (0 = ok, else an fs_status set by a kernel's bounded wait).
+constexpr size_t kHeader = 256;
+
 // Layout of the fs_attention_fwd workspace.
 struct Layout {
   size_t qb, kb, vb;       // bf16 copies (fp32 inputs only)
@@ -71,7 +75,7 @@ struct Layout {
 
 Layout make_layout(const Shape &sh, const fs_params &p, int dtype) {
   Layout L{};
-  size_t off = 0;
+  size_t off = kHeader;
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off = align_up(off + bytes);
@@ -88,7 +92,7 @@ Layout make_layout(const Shape &sh, const fs_params &p, int dtype) {
   L.pool_count = take((size_t)sh.BH() * sh.nblk() * sizeof(int32_t));
   L.sel = take((size_t)sh.BH() * sh.N * p.K * sizeof(int32_t));
   L.o_long = take(elems * sizeof(float));
-  L.rope = take(rope_table_bytes(sh));
+  L.rope = take(window_table_bytes(p.w));
   L.prune = take(prune_workspace_bytes(sh));
   L.total = off;
   return L;
@@ -153,7 +157,17 @@ size_t fs_prune_workspace_bytes(int batch, int H, int N, const fs_params *p) {
 
 size_t fs_window_workspace_bytes(int N, const fs_params *p) {
   if (check_params(p) || check_shape(1, 1, N, kD)) return 0;
-  return rope_table_bytes(Shape{1, 1, N, kD});
+  return kHeader + window_table_bytes(p->w);
+}
+
+int fs_check_status(const void *ws, void *stream) {
+  if (!ws) return FS_ERR_INVALID_ARG;
+  int word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FS_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FS_ERR_CUDA;
+  return word == 0 ? FS_OK : word;
 }
 
 int fs_cell_summarize(const void *k, int dtype, int batch, int H, int N, int d, int s,
@@ -193,7 +207,7 @@ int fs_select_cells(const void *q, int dtype, const float *kbar, const float *am
   if (!fs_mode && (!pool || !pool_count)) return FS_ERR_INVALID_ARG;
   return status_of(launch_select(q, kbar, amax, pool, pool_count, lambda, sigma,
                                  Shape{batch, H, N, d}, p->K, p->P + p->W, fs_mode, sel,
-                                 sel_score, static_cast<cudaStream_t>(stream)));
+                                 sel_score, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
@@ -217,11 +231,13 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const
   if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !ws || (o_long && !mix)) return FS_ERR_INVALID_ARG;
   const Shape sh{batch, H, N, d};
-  if (ws_bytes < rope_table_bytes(sh)) return FS_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader + window_table_bytes(p->w)) return FS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float2 *tables = static_cast<float2 *>(ws);
-  FS_TRY(status_of(launch_rope_tables(sh, p->rope_base, tables, st)));
-  return status_of(launch_window(q, k, v, o_long, mix, tables, sh, p->w, out, st));
+  char *base = static_cast<char *>(ws);
+  int *err = reinterpret_cast<int *>(base);
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  return status_of(launch_window_tc(q, k, v, o_long, mix, base + kHeader, sh, p->w, p->rope_base,
+                                    out, err, st));
 }
 
 int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype, int batch, int H,
@@ -260,8 +276,9 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   int32_t *pool_count = reinterpret_cast<int32_t *>(base + L.pool_count);
   int32_t *sel = reinterpret_cast<int32_t *>(base + L.sel);
   float *o_long = reinterpret_cast<float *>(base + L.o_long);
-  float2 *rope = reinterpret_cast<float2 *>(base + L.rope);
+  int *err = reinterpret_cast<int *>(base);
   const bool fs_mode = p->mode == FS_MODE_FS;
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
 
   auto mark = [&](int i) -> int {
     if (!stage_events || !stage_events[i]) return FS_OK;
@@ -274,12 +291,12 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
     FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));
   FS_TRY(mark(2));
   FS_TRY(status_of(launch_select(qb, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
-                                 p->P + p->W, fs_mode, sel, nullptr, st)));
+                                 p->P + p->W, fs_mode, sel, nullptr, err, st)));
   FS_TRY(mark(3));
   FS_TRY(status_of(launch_readout(qb, kb, vb, sel, sh, p->K, p->rms_eps, o_long, st)));
   FS_TRY(mark(4));
-  FS_TRY(status_of(launch_rope_tables(sh, p->rope_base, rope, st)));
-  FS_TRY(status_of(launch_window(qb, kb, vb, o_long, mix, rope, sh, p->w, out, st)));
+  FS_TRY(status_of(launch_window_tc(qb, kb, vb, o_long, mix, base + L.rope, sh, p->w,
+                                    p->rope_base, out, err, st)));
   return mark(5);
 }
 

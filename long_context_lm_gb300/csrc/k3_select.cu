@@ -1,4 +1,5 @@
-// k3_select.cu -- per-query cell scores and top-K selection.
+// k3_select.cu -- per-query cell scores and top-K selection on the tensor
+// cores (tcgen05 + TMEM).
 //
 // FreeSolo (paper.rainbus.top summary, 核心方法 and 方法步骤详情 ⑤; 局限与改进
 // for the erf factor g_h >= erf(2); ai.info summary, "Methodology in Plain
@@ -6,145 +7,220 @@
 //     u = q_n . kbar_c + lambda_h * a_c * erf(sigma_h * (n - p_c) / s),
 // p_c = c*s + s/2, with the unrotated query, and the K best cells are read.
 // Candidates are the block's FS-L pool (<= P+W cells) or, in FS mode, every
-// cell that ends at or before the block start.
+// cell that ends at or before the block start (processed in chunks of 128).
 //
-// One CTA per (head, 128-query block), one thread per query.  Candidate mean
-// keys are staged in shared memory in chunks of 64 cells and every thread
-// computes its dot products in fp32 (the scores decide integer indices, so
-// they are kept fp32-accurate).  The top-K list lives in registers and is
-// ranked by (u desc, c asc).
+// One CTA per (head, 128-query block).  The content term of all 128 queries
+// against all candidates is one tcgen05 product D[128 x Nc] in TMEM: q is
+// exactly bf16, and every fp32 mean key is split into three bf16 terms
+// (hi + mid + lo, 24 significant bits), so three MMA chains accumulating in
+// fp32 give fp32-grade dot products -- the scores decide indices, so they
+// must not carry bf16 rounding.  Each scoring thread owns one query row
+// (= TMEM lane): it adds the erf bias and keeps a register top-K ranked by
+// (u desc, c asc).  erf(x) is exactly 1 in fp32 once x >= 4 (erfc(4) = 1.5e-8
+// is below half an ulp of 1), which holds for every cell but the newest few,
+// so the special function is evaluated only below that point.
 #include "fs_common.cuh"
 #include "fs_internal.h"
+#include "tc05.cuh"
 
 namespace fs {
+namespace {
 
-constexpr int kSelChunk = 64;
+constexpr int kChunk = 128;       // candidates per MMA (N <= 128)
+constexpr int kThreads = 192;     // warps 0-3 score, warp 4 MMA, all stage operands
+constexpr uint32_t kOffQ = 0, kOffK = 16384;  // K split tiles: 3 x 16 KB
+constexpr uint32_t kSmemBytes = 16384 + 3 * 16384 + 1024;
 
 __device__ __forceinline__ bool ranks_before(float u, int c, float u2, int c2) {
   return u > u2 || (u == u2 && c < c2);
 }
 
-template <bool kFS>
-__global__ void __launch_bounds__(128) k3_select_kernel(
+__global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
     const float *__restrict__ amax, const int32_t *__restrict__ pool,
     const int32_t *__restrict__ pool_count, const float *__restrict__ lambda,
-    const float *__restrict__ sigma, int H, int N, int K, int cap,
-    int32_t *__restrict__ sel, float *__restrict__ sel_score) {
-  __shared__ __align__(16) float s_kb[kSelChunk][kD];
-  __shared__ float s_a[kSelChunk];
-  __shared__ int s_c[kSelChunk];
+    const float *__restrict__ sigma, int H, int N, int K, int cap, int fs_mode,
+    int32_t *__restrict__ sel, float *__restrict__ sel_score, int *err) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem =
+      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ int s_c[kChunk];
+  __shared__ float s_a[kChunk];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t s_tmem;
 
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int beta = blockIdx.x, bh = blockIdx.y, h = bh % H;
-  const int C = N / kS;
-  const int n = beta * kBq + threadIdx.x;
-  const size_t row = (size_t)bh * N + n;
+  const int C = N / kS, nblk = N / kBq;
+  const int b0 = beta * kBq;
+  const size_t head = (size_t)bh * N;
+  const int A = beta * (kBq / kS);
+  const int count = fs_mode ? A : min(max(pool_count[(size_t)bh * nblk + beta], 0), cap);
+  const int32_t *pl = fs_mode ? nullptr : pool + ((size_t)bh * nblk + beta) * cap;
 
-  float qf[kD];
-  {
-    const uint4 *src = reinterpret_cast<const uint4 *>(q + row * kD);
-#pragma unroll
-    for (int i = 0; i < kD / 8; ++i) {
-      const uint4 r = __ldg(src + i);
-      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        qf[8 * i + 2 * j] = bf16_lo(w[j]);
-        qf[8 * i + 2 * j + 1] = bf16_hi(w[j]);
-      }
-    }
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_fence_init();
   }
-  const float lam = lambda[h], sig = sigma[h];
-  const float inv_s = 1.0f / kS;
+  if (warp == 4) {
+    tc::tmem_alloc(&s_tmem, 128);
+    tc::tmem_relinquish();
+  }
+  // query tile -> shared (K-major SW128)
+  for (int p = tid; p < kBq * 8; p += kThreads) {
+    const int r = p >> 3, ch = p & 7;
+    *reinterpret_cast<uint4 *>(smem + kOffQ + swz128(r, ch)) =
+        __ldg(reinterpret_cast<const uint4 *>(q + (head + b0 + r) * kD) + ch);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  const uint32_t sbase = smem_u32(smem);
 
+  const int r = tid;  // query row of a scoring thread
+  const int n = b0 + r;
+  const float lam = lambda[h], sig_s = sigma[h] * (1.0f / kS);
   float bu[kMaxK];
   int bc[kMaxK];
 #pragma unroll
-  for (int r = 0; r < kMaxK; ++r) {
-    bu[r] = -INFINITY;
-    bc[r] = 0x7fffffff;
+  for (int i = 0; i < kMaxK; ++i) {
+    bu[i] = -INFINITY;
+    bc[i] = 0x7fffffff;
   }
-
-  const int A = beta * (kBq / kS);
-  const int count = kFS ? A : min(pool_count[(size_t)bh * (N / kBq) + beta], cap);
   int nvalid = 0;
-  const int32_t *pl = kFS ? nullptr : pool + ((size_t)bh * (N / kBq) + beta) * cap;
+  bool ok = true;
 
-  for (int base = 0; base < count; base += kSelChunk) {
-    const int m = min(kSelChunk, count - base);
-    __syncthreads();
-    if (threadIdx.x < m) {
-      int c = kFS ? base + threadIdx.x : pl[base + threadIdx.x];
-      if (c < 0 || c >= A) c = -1;  // not a cell this block may read: skipped
-      s_c[threadIdx.x] = c;
-      s_a[threadIdx.x] = c >= 0 ? amax[(size_t)bh * C + c] : 0.f;
-    }
-    __syncthreads();
-    // stage the m mean keys: m*16 float4 pieces over 128 threads
-    for (int i = threadIdx.x; i < m * (kD / 4); i += blockDim.x) {
-      const int cc = i / (kD / 4), part = i % (kD / 4);
-      const int c = s_c[cc];
-      reinterpret_cast<float4 *>(s_kb[cc])[part] =
-          c >= 0 ? __ldg(reinterpret_cast<const float4 *>(kbar + ((size_t)bh * C + c) * kD) + part)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-    for (int j = 0; j < m; ++j) {
-      if (s_c[j] < 0) continue;
-      const float4 *kb = reinterpret_cast<const float4 *>(s_kb[j]);
-      float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < kD / 4; i += 2) {
-        const float4 x = kb[i], y = kb[i + 1];
-        d0 = fmaf(qf[4 * i], x.x, d0);
-        d0 = fmaf(qf[4 * i + 1], x.y, d0);
-        d0 = fmaf(qf[4 * i + 2], x.z, d0);
-        d0 = fmaf(qf[4 * i + 3], x.w, d0);
-        d1 = fmaf(qf[4 * i + 4], y.x, d1);
-        d1 = fmaf(qf[4 * i + 5], y.y, d1);
-        d1 = fmaf(qf[4 * i + 6], y.z, d1);
-        d1 = fmaf(qf[4 * i + 7], y.w, d1);
+  for (int base = 0, chunk = 0; base < count; base += kChunk, ++chunk) {
+    const int nc = min(kChunk, count - base);
+    const int np = (nc + 15) / 16 * 16;
+    for (int j = tid; j < np; j += kThreads) {
+      int c = -1;
+      if (j < nc) {
+        c = fs_mode ? base + j : pl[base + j];
+        if (c < 0 || c >= A) c = -1;  // not a cell this block may read: skipped
       }
+      s_c[j] = c;
+      s_a[j] = c >= 0 ? amax[(size_t)bh * C + c] : 0.f;
+    }
+    __syncthreads();
+    // mean keys -> three bf16 split tiles (rows beyond nc or skipped: zero)
+    for (int p = tid; p < np * 8; p += kThreads) {
+      const int j = p >> 3, ch = p & 7;
       const int c = s_c[j];
-      const float pc = (float)(c * kS) + 0.5f * kS;
-      float u = (d0 + d1) + lam * s_a[j] * erff(sig * ((float)n - pc) * inv_s);
-      int cu = c;
-      ++nvalid;
+      float x[8];
+      if (c >= 0) {
+        const float4 *src = reinterpret_cast<const float4 *>(kbar + ((size_t)bh * C + c) * kD) + 2 * ch;
+        const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
+        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+      } else {
 #pragma unroll
-      for (int r = 0; r < kMaxK; ++r) {
-        if (r < K && ranks_before(u, cu, bu[r], bc[r])) {
-          const float tu = bu[r];
-          const int tc = bc[r];
-          bu[r] = u;
-          bc[r] = cu;
-          u = tu;
-          cu = tc;
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      }
+      uint32_t hw[4], mw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hw[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+        const float r0 = x[2 * e] - bf16_lo(hw[e]), r1 = x[2 * e + 1] - bf16_hi(hw[e]);
+        mw[e] = pack_bf16(r0, r1);
+        lw[e] = pack_bf16(r0 - bf16_lo(mw[e]), r1 - bf16_hi(mw[e]));
+      }
+      const uint32_t off = swz128(j, ch);
+      *reinterpret_cast<uint4 *>(smem + kOffK + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(smem + kOffK + 16384 + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+      *reinterpret_cast<uint4 *>(smem + kOffK + 32768 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+    if (tid == 128) {  // warp 4, one thread: D = Q.(hi + mid + lo)^T
+      tc::fence_after_sync();
+      const uint32_t id = tc::idesc_bf16(128, np, 0);
+      const uint32_t sq = sbase + kOffQ;
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint32_t sk = sbase + kOffK + part * 16384;
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k)
+          tc::mma_ss(tmem, tc::desc_sw128(sq + 32 * k), tc::desc_sw128(sk + 32 * k), id,
+                     (part > 0 || k > 0) ? 1u : 0u);
+      }
+      tc::mma_commit(&bar);
+    }
+    if (warp < 4) {
+      ok = tc::mbar_wait(&bar, chunk & 1, err) && ok;
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+      for (int j0 = 0; j0 < nc; j0 += 32) {
+        uint32_t d[32];
+        tc::tmem_ld32(taddr + j0, d);
+        tc::tmem_wait_ld();
+        const int jn = min(32, nc - j0);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          if (jj >= jn) break;
+          const int c = s_c[j0 + jj];
+          if (c < 0) continue;
+          const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
+          const float g = x < 4.0f ? erff(x) : 1.0f;
+          float u = __uint_as_float(d[jj]) + lam * s_a[j0 + jj] * g;
+          int cu = c;
+          ++nvalid;
+          float wu = bu[0];
+          int wc = bc[0];
+#pragma unroll
+          for (int i = 1; i < kMaxK; ++i)
+            if (i < K) {
+              wu = bu[i];
+              wc = bc[i];
+            }
+          if (!ranks_before(u, cu, wu, wc)) continue;
+#pragma unroll
+          for (int i = 0; i < kMaxK; ++i) {
+            if (i < K && ranks_before(u, cu, bu[i], bc[i])) {
+              const float tu = bu[i];
+              const int tcc = bc[i];
+              bu[i] = u;
+              bc[i] = cu;
+              u = tu;
+              cu = tcc;
+            }
+          }
         }
       }
     }
+    tc::fence_before_sync();
+    __syncthreads();  // shared tiles and TMEM are reused by the next chunk
   }
+  if (warp < 4 && ok) {
 #pragma unroll
-  for (int r = 0; r < kMaxK; ++r) {
-    if (r < K) {
-      const bool valid = r < nvalid;
-      sel[row * K + r] = valid ? bc[r] : -1;
-      if (sel_score) sel_score[row * K + r] = valid ? bu[r] : 0.f;
+    for (int i = 0; i < kMaxK; ++i) {
+      if (i < K) {
+        const bool valid = i < nvalid;
+        sel[(head + n) * K + i] = valid ? bc[i] : -1;
+        if (sel_score) sel_score[(head + n) * K + i] = valid ? bu[i] : 0.f;
+      }
     }
   }
+  if (warp == 4) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 128);
+  }
 }
+
+}  // namespace
 
 cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const int32_t *pool, const int32_t *pool_count, const float *lambda,
                           const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
-                          int32_t *sel, float *sel_score, cudaStream_t st) {
+                          int32_t *sel, float *sel_score, int *err, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k3_select_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
   dim3 grid(sh.nblk(), sh.BH());
-  const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(q);
-  if (fs_mode)
-    k3_select_kernel<true><<<grid, kBq, 0, st>>>(qb, kbar, amax, pool, pool_count, lambda, sigma,
-                                                 sh.H, sh.N, K, cap, sel, sel_score);
-  else
-    k3_select_kernel<false><<<grid, kBq, 0, st>>>(qb, kbar, amax, pool, pool_count, lambda,
-                                                  sigma, sh.H, sh.N, K, cap, sel, sel_score);
+  k3_select_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(
+      static_cast<const __nv_bfloat16 *>(q), kbar, amax, pool, pool_count, lambda, sigma, sh.H,
+      sh.N, K, cap, fs_mode ? 1 : 0, sel, sel_score, err);
   return cudaGetLastError();
 }
 

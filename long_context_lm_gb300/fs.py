@@ -27,7 +27,7 @@ FS_MODE_FSL, FS_MODE_FS = 0, 1
 SYMBOLS = ["fs_default_params", "fs_status_string", "fs_workspace_bytes",
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
-           "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view"]
+           "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status"]
 FS_N_STAGES = 5
 STAGE_NAMES = ["cell_summary", "prune", "select", "readout", "window"]
 
@@ -88,6 +88,7 @@ def load(build_if_stale: bool = True):
         L.fs_attention_fwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, Z, P]
         L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
         L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 6
+        L.fs_check_status.argtypes = [P, P]
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_workspace_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes"):
@@ -320,3 +321,9 @@ def fs_workspace_view(ws, batch, H, N, d, params=None, dtype=FS_BF16):
         nbytes = n * torch.tensor([], dtype=dtype_).element_size()
         res[name] = ws[off.value: off.value + nbytes].view(dtype_).view(shape)
     return res
+
+
+def fs_check_status(ws, stream=None):
+    """Synchronise the stream and raise FSError if a kernel recorded an error
+    (a bounded device wait that timed out) in the workspace header."""
+    _check(load().fs_check_status(_ptr(ws), _stream(stream)), "fs_check_status")

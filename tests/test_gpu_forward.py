@@ -22,6 +22,7 @@ def run_fwd(inp, params):
     out = fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], params,
                               ws=ws)
     view = fs.fs_workspace_view(ws, B, H, N, dd, params, code)
+    fs.fs_check_status(ws)  # raises if a bounded device wait gave up
     torch.cuda.synchronize()
     return (out.cpu().numpy().reshape(B * H, N, dd),
             view["sel"].cpu().numpy().reshape(B * H, N, -1), view)
