@@ -7,17 +7,21 @@
 //     o_win[n] = softmax_j((R(n) q_n . R(j) k_j) / sqrt(d)) v_j,  j in [n-w+1, n]
 //     out[n]   = o_win[n] + mix_h * o_long[n].
 //
-// One CTA (12 warps, one per SM) owns two adjacent 128-query tiles A and B of
+// One CTA (14 warps, one per SM) owns two adjacent 128-query tiles A and B of
 // one head and walks the 64-key tiles that cover both windows:
 //   warps 0-3   softmax of tile A (thread = query row = TMEM lane)
 //   warps 4-7   softmax of tile B
 //   warp  8     TMEM allocation and the single MMA-issuing thread
-//   warp  9     TMA producer: raw key tile and value tile of each key tile
-//   warps 10-11 rotate the queries once and every raw key tile once
+//   warp  9     TMA producer: key tile and value tile of each key tile
+//   warps 10-13 rotate the queries once and every key tile once, in place
+//               (two threads per 64-element row, disjoint 16-byte chunks)
 // RoPE is applied relative to tile A's first position b: q_n.k_j after
 // rotations by n-b and j-b equals the absolute-position product (R is
 // orthogonal and depends only on differences), so both query tiles share one
 // rotated copy of each key tile, and the angles stay small (|j-b| < w+256).
+// An offset t = 64*u + r is rotated with cos/sin of t*theta_i formed by the
+// angle-sum identity from two small shared tables (r*theta_i for r < 64 and
+// the few tile bases 64*u*theta_i), both taken from an fp64-computed table.
 // The rotated q and k are split into bf16 hi + lo halves; S = Q.K^T takes
 // three tcgen05.mma chains (hi.hi + hi.lo + lo.hi) accumulating in TMEM, which
 // keeps logits at ~2^-16 relative error (a single bf16 rounding of the
@@ -34,29 +38,31 @@ namespace fs {
 namespace {
 
 constexpr int kKT = 64;       // keys per tile
-constexpr int kRing = 3;      // raw-key / value ring depth
-constexpr int kRot = 2;       // rotated-key ring depth
-constexpr int kThreads = 384;
+constexpr int kRing = 3;      // key / value ring depth (keys rotated in place)
+constexpr int kThreads = 448;
 
 // shared-memory layout, offsets from a 1024-byte aligned base
-constexpr uint32_t kOffQ = 0;           // [A hi, A lo, B hi, B lo] x 16 KB
-constexpr uint32_t kOffP = 65536;       // [A, B] x 16 KB
-constexpr uint32_t kOffKT = 98304;      // kRot x [hi 8 KB, lo 8 KB]
-constexpr uint32_t kOffV = kOffKT + kRot * 16384;       // kRing x 8 KB
-constexpr uint32_t kOffKRaw = kOffV + kRing * 8192;     // kRing x 8 KB
-constexpr uint32_t kSmemUsed = kOffKRaw + kRing * 8192; // 176 KB
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;       // + alignment slack
+constexpr uint32_t kOffQ = 0;                           // [A hi, A lo, B hi, B lo] x 16 KB
+constexpr uint32_t kOffP = 65536;                       // [A, B] x 16 KB
+constexpr uint32_t kOffK = 98304;                       // kRing x [hi 8 KB, lo 8 KB]
+constexpr uint32_t kOffV = kOffK + kRing * 16384;       // kRing x 8 KB
+constexpr uint32_t kOffT64 = kOffV + kRing * 8192;      // 64 x 32 (cos, sin): 16 KB
+constexpr uint32_t kOffTB = kOffT64 + 64 * 256;         // bases x 32 (cos, sin)
+// key tiles a CTA walks at most, and the dynamic shared memory it needs
+__host__ __device__ constexpr int max_tiles(int w) { return (w + 318) / kKT + 1; }
+__host__ __device__ constexpr uint32_t smem_bytes(int w) {
+  return kOffTB + (4 + max_tiles(w)) * 256 + 1024;
+}
 
 // TMEM columns: S_A, O_A, S_B, O_B (64 fp32 columns each)
 constexpr uint32_t kTmemCols = 256;
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t raw_full[kRing];
-  uint64_t raw_empty[kRing];
-  uint64_t v_empty[kRing];
-  uint64_t kt_full[kRot];
-  uint64_t kt_empty[kRot];
+  uint64_t raw_full[kRing];   // TMA: key and value tile landed
+  uint64_t kt_full[kRing];    // key tile rotated
+  uint64_t kt_empty[kRing];   // S MMAs of the tile done
+  uint64_t v_empty[kRing];    // P.V MMAs of the tile done
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -75,36 +81,52 @@ struct Params {
   int *err;
 };
 
-// Rotate one 64-element row (bf16, 8 chunks of 8) by the angles of table row
-// `cs` and write bf16 hi / lo halves into two swizzled tiles at row r.
-__device__ __forceinline__ void rotate_row(const uint4 (&x)[8], const float2 *__restrict__ cs,
-                                           unsigned char *hi, unsigned char *lo, int r) {
+// Rotate half of one 64-element row in place: pairs i in [16*half, 16*half+16)
+// (dims 16*half.. and 32+16*half..), angles from the shared tables t64 (row
+// offset r) and tb (tile base), composed by the angle-sum identity.  The raw
+// row is read from `hi` (chunks 2*half, 2*half+1, 4+2*half, 5+2*half) and the
+// rotated bf16 hi / lo halves are written back to the same chunks of `hi`
+// and `lo`.
+__device__ __forceinline__ void rotate_half_row(unsigned char *hi, unsigned char *lo, int r,
+                                                int half, const float2 *t64r,
+                                                const float2 *tbr) {
+  uint4 xa[2], xb[2];
 #pragma unroll
-  for (int ig = 0; ig < 4; ++ig) {
-    const uint32_t wa[4] = {x[ig].x, x[ig].y, x[ig].z, x[ig].w};
-    const uint32_t wb[4] = {x[ig + 4].x, x[ig + 4].y, x[ig + 4].z, x[ig + 4].w};
+  for (int k = 0; k < 2; ++k) {
+    xa[k] = *reinterpret_cast<const uint4 *>(hi + swz128(r, 2 * half + k));
+    xb[k] = *reinterpret_cast<const uint4 *>(hi + swz128(r, 4 + 2 * half + k));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t wa[4] = {xa[k].x, xa[k].y, xa[k].z, xa[k].w};
+    const uint32_t wb[4] = {xb[k].x, xb[k].y, xb[k].z, xb[k].w};
     uint32_t ah[4], al[4], bh[4], bl[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + 8 * ig + 2 * j));
+      const int i0 = 16 * half + 8 * k + 2 * j;  // first pair of this 32-bit word
+      const float4 rr = *reinterpret_cast<const float4 *>(t64r + i0);
+      const float4 bb = *reinterpret_cast<const float4 *>(tbr + i0);
       float y0[2], y1[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float c = e ? t.z : t.x, s = e ? t.w : t.y;
+        const float cr = e ? rr.z : rr.x, sr = e ? rr.w : rr.y;
+        const float cb = e ? bb.z : bb.x, sb = e ? bb.w : bb.y;
+        const float c = fmaf(cb, cr, -sb * sr), sn = fmaf(sb, cr, cb * sr);
         const float x0 = e ? bf16_hi(wa[j]) : bf16_lo(wa[j]);
         const float x1 = e ? bf16_hi(wb[j]) : bf16_lo(wb[j]);
-        y0[e] = x0 * c - x1 * s;
-        y1[e] = x0 * s + x1 * c;
+        y0[e] = fmaf(x0, c, -x1 * sn);
+        y1[e] = fmaf(x0, sn, x1 * c);
       }
       ah[j] = pack_bf16(y0[0], y0[1]);
       al[j] = pack_bf16(y0[0] - bf16_lo(ah[j]), y0[1] - bf16_hi(ah[j]));
       bh[j] = pack_bf16(y1[0], y1[1]);
       bl[j] = pack_bf16(y1[0] - bf16_lo(bh[j]), y1[1] - bf16_hi(bh[j]));
     }
-    *reinterpret_cast<uint4 *>(hi + swz128(r, ig)) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-    *reinterpret_cast<uint4 *>(hi + swz128(r, ig + 4)) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-    *reinterpret_cast<uint4 *>(lo + swz128(r, ig)) = make_uint4(al[0], al[1], al[2], al[3]);
-    *reinterpret_cast<uint4 *>(lo + swz128(r, ig + 4)) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+    const int ca = 2 * half + k, cb = 4 + 2 * half + k;
+    *reinterpret_cast<uint4 *>(hi + swz128(r, ca)) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+    *reinterpret_cast<uint4 *>(hi + swz128(r, cb)) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+    *reinterpret_cast<uint4 *>(lo + swz128(r, ca)) = make_uint4(al[0], al[1], al[2], al[3]);
+    *reinterpret_cast<uint4 *>(lo + swz128(r, cb)) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
   }
 }
 
@@ -148,10 +170,10 @@ __device__ void role_mma(const TileRange &tr, Barriers &bar, uint32_t tmem, uint
   for (int t = 0; t <= tr.ntiles; ++t) {
     const bool tile = t < tr.ntiles;
     if (tile) {
-      if (!tc::mbar_wait(&bar.kt_full[t % kRot], (t / kRot) & 1, err)) return;
+      if (!tc::mbar_wait(&bar.kt_full[t % kRing], (t / kRing) & 1, err)) return;
     }
     tc::fence_after_sync();
-    const uint32_t sKh = base + kOffKT + (t % kRot) * 16384, sKl = sKh + 8192;
+    const uint32_t sKh = base + kOffK + (t % kRing) * 16384, sKl = sKh + 8192;
     bool any_pv = false;
     for (int x = 0; x < 2; ++x) {
       const uint32_t s_col = tmem + x * 128, o_col = s_col + 64;
@@ -184,7 +206,7 @@ __device__ void role_mma(const TileRange &tr, Barriers &bar, uint32_t tmem, uint
       }
     }
     if (any_pv) tc::mma_commit(&bar.v_empty[(t - 1) % kRing]);
-    if (tile) tc::mma_commit(&bar.kt_empty[t % kRot]);
+    if (tile) tc::mma_commit(&bar.kt_empty[t % kRing]);
   }
 }
 
@@ -194,49 +216,84 @@ __device__ void role_tma(const TileRange &tr, Barriers &bar, unsigned char *smem
     const int slot = t % kRing;
     if (t >= kRing) {
       const uint32_t ph = ((t / kRing) - 1) & 1;
-      if (!tc::mbar_wait(&bar.raw_empty[slot], ph, err)) return;
+      if (!tc::mbar_wait(&bar.kt_empty[slot], ph, err)) return;
       if (!tc::mbar_wait(&bar.v_empty[slot], ph, err)) return;
     }
     tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 2 * kKT * kD * 2);
     const int y = row0 + tr.kt0 + t * kKT;
-    tc::tma_load_2d(smem + kOffKRaw + slot * 8192, tk, &bar.raw_full[slot], 0, y);
+    tc::tma_load_2d(smem + kOffK + slot * 16384, tk, &bar.raw_full[slot], 0, y);
     tc::tma_load_2d(smem + kOffV + slot * 8192, tv, &bar.raw_full[slot], 0, y);
   }
 }
 
+// Table rows of the tile bases: [0, 4) query bases 0, 64, 128, 192 relative to
+// tile A; [4, 4 + ntiles) key-tile bases kt0 + 64 t - q0[A].
 __device__ void role_rotate(const TileRange &tr, Barriers &bar, unsigned char *smem,
-                            const Params &p, size_t head, int tr_id, int *err) {
-  // queries: rows tr_id and tr_id + 64 of A and of B (B only if present)
+                            const Params &p, size_t head, int tid_r, int *err) {
+  const float2 *t64 = reinterpret_cast<const float2 *>(smem + kOffT64);
+  const float2 *tb = reinterpret_cast<const float2 *>(smem + kOffTB);
+  const int r = tid_r >> 1, half = tid_r & 1;  // key row 0..63, half row
+  // queries: raw rows -> hi tile, then rotate in place; thread handles rows
+  // r and r + 64 (half of each) of A and of B
   for (int x = 0; x < 2; ++x) {
     if (tr.end[x] <= tr.begin[x]) continue;
+    unsigned char *qh = smem + kOffQ + x * 32768;
     for (int rr = 0; rr < 2; ++rr) {
-      const int r = tr_id + 64 * rr;
-      const int n = tr.q0[x] + r;
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (head + n) * kD);
-      uint4 raw[8];
+      const int row = r + 64 * rr;
+      const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (head + tr.q0[x] + row) * kD);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) raw[c] = __ldg(src + c);
-      unsigned char *qh = smem + kOffQ + x * 32768;
-      rotate_row(raw, p.rel + (size_t)(n - tr.q0[0] + p.rel_off) * (kD / 2), qh, qh + 16384, r);
+      for (int k = 0; k < 2; ++k) {
+        const int ca = 2 * half + k, cb = 4 + 2 * half + k;
+        *reinterpret_cast<uint4 *>(qh + swz128(row, ca)) = __ldg(src + ca);
+        *reinterpret_cast<uint4 *>(qh + swz128(row, cb)) = __ldg(src + cb);
+      }
+      rotate_half_row(qh, qh + 16384, row, half, t64 + r * (kD / 2),
+                      tb + (2 * x + rr) * (kD / 2));
     }
   }
   tc::fence_async_smem();
   tc::mbar_arrive(&bar.q_full);
   for (int t = 0; t < tr.ntiles; ++t) {
-    const int slot = t % kRing, s = t % kRot;
+    const int slot = t % kRing;
     if (!tc::mbar_wait(&bar.raw_full[slot], (t / kRing) & 1, err)) return;
-    if (t >= kRot && !tc::mbar_wait(&bar.kt_empty[s], ((t / kRot) - 1) & 1, err)) return;
-    const unsigned char *kr = smem + kOffKRaw + slot * 8192;
-    uint4 raw[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4 *>(kr + swz128(tr_id, c));
-    const int j = tr.kt0 + t * kKT + tr_id;
-    unsigned char *kh = smem + kOffKT + s * 16384;
-    rotate_row(raw, p.rel + (size_t)(j - tr.q0[0] + p.rel_off) * (kD / 2), kh, kh + 8192, tr_id);
+    unsigned char *kh = smem + kOffK + slot * 16384;
+    rotate_half_row(kh, kh + 8192, r, half, t64 + r * (kD / 2), tb + (4 + t) * (kD / 2));
     tc::fence_async_smem();
-    tc::mbar_arrive(&bar.kt_full[s]);
-    tc::mbar_arrive(&bar.raw_empty[slot]);
+    tc::mbar_arrive(&bar.kt_full[slot]);
   }
+}
+
+// One row of a 64-key score tile: running max m and sum l (log2 domain,
+// scale sl2 folded in), bf16 probabilities packed two per word into pk, and
+// the factor alpha that rescales the row's earlier accumulation.  kMask:
+// only columns [lo, hi] are inside the row's window.
+template <bool kMask>
+__device__ __forceinline__ void softmax_row(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
+                                            int lo, int hi, float sl2, float &m, float &l,
+                                            float &alpha, uint32_t (&pk)[32]) {
+  auto in = [&](int c) { return !kMask || (c >= lo && c <= hi); };
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    if (in(c)) mx = fmaxf(mx, __uint_as_float(s0[c]));
+    if (in(c + 32)) mx = fmaxf(mx, __uint_as_float(s1[c]));
+  }
+  const float mnew = fmaxf(m, mx * sl2);
+  alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
+  float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float e0 = in(c) ? tc::ex2(fmaf(__uint_as_float(s0[c]), sl2, -mnew)) : 0.f;
+    const float e1 = in(c + 1) ? tc::ex2(fmaf(__uint_as_float(s0[c + 1]), sl2, -mnew)) : 0.f;
+    const float f0 = in(c + 32) ? tc::ex2(fmaf(__uint_as_float(s1[c]), sl2, -mnew)) : 0.f;
+    const float f1 = in(c + 33) ? tc::ex2(fmaf(__uint_as_float(s1[c + 1]), sl2, -mnew)) : 0.f;
+    ls0 += e0 + e1;
+    ls1 += f0 + f1;
+    pk[c / 2] = pack_bf16(e0, e1);
+    pk[16 + c / 2] = pack_bf16(f0, f1);
+  }
+  l = l * alpha + (ls0 + ls1);
+  m = mnew;
 }
 
 __device__ void role_softmax(const TileRange &tr, Barriers &bar, unsigned char *smem,
@@ -262,30 +319,11 @@ __device__ void role_softmax(const TileRange &tr, Barriers &bar, unsigned char *
       tc::tmem_ld32(s_addr, s0);
       tc::tmem_ld32(s_addr + 32, s1);
       tc::tmem_wait_ld();
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (c >= lo && c <= hi) mx = fmaxf(mx, __uint_as_float(s0[c]));
-        if (c + 32 >= lo && c + 32 <= hi) mx = fmaxf(mx, __uint_as_float(s1[c]));
-      }
-      const float mnew = fmaxf(m, mx * sl2);
-      const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
-      float ls = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float e0 = (c >= lo && c <= hi) ? tc::ex2(fmaf(__uint_as_float(s0[c]), sl2, -mnew)) : 0.f;
-        float e1 = (c + 1 >= lo && c + 1 <= hi)
-                       ? tc::ex2(fmaf(__uint_as_float(s0[c + 1]), sl2, -mnew)) : 0.f;
-        float f0 = (c + 32 >= lo && c + 32 <= hi)
-                       ? tc::ex2(fmaf(__uint_as_float(s1[c]), sl2, -mnew)) : 0.f;
-        float f1 = (c + 33 >= lo && c + 33 <= hi)
-                       ? tc::ex2(fmaf(__uint_as_float(s1[c + 1]), sl2, -mnew)) : 0.f;
-        ls += (e0 + e1) + (f0 + f1);
-        pk[c / 2] = pack_bf16(e0, e1);
-        pk[16 + c / 2] = pack_bf16(f0, f1);
-      }
-      l = l * alpha + ls;
-      m = mnew;
+      float alpha;
+      if (__all_sync(0xffffffffu, lo == 0 && hi == kKT - 1))
+        softmax_row<false>(s0, s1, lo, hi, sl2, m, l, alpha, pk);
+      else
+        softmax_row<true>(s0, s1, lo, hi, sl2, m, l, alpha, pk);
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         uint32_t o0[32], o1[32];
         tc::tmem_ld32(o_addr, o0);
@@ -354,15 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
   const TileRange tr = tile_range(pair, p.nblk, p.w);
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bar.q_full, 64);
+    tc::mbar_init(&bar.q_full, 128);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&bar.raw_full[i], 1);
-      tc::mbar_init(&bar.raw_empty[i], 64);
-      tc::mbar_init(&bar.v_empty[i], 1);
-    }
-    for (int i = 0; i < kRot; ++i) {
-      tc::mbar_init(&bar.kt_full[i], 64);
+      tc::mbar_init(&bar.kt_full[i], 128);
       tc::mbar_init(&bar.kt_empty[i], 1);
+      tc::mbar_init(&bar.v_empty[i], 1);
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(&bar.s_full[x], 1);
@@ -395,7 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
   } else if (warp == 9) {
     if (lane == 0) role_tma(tr, bar, smem, &tmap_k, &tmap_v, (int)head, p.err);
   } else {
-    role_rotate(tr, bar, smem, p, head, threadIdx.x - 320, p.err);
+    // rotation warps: stage the angle tables, sync among themselves, rotate
+    const int tid_r = threadIdx.x - 320;
+    float4 *t64 = reinterpret_cast<float4 *>(smem + kOffT64);
+    for (int i = tid_r; i < 64 * 16; i += 128)
+      t64[i] = __ldg(reinterpret_cast<const float4 *>(p.rel + (size_t)p.rel_off * (kD / 2)) + i);
+    float4 *tb = reinterpret_cast<float4 *>(smem + kOffTB);
+    for (int i = tid_r; i < (4 + tr.ntiles) * 16; i += 128) {
+      const int row = i >> 4, part = i & 15;
+      const int off = row < 4 ? 64 * row : tr.kt0 + (row - 4) * kKT - tr.q0[0];
+      tb[i] = __ldg(reinterpret_cast<const float4 *>(p.rel + (size_t)(off + p.rel_off) * (kD / 2)) + part);
+    }
+    asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    role_rotate(tr, bar, smem, p, head, tid_r, p.err);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -476,11 +523,12 @@ cudaError_t launch_window_tc(const void *q, const void *k, const void *v, const 
   p.nblk = sh.nblk();
   p.out = out;
   p.err = err;
+  const uint32_t smem = smem_bytes(w);
   cudaError_t e = cudaFuncSetAttribute(k5_window_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((sh.nblk() + 1) / 2, sh.BH());
-  k5_window_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, p);
+  k5_window_tc_kernel<<<grid, kThreads, smem, st>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
