@@ -28,8 +28,12 @@ namespace {
 
 constexpr int kChunk = 128;       // candidates per MMA (N <= 128)
 constexpr int kThreads = 192;     // warps 0-3 score, warp 4 MMA, all stage operands
-constexpr uint32_t kOffQ = 0, kOffK = 16384;  // K split tiles: 3 x 16 KB
-constexpr uint32_t kSmemBytes = 16384 + 3 * 16384 + 1024;
+constexpr uint32_t kOffQ = 0, kOffK = 16384;  // then 3 split tiles of `rows` x 128 B
+
+// candidate rows a chunk holds: the pool capacity (FS-L) or a full chunk (FS)
+__host__ __device__ constexpr int chunk_rows(int fs_mode, int cap) {
+  return fs_mode ? kChunk : ((cap < kChunk ? cap : kChunk) + 15) / 16 * 16;
+}
 
 __device__ __forceinline__ bool ranks_before(float u, int c, float u2, int c2) {
   return u > u2 || (u == u2 && c < c2);
@@ -55,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
   const int b0 = beta * kBq;
   const size_t head = (size_t)bh * N;
   const int A = beta * (kBq / kS);
-  const int count = fs_mode ? A : min(max(pool_count[(size_t)bh * nblk + beta], 0), cap);
+  const int count = fs_mode ? A : min(max(pool_count[(size_t)bh * nblk + beta], 0), min(cap, kChunk));
   const int32_t *pl = fs_mode ? nullptr : pool + ((size_t)bh * nblk + beta) * cap;
 
   if (tid == 0) {
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
     }
     __syncthreads();
     // mean keys -> three bf16 split tiles (rows beyond nc or skipped: zero)
+    const uint32_t tile = (uint32_t)chunk_rows(fs_mode, cap) * 128;
     for (int p = tid; p < np * 8; p += kThreads) {
       const int j = p >> 3, ch = p & 7;
       const int c = s_c[j];
@@ -128,8 +133,8 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
       }
       const uint32_t off = swz128(j, ch);
       *reinterpret_cast<uint4 *>(smem + kOffK + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4 *>(smem + kOffK + 16384 + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-      *reinterpret_cast<uint4 *>(smem + kOffK + 32768 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4 *>(smem + kOffK + tile + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+      *reinterpret_cast<uint4 *>(smem + kOffK + 2 * tile + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     tc::fence_async_smem();
     __syncthreads();
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
       const uint32_t sq = sbase + kOffQ;
 #pragma unroll
       for (int part = 0; part < 3; ++part) {
-        const uint32_t sk = sbase + kOffK + part * 16384;
+        const uint32_t sk = sbase + kOffK + part * tile;
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k)
           tc::mma_ss(tmem, tc::desc_sw128(sq + 32 * k), tc::desc_sw128(sk + 32 * k), id,
@@ -214,11 +219,12 @@ cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const int32_t *pool, const int32_t *pool_count, const float *lambda,
                           const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
                           int32_t *sel, float *sel_score, int *err, cudaStream_t st) {
+  const int smem = 16384 + 3 * chunk_rows(fs_mode ? 1 : 0, cap) * 128 + 1024;
   cudaError_t e = cudaFuncSetAttribute(k3_select_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(sh.nblk(), sh.BH());
-  k3_select_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(
+  k3_select_tc_kernel<<<grid, kThreads, smem, st>>>(
       static_cast<const __nv_bfloat16 *>(q), kbar, amax, pool, pool_count, lambda, sigma, sh.H,
       sh.N, K, cap, fs_mode ? 1 : 0, sel, sel_score, err);
   return cudaGetLastError();

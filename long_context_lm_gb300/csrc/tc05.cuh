@@ -25,10 +25,10 @@ namespace tc {
 // ---------------------------------------------------------------------------
 // error reporting of bounded waits
 // ---------------------------------------------------------------------------
-// A wait that has not completed after this many polls (each poll backs off
-// with nanosleep, so the bound is seconds of wall time) gives up, records
-// FS_ERR_TIMEOUT in the caller's error word and lets the kernel wind down.
-constexpr uint32_t kWaitPolls = 1u << 24;
+// A wait that has not completed after kWaitCycles SM clock cycles (about two
+// seconds at GB300 clocks) gives up, records FS_ERR_TIMEOUT in the caller's
+// error word and lets the kernel wind down instead of hanging the GPU.
+constexpr long long kWaitCycles = 4000000000ll;
 
 __device__ __forceinline__ void report_error(int *err, int code) {
   if (err) atomicCAS(err, 0, code);
@@ -58,12 +58,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete.  Returns false (and
+// Wait for the phase with the given parity to complete.  try_wait itself
+// suspends the thread for a short hardware-defined time, so the loop is a
+// light spin; the clock is read only every 256 polls.  Returns false (and
 // records FS_ERR_TIMEOUT) when the bound is exceeded.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
+    if ((i & 255u) == 0 && clock64() - t0 > kWaitCycles) break;
   }
   report_error(err, FS_ERR_TIMEOUT);
   return false;
