@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t s_tmem;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int beta = blockIdx.x, bh = blockIdx.y, h = bh % H;
   const int C = N / kS, nblk = N / kBq;
   const int b0 = beta * kBq;

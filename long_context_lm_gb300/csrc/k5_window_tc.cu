@@ -7,27 +7,30 @@
 //     o_win[n] = softmax_j((R(n) q_n . R(j) k_j) / sqrt(d)) v_j,  j in [n-w+1, n]
 //     out[n]   = o_win[n] + mix_h * o_long[n].
 //
-// One CTA (14 warps, one per SM) owns two adjacent 128-query tiles A and B of
-// one head and walks the 64-key tiles that cover both windows:
+// One CTA (15 warps, one per SM) owns two adjacent 128-query tiles A and B of
+// one head and walks the 128-key tiles that cover both windows:
 //   warps 0-3   softmax of tile A (thread = query row = TMEM lane)
 //   warps 4-7   softmax of tile B
-//   warp  8     TMEM allocation and the single MMA-issuing thread
-//   warp  9     TMA producer: key tile and value tile of each key tile
-//   warps 10-13 rotate the queries once and every key tile once, in place
-//               (two threads per 64-element row, disjoint 16-byte chunks)
+//   warp  8     TMEM allocation; lane 0 issues every MMA of tile A
+//   warp  9     lane 0 issues every MMA of tile B (one issuing thread caps at
+//               roughly one tcgen05.mma per ~100 cycles, so the two query
+//               tiles get their own issuer)
+//   warp  10    TMA producer: key tile and value tile of each key tile
+//   warps 11-14 rotate the queries once and every key tile once, in place
 // RoPE is applied relative to tile A's first position b: q_n.k_j after
 // rotations by n-b and j-b equals the absolute-position product (R is
 // orthogonal and depends only on differences), so both query tiles share one
-// rotated copy of each key tile, and the angles stay small (|j-b| < w+256).
+// rotated copy of each key tile and the angles stay small (|j-b| < w+256).
 // An offset t = 64*u + r is rotated with cos/sin of t*theta_i formed by the
 // angle-sum identity from two small shared tables (r*theta_i for r < 64 and
 // the few tile bases 64*u*theta_i), both taken from an fp64-computed table.
 // The rotated q and k are split into bf16 hi + lo halves; S = Q.K^T takes
 // three tcgen05.mma chains (hi.hi + hi.lo + lo.hi) accumulating in TMEM, which
 // keeps logits at ~2^-16 relative error (a single bf16 rounding of the
-// rotated vectors exceeds the output tolerance on lognormal keys).  P is
-// written as bf16 into a swizzled shared tile and P.V accumulates into a TMEM
-// O that the softmax threads rescale when their running max grows.
+// rotated vectors exceeds the output tolerance on lognormal keys).  The
+// softmax threads write P as bf16 back into TMEM; P.V reads A = P from TMEM
+// and accumulates into a TMEM O that the softmax threads rescale when their
+// running max grows.
 #include <cuda.h>
 
 #include "fs_common.cuh"
@@ -37,36 +40,46 @@
 namespace fs {
 namespace {
 
-constexpr int kKT = 64;       // keys per tile
-constexpr int kRing = 3;      // key / value ring depth (keys rotated in place)
-constexpr int kThreads = 448;
+// Pipeline timeline probe (builds with -DFS_TRACE only): clock64() stamps of
+// each role's hand-offs for one sampled CTA, event e of tile t at [e*64 + t].
+#ifdef FS_TRACE
+__device__ long long *g_trace = nullptr;
+#define FS_TR(e, t)                                                              \
+  do {                                                                           \
+    if (g_trace && blockIdx.x == gridDim.x / 2 && blockIdx.y == 0 && (t) < 64)   \
+      g_trace[(e) * 64 + (t)] = clock64();                                       \
+  } while (0)
+#else
+#define FS_TR(e, t) \
+  do {              \
+  } while (0)
+#endif
+
+constexpr int kKT = 128;         // keys per tile
+constexpr int kRing = 2;         // key / value ring depth (keys rotated in place)
+constexpr int kThreads = 480;
+constexpr int kT64Stride = 272;  // bytes per row of the r*theta table (padded: no bank conflicts)
 
 // shared-memory layout, offsets from a 1024-byte aligned base
 constexpr uint32_t kOffQ = 0;                           // [A hi, A lo, B hi, B lo] x 16 KB
-constexpr uint32_t kOffP = 65536;                       // [A, B] x 16 KB
-constexpr uint32_t kOffK = 98304;                       // kRing x [hi 8 KB, lo 8 KB]
-constexpr uint32_t kOffV = kOffK + kRing * 16384;       // kRing x 8 KB
-constexpr uint32_t kOffT64 = kOffV + kRing * 8192;      // 64 x 32 (cos, sin): 16 KB
-constexpr uint32_t kOffTB = kOffT64 + 64 * 256;         // bases x 32 (cos, sin)
-// key tiles a CTA walks at most, and the dynamic shared memory it needs
-__host__ __device__ constexpr int max_tiles(int w) { return (w + 318) / kKT + 1; }
-__host__ __device__ constexpr uint32_t smem_bytes(int w) {
-  return kOffTB + (4 + max_tiles(w)) * 256 + 1024;
-}
+constexpr uint32_t kOffK = 65536;                       // kRing x [hi 16 KB, lo 16 KB]
+constexpr uint32_t kOffV = kOffK + kRing * 32768;       // kRing x 16 KB
+constexpr uint32_t kOffT64 = kOffV + kRing * 16384;     // 64 rows x 272 B
+constexpr uint32_t kOffTB = kOffT64 + 64 * kT64Stride;  // bases x 256 B
 
-// TMEM columns: S_A, O_A, S_B, O_B (64 fp32 columns each)
-constexpr uint32_t kTmemCols = 256;
+// TMEM columns of query tile x: S at 256x, P at 256x+128, O at 256x+192
+constexpr uint32_t kTmemCols = 512;
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t raw_full[kRing];   // TMA: key and value tile landed
-  uint64_t kt_full[kRing];    // key tile rotated
-  uint64_t kt_empty[kRing];   // S MMAs of the tile done
-  uint64_t v_empty[kRing];    // P.V MMAs of the tile done
+  uint64_t raw_full[kRing];  // TMA: key and value tile landed
+  uint64_t kt_full[kRing];   // key tile rotated
+  uint64_t k_empty[kRing];   // S MMAs of the tile done (both issuers commit)
+  uint64_t v_empty[kRing];   // P.V MMAs of the tile done (both issuers commit)
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t fin;
+  uint64_t fin[2];
   uint32_t tmem;
 };
 
@@ -82,8 +95,8 @@ struct Params {
 };
 
 // Rotate half of one 64-element row in place: pairs i in [16*half, 16*half+16)
-// (dims 16*half.. and 32+16*half..), angles from the shared tables t64 (row
-// offset r) and tb (tile base), composed by the angle-sum identity.  The raw
+// (dims 16*half.. and 32+16*half..), angles from the shared tables t64r (row
+// offset) and tbr (tile base), composed by the angle-sum identity.  The raw
 // row is read from `hi` (chunks 2*half, 2*half+1, 4+2*half, 5+2*half) and the
 // rotated bf16 hi / lo halves are written back to the same chunks of `hi`
 // and `lo`.
@@ -131,11 +144,11 @@ __device__ __forceinline__ void rotate_half_row(unsigned char *hi, unsigned char
 }
 
 struct TileRange {
-  int kt0;      // first key of tile 0
-  int ntiles;   // tiles walked by the CTA
-  int begin[2]; // first tile of query tile A / B
-  int end[2];   // one past the last tile of A / B (end <= begin: tile absent)
-  int q0[2];    // first query of A / B
+  int kt0;       // first key of tile 0
+  int ntiles;    // tiles walked by the CTA
+  int begin[2];  // first tile of query tile A / B
+  int end[2];    // one past the last tile of A / B (end <= begin: tile absent)
+  int q0[2];     // first query of A / B
 };
 
 __device__ __forceinline__ TileRange tile_range(int pair, int nblk, int w) {
@@ -161,52 +174,51 @@ __device__ __forceinline__ bool uses(const TileRange &tr, int x, int t) {
 // roles
 // --------------------------------------------------------------------------
 
-__device__ void role_mma(const TileRange &tr, Barriers &bar, uint32_t tmem, uint32_t base,
-                         int *err) {
+// Issuer of query tile x.  Walks every key tile so that the per-slot
+// "empty" barriers (two arrivals: one per issuer) pair up tile by tile.
+__device__ void role_issue(const TileRange &tr, Barriers &bar, int x, uint32_t tmem,
+                           uint32_t base, int *err) {
   const uint32_t id_qk = tc::idesc_bf16(128, kKT, 0);
   const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);
-  const uint32_t sQ = base + kOffQ, sP = base + kOffP;
+  const uint32_t s_col = tmem + 256 * x, p_col = s_col + 128, o_col = s_col + 192;
+  const uint32_t qh = base + kOffQ + x * 32768, ql = qh + 16384;
+  const uint64_t dqh = tc::desc_sw128(qh), dql = tc::desc_sw128(ql);
   if (!tc::mbar_wait(&bar.q_full, 0, err)) return;
+  FS_TR(1 + x, 0);
   for (int t = 0; t <= tr.ntiles; ++t) {
-    const bool tile = t < tr.ntiles;
-    if (tile) {
-      if (!tc::mbar_wait(&bar.kt_full[t % kRing], (t / kRing) & 1, err)) return;
-    }
+    if (t < tr.ntiles && !tc::mbar_wait(&bar.kt_full[t % kRing], (t / kRing) & 1, err)) return;
     tc::fence_after_sync();
-    const uint32_t sKh = base + kOffK + (t % kRing) * 16384, sKl = sKh + 8192;
-    bool any_pv = false;
-    for (int x = 0; x < 2; ++x) {
-      const uint32_t s_col = tmem + x * 128, o_col = s_col + 64;
-      // P.V of this query tile's previous key tile
-      if (t > 0 && uses(tr, x, t - 1)) {
+    if (t > 0) {
+      if (uses(tr, x, t - 1)) {  // P.V of the previous key tile
         const int i = t - 1 - tr.begin[x];
         if (!tc::mbar_wait(&bar.p_full[x], i & 1, err)) return;
         tc::fence_after_sync();
-        const uint32_t sV = base + kOffV + ((t - 1) % kRing) * 8192;
-        const uint32_t pa = sP + x * 16384;
+        const uint64_t dv = tc::desc_sw128(base + kOffV + ((t - 1) % kRing) * 16384);
 #pragma unroll
         for (int k = 0; k < kKT / 16; ++k)
-          tc::mma_ss(o_col, tc::desc_sw128(pa + 32 * k), tc::desc_sw128(sV + 2048 * k), id_pv,
+          tc::mma_ts(o_col, p_col + 8 * k, dv + (uint64_t)(k * 128), id_pv,
                      (i > 0 || k > 0) ? 1u : 0u);
-        any_pv = true;
+        FS_TR(10 + x, t - 1);
         if (t == tr.end[x]) tc::mma_commit(&bar.o_done[x]);
       }
-      // S = Q.K^T of this key tile (three split-precision chains)
-      if (tile && uses(tr, x, t)) {
-        const uint32_t qh = sQ + x * 32768, ql = qh + 16384;
-#pragma unroll
-        for (int part = 0; part < 3; ++part) {
-          const uint32_t a = part == 2 ? ql : qh, b = part == 1 ? sKl : sKh;
-#pragma unroll
-          for (int k = 0; k < kD / 16; ++k)
-            tc::mma_ss(s_col, tc::desc_sw128(a + 32 * k), tc::desc_sw128(b + 32 * k), id_qk,
-                       (part > 0 || k > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(&bar.s_full[x]);
-      }
+      tc::mma_commit(&bar.v_empty[(t - 1) % kRing]);
     }
-    if (any_pv) tc::mma_commit(&bar.v_empty[(t - 1) % kRing]);
-    if (tile) tc::mma_commit(&bar.kt_empty[t % kRing]);
+    if (t == tr.ntiles) break;
+    if (uses(tr, x, t)) {  // S = Q.K^T, three split-precision chains
+      const uint32_t kh = base + kOffK + (t % kRing) * 32768;
+      const uint64_t dkh = tc::desc_sw128(kh), dkl = tc::desc_sw128(kh + 16384);
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint64_t a = part == 2 ? dql : dqh, b = part == 1 ? dkl : dkh;
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k)
+          tc::mma_ss(s_col, a + (uint64_t)(2 * k), b + (uint64_t)(2 * k), id_qk,
+                     (part > 0 || k > 0) ? 1u : 0u);
+      }
+      tc::mma_commit(&bar.s_full[x]);
+      FS_TR(4 + x, t);
+    }
+    tc::mma_commit(&bar.k_empty[t % kRing]);
   }
 }
 
@@ -216,114 +228,118 @@ __device__ void role_tma(const TileRange &tr, Barriers &bar, unsigned char *smem
     const int slot = t % kRing;
     if (t >= kRing) {
       const uint32_t ph = ((t / kRing) - 1) & 1;
-      if (!tc::mbar_wait(&bar.kt_empty[slot], ph, err)) return;
+      if (!tc::mbar_wait(&bar.k_empty[slot], ph, err)) return;
       if (!tc::mbar_wait(&bar.v_empty[slot], ph, err)) return;
     }
     tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 2 * kKT * kD * 2);
     const int y = row0 + tr.kt0 + t * kKT;
-    tc::tma_load_2d(smem + kOffK + slot * 16384, tk, &bar.raw_full[slot], 0, y);
-    tc::tma_load_2d(smem + kOffV + slot * 8192, tv, &bar.raw_full[slot], 0, y);
+    tc::tma_load_2d(smem + kOffK + slot * 32768, tk, &bar.raw_full[slot], 0, y);
+    tc::tma_load_2d(smem + kOffV + slot * 16384, tv, &bar.raw_full[slot], 0, y);
+    FS_TR(3, t);
   }
 }
 
-// Table rows of the tile bases: [0, 4) query bases 0, 64, 128, 192 relative to
-// tile A; [4, 4 + ntiles) key-tile bases kt0 + 64 t - q0[A].
+// Base rows of the angle tables: [0, 4) query bases 0, 64, 128, 192 relative
+// to tile A; 4 + 2t + u: key-tile base kt0 + 128 t + 64 u - q0[A].
 __device__ void role_rotate(const TileRange &tr, Barriers &bar, unsigned char *smem,
-                            const Params &p, size_t head, int tid_r, int *err) {
-  const float2 *t64 = reinterpret_cast<const float2 *>(smem + kOffT64);
+                            const Params &p, size_t head, int r, int *err) {
+  const unsigned char *t64 = smem + kOffT64;
   const float2 *tb = reinterpret_cast<const float2 *>(smem + kOffTB);
-  const int r = tid_r >> 1, half = tid_r & 1;  // key row 0..63, half row
-  // queries: raw rows -> hi tile, then rotate in place; thread handles rows
-  // r and r + 64 (half of each) of A and of B
+  const float2 *t64r = reinterpret_cast<const float2 *>(t64 + (r & 63) * kT64Stride);
   for (int x = 0; x < 2; ++x) {
     if (tr.end[x] <= tr.begin[x]) continue;
     unsigned char *qh = smem + kOffQ + x * 32768;
-    for (int rr = 0; rr < 2; ++rr) {
-      const int row = r + 64 * rr;
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (head + tr.q0[x] + row) * kD);
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (head + tr.q0[x] + r) * kD);
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int ca = 2 * half + k, cb = 4 + 2 * half + k;
-        *reinterpret_cast<uint4 *>(qh + swz128(row, ca)) = __ldg(src + ca);
-        *reinterpret_cast<uint4 *>(qh + swz128(row, cb)) = __ldg(src + cb);
-      }
-      rotate_half_row(qh, qh + 16384, row, half, t64 + r * (kD / 2),
-                      tb + (2 * x + rr) * (kD / 2));
-    }
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = __ldg(src + c);
+    const float2 *tbr = tb + (2 * x + (r >> 6)) * (kD / 2);
+    rotate_half_row(qh, qh + 16384, r, 0, t64r, tbr);
+    rotate_half_row(qh, qh + 16384, r, 1, t64r, tbr);
   }
   tc::fence_async_smem();
   tc::mbar_arrive(&bar.q_full);
   for (int t = 0; t < tr.ntiles; ++t) {
     const int slot = t % kRing;
     if (!tc::mbar_wait(&bar.raw_full[slot], (t / kRing) & 1, err)) return;
-    unsigned char *kh = smem + kOffK + slot * 16384;
-    rotate_half_row(kh, kh + 8192, r, half, t64 + r * (kD / 2), tb + (4 + t) * (kD / 2));
+    unsigned char *kh = smem + kOffK + slot * 32768;
+    const float2 *tbr = tb + (4 + 2 * t + (r >> 6)) * (kD / 2);
+    rotate_half_row(kh, kh + 16384, r, 0, t64r, tbr);
+    rotate_half_row(kh, kh + 16384, r, 1, t64r, tbr);
     tc::fence_async_smem();
     tc::mbar_arrive(&bar.kt_full[slot]);
+    if (r == 0) FS_TR(6, t);
   }
 }
 
-// One row of a 64-key score tile: running max m and sum l (log2 domain,
-// scale sl2 folded in), bf16 probabilities packed two per word into pk, and
-// the factor alpha that rescales the row's earlier accumulation.  kMask:
-// only columns [lo, hi] are inside the row's window.
+// Pass 1: row maximum of the (masked) score tile, 4 chunks of 32 columns.
 template <bool kMask>
-__device__ __forceinline__ void softmax_row(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
-                                            int lo, int hi, float sl2, float &m, float &l,
-                                            float &alpha, uint32_t (&pk)[32]) {
-  auto in = [&](int c) { return !kMask || (c >= lo && c <= hi); };
+__device__ __forceinline__ float row_max(uint32_t s_addr, int lo, int hi) {
   float mx = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    if (in(c)) mx = fmaxf(mx, __uint_as_float(s0[c]));
-    if (in(c + 32)) mx = fmaxf(mx, __uint_as_float(s1[c]));
-  }
-  const float mnew = fmaxf(m, mx * sl2);
-  alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
-  float ls0 = 0.f, ls1 = 0.f;
+  for (int ch = 0; ch < kKT / 32; ++ch) {
+    uint32_t s[32];
+    tc::tmem_ld32(s_addr + 32 * ch, s);
+    tc::tmem_wait_ld();
 #pragma unroll
-  for (int c = 0; c < 32; c += 2) {
-    const float e0 = in(c) ? tc::ex2(fmaf(__uint_as_float(s0[c]), sl2, -mnew)) : 0.f;
-    const float e1 = in(c + 1) ? tc::ex2(fmaf(__uint_as_float(s0[c + 1]), sl2, -mnew)) : 0.f;
-    const float f0 = in(c + 32) ? tc::ex2(fmaf(__uint_as_float(s1[c]), sl2, -mnew)) : 0.f;
-    const float f1 = in(c + 33) ? tc::ex2(fmaf(__uint_as_float(s1[c + 1]), sl2, -mnew)) : 0.f;
-    ls0 += e0 + e1;
-    ls1 += f0 + f1;
-    pk[c / 2] = pack_bf16(e0, e1);
-    pk[16 + c / 2] = pack_bf16(f0, f1);
+    for (int c = 0; c < 32; ++c)
+      if (!kMask || (32 * ch + c >= lo && 32 * ch + c <= hi)) mx = fmaxf(mx, __uint_as_float(s[c]));
   }
-  l = l * alpha + (ls0 + ls1);
-  m = mnew;
+  return mx;
 }
 
-__device__ void role_softmax(const TileRange &tr, Barriers &bar, unsigned char *smem,
-                             uint32_t tmem, const Params &p, size_t head, int h, int x, int r,
-                             int *err) {
+// Pass 2: probabilities 2^(s*sl2 - m) written as bf16 into the P columns;
+// returns the row sum of the unrounded values.
+template <bool kMask>
+__device__ __forceinline__ float row_exp(uint32_t s_addr, uint32_t p_addr, int lo, int hi,
+                                         float sl2, float m) {
+  float ls = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < kKT / 32; ++ch) {
+    uint32_t s[32], pk[16];
+    tc::tmem_ld32(s_addr + 32 * ch, s);
+    tc::tmem_wait_ld();
+    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const int col = 32 * ch + c;
+      const float e0 = (!kMask || (col >= lo && col <= hi))
+                           ? tc::ex2(fmaf(__uint_as_float(s[c]), sl2, -m)) : 0.f;
+      const float e1 = (!kMask || (col + 1 >= lo && col + 1 <= hi))
+                           ? tc::ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -m)) : 0.f;
+      l0 += e0;
+      l1 += e1;
+      pk[c / 2] = pack_bf16(e0, e1);
+    }
+    ls += l0 + l1;
+    tc::tmem_st16(p_addr + 16 * ch, pk);
+  }
+  return ls;
+}
+
+__device__ void role_softmax(const TileRange &tr, Barriers &bar, uint32_t tmem, const Params &p,
+                             size_t head, int h, int x, int r, int *err) {
   const int warp = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t s_addr = tmem + x * 128 + lane_base, o_addr = s_addr + 64;
+  const uint32_t s_addr = tmem + 256 * x + lane_base, p_addr = s_addr + 128, o_addr = s_addr + 192;
   const int n = tr.q0[x] + r;
   const float sl2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
-  unsigned char *prow = smem + kOffP + x * 16384;
   float m = -INFINITY, l = 0.f;
   for (int t = tr.begin[x]; t < tr.end[x]; ++t) {
     const int i = t - tr.begin[x];
     if (!tc::mbar_wait(&bar.s_full[x], i & 1, err)) return;
     tc::fence_after_sync();
+    if (r == 0) FS_TR(7 + x, t);
     const int kt = tr.kt0 + t * kKT;
     const int lo = max(0, n - p.w + 1 - kt), hi = min(kKT - 1, n - kt);
-    const bool any = lo <= hi;
-    uint32_t pk[32];
-    if (__any_sync(0xffffffffu, any)) {
-      uint32_t s0[32], s1[32];
-      tc::tmem_ld32(s_addr, s0);
-      tc::tmem_ld32(s_addr + 32, s1);
-      tc::tmem_wait_ld();
-      float alpha;
-      if (__all_sync(0xffffffffu, lo == 0 && hi == kKT - 1))
-        softmax_row<false>(s0, s1, lo, hi, sl2, m, l, alpha, pk);
-      else
-        softmax_row<true>(s0, s1, lo, hi, sl2, m, l, alpha, pk);
+    if (__any_sync(0xffffffffu, lo <= hi)) {
+      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kKT - 1);
+      const float mx = full ? row_max<false>(s_addr, lo, hi) : row_max<true>(s_addr, lo, hi);
+      const float mnew = fmaxf(m, mx * sl2);
+      const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
+      const float ls = full ? row_exp<false>(s_addr, p_addr, lo, hi, sl2, mnew)
+                            : row_exp<true>(s_addr, p_addr, lo, hi, sl2, mnew);
+      l = l * alpha + ls;
+      m = mnew;
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         uint32_t o0[32], o1[32];
         tc::tmem_ld32(o_addr, o0);
@@ -336,23 +352,23 @@ __device__ void role_softmax(const TileRange &tr, Barriers &bar, unsigned char *
         }
         tc::tmem_st32(o_addr, o0);
         tc::tmem_st32(o_addr + 32, o1);
-        tc::tmem_wait_st();
       }
     } else {
+      uint32_t z[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = 0u;
+      for (int c = 0; c < 16; ++c) z[c] = 0u;
+#pragma unroll
+      for (int ch = 0; ch < kKT / 32; ++ch) tc::tmem_st16(p_addr + 16 * ch, z);
     }
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      *reinterpret_cast<uint4 *>(prow + swz128(r, ch)) =
-          make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-    tc::fence_async_smem();
+    tc::tmem_wait_st();
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&bar.p_full[x]);
+    if (r == 0) FS_TR(12 + x, t);
   }
   // epilogue: O / l (+ mix_h * o_long)
   if (!tc::mbar_wait(&bar.o_done[x], 0, err)) return;
+  if (r == 0) FS_TR(14 + x, 0);
   tc::fence_after_sync();
   uint32_t o0[32], o1[32];
   tc::tmem_ld32(o_addr, o0);
@@ -361,7 +377,8 @@ __device__ void role_softmax(const TileRange &tr, Barriers &bar, unsigned char *
   const float inv = 1.f / l;
   const float mh = p.mix ? p.mix[h] : 0.f;
   float4 *dst = reinterpret_cast<float4 *>(p.out + (head + n) * kD);
-  const float4 *ol = p.o_long ? reinterpret_cast<const float4 *>(p.o_long + (head + n) * kD) : nullptr;
+  const float4 *ol =
+      p.o_long ? reinterpret_cast<const float4 *>(p.o_long + (head + n) * kD) : nullptr;
 #pragma unroll
   for (int c4 = 0; c4 < 16; ++c4) {
     const uint32_t *src = c4 < 8 ? o0 : o1;
@@ -383,28 +400,29 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *smem =
-      reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Barriers bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
   const size_t head = (size_t)bh * p.N;
   const TileRange tr = tile_range(pair, p.nblk, p.w);
+  if (threadIdx.x == 0) FS_TR(0, 0);
 
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar.q_full, 128);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&bar.raw_full[i], 1);
       tc::mbar_init(&bar.kt_full[i], 128);
-      tc::mbar_init(&bar.kt_empty[i], 1);
-      tc::mbar_init(&bar.v_empty[i], 1);
+      tc::mbar_init(&bar.k_empty[i], 2);
+      tc::mbar_init(&bar.v_empty[i], 2);
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(&bar.s_full[x], 1);
       tc::mbar_init(&bar.p_full[x], 4);
       tc::mbar_init(&bar.o_done[x], 1);
+      tc::mbar_init(&bar.fin[x], 1);
     }
-    tc::mbar_init(&bar.fin, 1);
     tc::mbar_fence_init();
   }
   if (warp == 8) {
@@ -419,30 +437,33 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
 
   if (warp < 8) {
     const int x = warp >> 2;
-    if (tr.end[x] > tr.begin[x])
-      role_softmax(tr, bar, smem, tmem, p, head, h, x, threadIdx.x & 127, p.err);
-  } else if (warp == 8) {
+    if (tr.end[x] > tr.begin[x]) role_softmax(tr, bar, tmem, p, head, h, x, threadIdx.x & 127, p.err);
+  } else if (warp == 8 || warp == 9) {
     if (lane == 0) {
-      role_mma(tr, bar, tmem, sbase, p.err);
-      tc::mma_commit(&bar.fin);  // every issued MMA has completed once this arrives
-      tc::mbar_wait(&bar.fin, 0, p.err);
+      const int x = warp - 8;
+      role_issue(tr, bar, x, tmem, sbase, p.err);
+      tc::mma_commit(&bar.fin[x]);  // every MMA this thread issued has completed
+      tc::mbar_wait(&bar.fin[x], 0, p.err);
     }
-  } else if (warp == 9) {
+  } else if (warp == 10) {
     if (lane == 0) role_tma(tr, bar, smem, &tmap_k, &tmap_v, (int)head, p.err);
   } else {
     // rotation warps: stage the angle tables, sync among themselves, rotate
-    const int tid_r = threadIdx.x - 320;
-    float4 *t64 = reinterpret_cast<float4 *>(smem + kOffT64);
-    for (int i = tid_r; i < 64 * 16; i += 128)
-      t64[i] = __ldg(reinterpret_cast<const float4 *>(p.rel + (size_t)p.rel_off * (kD / 2)) + i);
-    float4 *tb = reinterpret_cast<float4 *>(smem + kOffTB);
-    for (int i = tid_r; i < (4 + tr.ntiles) * 16; i += 128) {
+    const int r = threadIdx.x - 352;
+    const float4 *rel = reinterpret_cast<const float4 *>(p.rel);
+    for (int i = r; i < 64 * 16; i += 128) {
       const int row = i >> 4, part = i & 15;
-      const int off = row < 4 ? 64 * row : tr.kt0 + (row - 4) * kKT - tr.q0[0];
-      tb[i] = __ldg(reinterpret_cast<const float4 *>(p.rel + (size_t)(off + p.rel_off) * (kD / 2)) + part);
+      *reinterpret_cast<float4 *>(smem + kOffT64 + row * kT64Stride + part * 16) =
+          __ldg(rel + (size_t)(row + p.rel_off) * 16 + part);
+    }
+    float4 *tb = reinterpret_cast<float4 *>(smem + kOffTB);
+    for (int i = r; i < (4 + 2 * tr.ntiles) * 16; i += 128) {
+      const int row = i >> 4, part = i & 15;
+      const int off = row < 4 ? 64 * row : tr.kt0 + (row - 4) * 64 - tr.q0[0];
+      tb[i] = __ldg(rel + (size_t)(off + p.rel_off) * 16 + part);
     }
     asm volatile("bar.sync 1, 128;\n" ::: "memory");
-    role_rotate(tr, bar, smem, p, head, tid_r, p.err);
+    role_rotate(tr, bar, smem, p, head, r, p.err);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -450,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0) FS_TR(16, 0);
 }
 
 __global__ void rel_rope_table_kernel(float2 *__restrict__ tab, int rows, int off, double base) {
@@ -480,23 +502,27 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// [rows, 64] bf16 row-major, boxes of 64 x 64 with the 128-byte swizzle.
-bool make_rows_map(CUtensorMap *map, const void *ptr, size_t rows) {
+// [rows, 64] bf16 row-major, boxes of box_rows x 64 with the 128-byte swizzle.
+bool make_rows_map(CUtensorMap *map, const void *ptr, size_t rows, int box_rows) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kKT};
+  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// key tiles a CTA walks at most, and the dynamic shared memory it needs
+constexpr int max_tiles(int w) { return (w + 126 + 256) / kKT + 1; }
+constexpr uint32_t smem_bytes(int w) { return kOffTB + (4 + 2 * max_tiles(w)) * 256 + 1024; }
+
 }  // namespace
 
 // Relative-angle table rows: offsets t in [-rel_off, 2*kBq).
-int window_rel_offset(int w) { return (w + 62 + kKT - 1) / kKT * kKT; }
+int window_rel_offset(int w) { return (w + 126 + 63) / 64 * 64; }
 size_t window_table_bytes(int w) {
   return (size_t)(window_rel_offset(w) + 2 * kBq) * (kD / 2) * sizeof(float2);
 }
@@ -510,7 +536,8 @@ cudaError_t launch_window_tc(const void *q, const void *k, const void *v, const 
   rel_rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(tab, rows, off, (double)base);
   CUtensorMap mk, mv;
   const size_t nrows = (size_t)sh.BH() * sh.N;
-  if (!make_rows_map(&mk, k, nrows) || !make_rows_map(&mv, v, nrows)) return cudaErrorInvalidValue;
+  if (!make_rows_map(&mk, k, nrows, kKT) || !make_rows_map(&mv, v, nrows, kKT))
+    return cudaErrorInvalidValue;
   Params p;
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.o_long = o_long;
@@ -533,3 +560,9 @@ cudaError_t launch_window_tc(const void *q, const void *k, const void *v, const 
 }
 
 }  // namespace fs
+
+#ifdef FS_TRACE
+extern "C" int fs_trace_set(long long *buf) {
+  return (int)cudaMemcpyToSymbol(fs::g_trace, &buf, sizeof(buf));
+}
+#endif
