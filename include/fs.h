@@ -21,7 +21,8 @@
  *  - Arguments are validated before anything is launched: a NULL pointer, a
  *    non-positive size, N not a multiple of Bq or Bq not a multiple of s
  *    give FS_ERR_INVALID_ARG; shapes the kernels are not built for (d != 64,
- *    s != 32, Bq != 128, P > 64, K > 8, w outside [1, 8192]) give
+ *    s != 32, Bq != 128, P > 64, K > 8, w outside [1, 4096], N > 2^24 or
+ *    batch*H*N >= 2^31) give
  *    FS_ERR_UNSUPPORTED.  A CUDA launch error gives FS_ERR_CUDA.  No call
  *    throws across the ABI.
  *  - Cell c covers tokens [c*s, (c+1)*s); C = N/s.  Query block beta covers

@@ -36,7 +36,7 @@ int check_params(const fs_params *p) {
   if (p->Bq % p->s) return FS_ERR_INVALID_ARG;
   if (!(p->rms_eps >= 0.f) || !(p->rope_base > 0.f)) return FS_ERR_INVALID_ARG;
   if (p->mode != FS_MODE_FSL && p->mode != FS_MODE_FS) return FS_ERR_INVALID_ARG;
-  if (p->s != kS || p->Bq != kBq || p->P > kMaxP || p->K > kMaxK || p->w > 8192)
+  if (p->s != kS || p->Bq != kBq || p->P > kMaxP || p->K > kMaxK || p->w > 4096)
     return FS_ERR_UNSUPPORTED;
   return FS_OK;
 }
@@ -47,6 +47,7 @@ int check_shape(int batch, int H, int N, int d) {
   if (d != kD) return FS_ERR_UNSUPPORTED;
   if ((long long)batch * H > 65535) return FS_ERR_UNSUPPORTED;
   if ((long long)N > (1ll << 24)) return FS_ERR_UNSUPPORTED;
+  if ((long long)batch * H * N >= (1ll << 31)) return FS_ERR_UNSUPPORTED;  // 32-bit TMA rows
   return FS_OK;
 }
 
