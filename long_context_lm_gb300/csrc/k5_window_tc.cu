@@ -8,7 +8,7 @@
 //     out[n]   = o_win[n] + mix_h * o_long[n].
 //
 // Persistent kernel: one CTA per SM walks 128-query tiles (q-tiles), each over
-// the 128-key tiles covering its window.  Eleven warps with fixed roles and
+// the 128-key tiles covering its window.  Nine warps with fixed roles and
 // mbarrier hand-offs; every counter runs across q-tiles so the producers
 // start the next q-tile while the softmax finishes the current one:
 //   warps 0-3   softmax (thread = query row = TMEM lane), epilogue
@@ -17,7 +17,7 @@
 //               sustains roughly one tcgen05.mma per ~100 cycles, so the two
 //               products get their own issuer)
 //   warp  6     lane 0: TMA producer of the key and value tiles
-//   warps 7-10  rotate the queries of each q-tile and every key tile, in place
+//   warps 7-8   rotate the queries of each q-tile and every key tile, in place
 // TMEM: S double-buffered (2 x 128 columns), P (64 columns of bf16 pairs,
 // the A operand of P.V), O (64 columns).  With two S buffers the MMAs of key
 // tile t+1 run while the softmax works on tile t.
@@ -56,7 +56,8 @@ __device__ long long *g_trace = nullptr;
 
 constexpr int kKT = 128;         // keys per tile
 constexpr int kRing = 3;         // key / value ring depth (keys rotated in place)
-constexpr int kThreads = 352;
+constexpr int kThreads = 288;
+constexpr int kRotThreads = 64;  // rotation threads: two 64-element rows each
 constexpr int kT64Stride = 272;  // bytes per row of the r*theta table (padded: no bank conflicts)
 
 // shared-memory layout, offsets from a 1024-byte aligned base
@@ -249,78 +250,114 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
   }
 }
 
-__device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int r) {
+__device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int tr) {
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
-    // queries: fetch the raw row first, then wait until the previous q-tile's
-    // S MMAs no longer read the query tile
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + r) * kD);
-    uint4 raw[8];
+    // queries (rows tr and tr + 64): fetch the raw rows first, then wait until
+    // the previous q-tile's S MMAs no longer read the query tile
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + tr) * kD);
+    uint4 raw[2][8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) raw[c] = __ldg(src + c);
+    for (int c = 0; c < 8; ++c) {
+      raw[0][c] = __ldg(src + c);
+      raw[1][c] = __ldg(src + 64 * (kD / 8) + c);
+    }
     if (i > 0 && !wait_nth(&bar.q_empty, i - 1, p.err)) return;
     unsigned char *qh = smem + kOffQ;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
-    rotate_row(qh, qh + 16384, r, r, smem, p.umin);
+    for (int h = 0; h < 2; ++h) {
+      const int r = tr + 64 * h;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[h][c];
+      rotate_row(qh, qh + 16384, r, r, smem, p.umin);
+    }
     tc::fence_async_smem();
     tc::mbar_arrive(&bar.q_full);
     for (int t = 0; t < it.ntiles; ++t, ++T) {
       const int slot = T % kRing;
       if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
       unsigned char *kh = smem + kOffK + slot * 32768;
-      rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int r = tr + 64 * h;
+        rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
+      }
       tc::fence_async_smem();
       tc::mbar_arrive(&bar.kt_full[slot]);
-      if (r == 0) FS_TR(1, T);
+      if (tr == 0) FS_TR(1, T);
     }
   }
 }
 
-// Pass 1: row maximum of the (masked) score tile, 4 chunks of 32 columns.
-template <bool kMask>
-__device__ __forceinline__ float row_max(uint32_t s_addr, int lo, int hi) {
-  float mx = -INFINITY;
+// One 128-column score row held in registers (4 x 32).  Columns outside
+// [lo, hi] (the row's window) are set to -inf; the decision is made per
+// 32-column chunk and is uniform across the warp except in the one or two
+// chunks a triangular edge crosses.
+struct Row128 {
+  uint32_t s[4][32];
+};
+
+__device__ __forceinline__ void load_row(uint32_t s_addr, Row128 &x) {
 #pragma unroll
-  for (int ch = 0; ch < kKT / 32; ++ch) {
-    uint32_t s[32];
-    tc::tmem_ld32(s_addr + 32 * ch, s);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 32; ++c)
-      if (!kMask || (32 * ch + c >= lo && 32 * ch + c <= hi)) mx = fmaxf(mx, __uint_as_float(s[c]));
-  }
-  return mx;
+  for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(s_addr + 32 * ch, x.s[ch]);
+  tc::tmem_wait_ld();
 }
 
-// Pass 2: probabilities 2^(s*sl2 - m) written as bf16 into the P columns;
-// returns the row sum of the unrounded values.
-template <bool kMask>
-__device__ __forceinline__ float row_exp(uint32_t s_addr, uint32_t p_addr, int lo, int hi,
-                                         float sl2, float m) {
-  float ls = 0.f;
+__device__ __forceinline__ void mask_row(Row128 &x, int lo, int hi) {
+  constexpr uint32_t kNegInf = 0xff800000u;
 #pragma unroll
-  for (int ch = 0; ch < kKT / 32; ++ch) {
-    uint32_t s[32], pk[16];
-    tc::tmem_ld32(s_addr + 32 * ch, s);
-    tc::tmem_wait_ld();
-    float l0 = 0.f, l1 = 0.f;
+  for (int ch = 0; ch < 4; ++ch) {
+    const bool full = lo <= 32 * ch && hi >= 32 * ch + 31;
+    const bool empty = hi < 32 * ch || lo > 32 * ch + 31;
+    if (__all_sync(0xffffffffu, full)) continue;
+    if (__all_sync(0xffffffffu, empty)) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x.s[ch][c] = kNegInf;
+      continue;
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int col = 32 * ch + c;
+      if (col < lo || col > hi) x.s[ch][c] = kNegInf;
+    }
+  }
+}
+
+__device__ __forceinline__ float max_row(const Row128 &x) {
+  float mx[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(x.s[j >> 1][(j & 1) * 16]);
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int j = (ch * 2 + (c >> 4)) & 7;
+      mx[j] = fmaxf(mx[j], __uint_as_float(x.s[ch][c]));
+    }
+  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
+// 2^(s*sl2 - m) for the whole row, written as bf16 pairs into the P columns;
+// returns the row sum of the unrounded values (8 partial sums).
+__device__ __forceinline__ float exp_row(const Row128 &x, uint32_t p_addr, float sl2, float m) {
+  float part[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[j] = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t pk[16];
 #pragma unroll
     for (int c = 0; c < 32; c += 2) {
-      const int col = 32 * ch + c;
-      const float e0 = (!kMask || (col >= lo && col <= hi))
-                           ? tc::ex2(fmaf(__uint_as_float(s[c]), sl2, -m)) : 0.f;
-      const float e1 = (!kMask || (col + 1 >= lo && col + 1 <= hi))
-                           ? tc::ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -m)) : 0.f;
-      l0 += e0;
-      l1 += e1;
+      const float e0 = tc::ex2(fmaf(__uint_as_float(x.s[ch][c]), sl2, -m));
+      const float e1 = tc::ex2(fmaf(__uint_as_float(x.s[ch][c + 1]), sl2, -m));
+      part[(c >> 2) & 7] += e0 + e1;
       pk[c / 2] = pack_bf16(e0, e1);
     }
-    ls += l0 + l1;
     tc::tmem_st16(p_addr + 16 * ch, pk);
   }
-  return ls;
+  return ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
 }
 
 __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int r) {
@@ -342,17 +379,24 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int 
       const int kt = it.kt0 + t * kKT;
       const int lo = max(0, n - p.w + 1 - kt), hi = min(kKT - 1, n - kt);
       const bool any = __any_sync(0xffffffffu, lo <= hi);
-      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kKT - 1);
-      float mx = -INFINITY;
-      if (any) mx = full ? row_max<false>(s_addr, lo, hi) : row_max<true>(s_addr, lo, hi);
-      // P and O belong to the previous P.V until it completes
+      Row128 x;
+      float mnew = m;
+      if (any) {
+        load_row(s_addr, x);
+        mask_row(x, lo, hi);
+        mnew = fmaxf(m, max_row(x) * sl2);
+      }
+      // the S buffer may be refilled; P and O still belong to the previous
+      // P.V until it completes
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar.s_free[b]);
       if (T > 0 && !wait_nth(&bar.pv_done, T - 1, p.err)) return;
       tc::fence_after_sync();
       if (any) {
-        const float mnew = fmaxf(m, mx * sl2);
         const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
-        const float ls = full ? row_exp<false>(s_addr, p_addr, lo, hi, sl2, mnew)
-                              : row_exp<true>(s_addr, p_addr, lo, hi, sl2, mnew);
+        const float muse = mnew == -INFINITY ? 0.f : mnew;
+        const float ls = exp_row(x, p_addr, sl2, muse);
         l = l * alpha + ls;
         m = mnew;
         if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -378,10 +422,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int 
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&bar.s_free[b]);
-        tc::mbar_arrive(&bar.p_full);
-      }
+      if (lane == 0) tc::mbar_arrive(&bar.p_full);
       if (r == 0) FS_TR(4, T);
     }
     // epilogue: O / l (+ mix_h * o_long)
@@ -418,7 +459,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
+__global__ void __maxnreg__(224) k5_window_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
   extern __shared__ unsigned char smem_raw[];
@@ -428,11 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bar.q_full, 128);
+    tc::mbar_init(&bar.q_full, kRotThreads);
     tc::mbar_init(&bar.q_empty, 1);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&bar.raw_full[i], 1);
-      tc::mbar_init(&bar.kt_full[i], 128);
+      tc::mbar_init(&bar.kt_full[i], kRotThreads);
       tc::mbar_init(&bar.k_empty[i], 1);
       tc::mbar_init(&bar.v_empty[i], 1);
     }
@@ -455,14 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
   if (warp >= 7) {
     const int r = threadIdx.x - 224;
     const float4 *rel = reinterpret_cast<const float4 *>(p.rel);
-    for (int i = r; i < 64 * 16; i += 128) {
+    for (int i = r; i < 64 * 16; i += kRotThreads) {
       const int row = i >> 4, part = i & 15;
       *reinterpret_cast<float4 *>(smem + kOffT64 + row * kT64Stride + part * 16) =
           __ldg(rel + (size_t)(row + p.rel_off) * 16 + part);
     }
     float4 *tu = reinterpret_cast<float4 *>(smem + kOffTU);
     const int nu = 3 - p.umin;  // u in [umin, 2]
-    for (int i = r; i < nu * 16; i += 128) {
+    for (int i = r; i < nu * 16; i += kRotThreads) {
       const int row = i >> 4, part = i & 15;
       tu[i] = __ldg(rel + (size_t)(64 * (row + p.umin) + p.rel_off) * 16 + part);
     }
