@@ -74,6 +74,10 @@ void fs_default_params(fs_params *p);
 /* Human-readable name of a status code (static string). */
 const char *fs_status_string(int status);
 
+/* Description of the CUDA error behind the calling thread's most recent
+ * FS_ERR_CUDA (static string; "no error" if there was none). */
+const char *fs_last_cuda_error(void);
+
 /* Device workspace bytes fs_attention_fwd needs for this shape (includes the
  * bf16 staging copies of q, k, v when dtype is FS_FP32).  0 on bad args. */
 size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p,

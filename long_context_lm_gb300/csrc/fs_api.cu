@@ -55,7 +55,13 @@ int check_dtype(int dtype) {
   return (dtype == FS_BF16 || dtype == FS_FP32) ? FS_OK : FS_ERR_INVALID_ARG;
 }
 
-int status_of(cudaError_t e) { return e == cudaSuccess ? FS_OK : FS_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int status_of(cudaError_t e) {
+  if (e == cudaSuccess) return FS_OK;
+  g_last_cuda_error = e;
+  return FS_ERR_CUDA;
+}
 
 #define FS_TRY(x)                  \
   do {                             \
@@ -129,6 +135,8 @@ const char *fs_status_string(int status) {
     default: return "unknown status";
   }
 }
+
+const char *fs_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p, int dtype) {
   if (check_params(p) || check_shape(batch, H, N, d) || check_dtype(dtype)) return 0;

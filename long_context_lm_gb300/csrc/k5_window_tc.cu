@@ -459,7 +459,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int 
   }
 }
 
-__global__ void __maxnreg__(224) k5_window_tc_kernel(
+__global__ void __maxnreg__(200) k5_window_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
   extern __shared__ unsigned char smem_raw[];

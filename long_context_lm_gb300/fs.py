@@ -24,7 +24,7 @@ FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT = ran
 FS_BF16, FS_FP32 = 0, 1
 FS_MODE_FSL, FS_MODE_FS = 0, 1
 
-SYMBOLS = ["fs_default_params", "fs_status_string", "fs_workspace_bytes",
+SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_workspace_bytes",
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status"]
@@ -45,7 +45,10 @@ class fs_params(ctypes.Structure):
 class FSError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        msg = f"{where}: {status_string(status)} (status {status})"
+        if status == FS_ERR_CUDA:
+            msg += ": " + load().fs_last_cuda_error().decode()
+        super().__init__(msg)
 
 
 _lock = threading.Lock()
@@ -74,6 +77,8 @@ def load(build_if_stale: bool = True):
         L.fs_default_params.restype = None
         L.fs_status_string.argtypes = [I]
         L.fs_status_string.restype = ctypes.c_char_p
+        L.fs_last_cuda_error.argtypes = []
+        L.fs_last_cuda_error.restype = ctypes.c_char_p
         L.fs_workspace_bytes.argtypes = [I, I, I, I, PP, I]
         L.fs_workspace_bytes.restype = Z
         L.fs_prune_workspace_bytes.argtypes = [I, I, I, PP]
@@ -90,7 +95,8 @@ def load(build_if_stale: bool = True):
         L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 6
         L.fs_check_status.argtypes = [P, P]
         for name in SYMBOLS:
-            if name not in ("fs_default_params", "fs_status_string", "fs_workspace_bytes",
+            if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
+                            "fs_workspace_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
