@@ -8,16 +8,20 @@
 //     out[n]   = o_win[n] + mix_h * o_long[n].
 //
 // Persistent kernel: one CTA per SM walks 128-query tiles (q-tiles), each over
-// the 128-key tiles covering its window.  Nine warps with fixed roles and
-// mbarrier hand-offs; every counter runs across q-tiles so the producers
-// start the next q-tile while the softmax finishes the current one:
-//   warps 0-3   softmax (thread = query row = TMEM lane), epilogue
-//   warp  4     TMEM allocation; lane 0 issues the S = Q.K^T MMAs
-//   warp  5     lane 0 issues the O += P.V MMAs (a single issuing thread
+// the 128-key tiles covering its window.  Sixteen warps (four per SM
+// sub-partition, 128 registers each) with fixed roles and mbarrier hand-offs;
+// every counter runs across q-tiles so the producers start the next q-tile
+// while the softmax finishes the current one:
+//   warps 0-7   softmax and epilogue: warp w owns TMEM lanes / query rows
+//               32*(w%4).. and key columns 64*(w/4).. of each 128-key tile;
+//               the two warps of a row block exchange their row maxima
+//               through shared memory (one named barrier per tile)
+//   warp  8     TMEM allocation; lane 0 issues the S = Q.K^T MMAs
+//   warp  9     lane 0 issues the O += P.V MMAs (a single issuing thread
 //               sustains roughly one tcgen05.mma per ~100 cycles, so the two
 //               products get their own issuer)
-//   warp  6     lane 0: TMA producer of the key and value tiles
-//   warps 7-8   rotate the queries of each q-tile and every key tile, in place
+//   warp  10    lane 0: TMA producer of the key and value tiles
+//   warps 12-15 rotate the queries of each q-tile and every key tile, in place
 // TMEM: S double-buffered (2 x 128 columns), P (64 columns of bf16 pairs,
 // the A operand of P.V), O (64 columns).  With two S buffers the MMAs of key
 // tile t+1 run while the softmax works on tile t.
@@ -56,8 +60,9 @@ __device__ long long *g_trace = nullptr;
 
 constexpr int kKT = 128;         // keys per tile
 constexpr int kRing = 3;         // key / value ring depth (keys rotated in place)
-constexpr int kThreads = 288;
-constexpr int kRotThreads = 64;  // rotation threads: two 64-element rows each
+constexpr int kThreads = 512;
+constexpr int kRotThreads = 128;  // rotation threads: one 64-element row each
+constexpr int kRotBase = 384;     // first rotation thread
 constexpr int kT64Stride = 272;  // bytes per row of the r*theta table (padded: no bank conflicts)
 
 // shared-memory layout, offsets from a 1024-byte aligned base
@@ -82,6 +87,8 @@ struct Barriers {
   uint64_t o_done, o_free;
   uint64_t fin[2];
   uint32_t tmem;
+  float xmax[2][128];  // per-half row maxima of the current tile
+  float xsum[2][128];  // per-half row sums at the end of a q-tile
 };
 
 struct Params {
@@ -250,66 +257,56 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
   }
 }
 
-__device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int tr) {
+__device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int r) {
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
-    // queries (rows tr and tr + 64): fetch the raw rows first, then wait until
-    // the previous q-tile's S MMAs no longer read the query tile
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + tr) * kD);
-    uint4 raw[2][8];
+    // query row r: fetch the raw row first, then wait until the previous
+    // q-tile's S MMAs no longer read the query tile
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + r) * kD);
+    uint4 raw[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      raw[0][c] = __ldg(src + c);
-      raw[1][c] = __ldg(src + 64 * (kD / 8) + c);
-    }
+    for (int c = 0; c < 8; ++c) raw[c] = __ldg(src + c);
     if (i > 0 && !wait_nth(&bar.q_empty, i - 1, p.err)) return;
     unsigned char *qh = smem + kOffQ;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = tr + 64 * h;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[h][c];
-      rotate_row(qh, qh + 16384, r, r, smem, p.umin);
-    }
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
+    rotate_row(qh, qh + 16384, r, r, smem, p.umin);
     tc::fence_async_smem();
     tc::mbar_arrive(&bar.q_full);
     for (int t = 0; t < it.ntiles; ++t, ++T) {
       const int slot = T % kRing;
       if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
       unsigned char *kh = smem + kOffK + slot * 32768;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int r = tr + 64 * h;
-        rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
-      }
+      rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
       tc::fence_async_smem();
       tc::mbar_arrive(&bar.kt_full[slot]);
-      if (tr == 0) FS_TR(1, T);
+      if (r == 0) FS_TR(1, T);
     }
   }
 }
 
-// One 128-column score row held in registers (4 x 32).  Columns outside
-// [lo, hi] (the row's window) are set to -inf; the decision is made per
-// 32-column chunk and is uniform across the warp except in the one or two
-// chunks a triangular edge crosses.
-struct Row128 {
-  uint32_t s[4][32];
+// Half of a score row (64 columns) held in registers.  Columns outside
+// [lo, hi] (the row's window, in tile columns) are set to -inf; the decision
+// is made per 32-column chunk and is uniform across the warp except in the
+// chunk a triangular edge crosses.
+struct Half64 {
+  uint32_t s[2][32];
 };
 
-__device__ __forceinline__ void load_row(uint32_t s_addr, Row128 &x) {
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(s_addr + 32 * ch, x.s[ch]);
+__device__ __forceinline__ void load_half(uint32_t s_addr, Half64 &x) {
+  tc::tmem_ld32(s_addr, x.s[0]);
+  tc::tmem_ld32(s_addr + 32, x.s[1]);
   tc::tmem_wait_ld();
 }
 
-__device__ __forceinline__ void mask_row(Row128 &x, int lo, int hi) {
+__device__ __forceinline__ void mask_half(Half64 &x, int lo, int hi, int col0) {
   constexpr uint32_t kNegInf = 0xff800000u;
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const bool full = lo <= 32 * ch && hi >= 32 * ch + 31;
-    const bool empty = hi < 32 * ch || lo > 32 * ch + 31;
+  for (int ch = 0; ch < 2; ++ch) {
+    const int c0 = col0 + 32 * ch;
+    const bool full = lo <= c0 && hi >= c0 + 31;
+    const bool empty = hi < c0 || lo > c0 + 31;
     if (__all_sync(0xffffffffu, full)) continue;
     if (__all_sync(0xffffffffu, empty)) {
 #pragma unroll
@@ -318,35 +315,35 @@ __device__ __forceinline__ void mask_row(Row128 &x, int lo, int hi) {
     }
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const int col = 32 * ch + c;
+      const int col = c0 + c;
       if (col < lo || col > hi) x.s[ch][c] = kNegInf;
     }
   }
 }
 
-__device__ __forceinline__ float max_row(const Row128 &x) {
+__device__ __forceinline__ float max_half(const Half64 &x) {
   float mx[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(x.s[j >> 1][(j & 1) * 16]);
+  for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(x.s[j >> 2][(j & 3) * 8]);
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch)
+  for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const int j = (ch * 2 + (c >> 4)) & 7;
+      const int j = (ch * 4 + (c >> 3)) & 7;
       mx[j] = fmaxf(mx[j], __uint_as_float(x.s[ch][c]));
     }
   return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
-// 2^(s*sl2 - m) for the whole row, written as bf16 pairs into the P columns;
-// returns the row sum of the unrounded values (8 partial sums).
-__device__ __forceinline__ float exp_row(const Row128 &x, uint32_t p_addr, float sl2, float m) {
+// 2^(s*sl2 - m) for the half row, written as bf16 pairs into its 32 P
+// columns; returns the sum of the unrounded values (8 partial sums).
+__device__ __forceinline__ float exp_half(const Half64 &x, uint32_t p_addr, float sl2, float m) {
   float part[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[j] = 0.f;
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
+  for (int ch = 0; ch < 2; ++ch) {
     uint32_t pk[16];
 #pragma unroll
     for (int c = 0; c < 32; c += 2) {
@@ -360,10 +357,18 @@ __device__ __forceinline__ float exp_row(const Row128 &x, uint32_t p_addr, float
   return ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
 }
 
-__device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int r) {
+// named barrier of the two softmax warps that share a row block
+__device__ __forceinline__ void pair_sync(int quarter) {
+  asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+}
+
+__device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t p_addr = tmem + kColP + lane_base, o_addr = tmem + kColO + lane_base;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int r = quarter * 32 + lane;  // query row of this thread
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const uint32_t p_addr = tmem + kColP + 32 * half + lane_base;
+  const uint32_t o_addr = tmem + kColO + 32 * half + lane_base;
   const float sl2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
@@ -372,80 +377,81 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int 
     float m = -INFINITY, l = 0.f;
     for (int t = 0; t < it.ntiles; ++t, ++T) {
       const int b = T & 1;
-      const uint32_t s_addr = tmem + kColS + 128 * b + lane_base;
+      const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
       if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
       tc::fence_after_sync();
-      if (r == 0) FS_TR(3, T);
+      if (r == 0 && half == 0) FS_TR(3, T);
       const int kt = it.kt0 + t * kKT;
       const int lo = max(0, n - p.w + 1 - kt), hi = min(kKT - 1, n - kt);
-      const bool any = __any_sync(0xffffffffu, lo <= hi);
-      Row128 x;
-      float mnew = m;
+      const bool any = __any_sync(0xffffffffu, lo <= hi && hi >= 64 * half && lo <= 64 * half + 63);
+      Half64 x;
+      float mx = -INFINITY;
       if (any) {
-        load_row(s_addr, x);
-        mask_row(x, lo, hi);
-        mnew = fmaxf(m, max_row(x) * sl2);
+        load_half(s_addr, x);
+        mask_half(x, lo, hi, 64 * half);
+        mx = max_half(x);
       }
-      // the S buffer may be refilled; P and O still belong to the previous
-      // P.V until it completes
+      // the S buffer may be refilled once both halves are in registers
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar.s_free[b]);
+      bar.xmax[half][r] = mx;
+      pair_sync(quarter);
+      mx = fmaxf(mx, bar.xmax[half ^ 1][r]);
+      pair_sync(quarter);  // the slot is rewritten next tile
+      const float mnew = fmaxf(m, mx * sl2);
+      const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
+      // P and O belong to the previous P.V until it completes
       if (T > 0 && !wait_nth(&bar.pv_done, T - 1, p.err)) return;
       tc::fence_after_sync();
       if (any) {
-        const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
         const float muse = mnew == -INFINITY ? 0.f : mnew;
-        const float ls = exp_row(x, p_addr, sl2, muse);
-        l = l * alpha + ls;
-        m = mnew;
-        if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          uint32_t o0[32], o1[32];
-          tc::tmem_ld32(o_addr, o0);
-          tc::tmem_ld32(o_addr + 32, o1);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            o0[c] = __float_as_uint(__uint_as_float(o0[c]) * alpha);
-            o1[c] = __float_as_uint(__uint_as_float(o1[c]) * alpha);
-          }
-          tc::tmem_st32(o_addr, o0);
-          tc::tmem_st32(o_addr + 32, o1);
-        }
+        l = l * alpha + exp_half(x, p_addr, sl2, muse);
       } else {
+        l = l * alpha;
         uint32_t z[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) z[c] = 0u;
+        tc::tmem_st16(p_addr, z);
+        tc::tmem_st16(p_addr + 16, z);
+      }
+      m = mnew;
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        uint32_t o[32];
+        tc::tmem_ld32(o_addr, o);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int ch = 0; ch < kKT / 32; ++ch) tc::tmem_st16(p_addr + 16 * ch, z);
+        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+        tc::tmem_st32(o_addr, o);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar.p_full);
-      if (r == 0) FS_TR(4, T);
+      if (r == 0 && half == 0) FS_TR(4, T);
     }
-    // epilogue: O / l (+ mix_h * o_long)
+    // epilogue: O / l (+ mix_h * o_long); each warp writes its 32 columns
+    bar.xsum[half][r] = l;
     if (!wait_nth(&bar.o_done, i, p.err)) return;
     tc::fence_after_sync();
-    uint32_t o0[32], o1[32];
-    tc::tmem_ld32(o_addr, o0);
-    tc::tmem_ld32(o_addr + 32, o1);
+    uint32_t o[32];
+    tc::tmem_ld32(o_addr, o);
     tc::tmem_wait_ld();
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&bar.o_free);
-    const float inv = 1.f / l;
+    pair_sync(quarter);
+    const float inv = 1.f / (l + bar.xsum[half ^ 1][r]);
+    pair_sync(quarter);
     const size_t row = (size_t)it.bh * p.N + n;
     const float mh = p.mix ? p.mix[it.bh % p.H] : 0.f;
-    float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD);
-    const float4 *ol = p.o_long ? reinterpret_cast<const float4 *>(p.o_long + row * kD) : nullptr;
+    float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD + 32 * half);
+    const float4 *ol =
+        p.o_long ? reinterpret_cast<const float4 *>(p.o_long + row * kD + 32 * half) : nullptr;
 #pragma unroll
-    for (int c4 = 0; c4 < 16; ++c4) {
-      const uint32_t *src = c4 < 8 ? o0 : o1;
-      const int bb = (c4 & 7) * 4;
-      float4 v = make_float4(__uint_as_float(src[bb]) * inv, __uint_as_float(src[bb + 1]) * inv,
-                             __uint_as_float(src[bb + 2]) * inv, __uint_as_float(src[bb + 3]) * inv);
+    for (int c4 = 0; c4 < 8; ++c4) {
+      float4 v = make_float4(__uint_as_float(o[4 * c4]) * inv, __uint_as_float(o[4 * c4 + 1]) * inv,
+                             __uint_as_float(o[4 * c4 + 2]) * inv, __uint_as_float(o[4 * c4 + 3]) * inv);
       if (ol) {
         const float4 u4 = __ldg(ol + c4);
         v.x = fmaf(mh, u4.x, v.x);
@@ -455,11 +461,11 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, int 
       }
       dst[c4] = v;
     }
-    if (r == 0) FS_TR(6, i);
+    if (r == 0 && half == 0) FS_TR(6, i);
   }
 }
 
-__global__ void __maxnreg__(200) k5_window_tc_kernel(
+__global__ void __launch_bounds__(kThreads, 1) k5_window_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const Params p) {
   extern __shared__ unsigned char smem_raw[];
@@ -479,22 +485,22 @@ __global__ void __maxnreg__(200) k5_window_tc_kernel(
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bar.s_full[b], 1);
-      tc::mbar_init(&bar.s_free[b], 4);
+      tc::mbar_init(&bar.s_free[b], 8);
       tc::mbar_init(&bar.fin[b], 1);
     }
-    tc::mbar_init(&bar.p_full, 4);
+    tc::mbar_init(&bar.p_full, 8);
     tc::mbar_init(&bar.pv_done, 1);
     tc::mbar_init(&bar.o_done, 1);
-    tc::mbar_init(&bar.o_free, 4);
+    tc::mbar_init(&bar.o_free, 8);
     tc::mbar_fence_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tc::tmem_alloc(&bar.tmem, kTmemCols);
     tc::tmem_relinquish();
   }
   // angle tables, staged once per CTA by the rotation warps
-  if (warp >= 7) {
-    const int r = threadIdx.x - 224;
+  if (threadIdx.x >= kRotBase) {
+    const int r = threadIdx.x - kRotBase;
     const float4 *rel = reinterpret_cast<const float4 *>(p.rel);
     for (int i = r; i < 64 * 16; i += kRotThreads) {
       const int row = i >> 4, part = i & 15;
@@ -514,25 +520,25 @@ __global__ void __maxnreg__(200) k5_window_tc_kernel(
   const uint32_t tmem = bar.tmem;
   const uint32_t sbase = smem_u32(smem);
 
-  if (warp < 4) {
-    role_softmax(p, bar, tmem, threadIdx.x);
-  } else if (warp == 4 || warp == 5) {
+  if (warp < 8) {
+    role_softmax(p, bar, tmem);
+  } else if (warp == 8 || warp == 9) {
     if (lane == 0) {
-      if (warp == 4)
+      if (warp == 8)
         role_qk(p, bar, tmem, sbase);
       else
         role_pv(p, bar, tmem, sbase);
-      tc::mma_commit(&bar.fin[warp - 4]);  // every MMA this thread issued has completed
-      tc::mbar_wait(&bar.fin[warp - 4], 0, p.err);
+      tc::mma_commit(&bar.fin[warp - 8]);  // every MMA this thread issued has completed
+      tc::mbar_wait(&bar.fin[warp - 8], 0, p.err);
     }
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     if (lane == 0) role_tma(p, bar, smem, &tmap_k, &tmap_v);
-  } else {
-    role_rotate(p, bar, smem, threadIdx.x - 224);
+  } else if (threadIdx.x >= kRotBase) {
+    role_rotate(p, bar, smem, threadIdx.x - kRotBase);
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
