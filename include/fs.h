@@ -21,7 +21,7 @@
  *  - Arguments are validated before anything is launched: a NULL pointer, a
  *    non-positive size, N not a multiple of Bq or Bq not a multiple of s
  *    give FS_ERR_INVALID_ARG; shapes the kernels are not built for (d != 64,
- *    s != 32, Bq != 128, P > 64, K > 8, w outside [1, 4096], N > 2^24 or
+ *    s != 32, Bq != 128, P > 64, K > 8, w outside [1, 1024], N > 2^24 or
  *    batch*H*N >= 2^31) give
  *    FS_ERR_UNSUPPORTED.  A CUDA launch error gives FS_ERR_CUDA.  No call
  *    throws across the ABI.
@@ -139,7 +139,7 @@ int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
                       const int32_t *sel, int batch, int H, int N, int d,
                       const fs_params *p, float *o_long, void *stream);
 
-/* Workspace bytes fs_window_attn needs (RoPE angle tables). */
+/* Workspace bytes fs_window_attn needs (header + RoPE angle table). */
 size_t fs_window_workspace_bytes(int N, const fs_params *p);
 
 /* Sliding-window RoPE branch and branch mix (paper.rainbus.top summary,
@@ -155,7 +155,7 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype,
                    size_t ws_bytes, void *stream);
 
 /* Whole FS-L (or FS) attention forward: cell summaries, pools, selection,
- * readout, window and mix, all on `stream`.
+ * then both attention branches and the mix in one kernel, all on `stream`.
  *   q, k, v   [batch,H,N,d] bf16 or f32 (f32 is rounded to bf16 once)
  *   lambda, sigma, mix   [H] f32
  *   out       [batch,H,N,d] f32
@@ -167,8 +167,9 @@ int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype,
                      float *out, void *ws, size_t ws_bytes, void *stream);
 
 /* Number of timed stages of fs_attention_fwd_traced: cell summaries,
- * pruning, selection, readout, window (RoPE tables + window + mix). */
-#define FS_N_STAGES 5
+ * pruning, selection, attention (window branch, NoPE readout of the selected
+ * cells and the mix, in one kernel). */
+#define FS_N_STAGES 4
 
 /* fs_attention_fwd that also records CUDA events between its stages, for
  * per-kernel timing on the launch stream.  stage_events: NULL, or an array of
@@ -192,12 +193,13 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v,
 int fs_check_status(const void *ws, void *stream);
 
 /* Byte offsets of the intermediates inside an fs_attention_fwd workspace,
- * for inspection: kbar, amax, pool, pool_count, sel, o_long (any may be
- * NULL).  Returns FS_OK or FS_ERR_INVALID_ARG. */
+ * for inspection: kbar, amax, pool, pool_count, sel (any may be NULL).  The
+ * long-branch output is never materialised: the attention kernel mixes it
+ * into `out` directly.  Returns FS_OK or FS_ERR_INVALID_ARG. */
 int fs_workspace_view(int batch, int H, int N, int d, const fs_params *p,
                       int dtype, size_t *off_kbar, size_t *off_amax,
                       size_t *off_pool, size_t *off_pool_count,
-                      size_t *off_sel, size_t *off_o_long);
+                      size_t *off_sel);
 
 #ifdef __cplusplus
 }

@@ -36,7 +36,7 @@ int check_params(const fs_params *p) {
   if (p->Bq % p->s) return FS_ERR_INVALID_ARG;
   if (!(p->rms_eps >= 0.f) || !(p->rope_base > 0.f)) return FS_ERR_INVALID_ARG;
   if (p->mode != FS_MODE_FSL && p->mode != FS_MODE_FS) return FS_ERR_INVALID_ARG;
-  if (p->s != kS || p->Bq != kBq || p->P > kMaxP || p->K > kMaxK || p->w > 4096)
+  if (p->s != kS || p->Bq != kBq || p->P > kMaxP || p->K > kMaxK || p->w > 1024)
     return FS_ERR_UNSUPPORTED;
   return FS_OK;
 }
@@ -76,7 +76,7 @@ constexpr size_t kHeader = 256;
 // Layout of the fs_attention_fwd workspace.
 struct Layout {
   size_t qb, kb, vb;       // bf16 copies (fp32 inputs only)
-  size_t kbar, amax, pool, pool_count, sel, o_long, rope, prune;
+  size_t kbar, amax, pool, pool_count, sel, rope, prune;
   size_t total;
 };
 
@@ -98,8 +98,7 @@ Layout make_layout(const Shape &sh, const fs_params &p, int dtype) {
   L.pool = take((size_t)sh.BH() * sh.nblk() * (p.P + p.W) * sizeof(int32_t));
   L.pool_count = take((size_t)sh.BH() * sh.nblk() * sizeof(int32_t));
   L.sel = take((size_t)sh.BH() * sh.N * p.K * sizeof(int32_t));
-  L.o_long = take(elems * sizeof(float));
-  L.rope = take(window_table_bytes(p.w));
+  L.rope = take(attn_table_bytes(p.w));
   L.prune = take(prune_workspace_bytes(sh));
   L.total = off;
   return L;
@@ -145,7 +144,7 @@ size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p, in
 
 int fs_workspace_view(int batch, int H, int N, int d, const fs_params *p, int dtype,
                       size_t *off_kbar, size_t *off_amax, size_t *off_pool,
-                      size_t *off_pool_count, size_t *off_sel, size_t *off_o_long) {
+                      size_t *off_pool_count, size_t *off_sel) {
   FS_TRY(check_params(p));
   FS_TRY(check_shape(batch, H, N, d));
   FS_TRY(check_dtype(dtype));
@@ -155,7 +154,6 @@ int fs_workspace_view(int batch, int H, int N, int d, const fs_params *p, int dt
   if (off_pool) *off_pool = L.pool;
   if (off_pool_count) *off_pool_count = L.pool_count;
   if (off_sel) *off_sel = L.sel;
-  if (off_o_long) *off_o_long = L.o_long;
   return FS_OK;
 }
 
@@ -166,7 +164,7 @@ size_t fs_prune_workspace_bytes(int batch, int H, int N, const fs_params *p) {
 
 size_t fs_window_workspace_bytes(int N, const fs_params *p) {
   if (check_params(p) || check_shape(1, 1, N, kD)) return 0;
-  return kHeader + window_table_bytes(p->w);
+  return kHeader + attn_table_bytes(p->w);
 }
 
 int fs_check_status(const void *ws, void *stream) {
@@ -227,8 +225,20 @@ int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
   FS_TRY(check_dtype(dtype));
   if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
   if (!q || !k || !v || !sel || !o_long) return FS_ERR_INVALID_ARG;
-  return status_of(launch_readout(q, k, v, sel, Shape{batch, H, N, d}, p->K, p->rms_eps, o_long,
-                                  static_cast<cudaStream_t>(stream)));
+  AttnArgs a{};
+  a.sh = Shape{batch, H, N, d};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.sel = sel;
+  a.w = p->w;
+  a.K = p->K;
+  a.rope_base = p->rope_base;
+  a.rms_eps = p->rms_eps;
+  a.window = false;
+  a.write_long = true;
+  a.out = o_long;
+  return status_of(launch_attn_tc(a, static_cast<cudaStream_t>(stream)));
 }
 
 int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const float *o_long,
@@ -239,14 +249,27 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const
   FS_TRY(check_dtype(dtype));
   if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !ws || (o_long && !mix)) return FS_ERR_INVALID_ARG;
-  const Shape sh{batch, H, N, d};
-  if (ws_bytes < kHeader + window_table_bytes(p->w)) return FS_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader + attn_table_bytes(p->w)) return FS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *base = static_cast<char *>(ws);
   int *err = reinterpret_cast<int *>(base);
   FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
-  return status_of(launch_window_tc(q, k, v, o_long, mix, base + kHeader, sh, p->w, p->rope_base,
-                                    out, err, st));
+  AttnArgs a{};
+  a.sh = Shape{batch, H, N, d};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_long_in = o_long;
+  a.mix = mix;
+  a.table = base + kHeader;
+  a.w = p->w;
+  a.K = p->K;
+  a.rope_base = p->rope_base;
+  a.rms_eps = p->rms_eps;
+  a.window = true;
+  a.out = out;
+  a.err = err;
+  return status_of(launch_attn_tc(a, st));
 }
 
 int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype, int batch, int H,
@@ -284,7 +307,6 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   int32_t *pool = reinterpret_cast<int32_t *>(base + L.pool);
   int32_t *pool_count = reinterpret_cast<int32_t *>(base + L.pool_count);
   int32_t *sel = reinterpret_cast<int32_t *>(base + L.sel);
-  float *o_long = reinterpret_cast<float *>(base + L.o_long);
   int *err = reinterpret_cast<int *>(base);
   const bool fs_mode = p->mode == FS_MODE_FS;
   FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
@@ -302,11 +324,23 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   FS_TRY(status_of(launch_select(qb, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
                                  p->P + p->W, fs_mode, sel, nullptr, err, st)));
   FS_TRY(mark(3));
-  FS_TRY(status_of(launch_readout(qb, kb, vb, sel, sh, p->K, p->rms_eps, o_long, st)));
-  FS_TRY(mark(4));
-  FS_TRY(status_of(launch_window_tc(qb, kb, vb, o_long, mix, base + L.rope, sh, p->w,
-                                    p->rope_base, out, err, st)));
-  return mark(5);
+  AttnArgs a{};
+  a.sh = sh;
+  a.q = qb;
+  a.k = kb;
+  a.v = vb;
+  a.sel = sel;
+  a.mix = mix;
+  a.table = base + L.rope;
+  a.w = p->w;
+  a.K = p->K;
+  a.rope_base = p->rope_base;
+  a.rms_eps = p->rms_eps;
+  a.window = true;
+  a.out = out;
+  a.err = err;
+  FS_TRY(status_of(launch_attn_tc(a, st)));
+  return mark(4);
 }
 
 }  // extern "C"

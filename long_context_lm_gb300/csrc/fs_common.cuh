@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "fs.h"
+#include "fs_internal.h"
 
 namespace fs {
 
@@ -15,13 +16,6 @@ constexpr int kBq = 128;     // query block / query tile
 constexpr int kMaxP = 64;    // largest P the prune kernels keep
 constexpr int kMaxK = 8;     // largest K the select kernel keeps
 
-// Internal launch parameters (validated copies of fs_params).
-struct Shape {
-  int batch, H, N, d;
-  int BH() const { return batch * H; }
-  int C() const { return N / kS; }
-  int nblk() const { return N / kBq; }
-};
 
 // ---------------------------------------------------------------------------
 // warp helpers

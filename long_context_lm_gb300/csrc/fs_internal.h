@@ -7,7 +7,12 @@
 
 namespace fs {
 
-struct Shape;
+struct Shape {
+  int batch, H, N, d;
+  int BH() const { return batch * H; }
+  int C() const { return N / 32; }
+  int nblk() const { return N / 128; }
+};
 
 cudaError_t launch_round_bf16(const float *src, void *dst, size_t n, cudaStream_t st);
 cudaError_t launch_cell_summary(const void *k, bool f32, const Shape &sh, float *kbar,
@@ -19,12 +24,25 @@ cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const int32_t *pool, const int32_t *pool_count, const float *lambda,
                           const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
                           int32_t *sel, float *sel_score, int *err, cudaStream_t st);
-cudaError_t launch_readout(const void *q, const void *k, const void *v, const int32_t *sel,
-                           const Shape &sh, int K, float rms_eps, float *o_long,
-                           cudaStream_t st);
-size_t window_table_bytes(int w);
-cudaError_t launch_window_tc(const void *q, const void *k, const void *v, const float *o_long,
-                             const float *mix, void *table, const Shape &sh, int w, float base,
-                             float *out, int *err, cudaStream_t st);
+// Both attention branches (window RoPE branch, NoPE readout of the selected
+// cells) in one persistent tcgen05 kernel.  window: run the window branch;
+// sel != nullptr: run the long branch; write_long: write RMSNorm(o_long) to
+// `out` instead of the mixed output; o_long_in (window only, nullable): a
+// precomputed long branch to mix in.
+struct AttnArgs {
+  Shape sh;
+  const void *q, *k, *v;
+  const int32_t *sel;
+  const float *o_long_in;
+  const float *mix;
+  void *table;  // attn_table_bytes(w) of device scratch (window only)
+  int w, K;
+  float rope_base, rms_eps;
+  bool window, write_long;
+  float *out;
+  int *err;
+};
+size_t attn_table_bytes(int w);
+cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace fs

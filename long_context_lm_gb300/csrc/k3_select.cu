@@ -39,11 +39,16 @@ __device__ __forceinline__ bool ranks_before(float u, int c, float u2, int c2) {
   return u > u2 || (u == u2 && c < c2);
 }
 
+// erf of the bias argument; only the newest few cells need it (x < 4), so it
+// is kept out of line to keep the unrolled scoring loop small
+__device__ __noinline__ float erf_bias(float x) { return erff(x); }
+
+template <int K>
 __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
     const float *__restrict__ amax, const int32_t *__restrict__ pool,
     const int32_t *__restrict__ pool_count, const float *__restrict__ lambda,
-    const float *__restrict__ sigma, int H, int N, int K, int cap, int fs_mode,
+    const float *__restrict__ sigma, int H, int N, int cap, int fs_mode,
     int32_t *__restrict__ sel, float *__restrict__ sel_score, int *err) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem =
@@ -85,13 +90,17 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
   const int r = tid;  // query row of a scoring thread
   const int n = b0 + r;
   const float lam = lambda[h], sig_s = sigma[h] * (1.0f / kS);
-  float bu[kMaxK];
-  int bc[kMaxK];
+  // ranked top-K (u desc, c asc) in registers; (wu, wc) mirrors the K-th
+  // entry so that most candidates are rejected by one comparison
+  float bu[K];
+  int bc[K];
 #pragma unroll
-  for (int i = 0; i < kMaxK; ++i) {
+  for (int i = 0; i < K; ++i) {
     bu[i] = -INFINITY;
     bc[i] = 0x7fffffff;
   }
+  float wu = -INFINITY;
+  int wc = 0x7fffffff;
   int nvalid = 0;
   bool ok = true;
 
@@ -166,31 +175,25 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
           if (jj >= jn) break;
           const int c = s_c[j0 + jj];
           if (c < 0) continue;
-          const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
-          const float g = x < 4.0f ? erff(x) : 1.0f;
-          float u = __uint_as_float(d[jj]) + lam * s_a[j0 + jj] * g;
-          int cu = c;
           ++nvalid;
-          float wu = bu[0];
-          int wc = bc[0];
+          const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
+          const float g = x < 4.0f ? erf_bias(x) : 1.0f;
+          float u = __uint_as_float(d[jj]) + lam * s_a[j0 + jj] * g;
+          if (!ranks_before(u, c, wu, wc)) continue;
+          int cu = c;
 #pragma unroll
-          for (int i = 1; i < kMaxK; ++i)
-            if (i < K) {
-              wu = bu[i];
-              wc = bc[i];
-            }
-          if (!ranks_before(u, cu, wu, wc)) continue;
-#pragma unroll
-          for (int i = 0; i < kMaxK; ++i) {
-            if (i < K && ranks_before(u, cu, bu[i], bc[i])) {
-              const float tu = bu[i];
-              const int tcc = bc[i];
-              bu[i] = u;
-              bc[i] = cu;
+          for (int k = 0; k < K; ++k) {
+            if (ranks_before(u, cu, bu[k], bc[k])) {
+              const float tu = bu[k];
+              const int tcc = bc[k];
+              bu[k] = u;
+              bc[k] = cu;
               u = tu;
               cu = tcc;
             }
           }
+          wu = bu[K - 1];
+          wc = bc[K - 1];
         }
       }
     }
@@ -199,12 +202,10 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
   }
   if (warp < 4 && ok) {
 #pragma unroll
-    for (int i = 0; i < kMaxK; ++i) {
-      if (i < K) {
-        const bool valid = i < nvalid;
-        sel[(head + n) * K + i] = valid ? bc[i] : -1;
-        if (sel_score) sel_score[(head + n) * K + i] = valid ? bu[i] : 0.f;
-      }
+    for (int i = 0; i < K; ++i) {
+      const bool valid = i < nvalid;
+      sel[(head + n) * K + i] = valid ? bc[i] : -1;
+      if (sel_score) sel_score[(head + n) * K + i] = valid ? bu[i] : 0.f;
     }
   }
   if (warp == 4) {
@@ -220,13 +221,28 @@ cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
                           int32_t *sel, float *sel_score, int *err, cudaStream_t st) {
   const int smem = 16384 + 3 * chunk_rows(fs_mode ? 1 : 0, cap) * 128 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k3_select_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   dim3 grid(sh.nblk(), sh.BH());
-  k3_select_tc_kernel<<<grid, kThreads, smem, st>>>(
-      static_cast<const __nv_bfloat16 *>(q), kbar, amax, pool, pool_count, lambda, sigma, sh.H,
-      sh.N, K, cap, fs_mode ? 1 : 0, sel, sel_score, err);
+  const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(q);
+  const int fsm = fs_mode ? 1 : 0;
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(qb, kbar, amax, pool, pool_count, lambda, sigma, sh.H,
+                                       sh.N, cap, fsm, sel, sel_score, err);
+    return cudaSuccess;
+  };
+  cudaError_t e;
+  switch (K) {
+    case 1: e = go(k3_select_tc_kernel<1>); break;
+    case 2: e = go(k3_select_tc_kernel<2>); break;
+    case 3: e = go(k3_select_tc_kernel<3>); break;
+    case 4: e = go(k3_select_tc_kernel<4>); break;
+    case 5: e = go(k3_select_tc_kernel<5>); break;
+    case 6: e = go(k3_select_tc_kernel<6>); break;
+    case 7: e = go(k3_select_tc_kernel<7>); break;
+    default: e = go(k3_select_tc_kernel<8>); break;
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

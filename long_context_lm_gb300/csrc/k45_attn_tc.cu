@@ -1,0 +1,868 @@
+// k45_attn_tc.cu -- both attention branches of FS-L on the 5th-generation
+// tensor cores (tcgen05 + TMEM), with the branch mix in the epilogue.
+//
+// FreeSolo (paper.rainbus.top summary, 方法步骤详情 ② window branch, ⑥ "选中
+// token 上做 NoPE softmax 再 RMSNorm，与局部分支相加", 前置知识 RoPE / NoPE;
+// ai.info summary, "Methodology in Plain English"):
+//     o_win[n]  = softmax_j((R(n) q_n . R(j) k_j) / sqrt(d)) v_j,  j in [n-w+1, n]
+//     o_long[n] = RMSNorm(softmax_t(q_n . k_t / sqrt(d)) v_t),     t in the K
+//                 selected cells of n (no rotation), 0 if none
+//     out[n]    = o_win[n] + mix_h * o_long[n].
+//
+// Persistent kernel: one CTA per SM walks 128-query tiles (q-tiles).  Each
+// q-tile is a list of 128-key tiles: first the window tiles covering
+// [b - w + 1, b + 127], then the "long" tiles, each gathering four of the
+// cells that any query of the tile selected (their union, built per q-tile).
+// Sixteen warps with fixed roles and mbarrier hand-offs; every counter runs
+// across q-tiles, so producers start the next q-tile while the softmax
+// finishes the current one:
+//   warps 0-7   softmax + epilogue: warp w owns TMEM lanes / query rows
+//               32*(w%4).. and key columns 64*(w/4).. of each key tile; the
+//               two warps of a row block exchange row maxima through shared
+//               memory (one named barrier per tile)
+//   warp  8     TMEM allocation; lane 0 issues the S = Q.K^T MMAs
+//   warp  9     lane 0 issues the P.V MMAs (one issuing thread sustains about
+//               one tcgen05.mma per ~100 cycles, hence two issuers)
+//   warp  10    lane 0: TMA producer (contiguous window tiles; gathered cells)
+//   warp  11    builds the union of the q-tile's selected cells
+//   warps 12-15 rotate the queries and every window key tile, in place
+// TMEM: S double-buffered (2 x 128 columns), P and P_lo (64 columns each of
+// bf16 pairs: the A operand of P.V), O_win and O_long (64 columns each).
+//
+// Precision.  Window: RoPE is applied relative to the q-tile's first position
+// b (q_n.k_j after rotations by n-b and j-b equals the absolute product), the
+// rotated q and k are split into bf16 hi + lo halves and S takes three MMA
+// chains (hi.hi + hi.lo + lo.hi): a single bf16 rounding of the rotated
+// vectors exceeds the output tolerance on lognormal keys.  Long branch: q and
+// k are exact bf16, so S is one chain; P is split into bf16 hi + lo halves
+// (two P.V chains) because RMSNorm rescales the branch output and would
+// amplify a plain bf16 rounding of P.
+#include <cuda.h>
+
+#include "fs_common.cuh"
+#include "fs_internal.h"
+#include "tc05.cuh"
+
+namespace fs {
+namespace {
+
+constexpr int kKT = 128;          // keys per tile
+constexpr int kRing = 3;          // key / value ring depth
+constexpr int kThreads = 512;
+constexpr int kRotBase = 384;     // first rotation thread (warps 12-15)
+constexpr int kRotThreads = 128;  // one 64-element row each
+constexpr int kT64Stride = 272;   // bytes per row of the r*theta table (padded: no bank conflicts)
+constexpr int kMaxSel = kBq * kMaxK;
+
+// shared-memory layout, offsets from a 1024-byte aligned base
+constexpr uint32_t kOffQ = 0;                          // rotated query [hi 16 KB, lo 16 KB]
+constexpr uint32_t kOffQR = 32768;                     // raw query 16 KB
+constexpr uint32_t kOffK = 49152;                      // kRing x [hi 16 KB, lo 16 KB]
+constexpr uint32_t kOffV = kOffK + kRing * 32768;      // kRing x 16 KB
+constexpr uint32_t kOffT64 = kOffV + kRing * 16384;    // 64 rows x 272 B
+constexpr uint32_t kOffUL = kOffT64 + 64 * kT64Stride; // union list: kMaxSel int32
+constexpr uint32_t kOffRS = kOffUL + kMaxSel * 4;      // per row / pick: union slot, uint16
+constexpr uint32_t kOffTU = kOffRS + kMaxSel * 2;      // rows of 64*u*theta, 256 B each
+
+// TMEM columns
+constexpr uint32_t kColS = 0, kColP = 256, kColPL = 320, kColOW = 384, kColOL = 448;
+constexpr uint32_t kTmemCols = 512;
+
+struct Barriers {
+  uint64_t q_full, q_empty;
+  uint64_t raw_full[kRing];  // TMA: key and value tile landed
+  uint64_t kt_full[kRing];   // key tile rotated (window) / landed (long)
+  uint64_t k_empty[kRing];   // S MMAs of the tile done
+  uint64_t v_empty[kRing];   // P.V MMAs of the tile done
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done;
+  uint64_t o_done, o_free;
+  uint64_t u_full, u_free;   // union of the q-tile's cells built / consumed
+  uint64_t fin[2];
+  uint32_t tmem;
+  int nu;                    // cells in the current union
+  float xmax[2][128];        // per-half row maxima of the current tile
+  float xsum[2][128];        // per-half partial sums exchanged in the epilogue
+};
+
+struct Params {
+  const __nv_bfloat16 *q;
+  const int32_t *sel;      // [BH, N, K] selected cells (long branch)
+  const float *o_long_in;  // window-only mode: branch to mix in (nullable)
+  const float *mix;
+  const float2 *rel;       // (cos, sin) of o*theta_i, row o + rel_off
+  int rel_off, umin;
+  int H, N, w, K, nblk, nitems;
+  int has_window, has_long, write_long;  // write_long: output RMSNorm(o_long) only
+  float rms_eps;
+  size_t nrows;            // BH * N (first out-of-range key row: zero fill)
+  float *out;
+  int *err;
+};
+
+__device__ __forceinline__ bool wait_nth(uint64_t *bar, uint32_t k, int *err) {
+  return tc::mbar_wait(bar, k & 1, err);
+}
+
+struct Item {
+  int bh, b0, kt0, nw;  // nw: window tiles
+};
+__device__ __forceinline__ Item item_of(const Params &p, int g) {
+  Item it;
+  it.bh = g / p.nblk;
+  it.b0 = (g % p.nblk) * kBq;
+  it.kt0 = max(0, it.b0 - p.w + 1) / kKT * kKT;
+  it.nw = p.has_window ? (it.b0 + kBq - it.kt0) / kKT : 0;
+  return it;
+}
+__device__ __forceinline__ int long_tiles(const Barriers &bar, const Params &p) {
+  return p.has_long ? (bar.nu + 3) / 4 : 0;
+}
+
+// --------------------------------------------------------------------------
+// RoPE rotation (window tiles)
+// --------------------------------------------------------------------------
+// Rotate half of one 64-element row in place: pairs i in [16*half, 16*half+16)
+// (dims 16*half.. and 32+16*half..), angles composed from rows t64r (offset
+// mod 64) and tur (64*u) by the angle-sum identity.  The raw row is read from
+// `hi` (chunks 2*half, 2*half+1, 4+2*half, 5+2*half) and the rotated bf16
+// hi / lo halves are written back to the same chunks of `hi` and `lo`.
+__device__ __forceinline__ void rotate_half_row(unsigned char *hi, unsigned char *lo, int r,
+                                                int half, const float2 *t64r,
+                                                const float2 *tur) {
+  uint4 xa[2], xb[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    xa[k] = *reinterpret_cast<const uint4 *>(hi + swz128(r, 2 * half + k));
+    xb[k] = *reinterpret_cast<const uint4 *>(hi + swz128(r, 4 + 2 * half + k));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t wa[4] = {xa[k].x, xa[k].y, xa[k].z, xa[k].w};
+    const uint32_t wb[4] = {xb[k].x, xb[k].y, xb[k].z, xb[k].w};
+    uint32_t ah[4], al[4], bh[4], bl[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i0 = 16 * half + 8 * k + 2 * j;  // first pair of this 32-bit word
+      const float4 rr = *reinterpret_cast<const float4 *>(t64r + i0);
+      const float4 bb = *reinterpret_cast<const float4 *>(tur + i0);
+      float y0[2], y1[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float cr = e ? rr.z : rr.x, sr = e ? rr.w : rr.y;
+        const float cb = e ? bb.z : bb.x, sb = e ? bb.w : bb.y;
+        const float c = fmaf(cb, cr, -sb * sr), sn = fmaf(sb, cr, cb * sr);
+        const float x0 = e ? bf16_hi(wa[j]) : bf16_lo(wa[j]);
+        const float x1 = e ? bf16_hi(wb[j]) : bf16_lo(wb[j]);
+        y0[e] = fmaf(x0, c, -x1 * sn);
+        y1[e] = fmaf(x0, sn, x1 * c);
+      }
+      ah[j] = pack_bf16(y0[0], y0[1]);
+      al[j] = pack_bf16(y0[0] - bf16_lo(ah[j]), y0[1] - bf16_hi(ah[j]));
+      bh[j] = pack_bf16(y1[0], y1[1]);
+      bl[j] = pack_bf16(y1[0] - bf16_lo(bh[j]), y1[1] - bf16_hi(bh[j]));
+    }
+    const int ca = 2 * half + k, cb = 4 + 2 * half + k;
+    *reinterpret_cast<uint4 *>(hi + swz128(r, ca)) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+    *reinterpret_cast<uint4 *>(hi + swz128(r, cb)) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+    *reinterpret_cast<uint4 *>(lo + swz128(r, ca)) = make_uint4(al[0], al[1], al[2], al[3]);
+    *reinterpret_cast<uint4 *>(lo + swz128(r, cb)) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+  }
+}
+
+// Rotate row r (64 elements, in place) by the relative offset o.
+__device__ __forceinline__ void rotate_row(unsigned char *hi, unsigned char *lo, int r, int o,
+                                           const unsigned char *smem, int umin) {
+  const float2 *t64r = reinterpret_cast<const float2 *>(smem + kOffT64 + (o & 63) * kT64Stride);
+  const float2 *tur =
+      reinterpret_cast<const float2 *>(smem + kOffTU) + ((o >> 6) - umin) * (kD / 2);
+  rotate_half_row(hi, lo, r, 0, t64r, tur);
+  rotate_half_row(hi, lo, r, 1, t64r, tur);
+}
+
+// --------------------------------------------------------------------------
+// roles
+// --------------------------------------------------------------------------
+
+__device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t base) {
+  const uint32_t id_qk = tc::idesc_bf16(128, kKT, 0);
+  const uint64_t dqh = tc::desc_sw128(base + kOffQ), dql = tc::desc_sw128(base + kOffQ + 16384);
+  const uint64_t dqr = tc::desc_sw128(base + kOffQR);
+  uint32_t T = 0, i = 0;
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
+    if (!wait_nth(&bar.q_full, i, p.err)) return;
+    int nl = 0;
+    for (int t = 0;; ++t, ++T) {
+      if (t == it.nw) {  // the window tiles do not wait for the union
+        if (!wait_nth(&bar.u_full, i, p.err)) return;
+        nl = long_tiles(bar, p);
+        tc::mbar_arrive(&bar.u_free);
+      }
+      if (t >= it.nw + nl) break;
+      const int slot = T % kRing, b = T & 1;
+      if (!wait_nth(&bar.kt_full[slot], T / kRing, p.err)) return;
+      if (T >= 2 && !wait_nth(&bar.s_free[b], T / 2 - 1, p.err)) return;
+      tc::fence_after_sync();
+      const uint32_t kh = base + kOffK + slot * 32768;
+      const uint64_t dkh = tc::desc_sw128(kh), dkl = tc::desc_sw128(kh + 16384);
+      const uint32_t s_col = tmem + kColS + 128 * b;
+      if (t < it.nw) {  // window: three split-precision chains
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const uint64_t a = part == 2 ? dql : dqh, bd = part == 1 ? dkl : dkh;
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k)
+            tc::mma_ss(s_col, a + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), id_qk,
+                       (part > 0 || k > 0) ? 1u : 0u);
+        }
+      } else {  // long: unrotated query against the gathered cells
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k)
+          tc::mma_ss(s_col, dqr + (uint64_t)(2 * k), dkh + (uint64_t)(2 * k), id_qk,
+                     k > 0 ? 1u : 0u);
+      }
+      tc::mma_commit(&bar.s_full[b]);
+      tc::mma_commit(&bar.k_empty[slot]);
+    }
+    tc::mma_commit(&bar.q_empty);
+  }
+}
+
+__device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t base) {
+  const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);
+  uint32_t T = 0, i = 0;
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
+    // the accumulators are reused once the previous epilogue has read them
+    if (i > 0 && !wait_nth(&bar.o_free, i - 1, p.err)) return;
+    int nl = 0;
+    for (int t = 0;; ++t, ++T) {
+      if (t == it.nw) {
+        if (!wait_nth(&bar.u_full, i, p.err)) return;
+        nl = long_tiles(bar, p);
+        tc::mbar_arrive(&bar.u_free);
+      }
+      if (t >= it.nw + nl) break;
+      const int slot = T % kRing;
+      if (!wait_nth(&bar.p_full, T, p.err)) return;
+      tc::fence_after_sync();
+      const uint64_t dv = tc::desc_sw128(base + kOffV + slot * 16384);
+      if (t < it.nw) {
+#pragma unroll
+        for (int k = 0; k < kKT / 16; ++k)
+          tc::mma_ts(tmem + kColOW, tmem + kColP + 8 * k, dv + (uint64_t)(k * 128), id_pv,
+                     (t > 0 || k > 0) ? 1u : 0u);
+      } else {
+        const bool first = t == it.nw;
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int k = 0; k < kKT / 16; ++k)
+            tc::mma_ts(tmem + kColOL, tmem + (part ? kColPL : kColP) + 8 * k,
+                       dv + (uint64_t)(k * 128), id_pv, (!first || part > 0 || k > 0) ? 1u : 0u);
+      }
+      tc::mma_commit(&bar.pv_done);
+      tc::mma_commit(&bar.v_empty[slot]);
+    }
+    tc::mma_commit(&bar.o_done);
+  }
+}
+
+__device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
+                         const CUtensorMap *tk, const CUtensorMap *tv, const CUtensorMap *ck,
+                         const CUtensorMap *cv) {
+  uint32_t T = 0, i = 0;
+  const int *ul = reinterpret_cast<const int *>(smem + kOffUL);
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
+    const int row0 = it.bh * p.N;
+    int nl = 0;
+    for (int t = 0;; ++t, ++T) {
+      if (t == it.nw) {
+        if (!wait_nth(&bar.u_full, i, p.err)) return;
+        nl = long_tiles(bar, p);
+      }
+      if (t >= it.nw + nl) break;
+      const int slot = T % kRing;
+      if (T >= kRing) {
+        if (!wait_nth(&bar.k_empty[slot], T / kRing - 1, p.err)) return;
+        if (!wait_nth(&bar.v_empty[slot], T / kRing - 1, p.err)) return;
+      }
+      unsigned char *kd = smem + kOffK + slot * 32768, *vd = smem + kOffV + slot * 16384;
+      tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 2 * kKT * kD * 2);
+      if (t < it.nw) {
+        const int y = row0 + it.kt0 + t * kKT;
+        tc::tma_load_2d(kd, tk, &bar.raw_full[slot], 0, y);
+        tc::tma_load_2d(vd, tv, &bar.raw_full[slot], 0, y);
+      } else {
+        // four cells of the union; a missing cell reads zeros from past the
+        // last row, so stale data never meets a zero probability
+        const int lt = t - it.nw;
+#pragma unroll
+        for (int cs = 0; cs < 4; ++cs) {
+          const int u = 4 * lt + cs;
+          const int y = u < bar.nu ? row0 + ul[u] * kS : (int)p.nrows;
+          tc::tma_load_2d(kd + cs * 4096, ck, &bar.raw_full[slot], 0, y);
+          tc::tma_load_2d(vd + cs * 4096, cv, &bar.raw_full[slot], 0, y);
+        }
+      }
+    }
+    tc::mbar_arrive(&bar.u_free);  // the union list is no longer read
+  }
+}
+
+// Union of the q-tile's selected cells, sorted ascending, by repeated
+// extraction of the smallest remaining id (cheap: the union is small); each
+// selection's slot in the union is recorded for the softmax masks.
+__device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) {
+  const int lane = threadIdx.x & 31;
+  int *ul = reinterpret_cast<int *>(smem + kOffUL);
+  uint16_t *rs = reinterpret_cast<uint16_t *>(smem + kOffRS);
+  uint32_t i = 0;
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
+    if (i > 0 && !wait_nth(&bar.u_free, i - 1, p.err)) return;
+    int nu = 0;
+    if (p.has_long) {
+      const int A = it.b0 / kS;  // cells ending at or before the block start
+      const int nsel = kBq * p.K;
+      const int32_t *src = p.sel + ((size_t)it.bh * p.N + it.b0) * p.K;
+      int v[kMaxSel / 32];
+#pragma unroll
+      for (int e = 0; e < kMaxSel / 32; ++e) {
+        const int idx = e * 32 + lane;
+        int c = idx < nsel ? src[idx] : -1;
+        v[e] = (c >= 0 && c < A) ? c : 0x7fffffff;
+        if (idx < nsel) rs[idx] = 0xffff;
+      }
+      while (true) {
+        int mn = 0x7fffffff;
+#pragma unroll
+        for (int e = 0; e < kMaxSel / 32; ++e) mn = min(mn, v[e]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        if (mn == 0x7fffffff) break;
+#pragma unroll
+        for (int e = 0; e < kMaxSel / 32; ++e)
+          if (v[e] == mn) {
+            rs[e * 32 + lane] = (uint16_t)nu;
+            v[e] = 0x7fffffff;
+          }
+        if (lane == 0) ul[nu] = mn;
+        ++nu;
+      }
+    }
+    if (lane == 0) bar.nu = nu;
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bar.u_full);
+  }
+}
+
+__device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int r) {
+  uint32_t T = 0, i = 0;
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
+    // query row r: fetch it first, then wait until the previous q-tile's S
+    // MMAs no longer read the query tiles
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + r) * kD);
+    uint4 raw[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) raw[c] = __ldg(src + c);
+    if (i > 0 && !wait_nth(&bar.q_empty, i - 1, p.err)) return;
+    unsigned char *qh = smem + kOffQ, *qr = smem + kOffQR;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      *reinterpret_cast<uint4 *>(qr + swz128(r, c)) = raw[c];
+      *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
+    }
+    if (p.has_window) rotate_row(qh, qh + 16384, r, r, smem, p.umin);
+    tc::fence_async_smem();
+    tc::mbar_arrive(&bar.q_full);
+    // every tile passes the rotation threads so the per-slot phases line up;
+    // window tiles are rotated, long tiles only wait for their data
+    int nl = 0;
+    for (int t = 0;; ++t, ++T) {
+      if (t == it.nw) {
+        if (!wait_nth(&bar.u_full, i, p.err)) return;
+        nl = long_tiles(bar, p);
+        __syncwarp();
+        if ((r & 31) == 0) tc::mbar_arrive(&bar.u_free);
+      }
+      if (t >= it.nw + nl) break;
+      const int slot = T % kRing;
+      if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
+      if (t < it.nw) {
+        unsigned char *kh = smem + kOffK + slot * 32768;
+        rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
+        tc::fence_async_smem();
+      }
+      tc::mbar_arrive(&bar.kt_full[slot]);
+    }
+  }
+}
+
+// A 32-column chunk of a score row held in registers.  The softmax reads a
+// warp's 64 columns as two chunks, twice (max pass, then exp pass), which
+// keeps the register footprint at 32 scores per thread.
+constexpr uint32_t kNegInf = 0xff800000u;
+
+// window: columns outside [lo, hi] (tile columns) become -inf; the test is
+// uniform across the warp except in a chunk a triangular edge crosses
+__device__ __forceinline__ void mask_window(uint32_t (&x)[32], int lo, int hi, int c0) {
+  const bool full = lo <= c0 && hi >= c0 + 31;
+  const bool empty = hi < c0 || lo > c0 + 31;
+  if (__all_sync(0xffffffffu, full)) return;
+  if (__all_sync(0xffffffffu, empty)) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) x[c] = kNegInf;
+    return;
+  }
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const int col = c0 + c;
+    if (col < lo || col > hi) x[c] = kNegInf;
+  }
+}
+
+// Load chunk ch (columns 32*ch.. of this warp's half) and apply the mask:
+// window band, or (long tile) the whole chunk is one cell the row picked or not.
+__device__ __forceinline__ void load_chunk(uint32_t s_addr, int ch, bool is_long, int lo, int hi,
+                                           int col0, bool keep, uint32_t (&x)[32]) {
+  tc::tmem_ld32(s_addr + 32 * ch, x);
+  tc::tmem_wait_ld();
+  if (!is_long) {
+    mask_window(x, lo, hi, col0 + 32 * ch);
+  } else if (!keep) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) x[c] = kNegInf;
+  }
+}
+
+__device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
+  float mx[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) mx[j] = __uint_as_float(x[j]);
+#pragma unroll
+  for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(x[c]));
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// 2^(s*sl2 - m) for one chunk, written as bf16 pairs into 16 P columns (and,
+// with kSplit, the rounding remainders into 16 P_lo columns), 16 scores at a
+// time; returns the sum of the unrounded values.
+template <bool kSplit>
+__device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_addr,
+                                           uint32_t pl_addr, float sl2, float m) {
+  float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int h16 = 0; h16 < 2; ++h16) {
+    uint32_t pk[8], pl[8];
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const float e0 = tc::ex2(fmaf(__uint_as_float(x[16 * h16 + c]), sl2, -m));
+      const float e1 = tc::ex2(fmaf(__uint_as_float(x[16 * h16 + c + 1]), sl2, -m));
+      part[(c >> 1) & 3] += e0 + e1;
+      pk[c / 2] = pack_bf16(e0, e1);
+      if (kSplit) pl[c / 2] = pack_bf16(e0 - bf16_lo(pk[c / 2]), e1 - bf16_hi(pk[c / 2]));
+    }
+    tc::tmem_st8(p_addr + 8 * h16, pk);
+    if (kSplit) tc::tmem_st8(pl_addr + 8 * h16, pl);
+  }
+  return (part[0] + part[1]) + (part[2] + part[3]);
+}
+
+__device__ __forceinline__ void pair_sync(int quarter) {
+  asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
+}
+
+__device__ __forceinline__ void rescale(uint32_t addr, float alpha) {
+  uint32_t o[32];
+  tc::tmem_ld32(addr, o);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+  tc::tmem_st32(addr, o);
+}
+
+__device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsigned char *smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int r = quarter * 32 + lane;  // query row of this thread
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const uint32_t p_addr = tmem + kColP + 32 * half + lane_base;
+  const uint32_t pl_addr = tmem + kColPL + 32 * half + lane_base;
+  const uint32_t ow_addr = tmem + kColOW + 32 * half + lane_base;
+  const uint32_t ol_addr = tmem + kColOL + 32 * half + lane_base;
+  const uint16_t *rs = reinterpret_cast<const uint16_t *>(smem + kOffRS);
+  const float sl2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
+  uint32_t T = 0, i = 0;
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
+    const int n = it.b0 + r;
+    float mw = -INFINITY, lw = 0.f, ml = -INFINITY, ll = 0.f;
+    int nl = 0;
+    uint32_t pick[kMaxK / 2];  // this row's union slots, two 16-bit slots per word
+    for (int t = 0;; ++t, ++T) {
+      if (t == it.nw) {
+        if (!wait_nth(&bar.u_full, i, p.err)) return;
+        nl = long_tiles(bar, p);
+#pragma unroll
+        for (int k = 0; k < kMaxK / 2; ++k) {
+          const uint32_t a = (2 * k < p.K) ? rs[r * p.K + 2 * k] : 0xffffu;
+          const uint32_t b = (2 * k + 1 < p.K) ? rs[r * p.K + 2 * k + 1] : 0xffffu;
+          pick[k] = a | (b << 16);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar.u_free);  // union data read
+      }
+      if (t >= it.nw && t >= it.nw + nl) break;
+      const bool is_long = t >= it.nw;
+      const int b = T & 1;
+      const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
+      if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
+      tc::fence_after_sync();
+      bool any, cell[2] = {false, false};
+      int lo = 0, hi = -1;
+      if (!is_long) {
+        const int kt = it.kt0 + t * kKT;
+        lo = max(0, n - p.w + 1 - kt);
+        hi = min(kKT - 1, n - kt);
+        any = __any_sync(0xffffffffu, lo <= hi && hi >= 64 * half && lo <= 64 * half + 63);
+      } else {
+        const uint32_t u0 = 4 * (t - it.nw) + 2 * half;
+#pragma unroll
+        for (int k = 0; k < kMaxK / 2; ++k) {
+          const uint32_t a = pick[k] & 0xffffu, b = pick[k] >> 16;
+          cell[0] |= (a == u0) || (b == u0);
+          cell[1] |= (a == u0 + 1) || (b == u0 + 1);
+        }
+        any = __any_sync(0xffffffffu, cell[0] || cell[1]);
+      }
+      float mx = -INFINITY;
+      if (any) {
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t x[32];
+          load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
+          mx = fmaxf(mx, max_chunk(x));
+        }
+      }
+      bar.xmax[half][r] = mx;
+      pair_sync(quarter);
+      mx = fmaxf(mx, bar.xmax[half ^ 1][r]);
+      pair_sync(quarter);  // the slot is rewritten next tile
+      const float m = is_long ? ml : mw;
+      float l = is_long ? ll : lw;
+      const float mnew = fmaxf(m, mx * sl2);
+      const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
+      // P and the accumulators belong to the previous P.V until it completes
+      if (T > 0 && !wait_nth(&bar.pv_done, T - 1, p.err)) return;
+      tc::fence_after_sync();
+      const float muse = mnew == -INFINITY ? 0.f : mnew;
+      l = l * alpha;
+      if (any) {
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t x[32];
+          load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
+          l += is_long ? exp_chunk<true>(x, p_addr + 16 * ch, pl_addr + 16 * ch, sl2, muse)
+                       : exp_chunk<false>(x, p_addr + 16 * ch, pl_addr + 16 * ch, sl2, muse);
+        }
+      } else {
+        uint32_t z[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) z[c] = 0u;
+        tc::tmem_st16(p_addr, z);
+        tc::tmem_st16(p_addr + 16, z);
+        if (is_long) {
+          tc::tmem_st16(pl_addr, z);
+          tc::tmem_st16(pl_addr + 16, z);
+        }
+      }
+      // both passes have read S: the buffer may be refilled
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar.s_free[b]);
+      if (is_long) {
+        ml = mnew;
+        ll = l;
+      } else {
+        mw = mnew;
+        lw = l;
+      }
+      const bool first = is_long ? t == it.nw : t == 0;
+      if (!first && __any_sync(0xffffffffu, alpha != 1.f)) rescale(is_long ? ol_addr : ow_addr, alpha);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar.p_full);
+    }
+    // ---- epilogue (TMEM read in 16-column pieces to keep registers low)
+    if (!wait_nth(&bar.o_done, i, p.err)) return;
+    tc::fence_after_sync();
+    // long branch: O_long / l_long, RMSNorm over the 64 columns (two halves)
+    float lo_scale = 0.f;
+    if (p.has_long) {
+      bar.xsum[half][r] = ll;
+      pair_sync(quarter);
+      const float ltot = ll + bar.xsum[half ^ 1][r];
+      pair_sync(quarter);
+      const float invl = ltot > 0.f ? 1.f / ltot : 0.f;
+      float ss = 0.f;
+      if (nl > 0) {
+#pragma unroll
+        for (int c16 = 0; c16 < 2; ++c16) {
+          uint32_t o[16];
+          tc::tmem_ld16(ol_addr + 16 * c16, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float y = __uint_as_float(o[c]) * invl;
+            ss = fmaf(y, y, ss);
+          }
+        }
+      }
+      bar.xsum[half][r] = ss;
+      pair_sync(quarter);
+      ss += bar.xsum[half ^ 1][r];
+      pair_sync(quarter);
+      lo_scale = (nl > 0 && ltot > 0.f) ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
+    }
+    float wscale = 0.f;
+    if (it.nw > 0) {
+      bar.xsum[half][r] = lw;
+      pair_sync(quarter);
+      wscale = 1.f / (lw + bar.xsum[half ^ 1][r]);
+      pair_sync(quarter);
+    }
+    const size_t row = (size_t)it.bh * p.N + n;
+    float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD + 32 * half);
+    const float mh = p.mix ? p.mix[it.bh % p.H] : 0.f;
+    const bool use_long = lo_scale != 0.f;
+    const float4 *oin = (!p.write_long && !use_long && p.o_long_in)
+        ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD + 32 * half) : nullptr;
+    const float ls = p.write_long ? lo_scale : mh * lo_scale;
+#pragma unroll
+    for (int c16 = 0; c16 < 2; ++c16) {
+      uint32_t ow[16], ol[16];
+      if (!p.write_long && it.nw > 0) tc::tmem_ld16(ow_addr + 16 * c16, ow);
+      if (use_long) tc::tmem_ld16(ol_addr + 16 * c16, ol);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!p.write_long && it.nw > 0)
+          v = make_float4(__uint_as_float(ow[4 * c4]) * wscale, __uint_as_float(ow[4 * c4 + 1]) * wscale,
+                          __uint_as_float(ow[4 * c4 + 2]) * wscale,
+                          __uint_as_float(ow[4 * c4 + 3]) * wscale);
+        if (use_long) {
+          v.x = fmaf(ls, __uint_as_float(ol[4 * c4]), v.x);
+          v.y = fmaf(ls, __uint_as_float(ol[4 * c4 + 1]), v.y);
+          v.z = fmaf(ls, __uint_as_float(ol[4 * c4 + 2]), v.z);
+          v.w = fmaf(ls, __uint_as_float(ol[4 * c4 + 3]), v.w);
+        } else if (oin) {
+          const float4 u4 = __ldg(oin + 4 * c16 + c4);
+          v.x = fmaf(mh, u4.x, v.x);
+          v.y = fmaf(mh, u4.y, v.y);
+          v.z = fmaf(mh, u4.z, v.z);
+          v.w = fmaf(mh, u4.w, v.w);
+        }
+        dst[4 * c16 + c4] = v;
+      }
+    }
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bar.o_free);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+    const __grid_constant__ CUtensorMap cmap_k, const __grid_constant__ CUtensorMap cmap_v,
+    const Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Barriers bar;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar.q_full, kRotThreads);
+    tc::mbar_init(&bar.q_empty, 1);
+    for (int i = 0; i < kRing; ++i) {
+      tc::mbar_init(&bar.raw_full[i], 1);
+      tc::mbar_init(&bar.kt_full[i], kRotThreads);
+      tc::mbar_init(&bar.k_empty[i], 1);
+      tc::mbar_init(&bar.v_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bar.s_full[b], 1);
+      tc::mbar_init(&bar.s_free[b], 8);
+      tc::mbar_init(&bar.fin[b], 1);
+    }
+    tc::mbar_init(&bar.p_full, 8);
+    tc::mbar_init(&bar.pv_done, 1);
+    tc::mbar_init(&bar.o_done, 1);
+    tc::mbar_init(&bar.o_free, 8);
+    tc::mbar_init(&bar.u_full, 1);
+    // the union may be rebuilt once every role has read it: 8 softmax warps,
+    // 4 rotation warps, the two issuers and the TMA thread
+    tc::mbar_init(&bar.u_free, 15);
+    tc::mbar_fence_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(&bar.tmem, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  // angle tables, staged once per CTA by the rotation warps (window only)
+  if (threadIdx.x >= kRotBase && p.has_window) {
+    const int r = threadIdx.x - kRotBase;
+    const float4 *rel = reinterpret_cast<const float4 *>(p.rel);
+    for (int i = r; i < 64 * 16; i += kRotThreads) {
+      const int row = i >> 4, part = i & 15;
+      *reinterpret_cast<float4 *>(smem + kOffT64 + row * kT64Stride + part * 16) =
+          __ldg(rel + (size_t)(row + p.rel_off) * 16 + part);
+    }
+    float4 *tu = reinterpret_cast<float4 *>(smem + kOffTU);
+    const int nu = 3 - p.umin;  // u in [umin, 2]
+    for (int i = r; i < nu * 16; i += kRotThreads) {
+      const int row = i >> 4, part = i & 15;
+      tu[i] = __ldg(rel + (size_t)(64 * (row + p.umin) + p.rel_off) * 16 + part);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bar.tmem;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp < 8) {
+    role_softmax(p, bar, tmem, smem);
+  } else if (warp == 8 || warp == 9) {
+    if (lane == 0) {
+      if (warp == 8)
+        role_qk(p, bar, tmem, sbase);
+      else
+        role_pv(p, bar, tmem, sbase);
+      tc::mma_commit(&bar.fin[warp - 8]);  // every MMA this thread issued has completed
+      tc::mbar_wait(&bar.fin[warp - 8], 0, p.err);
+    }
+  } else if (warp == 10) {
+    if (lane == 0) role_tma(p, bar, smem, &tmap_k, &tmap_v, &cmap_k, &cmap_v);
+  } else if (warp == 11) {
+    role_union(p, bar, smem);
+  } else {
+    role_rotate(p, bar, smem, threadIdx.x - kRotBase);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+__global__ void rel_rope_table_kernel(float2 *__restrict__ tab, int rows, int off, double base) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * (kD / 2)) return;
+  const int row = idx / (kD / 2), i = idx % (kD / 2);
+  const double theta = pow(base, -2.0 * (double)i / (double)kD);
+  double s, c;
+  sincos((double)(row - off) * theta, &s, &c);
+  tab[idx] = make_float2((float)c, (float)s);
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// [rows, 64] bf16 row-major, boxes of box_rows x 64 with the 128-byte swizzle;
+// rows past the end read as zeros.
+bool make_rows_map(CUtensorMap *map, const void *ptr, size_t rows, int box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+int rel_offset(int w) { return (w + 127 + 63) / 64 * 64; }
+
+}  // namespace
+
+// Relative-angle table rows: offsets o in [-rel_offset, kBq + 64); the kernel
+// needs o*theta for o = 64*u (u >= umin) and o in [0, 64).
+size_t attn_table_bytes(int w) {
+  return (size_t)(rel_offset(w) + kBq + 64) * (kD / 2) * sizeof(float2);
+}
+
+cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
+  const Shape &sh = a.sh;
+  const int off = rel_offset(a.w);
+  const int rows = off + kBq + 64;
+  float2 *tab = static_cast<float2 *>(a.table);
+  rel_rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(tab, rows, off,
+                                                                      (double)a.rope_base);
+  CUtensorMap mk, mv, ck, cv;
+  const size_t nrows = (size_t)sh.BH() * sh.N;
+  if (!make_rows_map(&mk, a.k, nrows, kKT) || !make_rows_map(&mv, a.v, nrows, kKT) ||
+      !make_rows_map(&ck, a.k, nrows, kS) || !make_rows_map(&cv, a.v, nrows, kS))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.q = static_cast<const __nv_bfloat16 *>(a.q);
+  p.sel = a.sel;
+  p.o_long_in = a.o_long_in;
+  p.mix = a.mix;
+  p.rel = tab;
+  p.rel_off = off;
+  p.umin = -(off / 64);
+  p.H = sh.H;
+  p.N = sh.N;
+  p.w = a.w;
+  p.K = a.K;
+  p.nblk = sh.nblk();
+  p.nitems = sh.BH() * sh.nblk();
+  p.has_window = a.window ? 1 : 0;
+  p.has_long = a.sel ? 1 : 0;
+  p.write_long = a.write_long ? 1 : 0;
+  p.rms_eps = a.rms_eps;
+  p.nrows = nrows;
+  p.out = a.out;
+  p.err = a.err;
+  const uint32_t smem = kOffTU + (3 - p.umin) * 256 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fs_attn_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.nitems < sm_count() ? p.nitems : sm_count();
+  fs_attn_tc_kernel<<<grid, kThreads, smem, st>>>(mk, mv, ck, cv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fs

@@ -28,8 +28,8 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status"]
-FS_N_STAGES = 5
-STAGE_NAMES = ["cell_summary", "prune", "select", "readout", "window"]
+FS_N_STAGES = 4
+STAGE_NAMES = ["cell_summary", "prune", "select", "attention"]
 
 
 class fs_params(ctypes.Structure):
@@ -92,7 +92,7 @@ def load(build_if_stale: bool = True):
         L.fs_window_attn.argtypes = [P, P, P, I, P, P, I, I, I, I, PP, P, P, Z, P]
         L.fs_attention_fwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, Z, P]
         L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
-        L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 6
+        L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 5
         L.fs_check_status.argtypes = [P, P]
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
@@ -308,17 +308,17 @@ def fs_attention_fwd_traced(q, k, v, lam, sigma, mix, events, params=None, out=N
 
 def fs_workspace_view(ws, batch, H, N, d, params=None, dtype=FS_BF16):
     """Views of the intermediates an fs_attention_fwd call left in ``ws``:
-    dict with kbar, amax, pool, pool_count, sel, o_long."""
+    dict with kbar, amax, pool, pool_count, sel."""
     L = load()
     p = _params(params)
-    offs = [ctypes.c_size_t() for _ in range(6)]
+    offs = [ctypes.c_size_t() for _ in range(5)]
     _check(L.fs_workspace_view(batch, H, N, d, ctypes.byref(p), dtype,
                                *[ctypes.byref(o) for o in offs]), "fs_workspace_view")
     C, nblk = N // p.s, N // p.Bq
     spec = [("kbar", (batch, H, C, d), torch.float32), ("amax", (batch, H, C), torch.float32),
             ("pool", (batch, H, nblk, p.P + p.W), torch.int32),
             ("pool_count", (batch, H, nblk), torch.int32),
-            ("sel", (batch, H, N, p.K), torch.int32), ("o_long", (batch, H, N, d), torch.float32)]
+            ("sel", (batch, H, N, p.K), torch.int32)]
     res = {}
     for (name, shape, dtype_), off in zip(spec, offs):
         n = 1
