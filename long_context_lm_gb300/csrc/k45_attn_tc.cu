@@ -828,8 +828,12 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   const int off = rel_offset(a.w);
   const int rows = off + kBq + 64;
   float2 *tab = static_cast<float2 *>(a.table);
-  rel_rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(tab, rows, off,
-                                                                      (double)a.rope_base);
+  if (a.window) {  // the angle table is used (and written) by the window branch only
+    if (!tab) return cudaErrorInvalidValue;
+    rel_rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(tab, rows, off,
+                                                                        (double)a.rope_base);
+  }
+  if (!a.window && !a.sel) return cudaErrorInvalidValue;
   CUtensorMap mk, mv, ck, cv;
   const size_t nrows = (size_t)sh.BH() * sh.N;
   if (!make_rows_map(&mk, a.k, nrows, kKT) || !make_rows_map(&mv, a.v, nrows, kKT) ||
