@@ -123,20 +123,20 @@ def stage_work(wl, distinct_cells, sel_counts):
     K, cap = p["K"], p["P"] + p["W"]
     tok = BH * N
     work = {}
-    # K1: read k (bf16), write kbar (fp32) and amax
+    # cell summaries: read k (bf16), write kbar (fp32) and amax
     work["cell_summary"] = dict(bound="hbm", bytes=tok * d * 2 + BH * C * (d * 4 + 4))
-    # K2: read amax (per chunk sort + per block), write pools
+    # prune: read amax (chunk sort + per block), write pools
     work["prune"] = dict(bound="latency", bytes=BH * C * 4 * 2 + BH * nblk * (cap + 1) * 4)
-    # K3: q (bf16), pool ids, mean keys of pool cells once per block (fp32), sel out
-    work["select"] = dict(bound="alu", bytes=tok * d * 2 + BH * nblk * cap * (d * 4 + 8) + tok * K * 4,
+    # select: q (bf16), pool ids, mean keys of the pool cells once per block
+    # (fp32), sel out; flops: q.kbar for every candidate of every query
+    work["select"] = dict(bound="tensor", bytes=tok * d * 2 + BH * nblk * cap * (d * 4 + 8) + tok * K * 4,
                           flops=2.0 * d * float(sel_counts["cands"]))
-    # K4: q, sel, o_long out (fp32) + k/v of every distinct selected cell once
-    work["readout"] = dict(bound="hbm", bytes=tok * d * 2 + tok * K * 4 + tok * d * 4
-                           + distinct_cells * 32 * d * 2 * 2,
-                           flops=4.0 * d * float(sel_counts["tokens_read"]))
-    # K5: q, k, v (bf16), o_long in (fp32), out (fp32); flops of the window
-    work["window"] = dict(bound="tensor", bytes=tok * d * (2 * 3 + 4 + 4),
-                          flops=window_flops(BH, N, p["w"], d))
+    # attention (both branches + mix): q, k, v (bf16), sel, out (fp32), the k/v
+    # of every distinct selected cell once; flops: QK^T and PV over the window
+    # keys of every query plus the tokens of its selected cells
+    work["attention"] = dict(bound="tensor",
+                             bytes=tok * d * (2 * 3 + 4) + tok * K * 4 + distinct_cells * 32 * d * 2 * 2,
+                             flops=window_flops(BH, N, p["w"], d) + 4.0 * d * float(sel_counts["tokens_read"]))
     return work
 
 
@@ -254,9 +254,9 @@ def run_ours(args, rank, world, local_rank):
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
                 "frac": ach / pk["hbm"], "traffic": None, "peak_source": pk["source"]}
     # our kernels per step: cells 1, prune (sort, scan when >1 chunk, emit),
-    # select 1, readout 1, RoPE tables 1, window 1 (+3 roundings for fp32)
+    # select 1, RoPE angle table 1, attention 1 (+3 roundings for fp32)
     prune_launches = 0 if params.mode == fs.FS_MODE_FS else 2 + (1 if N // 32 > 64 else 0)
-    launches_per_step = 1 + prune_launches + 1 + 1 + 2 + (3 if code == fs.FS_FP32 else 0)
+    launches_per_step = 1 + prune_launches + 1 + 2 + (3 if code == fs.FS_FP32 else 0)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
