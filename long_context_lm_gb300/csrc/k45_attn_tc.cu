@@ -46,6 +46,25 @@
 namespace fs {
 namespace {
 
+// Pipeline timeline probe (builds with -DFS_TRACE only): clock64() stamps of
+// each role's hand-offs in CTA 0, event e of global tile / q-tile t at
+// [e*64 + t].
+#ifdef FS_TRACE
+__device__ long long *g_trace = nullptr;
+#define FS_TR(e, t)                                                                   \
+  do {                                                                                \
+    if (g_trace && blockIdx.x == 0 && (t) < 64) g_trace[(e) * 64 + (t)] = clock64(); \
+  } while (0)
+__device__ __forceinline__ bool g_trace_nu_enabled() { return g_trace && blockIdx.x == 0; }
+__device__ __forceinline__ void g_trace_nu(int i, int nu) { g_trace[9 * 64 + i] = nu; }
+#else
+__device__ __forceinline__ bool g_trace_nu_enabled() { return false; }
+__device__ __forceinline__ void g_trace_nu(int, int) {}
+#define FS_TR(e, t) \
+  do {              \
+  } while (0)
+#endif
+
 constexpr int kKT = 128;          // keys per tile
 constexpr int kRing = 3;          // key / value ring depth
 constexpr int kThreads = 512;
@@ -224,6 +243,7 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       }
       tc::mma_commit(&bar.s_full[b]);
       tc::mma_commit(&bar.k_empty[slot]);
+      FS_TR(2, T);
     }
     tc::mma_commit(&bar.q_empty);
   }
@@ -264,6 +284,7 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       }
       tc::mma_commit(&bar.pv_done);
       tc::mma_commit(&bar.v_empty[slot]);
+      FS_TR(5, T);
     }
     tc::mma_commit(&bar.o_done);
   }
@@ -285,6 +306,7 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
       }
       if (t >= it.nw + nl) break;
       const int slot = T % kRing;
+      FS_TR(0, T);
       if (T >= kRing) {
         if (!wait_nth(&bar.k_empty[slot], T / kRing - 1, p.err)) return;
         if (!wait_nth(&bar.v_empty[slot], T / kRing - 1, p.err)) return;
@@ -323,6 +345,7 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
     if (i > 0 && !wait_nth(&bar.u_free, i - 1, p.err)) return;
+    if (lane == 0) FS_TR(8, i);
     int nu = 0;
     if (p.has_long) {
       const int A = it.b0 / kS;  // cells ending at or before the block start
@@ -356,6 +379,8 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
     if (lane == 0) bar.nu = nu;
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&bar.u_full);
+    if (lane == 0) FS_TR(7, i);
+    if (lane == 0 && i < 64 && g_trace_nu_enabled()) g_trace_nu(i, nu);
   }
 }
 
@@ -398,6 +423,7 @@ __device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem,
         tc::fence_async_smem();
       }
       tc::mbar_arrive(&bar.kt_full[slot]);
+      if (r == 0) FS_TR(1, T);
     }
   }
 }
@@ -522,6 +548,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
       const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
       if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
       tc::fence_after_sync();
+      if (r == 0 && half == 0) FS_TR(3, T);
       bool any, cell[2] = {false, false};
       int lo = 0, hi = -1;
       if (!is_long) {
@@ -597,6 +624,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&bar.p_full);
+      if (r == 0 && half == 0) FS_TR(4, T);
     }
     // ---- epilogue (TMEM read in 16-column pieces to keep registers low)
     if (!wait_nth(&bar.o_done, i, p.err)) return;
@@ -674,6 +702,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&bar.o_free);
+    if (r == 0 && half == 0) FS_TR(6, i);
   }
 }
 
@@ -870,3 +899,9 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
 }
 
 }  // namespace fs
+
+#ifdef FS_TRACE
+extern "C" int fs_trace_set(long long *buf) {
+  return (int)cudaMemcpyToSymbol(fs::g_trace, &buf, sizeof(buf));
+}
+#endif
