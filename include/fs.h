@@ -44,7 +44,9 @@ typedef enum {
   FS_ERR_INVALID_ARG = 1,
   FS_ERR_UNSUPPORTED = 2,
   FS_ERR_CUDA = 3,
-  FS_ERR_TIMEOUT = 4
+  FS_ERR_TIMEOUT = 4,
+  FS_ERR_RANGE = 5 /* a finite value of v read by the window branch has
+                      |v| >= 65520: past the fp16 range of its P.V product */
 } fs_status;
 
 typedef enum { FS_BF16 = 0, FS_FP32 = 1 } fs_dtype;
@@ -187,7 +189,10 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v,
 /* Every workspace begins with a 256-byte header whose first int is a device
  * error word, cleared at the start of each call.  Kernels that wait on
  * mbarriers give up after a bounded number of polls (seconds) and record
- * FS_ERR_TIMEOUT there instead of hanging.  fs_check_status synchronises
+ * FS_ERR_TIMEOUT there instead of hanging; the window branch records
+ * FS_ERR_RANGE there when a value of v is outside the fp16 range (its
+ * probabilities and values meet in an fp16 product, fp32 accumulation), and
+ * the output is then not valid.  fs_check_status synchronises
  * `stream` and returns FS_OK or the recorded status (FS_ERR_CUDA if the copy
  * or the synchronisation fails). */
 int fs_check_status(const void *ws, void *stream);

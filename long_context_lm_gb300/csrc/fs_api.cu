@@ -131,6 +131,7 @@ const char *fs_status_string(int status) {
     case FS_ERR_UNSUPPORTED: return "unsupported shape or parameter";
     case FS_ERR_CUDA: return "CUDA error";
     case FS_ERR_TIMEOUT: return "device wait timed out";
+    case FS_ERR_RANGE: return "a value of v is outside the fp16 range of the window product";
     default: return "unknown status";
   }
 }

@@ -26,17 +26,23 @@
 //   warp  10    lane 0: TMA producer (contiguous window tiles; gathered cells)
 //   warp  11    builds the union of the q-tile's selected cells
 //   warps 12-15 rotate the queries and every window key tile, in place
-// TMEM: S double-buffered (2 x 128 columns), P and P_lo (64 columns each of
-// bf16 pairs: the A operand of P.V), O_win and O_long (64 columns each).
+// TMEM: two 128-column score buffers S; the softmax overwrites each with
+// its tile's probabilities (bf16 pairs, the A operand of P.V) in place, so
+// P is double-buffered with S.  Two accumulator sets (O_win, O_long; 64
+// columns each) alternate between q-tiles, and the epilogue of a q-tile runs
+// after the softmax of the next q-tile's first key tile, off the MMA path.
 //
 // Precision.  Window: RoPE is applied relative to the q-tile's first position
 // b (q_n.k_j after rotations by n-b and j-b equals the absolute product), the
 // rotated q and k are split into bf16 hi + lo halves and S takes three MMA
 // chains (hi.hi + hi.lo + lo.hi): a single bf16 rounding of the rotated
-// vectors exceeds the output tolerance on lognormal keys.  Long branch: q and
-// k are exact bf16, so S is one chain; P is split into bf16 hi + lo halves
-// (two P.V chains) because RMSNorm rescales the branch output and would
-// amplify a plain bf16 rounding of P.
+// vectors exceeds the output tolerance on lognormal keys.  The window P.V
+// product runs in fp16 (P below 256, V re-encoded exactly from bf16): with a
+// lagging maximum the dominant probability is not exactly 1, and bf16's
+// 8-bit significand on it alone reaches the tolerance on peaked rows.  Long
+// branch: q and k are exact bf16, so S is one chain; P is split into bf16
+// hi + lo halves (two P.V chains) because RMSNorm rescales the branch output
+// and would amplify a plain bf16 rounding of P.
 #include <cuda.h>
 
 #include "fs_common.cuh"
@@ -83,9 +89,20 @@ constexpr uint32_t kOffUL = kOffT64 + 64 * kT64Stride; // union list: kMaxSel in
 constexpr uint32_t kOffRS = kOffUL + kMaxSel * 4;      // per row / pick: union slot, uint16
 constexpr uint32_t kOffTU = kOffRS + kMaxSel * 2;      // rows of 64*u*theta, 256 B each
 
-// TMEM columns
-constexpr uint32_t kColS = 0, kColP = 256, kColPL = 320, kColOW = 384, kColOL = 448;
+// TMEM columns: S / P buffers at 0 and 128; accumulator sets at 256 and 384
+// (O_win at +0, O_long at +64).  Inside a score buffer, key chunk c (32 keys)
+// keeps its P in columns 32c..32c+15 and P_lo in 32c+16..32c+31, so each
+// softmax warp writes only the columns it has already read.
+constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint32_t kTmemCols = 512;
+// The running maximum is raised only when a tile's maximum exceeds it by more
+// than 2^8 (log2 units): probabilities stay below 256, and the accumulators
+// are rescaled (which waits for the previous P.V) only on such a jump.
+constexpr float kLazyMax = 8.f;
+
+__device__ __forceinline__ uint32_t p_col(int k) {  // P of key group k (16 keys)
+  return 32 * (k >> 1) + 8 * (k & 1);
+}
 
 struct Barriers {
   uint64_t q_full, q_empty;
@@ -93,9 +110,11 @@ struct Barriers {
   uint64_t kt_full[kRing];   // key tile rotated (window) / landed (long)
   uint64_t k_empty[kRing];   // S MMAs of the tile done
   uint64_t v_empty[kRing];   // P.V MMAs of the tile done
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done;
-  uint64_t o_done, o_free;
+  uint64_t s_full[2], s_free[2];  // s_free: the tile's P.V (last reader of S / P) done
+  uint64_t p_full[2], pv_done;     // p_full per score buffer: the softmax may run a
+                                  // tile ahead of the P.V issuer
+  uint64_t o_done[2], o_free[2];  // per accumulator set
+  uint64_t pair[4];               // the two softmax warps of a row block meet here
   uint64_t u_full, u_free;   // union of the q-tile's cells built / consumed
   uint64_t fin[2];
   uint32_t tmem;
@@ -250,12 +269,14 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
 }
 
 __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t base) {
-  const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);
+  const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);  // long: bf16 P hi / lo, bf16 V
+  const uint32_t id_pv_h = tc::idesc_f16(128, kD, 1);  // window: fp16 P, fp16 V
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
-    // the accumulators are reused once the previous epilogue has read them
-    if (i > 0 && !wait_nth(&bar.o_free, i - 1, p.err)) return;
+    const uint32_t ob = tmem + kColO + 128 * (i & 1);
+    // an accumulator set is reused once the epilogue two q-tiles back has read it
+    if (i >= 2 && !wait_nth(&bar.o_free[i & 1], (i - 2) >> 1, p.err)) return;
     int nl = 0;
     for (int t = 0;; ++t, ++T) {
       if (t == it.nw) {
@@ -264,14 +285,17 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
         tc::mbar_arrive(&bar.u_free);
       }
       if (t >= it.nw + nl) break;
-      const int slot = T % kRing;
-      if (!wait_nth(&bar.p_full, T, p.err)) return;
+      const int slot = T % kRing, b = T & 1;
+      if (!wait_nth(&bar.p_full[b], T / 2, p.err)) return;
+      // window tiles: the fp16 values written by the rotation threads
+      if (t < it.nw && !wait_nth(&bar.kt_full[slot], T / kRing, p.err)) return;
       tc::fence_after_sync();
       const uint64_t dv = tc::desc_sw128(base + kOffV + slot * 16384);
+      const uint32_t sp = tmem + kColS + 128 * b;
       if (t < it.nw) {
 #pragma unroll
         for (int k = 0; k < kKT / 16; ++k)
-          tc::mma_ts(tmem + kColOW, tmem + kColP + 8 * k, dv + (uint64_t)(k * 128), id_pv,
+          tc::mma_ts(ob, sp + p_col(k), dv + (uint64_t)(k * 128), id_pv_h,
                      (t > 0 || k > 0) ? 1u : 0u);
       } else {
         const bool first = t == it.nw;
@@ -279,14 +303,15 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int k = 0; k < kKT / 16; ++k)
-            tc::mma_ts(tmem + kColOL, tmem + (part ? kColPL : kColP) + 8 * k,
-                       dv + (uint64_t)(k * 128), id_pv, (!first || part > 0 || k > 0) ? 1u : 0u);
+            tc::mma_ts(ob + 64, sp + p_col(k) + 16 * part, dv + (uint64_t)(k * 128), id_pv,
+                       (!first || part > 0 || k > 0) ? 1u : 0u);
       }
       tc::mma_commit(&bar.pv_done);
       tc::mma_commit(&bar.v_empty[slot]);
+      tc::mma_commit(&bar.s_free[b]);
       FS_TR(5, T);
     }
-    tc::mma_commit(&bar.o_done);
+    tc::mma_commit(&bar.o_done[i & 1]);
   }
 }
 
@@ -384,6 +409,30 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   }
 }
 
+// Window value rows are re-encoded from bf16 to fp16 in place (exact for
+// |v| in [2^-14, 65504]; smaller values keep an absolute error below 2^-25):
+// the window P.V product runs in fp16, whose 11-bit significand holds the
+// probabilities (kept below 256 by the lazy maximum) four times more finely
+// than bf16.  Returns false if a finite value lies past the fp16 range.
+__device__ __forceinline__ bool v_row_to_f16(unsigned char *vt, int r) {
+  float big = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(vt + swz128(r, c));
+    const uint4 x = *ptr;
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+      big = fmaxf(big, fmaxf(fabsf(lo), fabsf(hi)));
+      h[j] = pack_f16(lo, hi);
+    }
+    *ptr = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+  return !(big >= 65520.f && big != INFINITY);
+}
+
 __device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int r) {
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
@@ -420,6 +469,7 @@ __device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem,
       if (t < it.nw) {
         unsigned char *kh = smem + kOffK + slot * 32768;
         rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
+        if (!v_row_to_f16(smem + kOffV + slot * 16384, r)) tc::report_error(p.err, FS_ERR_RANGE);
         tc::fence_async_smem();
       }
       tc::mbar_arrive(&bar.kt_full[slot]);
@@ -474,9 +524,9 @@ __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
   return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
-// 2^(s*sl2 - m) for one chunk, written as bf16 pairs into 16 P columns (and,
-// with kSplit, the rounding remainders into 16 P_lo columns), 16 scores at a
-// time; returns the sum of the unrounded values.
+// 2^(s*sl2 - m) for one chunk, written as pairs into 16 P columns: fp16 for a
+// window tile; bf16 for a long tile, with the bf16 rounding remainders in 16
+// P_lo columns (kSplit).  Returns the sum of the unrounded values.
 template <bool kSplit>
 __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_addr,
                                            uint32_t pl_addr, float sl2, float m) {
@@ -489,8 +539,12 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_a
       const float e0 = tc::ex2(fmaf(__uint_as_float(x[16 * h16 + c]), sl2, -m));
       const float e1 = tc::ex2(fmaf(__uint_as_float(x[16 * h16 + c + 1]), sl2, -m));
       part[(c >> 1) & 3] += e0 + e1;
-      pk[c / 2] = pack_bf16(e0, e1);
-      if (kSplit) pl[c / 2] = pack_bf16(e0 - bf16_lo(pk[c / 2]), e1 - bf16_hi(pk[c / 2]));
+      if (kSplit) {  // long tile: bf16 hi + lo
+        pk[c / 2] = pack_bf16(e0, e1);
+        pl[c / 2] = pack_bf16(e0 - bf16_lo(pk[c / 2]), e1 - bf16_hi(pk[c / 2]));
+      } else {  // window tile: fp16
+        pk[c / 2] = pack_f16(e0, e1);
+      }
     }
     tc::tmem_st8(p_addr + 8 * h16, pk);
     if (kSplit) tc::tmem_st8(pl_addr + 8 * h16, pl);
@@ -498,9 +552,17 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_a
   return (part[0] + part[1]) + (part[2] + part[3]);
 }
 
-__device__ __forceinline__ void pair_sync(int quarter) {
-  asm volatile("bar.sync %0, 64;\n" ::"r"(1 + quarter) : "memory");
-}
+// Rendezvous of the two softmax warps that share a row block (one mbarrier
+// phase per meeting; bounded wait, so a failed partner cannot hang the CTA).
+struct Pair {
+  uint64_t *bar;
+  uint32_t phase;
+  __device__ __forceinline__ bool sync(int lane, int *err) {
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar);
+    return tc::mbar_wait(bar, phase++ & 1, err);
+  }
+};
 
 __device__ __forceinline__ void rescale(uint32_t addr, float alpha) {
   uint32_t o[32];
@@ -511,26 +573,131 @@ __device__ __forceinline__ void rescale(uint32_t addr, float alpha) {
   tc::tmem_st32(addr, o);
 }
 
+// Per-row state of a finished q-tile, kept until its epilogue runs.
+struct Done {
+  Item it;
+  uint32_t i;  // q-tile index of this CTA (accumulator set i & 1)
+  int nl;
+  float ll, lw;
+};
+
+// Epilogue of one q-tile: O_long / l_long and its RMSNorm over the 64
+// columns (the two warps of a row block exchange partial sums), O_win / l_win,
+// the mix, the store.  TMEM is read in 16-column pieces to keep registers low.
+__device__ __forceinline__ bool epilogue(const Params &p, Barriers &bar, uint32_t tmem,
+                                         const Done &d, Pair &pr, int quarter, int half,
+                                         int lane) {
+  const int r = quarter * 32 + lane;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const uint32_t ow_addr = tmem + kColO + 128 * (d.i & 1) + 32 * half + lane_base;
+  const uint32_t ol_addr = ow_addr + 64;
+  if (!wait_nth(&bar.o_done[d.i & 1], d.i >> 1, p.err)) return false;
+  tc::fence_after_sync();
+  if (r == 0 && half == 0) FS_TR(10, d.i);
+  float lo_scale = 0.f;
+  if (p.has_long) {
+    bar.xsum[half][r] = d.ll;
+    if (!pr.sync(lane, p.err)) return false;
+    const float ltot = d.ll + bar.xsum[half ^ 1][r];
+    if (!pr.sync(lane, p.err)) return false;
+    const float invl = ltot > 0.f ? 1.f / ltot : 0.f;
+    float ss = 0.f;
+    if (d.nl > 0) {
+#pragma unroll
+      for (int c16 = 0; c16 < 2; ++c16) {
+        uint32_t o[16];
+        tc::tmem_ld16(ol_addr + 16 * c16, o);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float y = __uint_as_float(o[c]) * invl;
+          ss = fmaf(y, y, ss);
+        }
+      }
+    }
+    bar.xsum[half][r] = ss;
+    if (!pr.sync(lane, p.err)) return false;
+    ss += bar.xsum[half ^ 1][r];
+    if (!pr.sync(lane, p.err)) return false;
+    lo_scale = (d.nl > 0 && ltot > 0.f) ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
+  }
+  float wscale = 0.f;
+  if (d.it.nw > 0) {
+    bar.xsum[half][r] = d.lw;
+    if (!pr.sync(lane, p.err)) return false;
+    wscale = 1.f / (d.lw + bar.xsum[half ^ 1][r]);
+    if (!pr.sync(lane, p.err)) return false;
+  }
+  const size_t row = (size_t)d.it.bh * p.N + d.it.b0 + r;
+  float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD + 32 * half);
+  const float mh = p.mix ? p.mix[d.it.bh % p.H] : 0.f;
+  const bool use_long = lo_scale != 0.f;
+  const bool use_win = !p.write_long && d.it.nw > 0;
+  const float4 *oin = (!p.write_long && !use_long && p.o_long_in)
+      ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD + 32 * half) : nullptr;
+  const float ls = p.write_long ? lo_scale : mh * lo_scale;
+#pragma unroll
+  for (int c16 = 0; c16 < 2; ++c16) {
+    uint32_t ow[16], ol[16];
+    if (use_win) tc::tmem_ld16(ow_addr + 16 * c16, ow);
+    if (use_long) tc::tmem_ld16(ol_addr + 16 * c16, ol);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (use_win)
+        v = make_float4(__uint_as_float(ow[4 * c4]) * wscale, __uint_as_float(ow[4 * c4 + 1]) * wscale,
+                        __uint_as_float(ow[4 * c4 + 2]) * wscale,
+                        __uint_as_float(ow[4 * c4 + 3]) * wscale);
+      if (use_long) {
+        v.x = fmaf(ls, __uint_as_float(ol[4 * c4]), v.x);
+        v.y = fmaf(ls, __uint_as_float(ol[4 * c4 + 1]), v.y);
+        v.z = fmaf(ls, __uint_as_float(ol[4 * c4 + 2]), v.z);
+        v.w = fmaf(ls, __uint_as_float(ol[4 * c4 + 3]), v.w);
+      } else if (oin) {
+        const float4 u4 = __ldg(oin + 4 * c16 + c4);
+        v.x = fmaf(mh, u4.x, v.x);
+        v.y = fmaf(mh, u4.y, v.y);
+        v.z = fmaf(mh, u4.z, v.z);
+        v.w = fmaf(mh, u4.w, v.w);
+      }
+      dst[4 * c16 + c4] = v;
+    }
+  }
+  tc::fence_before_sync();
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(&bar.o_free[d.i & 1]);
+  if (r == 0 && half == 0) FS_TR(6, d.i);
+  return true;
+}
+
 __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsigned char *smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, half = warp >> 2;
   const int r = quarter * 32 + lane;  // query row of this thread
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-  const uint32_t p_addr = tmem + kColP + 32 * half + lane_base;
-  const uint32_t pl_addr = tmem + kColPL + 32 * half + lane_base;
-  const uint32_t ow_addr = tmem + kColOW + 32 * half + lane_base;
-  const uint32_t ol_addr = tmem + kColOL + 32 * half + lane_base;
   const uint16_t *rs = reinterpret_cast<const uint16_t *>(smem + kOffRS);
   const float sl2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
   uint32_t T = 0, i = 0;
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
+  Done prev;
+  bool pending = false;
+  Pair pr{&bar.pair[quarter], 0u};
+  // one pass past the last q-tile runs the final epilogue
+  for (int g = blockIdx.x;; g += gridDim.x, ++i) {
+    const bool real = g < p.nitems;
+    Item it;
+    if (real) {
+      it = item_of(p, g);
+    } else {
+      it.bh = it.b0 = it.kt0 = it.nw = 0;
+    }
     const int n = it.b0 + r;
+    const uint32_t ow_addr = tmem + kColO + 128 * (i & 1) + 32 * half + lane_base;
     float mw = -INFINITY, lw = 0.f, ml = -INFINITY, ll = 0.f;
     int nl = 0;
     uint32_t pick[kMaxK / 2];  // this row's union slots, two 16-bit slots per word
     for (int t = 0;; ++t, ++T) {
-      if (t == it.nw) {
+      if (real && t == it.nw) {
         if (!wait_nth(&bar.u_full, i, p.err)) return;
         nl = long_tiles(bar, p);
 #pragma unroll
@@ -542,167 +709,109 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bar.u_free);  // union data read
       }
-      if (t >= it.nw && t >= it.nw + nl) break;
-      const bool is_long = t >= it.nw;
-      const int b = T & 1;
-      const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
-      if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
-      tc::fence_after_sync();
-      if (r == 0 && half == 0) FS_TR(3, T);
-      bool any, cell[2] = {false, false};
-      int lo = 0, hi = -1;
-      if (!is_long) {
-        const int kt = it.kt0 + t * kKT;
-        lo = max(0, n - p.w + 1 - kt);
-        hi = min(kKT - 1, n - kt);
-        any = __any_sync(0xffffffffu, lo <= hi && hi >= 64 * half && lo <= 64 * half + 63);
-      } else {
-        const uint32_t u0 = 4 * (t - it.nw) + 2 * half;
+      const bool done = !real || t >= it.nw + nl;
+      if (!done) {
+        const bool is_long = t >= it.nw;
+        const int b = T & 1;
+        const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
+        if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
+        tc::fence_after_sync();
+        if (r == 0 && half == 0) FS_TR(3, T);
+        bool any, cell[2] = {false, false};
+        int lo = 0, hi = -1;
+        if (!is_long) {
+          const int kt = it.kt0 + t * kKT;
+          lo = max(0, n - p.w + 1 - kt);
+          hi = min(kKT - 1, n - kt);
+          any = __any_sync(0xffffffffu, lo <= hi && hi >= 64 * half && lo <= 64 * half + 63);
+        } else {
+          const uint32_t u0 = 4 * (t - it.nw) + 2 * half;
 #pragma unroll
-        for (int k = 0; k < kMaxK / 2; ++k) {
-          const uint32_t a = pick[k] & 0xffffu, b = pick[k] >> 16;
-          cell[0] |= (a == u0) || (b == u0);
-          cell[1] |= (a == u0 + 1) || (b == u0 + 1);
+          for (int k = 0; k < kMaxK / 2; ++k) {
+            const uint32_t a = pick[k] & 0xffffu, bb = pick[k] >> 16;
+            cell[0] |= (a == u0) || (bb == u0);
+            cell[1] |= (a == u0 + 1) || (bb == u0 + 1);
+          }
+          any = __any_sync(0xffffffffu, cell[0] || cell[1]);
         }
-        any = __any_sync(0xffffffffu, cell[0] || cell[1]);
-      }
-      float mx = -INFINITY;
-      if (any) {
+        float mx = -INFINITY;
+        if (any) {
 #pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t x[32];
-          load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
-          mx = fmaxf(mx, max_chunk(x));
-        }
-      }
-      bar.xmax[half][r] = mx;
-      pair_sync(quarter);
-      mx = fmaxf(mx, bar.xmax[half ^ 1][r]);
-      pair_sync(quarter);  // the slot is rewritten next tile
-      const float m = is_long ? ml : mw;
-      float l = is_long ? ll : lw;
-      const float mnew = fmaxf(m, mx * sl2);
-      const float alpha = (mnew == m) ? 1.f : tc::ex2(m - mnew);
-      // P and the accumulators belong to the previous P.V until it completes
-      if (T > 0 && !wait_nth(&bar.pv_done, T - 1, p.err)) return;
-      tc::fence_after_sync();
-      const float muse = mnew == -INFINITY ? 0.f : mnew;
-      l = l * alpha;
-      if (any) {
-#pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t x[32];
-          load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
-          l += is_long ? exp_chunk<true>(x, p_addr + 16 * ch, pl_addr + 16 * ch, sl2, muse)
-                       : exp_chunk<false>(x, p_addr + 16 * ch, pl_addr + 16 * ch, sl2, muse);
-        }
-      } else {
-        uint32_t z[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) z[c] = 0u;
-        tc::tmem_st16(p_addr, z);
-        tc::tmem_st16(p_addr + 16, z);
-        if (is_long) {
-          tc::tmem_st16(pl_addr, z);
-          tc::tmem_st16(pl_addr + 16, z);
-        }
-      }
-      // both passes have read S: the buffer may be refilled
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar.s_free[b]);
-      if (is_long) {
-        ml = mnew;
-        ll = l;
-      } else {
-        mw = mnew;
-        lw = l;
-      }
-      const bool first = is_long ? t == it.nw : t == 0;
-      if (!first && __any_sync(0xffffffffu, alpha != 1.f)) rescale(is_long ? ol_addr : ow_addr, alpha);
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bar.p_full);
-      if (r == 0 && half == 0) FS_TR(4, T);
-    }
-    // ---- epilogue (TMEM read in 16-column pieces to keep registers low)
-    if (!wait_nth(&bar.o_done, i, p.err)) return;
-    tc::fence_after_sync();
-    // long branch: O_long / l_long, RMSNorm over the 64 columns (two halves)
-    float lo_scale = 0.f;
-    if (p.has_long) {
-      bar.xsum[half][r] = ll;
-      pair_sync(quarter);
-      const float ltot = ll + bar.xsum[half ^ 1][r];
-      pair_sync(quarter);
-      const float invl = ltot > 0.f ? 1.f / ltot : 0.f;
-      float ss = 0.f;
-      if (nl > 0) {
-#pragma unroll
-        for (int c16 = 0; c16 < 2; ++c16) {
-          uint32_t o[16];
-          tc::tmem_ld16(ol_addr + 16 * c16, o);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float y = __uint_as_float(o[c]) * invl;
-            ss = fmaf(y, y, ss);
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t x[32];
+            load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
+            mx = fmaxf(mx, max_chunk(x));
           }
         }
-      }
-      bar.xsum[half][r] = ss;
-      pair_sync(quarter);
-      ss += bar.xsum[half ^ 1][r];
-      pair_sync(quarter);
-      lo_scale = (nl > 0 && ltot > 0.f) ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
-    }
-    float wscale = 0.f;
-    if (it.nw > 0) {
-      bar.xsum[half][r] = lw;
-      pair_sync(quarter);
-      wscale = 1.f / (lw + bar.xsum[half ^ 1][r]);
-      pair_sync(quarter);
-    }
-    const size_t row = (size_t)it.bh * p.N + n;
-    float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD + 32 * half);
-    const float mh = p.mix ? p.mix[it.bh % p.H] : 0.f;
-    const bool use_long = lo_scale != 0.f;
-    const float4 *oin = (!p.write_long && !use_long && p.o_long_in)
-        ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD + 32 * half) : nullptr;
-    const float ls = p.write_long ? lo_scale : mh * lo_scale;
+        bar.xmax[half][r] = mx;
+        if (r == 0 && half == 0) FS_TR(11, T);
+        if (!pr.sync(lane, p.err)) return;
+        mx = fmaxf(mx, bar.xmax[half ^ 1][r]);
+        if (!pr.sync(lane, p.err)) return;  // the slot is rewritten next tile
+        if (r == 0 && half == 0) FS_TR(12, T);
+        const float m = is_long ? ml : mw;
+        float l = is_long ? ll : lw;
+        const float mt = mx * sl2;
+        const float mnew = mt > m + kLazyMax ? mt : m;
+        const bool first = is_long ? t == it.nw : t == 0;
+        // the accumulator holds exact zeros while m is -inf: nothing to rescale
+        const bool resc = !first && m != -INFINITY && mnew != m;
+        const float alpha = resc ? tc::ex2(m - mnew) : 1.f;
+        const float muse = mnew == -INFINITY ? 0.f : mnew;
+        l = l * alpha;
+        if (any) {
+#pragma unroll 1
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t x[32];
+            load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
+            l += is_long ? exp_chunk<true>(x, s_addr + 32 * ch, s_addr + 32 * ch + 16, sl2, muse)
+                         : exp_chunk<false>(x, s_addr + 32 * ch, s_addr + 32 * ch + 16, sl2, muse);
+          }
+        } else {
+          uint32_t z[16];
 #pragma unroll
-    for (int c16 = 0; c16 < 2; ++c16) {
-      uint32_t ow[16], ol[16];
-      if (!p.write_long && it.nw > 0) tc::tmem_ld16(ow_addr + 16 * c16, ow);
-      if (use_long) tc::tmem_ld16(ol_addr + 16 * c16, ol);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!p.write_long && it.nw > 0)
-          v = make_float4(__uint_as_float(ow[4 * c4]) * wscale, __uint_as_float(ow[4 * c4 + 1]) * wscale,
-                          __uint_as_float(ow[4 * c4 + 2]) * wscale,
-                          __uint_as_float(ow[4 * c4 + 3]) * wscale);
-        if (use_long) {
-          v.x = fmaf(ls, __uint_as_float(ol[4 * c4]), v.x);
-          v.y = fmaf(ls, __uint_as_float(ol[4 * c4 + 1]), v.y);
-          v.z = fmaf(ls, __uint_as_float(ol[4 * c4 + 2]), v.z);
-          v.w = fmaf(ls, __uint_as_float(ol[4 * c4 + 3]), v.w);
-        } else if (oin) {
-          const float4 u4 = __ldg(oin + 4 * c16 + c4);
-          v.x = fmaf(mh, u4.x, v.x);
-          v.y = fmaf(mh, u4.y, v.y);
-          v.z = fmaf(mh, u4.z, v.z);
-          v.w = fmaf(mh, u4.w, v.w);
+          for (int c = 0; c < 16; ++c) z[c] = 0u;
+          tc::tmem_st16(s_addr, z);
+          tc::tmem_st16(s_addr + 32, z);
+          if (is_long) {
+            tc::tmem_st16(s_addr + 16, z);
+            tc::tmem_st16(s_addr + 48, z);
+          }
         }
-        dst[4 * c16 + c4] = v;
+        if (is_long) {
+          ml = mnew;
+          ll = l;
+        } else {
+          mw = mnew;
+          lw = l;
+        }
+        if (r == 0 && half == 0) FS_TR(13, T);
+        if (__any_sync(0xffffffffu, resc)) {
+          if (lane == 0 && half == 0) FS_TR(14 + (quarter >> 1), T);
+          // the previous P.V accumulates into the same set: let it finish
+          if (!wait_nth(&bar.pv_done, T - 1, p.err)) return;
+          tc::fence_after_sync();
+          rescale(ow_addr + (is_long ? 64 : 0), alpha);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bar.p_full[b]);
+        if (r == 0 && half == 0) FS_TR(4, T);
       }
+      if (pending && t == 0) {  // the previous q-tile's epilogue, off the MMA path
+        if (!epilogue(p, bar, tmem, prev, pr, quarter, half, lane)) return;
+        pending = false;
+      }
+      if (done) break;
     }
-    tc::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&bar.o_free);
-    if (r == 0 && half == 0) FS_TR(6, i);
+    if (!real) break;
+    prev.it = it;
+    prev.i = i;
+    prev.nl = nl;
+    prev.ll = ll;
+    prev.lw = lw;
+    pending = true;
   }
 }
 
@@ -727,13 +836,14 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bar.s_full[b], 1);
-      tc::mbar_init(&bar.s_free[b], 8);
+      tc::mbar_init(&bar.s_free[b], 1);
       tc::mbar_init(&bar.fin[b], 1);
+      tc::mbar_init(&bar.o_done[b], 1);
+      tc::mbar_init(&bar.o_free[b], 8);
     }
-    tc::mbar_init(&bar.p_full, 8);
+    for (int b = 0; b < 2; ++b) tc::mbar_init(&bar.p_full[b], 8);
+    for (int q4 = 0; q4 < 4; ++q4) tc::mbar_init(&bar.pair[q4], 2);
     tc::mbar_init(&bar.pv_done, 1);
-    tc::mbar_init(&bar.o_done, 1);
-    tc::mbar_init(&bar.o_free, 8);
     tc::mbar_init(&bar.u_full, 1);
     // the union may be rebuilt once every role has read it: 8 softmax warps,
     // 4 rotation warps, the two issuers and the TMA thread
@@ -766,6 +876,13 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   const uint32_t tmem = bar.tmem;
   const uint32_t sbase = smem_u32(smem);
 
+  // registers: the issuer / TMA / union warpgroup (warps 8-11) gives up 48 per
+  // thread, the softmax (0-7) and rotation (12-15) warpgroups take 16 more:
+  // 4*32*80 + 12*32*144 = 65536, the block's launch allotment of 512 x 128
+  if (warp >= 8 && warp < 12)
+    tc::regs_dec<80>();
+  else
+    tc::regs_inc<144>();
   if (warp < 8) {
     role_softmax(p, bar, tmem, smem);
   } else if (warp == 8 || warp == 9) {

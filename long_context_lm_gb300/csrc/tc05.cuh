@@ -27,7 +27,10 @@ namespace tc {
 // ---------------------------------------------------------------------------
 // A wait that has not completed after kWaitCycles SM clock cycles (about two
 // seconds at GB300 clocks) gives up, records FS_ERR_TIMEOUT in the caller's
-// error word and lets the kernel wind down instead of hanging the GPU.
+// error word and lets the kernel wind down instead of hanging the GPU.  Once
+// any thread has recorded an error, every other wait of the launch gives up
+// at its next check, so a failed pipeline drains in one timeout, not one per
+// wait.
 constexpr long long kWaitCycles = 4000000000ll;
 
 __device__ __forceinline__ void report_error(int *err, int code) {
@@ -67,10 +70,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && clock64() - t0 > kWaitCycles) break;
+    if ((i & 255u) == 0) {
+      if (clock64() - t0 > kWaitCycles) break;
+      if (err && *reinterpret_cast<volatile int *>(err) != 0) return false;
+    }
   }
   report_error(err, FS_ERR_TIMEOUT);
   return false;
+}
+
+// Warpgroup register rebalancing: every warp of a warpgroup executes the same
+// call; increases are granted from what decreases have released, within the
+// registers the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
 }
 
 // generic-proxy shared-memory writes -> visible to the tensor core
@@ -172,6 +190,11 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with fp16 A and B (format code 0 in both operand fields).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn) {
+  return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // D(tmem) (+)= A(smem) * B(smem)^T, issued by one thread.

@@ -20,7 +20,7 @@ import torch
 
 from . import build as _build
 
-FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT = range(5)
+FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_RANGE = range(6)
 FS_BF16, FS_FP32 = 0, 1
 FS_MODE_FSL, FS_MODE_FS = 0, 1
 
