@@ -141,8 +141,10 @@ int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
                       const int32_t *sel, int batch, int H, int N, int d,
                       const fs_params *p, float *o_long, void *stream);
 
-/* Workspace bytes fs_window_attn needs (header + RoPE angle table). */
-size_t fs_window_workspace_bytes(int N, const fs_params *p);
+/* Workspace bytes fs_window_attn needs: header, RoPE angle table, keys
+ * rotated by their positions (bf16 hi | lo, 256 B per token-head) and fp16
+ * values (128 B per token-head).  0 for invalid arguments. */
+size_t fs_window_workspace_bytes(int batch, int H, int N, int d, const fs_params *p);
 
 /* Sliding-window RoPE branch and branch mix (paper.rainbus.top summary,
  * 方法步骤详情 ② and ⑥; ai.info, "Methodology in Plain English"):

@@ -2,6 +2,8 @@
 // argument validation, workspace carving and stream-ordered launches.
 #include <stdio.h>
 
+#include <functional>
+
 #include "fs_common.cuh"
 #include "fs_internal.h"
 
@@ -73,10 +75,26 @@ int status_of(cudaError_t e) {
 // error word (0 = ok, else an fs_status set by a kernel's bounded wait).
 constexpr size_t kHeader = 256;
 
+// Window-branch operands: RoPE angle table, rotated keys (bf16 hi | lo),
+// fp16 values.
+struct WindowLayout {
+  size_t tab, kt, v16;
+};
+
+WindowLayout take_window(const Shape &sh, const std::function<size_t(size_t)> &take) {
+  WindowLayout W;
+  const size_t rows = (size_t)sh.BH() * sh.N;
+  W.tab = take(rope_table_bytes(sh.N));
+  W.kt = take(rows * 2 * kD * 2);
+  W.v16 = take(rows * kD * 2);
+  return W;
+}
+
 // Layout of the fs_attention_fwd workspace.
 struct Layout {
   size_t qb, kb, vb;       // bf16 copies (fp32 inputs only)
-  size_t kbar, amax, pool, pool_count, sel, rope, prune;
+  size_t kbar, amax, pool, pool_count, sel, prune;
+  WindowLayout win;
   size_t total;
 };
 
@@ -98,10 +116,30 @@ Layout make_layout(const Shape &sh, const fs_params &p, int dtype) {
   L.pool = take((size_t)sh.BH() * sh.nblk() * (p.P + p.W) * sizeof(int32_t));
   L.pool_count = take((size_t)sh.BH() * sh.nblk() * sizeof(int32_t));
   L.sel = take((size_t)sh.BH() * sh.N * p.K * sizeof(int32_t));
-  L.rope = take(attn_table_bytes(p.w));
   L.prune = take(prune_workspace_bytes(sh));
+  L.win = take_window(sh, take);
   L.total = off;
   return L;
+}
+
+// Workspace of fs_window_attn: header, then the window operands.
+size_t window_total(const Shape &sh, WindowLayout *W) {
+  size_t off = kHeader;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  const WindowLayout L = take_window(sh, take);
+  if (W) *W = L;
+  return off;
+}
+
+// Angle table, then rotated keys and fp16 values, on `st`.
+int prepare_window(const Shape &sh, const void *k, const void *v, float rope_base, char *base,
+                   const WindowLayout &W, int *err, cudaStream_t st) {
+  FS_TRY(status_of(launch_rope_table(base + W.tab, sh.N, rope_base, st)));
+  return status_of(launch_prep(k, v, base + W.tab, sh, base + W.kt, base + W.v16, err, st));
 }
 
 }  // namespace
@@ -163,9 +201,9 @@ size_t fs_prune_workspace_bytes(int batch, int H, int N, const fs_params *p) {
   return prune_workspace_bytes(Shape{batch, H, N, kD});
 }
 
-size_t fs_window_workspace_bytes(int N, const fs_params *p) {
-  if (check_params(p) || check_shape(1, 1, N, kD)) return 0;
-  return kHeader + attn_table_bytes(p->w);
+size_t fs_window_workspace_bytes(int batch, int H, int N, int d, const fs_params *p) {
+  if (check_params(p) || check_shape(batch, H, N, d)) return 0;
+  return window_total(Shape{batch, H, N, d}, nullptr);
 }
 
 int fs_check_status(const void *ws, void *stream) {
@@ -234,7 +272,6 @@ int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
   a.sel = sel;
   a.w = p->w;
   a.K = p->K;
-  a.rope_base = p->rope_base;
   a.rms_eps = p->rms_eps;
   a.window = false;
   a.write_long = true;
@@ -250,22 +287,26 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const
   FS_TRY(check_dtype(dtype));
   if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !ws || (o_long && !mix)) return FS_ERR_INVALID_ARG;
-  if (ws_bytes < kHeader + attn_table_bytes(p->w)) return FS_ERR_INVALID_ARG;
+  const Shape sh{batch, H, N, d};
+  WindowLayout W;
+  if (ws_bytes < window_total(sh, &W)) return FS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *base = static_cast<char *>(ws);
   int *err = reinterpret_cast<int *>(base);
   FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  FS_TRY(prepare_window(sh, k, v, p->rope_base, base, W, err, st));
   AttnArgs a{};
-  a.sh = Shape{batch, H, N, d};
+  a.sh = sh;
   a.q = q;
   a.k = k;
   a.v = v;
+  a.kt = base + W.kt;
+  a.v16 = base + W.v16;
+  a.tab = base + W.tab;
   a.o_long_in = o_long;
   a.mix = mix;
-  a.table = base + kHeader;
   a.w = p->w;
   a.K = p->K;
-  a.rope_base = p->rope_base;
   a.rms_eps = p->rms_eps;
   a.window = true;
   a.out = out;
@@ -318,6 +359,7 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   };
   FS_TRY(mark(0));
   FS_TRY(status_of(launch_cell_summary(kb, false, sh, kbar, amax, st)));
+  FS_TRY(prepare_window(sh, kb, vb, p->rope_base, base, L.win, err, st));
   FS_TRY(mark(1));
   if (!fs_mode)
     FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));
@@ -330,12 +372,13 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   a.q = qb;
   a.k = kb;
   a.v = vb;
+  a.kt = base + L.win.kt;
+  a.v16 = base + L.win.v16;
+  a.tab = base + L.win.tab;
   a.sel = sel;
   a.mix = mix;
-  a.table = base + L.rope;
   a.w = p->w;
   a.K = p->K;
-  a.rope_base = p->rope_base;
   a.rms_eps = p->rms_eps;
   a.window = true;
   a.out = out;

@@ -24,25 +24,32 @@ cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const int32_t *pool, const int32_t *pool_count, const float *lambda,
                           const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
                           int32_t *sel, float *sel_score, int *err, cudaStream_t st);
+// RoPE angle table (rope_table_bytes(N) of device memory, written by
+// launch_rope_table) and the window operands prepared from it: kt = rotated
+// keys [rows, 128] bf16 (hi | lo), v16 = values [rows, 64] fp16.
+size_t rope_table_bytes(int N);
+cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st);
+cudaError_t launch_prep(const void *k, const void *v, const void *tab, const Shape &sh, void *kt,
+                        void *v16, int *err, cudaStream_t st);
 // Both attention branches (window RoPE branch, NoPE readout of the selected
-// cells) in one persistent tcgen05 kernel.  window: run the window branch;
-// sel != nullptr: run the long branch; write_long: write RMSNorm(o_long) to
-// `out` instead of the mixed output; o_long_in (window only, nullable): a
-// precomputed long branch to mix in.
+// cells) in one persistent tcgen05 kernel.  window: run the window branch
+// (reads kt, v16, tab); sel != nullptr: run the long branch (reads the raw
+// k, v cells); write_long: write RMSNorm(o_long) to `out` instead of the
+// mixed output; o_long_in (window only, nullable): a precomputed long branch
+// to mix in.
 struct AttnArgs {
   Shape sh;
   const void *q, *k, *v;
+  const void *kt, *v16, *tab;
   const int32_t *sel;
   const float *o_long_in;
   const float *mix;
-  void *table;  // attn_table_bytes(w) of device scratch (window only)
   int w, K;
-  float rope_base, rms_eps;
+  float rms_eps;
   bool window, write_long;
   float *out;
   int *err;
 };
-size_t attn_table_bytes(int w);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 
 }  // namespace fs

@@ -1,0 +1,121 @@
+// k0_prep.cu -- window-branch operands, prepared once per call.
+//
+// FreeSolo (paper.rainbus.top summary, 方法步骤详情 ② window branch, 前置知识
+// RoPE; ai.info summary, "Methodology in Plain English"): the sliding-window
+// branch scores q_n . k_j after rotating both by their own positions (RoPE,
+// half-split pairs (i, i + d/2) at angles p * theta_i, theta_i =
+// base^(-2i/d)).  A key enters the windows of about (w + Bq) / Bq query
+// tiles, so it is rotated here once, at its absolute position, instead of
+// once per query tile inside the attention kernel:
+//   kt[row] = [bf16 hi (64) | bf16 lo (64)] of R(n) k_n (fp32), 256 B per row
+//   v16[row] = fp16(v_n) (exact from bf16 inside the fp16 range), 128 B per row
+// Streaming, HBM-bound: per token-head it reads 256 B and writes 384 B.
+//
+// Angles: row r < 64 of the table holds (cos, sin)(r theta_i); row 64 + u
+// holds (cos, sin)(64 u theta_i); both are evaluated in fp64 and rounded
+// once, and an absolute angle is composed from its two rows by the angle-sum
+// identity in fp32 (error of a few fp32 ulps, independent of the position).
+#include "fs_common.cuh"
+#include "fs_internal.h"
+#include "tc05.cuh"
+
+namespace fs {
+namespace {
+
+__global__ void rope_table_kernel(float2 *__restrict__ tab, int rows, double base) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * (kD / 2)) return;
+  const int row = idx / (kD / 2), i = idx % (kD / 2);
+  const double theta = pow(base, -2.0 * (double)i / (double)kD);
+  const double pos = row < 64 ? (double)row : 64.0 * (double)(row - 64);
+  double s, c;
+  sincos(pos * theta, &s, &c);
+  tab[idx] = make_float2((float)c, (float)s);
+}
+
+// Four threads per token row; thread part p rotates pairs 8p .. 8p+7 (dims
+// 8p.. and 32+8p..) and re-encodes value dims 16p .. 16p+15.  Eight rows per
+// warp: every load and store instruction of a warp covers contiguous bytes.
+__global__ void __launch_bounds__(256) k0_prep_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const float4 *__restrict__ tab,
+    int N, long long rows, uint4 *__restrict__ kt, uint4 *__restrict__ v16, int *err) {
+  const long long nthreads = rows * 4;
+  bool range_ok = true;
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < nthreads;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long row = t >> 2;
+    const int part = (int)(t & 3);
+    const int n = (int)(row % N);
+    const uint4 xa = __ldg(k + row * 8 + part), xb = __ldg(k + row * 8 + 4 + part);
+    const uint4 va = __ldg(v + row * 8 + 2 * part), vb = __ldg(v + row * 8 + 2 * part + 1);
+    // (cos, sin) pairs 8p..8p+7 of rows n mod 64 and 64 + n / 64: four float4 each
+    const float4 *tr = tab + (size_t)(n & 63) * 16 + 4 * part;
+    const float4 *tu = tab + (size_t)(64 + (n >> 6)) * 16 + 4 * part;
+    const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
+    uint32_t ah[4], al[4], bh[4], bl[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // pairs 8p + 2j, 8p + 2j + 1
+      const float4 rr = __ldg(tr + j), uu = __ldg(tu + j);
+      float y0[2], y1[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float cr = e ? rr.z : rr.x, sr = e ? rr.w : rr.y;
+        const float cu = e ? uu.z : uu.x, su = e ? uu.w : uu.y;
+        const float c = fmaf(cu, cr, -su * sr), sn = fmaf(su, cr, cu * sr);
+        const float x0 = e ? bf16_hi(wa[j]) : bf16_lo(wa[j]);
+        const float x1 = e ? bf16_hi(wb[j]) : bf16_lo(wb[j]);
+        y0[e] = fmaf(x0, c, -x1 * sn);
+        y1[e] = fmaf(x0, sn, x1 * c);
+      }
+      ah[j] = pack_bf16(y0[0], y0[1]);
+      al[j] = pack_bf16(y0[0] - bf16_lo(ah[j]), y0[1] - bf16_hi(ah[j]));
+      bh[j] = pack_bf16(y1[0], y1[1]);
+      bl[j] = pack_bf16(y1[0] - bf16_lo(bh[j]), y1[1] - bf16_hi(bh[j]));
+    }
+    uint4 *dst = kt + row * 16;
+    dst[part] = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+    dst[4 + part] = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+    dst[8 + part] = make_uint4(al[0], al[1], al[2], al[3]);
+    dst[12 + part] = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+    // values: bf16 -> fp16; a finite |v| >= 65520 would round to infinity
+    const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+    uint32_t h[8];
+    float big = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float lo = bf16_lo(vw[j]), hi = bf16_hi(vw[j]);
+      big = fmaxf(big, fmaxf(fabsf(lo), fabsf(hi)));
+      h[j] = pack_f16(lo, hi);
+    }
+    range_ok &= !(big >= 65520.f && big != INFINITY);
+    uint4 *vd = v16 + row * 8 + 2 * part;
+    vd[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    vd[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+  if (!range_ok) tc::report_error(err, FS_ERR_RANGE);
+}
+
+}  // namespace
+
+size_t rope_table_bytes(int N) { return (size_t)(64 + (N + 63) / 64) * (kD / 2) * sizeof(float2); }
+
+cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st) {
+  const int rows = 64 + (N + 63) / 64;
+  rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(static_cast<float2 *>(tab),
+                                                                  rows, (double)rope_base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const void *k, const void *v, const void *tab, const Shape &sh, void *kt,
+                        void *v16, int *err, cudaStream_t st) {
+  const long long rows = (long long)sh.BH() * sh.N;
+  const long long blocks = (rows * 4 + 255) / 256;
+  const int grid = (int)(blocks < 152 * 8 ? blocks : 152 * 8);
+  k0_prep_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4 *>(k),
+                                       static_cast<const uint4 *>(v),
+                                       static_cast<const float4 *>(tab), sh.N, rows,
+                                       static_cast<uint4 *>(kt), static_cast<uint4 *>(v16), err);
+  return cudaGetLastError();
+}
+
+}  // namespace fs

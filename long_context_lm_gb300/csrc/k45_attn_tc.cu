@@ -25,16 +25,18 @@
 //               one tcgen05.mma per ~100 cycles, hence two issuers)
 //   warp  10    lane 0: TMA producer (contiguous window tiles; gathered cells)
 //   warp  11    builds the union of the q-tile's selected cells
-//   warps 12-15 rotate the queries and every window key tile, in place
+//   warps 12-15 stage the query tile: raw (long branch) and rotated (window)
+// Window key tiles arrive already rotated (absolute positions, bf16 hi | lo)
+// with fp16 values, from the preparation pass; the query tile is rotated
+// here by the same absolute angles, so q_n . k_j carries R(n - j).
 // TMEM: two 128-column score buffers S; the softmax overwrites each with
 // its tile's probabilities (bf16 pairs, the A operand of P.V) in place, so
 // P is double-buffered with S.  Two accumulator sets (O_win, O_long; 64
 // columns each) alternate between q-tiles, and the epilogue of a q-tile runs
 // after the softmax of the next q-tile's first key tile, off the MMA path.
 //
-// Precision.  Window: RoPE is applied relative to the q-tile's first position
-// b (q_n.k_j after rotations by n-b and j-b equals the absolute product), the
-// rotated q and k are split into bf16 hi + lo halves and S takes three MMA
+// Precision.  Window: the rotated q and k (fp32, absolute angles from an
+// fp64 table) are split into bf16 hi + lo halves and S takes three MMA
 // chains (hi.hi + hi.lo + lo.hi): a single bf16 rounding of the rotated
 // vectors exceeds the output tolerance on lognormal keys.  The window P.V
 // product runs in fp16 (P below 256, V re-encoded exactly from bf16): with a
@@ -44,6 +46,7 @@
 // hi + lo halves (two P.V chains) because RMSNorm rescales the branch output
 // and would amplify a plain bf16 rounding of P.
 #include <cuda.h>
+#include <string.h>
 
 #include "fs_common.cuh"
 #include "fs_internal.h"
@@ -74,7 +77,7 @@ __device__ __forceinline__ void g_trace_nu(int, int) {}
 constexpr int kKT = 128;          // keys per tile
 constexpr int kRing = 3;          // key / value ring depth
 constexpr int kThreads = 512;
-constexpr int kRotBase = 384;     // first rotation thread (warps 12-15)
+constexpr int kRotBase = 384;     // first query-staging thread (warps 12-15)
 constexpr int kRotThreads = 128;  // one 64-element row each
 constexpr int kT64Stride = 272;   // bytes per row of the r*theta table (padded: no bank conflicts)
 constexpr int kMaxSel = kBq * kMaxK;
@@ -87,7 +90,7 @@ constexpr uint32_t kOffV = kOffK + kRing * 32768;      // kRing x 16 KB
 constexpr uint32_t kOffT64 = kOffV + kRing * 16384;    // 64 rows x 272 B
 constexpr uint32_t kOffUL = kOffT64 + 64 * kT64Stride; // union list: kMaxSel int32
 constexpr uint32_t kOffRS = kOffUL + kMaxSel * 4;      // per row / pick: union slot, uint16
-constexpr uint32_t kOffTU = kOffRS + kMaxSel * 2;      // rows of 64*u*theta, 256 B each
+constexpr uint32_t kSmemBytes = kOffRS + kMaxSel * 2 + 1024;  // + alignment slack
 
 // TMEM columns: S / P buffers at 0 and 128; accumulator sets at 256 and 384
 // (O_win at +0, O_long at +64).  Inside a score buffer, key chunk c (32 keys)
@@ -107,7 +110,6 @@ __device__ __forceinline__ uint32_t p_col(int k) {  // P of key group k (16 keys
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t raw_full[kRing];  // TMA: key and value tile landed
-  uint64_t kt_full[kRing];   // key tile rotated (window) / landed (long)
   uint64_t k_empty[kRing];   // S MMAs of the tile done
   uint64_t v_empty[kRing];   // P.V MMAs of the tile done
   uint64_t s_full[2], s_free[2];  // s_free: the tile's P.V (last reader of S / P) done
@@ -119,8 +121,8 @@ struct Barriers {
   uint64_t fin[2];
   uint32_t tmem;
   int nu;                    // cells in the current union
-  float xmax[2][128];        // per-half row maxima of the current tile
-  float xsum[2][128];        // per-half partial sums exchanged in the epilogue
+  float2 xch[2][2][128];     // row values the two softmax warps of a row block
+                             // exchange: [exchange parity][warp half][row]
 };
 
 struct Params {
@@ -128,8 +130,7 @@ struct Params {
   const int32_t *sel;      // [BH, N, K] selected cells (long branch)
   const float *o_long_in;  // window-only mode: branch to mix in (nullable)
   const float *mix;
-  const float2 *rel;       // (cos, sin) of o*theta_i, row o + rel_off
-  int rel_off, umin;
+  const float2 *tab;       // (cos, sin) of r*theta_i (rows r < 64), 64*u*theta_i (row 64 + u)
   int H, N, w, K, nblk, nitems;
   int has_window, has_long, write_long;  // write_long: output RMSNorm(o_long) only
   float rms_eps;
@@ -161,8 +162,8 @@ __device__ __forceinline__ int long_tiles(const Barriers &bar, const Params &p) 
 // RoPE rotation (window tiles)
 // --------------------------------------------------------------------------
 // Rotate half of one 64-element row in place: pairs i in [16*half, 16*half+16)
-// (dims 16*half.. and 32+16*half..), angles composed from rows t64r (offset
-// mod 64) and tur (64*u) by the angle-sum identity.  The raw row is read from
+// (dims 16*half.. and 32+16*half..), angles composed from rows t64r (position
+// mod 64, shared memory) and tur (64*u, global) by the angle-sum identity.  The raw row is read from
 // `hi` (chunks 2*half, 2*half+1, 4+2*half, 5+2*half) and the rotated bf16
 // hi / lo halves are written back to the same chunks of `hi` and `lo`.
 __device__ __forceinline__ void rotate_half_row(unsigned char *hi, unsigned char *lo, int r,
@@ -183,7 +184,7 @@ __device__ __forceinline__ void rotate_half_row(unsigned char *hi, unsigned char
     for (int j = 0; j < 4; ++j) {
       const int i0 = 16 * half + 8 * k + 2 * j;  // first pair of this 32-bit word
       const float4 rr = *reinterpret_cast<const float4 *>(t64r + i0);
-      const float4 bb = *reinterpret_cast<const float4 *>(tur + i0);
+      const float4 bb = __ldg(reinterpret_cast<const float4 *>(tur + i0));
       float y0[2], y1[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -208,12 +209,11 @@ __device__ __forceinline__ void rotate_half_row(unsigned char *hi, unsigned char
   }
 }
 
-// Rotate row r (64 elements, in place) by the relative offset o.
-__device__ __forceinline__ void rotate_row(unsigned char *hi, unsigned char *lo, int r, int o,
-                                           const unsigned char *smem, int umin) {
-  const float2 *t64r = reinterpret_cast<const float2 *>(smem + kOffT64 + (o & 63) * kT64Stride);
-  const float2 *tur =
-      reinterpret_cast<const float2 *>(smem + kOffTU) + ((o >> 6) - umin) * (kD / 2);
+// Rotate row r (64 elements, in place) by the absolute position n.
+__device__ __forceinline__ void rotate_row(unsigned char *hi, unsigned char *lo, int r, int n,
+                                           const unsigned char *smem, const float2 *tab) {
+  const float2 *t64r = reinterpret_cast<const float2 *>(smem + kOffT64 + (n & 63) * kT64Stride);
+  const float2 *tur = tab + (size_t)(64 + (n >> 6)) * (kD / 2);
   rotate_half_row(hi, lo, r, 0, t64r, tur);
   rotate_half_row(hi, lo, r, 1, t64r, tur);
 }
@@ -239,7 +239,7 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       }
       if (t >= it.nw + nl) break;
       const int slot = T % kRing, b = T & 1;
-      if (!wait_nth(&bar.kt_full[slot], T / kRing, p.err)) return;
+      if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
       if (T >= 2 && !wait_nth(&bar.s_free[b], T / 2 - 1, p.err)) return;
       tc::fence_after_sync();
       const uint32_t kh = base + kOffK + slot * 32768;
@@ -287,8 +287,8 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       if (t >= it.nw + nl) break;
       const int slot = T % kRing, b = T & 1;
       if (!wait_nth(&bar.p_full[b], T / 2, p.err)) return;
-      // window tiles: the fp16 values written by the rotation threads
-      if (t < it.nw && !wait_nth(&bar.kt_full[slot], T / kRing, p.err)) return;
+      // the value tile is read by this thread's MMAs: observe its arrival here too
+      if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
       tc::fence_after_sync();
       const uint64_t dv = tc::desc_sw128(base + kOffV + slot * 16384);
       const uint32_t sp = tmem + kColS + 128 * b;
@@ -316,7 +316,7 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
 }
 
 __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
-                         const CUtensorMap *tk, const CUtensorMap *tv, const CUtensorMap *ck,
+                         const CUtensorMap *tkt, const CUtensorMap *tv16, const CUtensorMap *ck,
                          const CUtensorMap *cv) {
   uint32_t T = 0, i = 0;
   const int *ul = reinterpret_cast<const int *>(smem + kOffUL);
@@ -337,12 +337,14 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
         if (!wait_nth(&bar.v_empty[slot], T / kRing - 1, p.err)) return;
       }
       unsigned char *kd = smem + kOffK + slot * 32768, *vd = smem + kOffV + slot * 16384;
-      tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 2 * kKT * kD * 2);
-      if (t < it.nw) {
+      if (t < it.nw) {  // rotated keys (hi, lo) and fp16 values: 48 KB
         const int y = row0 + it.kt0 + t * kKT;
-        tc::tma_load_2d(kd, tk, &bar.raw_full[slot], 0, y);
-        tc::tma_load_2d(vd, tv, &bar.raw_full[slot], 0, y);
-      } else {
+        tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 3 * kKT * kD * 2);
+        tc::tma_load_2d(kd, tkt, &bar.raw_full[slot], 0, y);
+        tc::tma_load_2d(kd + 16384, tkt, &bar.raw_full[slot], kD, y);
+        tc::tma_load_2d(vd, tv16, &bar.raw_full[slot], 0, y);
+      } else {  // raw keys and values of four cells: 32 KB
+        tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 2 * kKT * kD * 2);
         // four cells of the union; a missing cell reads zeros from past the
         // last row, so stale data never meets a zero probability
         const int lt = t - it.nw;
@@ -409,36 +411,14 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   }
 }
 
-// Window value rows are re-encoded from bf16 to fp16 in place (exact for
-// |v| in [2^-14, 65504]; smaller values keep an absolute error below 2^-25):
-// the window P.V product runs in fp16, whose 11-bit significand holds the
-// probabilities (kept below 256 by the lazy maximum) four times more finely
-// than bf16.  Returns false if a finite value lies past the fp16 range.
-__device__ __forceinline__ bool v_row_to_f16(unsigned char *vt, int r) {
-  float big = 0.f;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4 *ptr = reinterpret_cast<uint4 *>(vt + swz128(r, c));
-    const uint4 x = *ptr;
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t h[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-      big = fmaxf(big, fmaxf(fabsf(lo), fabsf(hi)));
-      h[j] = pack_f16(lo, hi);
-    }
-    *ptr = make_uint4(h[0], h[1], h[2], h[3]);
-  }
-  return !(big >= 65520.f && big != INFINITY);
-}
-
-__device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem, int r) {
-  uint32_t T = 0, i = 0;
+// Query staging: row r of each q-tile, raw (NoPE long branch) and, for the
+// window, rotated by its absolute position and split into bf16 hi / lo.
+__device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, int r) {
+  uint32_t i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
-    // query row r: fetch it first, then wait until the previous q-tile's S
-    // MMAs no longer read the query tiles
+    // fetch the row first, then wait until the previous q-tile's S MMAs no
+    // longer read the query tiles
     const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + r) * kD);
     uint4 raw[8];
 #pragma unroll
@@ -446,41 +426,21 @@ __device__ void role_rotate(const Params &p, Barriers &bar, unsigned char *smem,
     if (i > 0 && !wait_nth(&bar.q_empty, i - 1, p.err)) return;
     unsigned char *qh = smem + kOffQ, *qr = smem + kOffQR;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      *reinterpret_cast<uint4 *>(qr + swz128(r, c)) = raw[c];
-      *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qr + swz128(r, c)) = raw[c];
+    if (p.has_window) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
+      rotate_row(qh, qh + 16384, r, it.b0 + r, smem, p.tab);
     }
-    if (p.has_window) rotate_row(qh, qh + 16384, r, r, smem, p.umin);
     tc::fence_async_smem();
     tc::mbar_arrive(&bar.q_full);
-    // every tile passes the rotation threads so the per-slot phases line up;
-    // window tiles are rotated, long tiles only wait for their data
-    int nl = 0;
-    for (int t = 0;; ++t, ++T) {
-      if (t == it.nw) {
-        if (!wait_nth(&bar.u_full, i, p.err)) return;
-        nl = long_tiles(bar, p);
-        __syncwarp();
-        if ((r & 31) == 0) tc::mbar_arrive(&bar.u_free);
-      }
-      if (t >= it.nw + nl) break;
-      const int slot = T % kRing;
-      if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
-      if (t < it.nw) {
-        unsigned char *kh = smem + kOffK + slot * 32768;
-        rotate_row(kh, kh + 16384, r, it.kt0 + t * kKT + r - it.b0, smem, p.umin);
-        if (!v_row_to_f16(smem + kOffV + slot * 16384, r)) tc::report_error(p.err, FS_ERR_RANGE);
-        tc::fence_async_smem();
-      }
-      tc::mbar_arrive(&bar.kt_full[slot]);
-      if (r == 0) FS_TR(1, T);
-    }
+    if (r == 0) FS_TR(1, i);
   }
 }
 
-// A 32-column chunk of a score row held in registers.  The softmax reads a
-// warp's 64 columns as two chunks, twice (max pass, then exp pass), which
-// keeps the register footprint at 32 scores per thread.
+// A warp's 64 score columns of a row are held in registers as two 32-column
+// chunks: loaded once, masked, reduced to the row maximum, then turned into
+// probabilities in place of the scores.
 constexpr uint32_t kNegInf = 0xff800000u;
 
 // window: columns outside [lo, hi] (tile columns) become -inf; the test is
@@ -501,14 +461,12 @@ __device__ __forceinline__ void mask_window(uint32_t (&x)[32], int lo, int hi, i
   }
 }
 
-// Load chunk ch (columns 32*ch.. of this warp's half) and apply the mask:
-// window band, or (long tile) the whole chunk is one cell the row picked or not.
-__device__ __forceinline__ void load_chunk(uint32_t s_addr, int ch, bool is_long, int lo, int hi,
-                                           int col0, bool keep, uint32_t (&x)[32]) {
-  tc::tmem_ld32(s_addr + 32 * ch, x);
-  tc::tmem_wait_ld();
+// Mask a 32-column chunk starting at tile column c0: window band [lo, hi],
+// or (long tile) the whole chunk is one cell the row picked or not.
+__device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], bool is_long, int lo, int hi,
+                                           int c0, bool keep) {
   if (!is_long) {
-    mask_window(x, lo, hi, col0 + 32 * ch);
+    mask_window(x, lo, hi, c0);
   } else if (!keep) {
 #pragma unroll
     for (int c = 0; c < 32; ++c) x[c] = kNegInf;
@@ -552,15 +510,25 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_a
   return (part[0] + part[1]) + (part[2] + part[3]);
 }
 
-// Rendezvous of the two softmax warps that share a row block (one mbarrier
-// phase per meeting; bounded wait, so a failed partner cannot hang the CTA).
+// The two softmax warps that share a row block swap one float2 per row:
+// publish, meet on an mbarrier (one phase per swap; bounded wait, so a failed
+// partner cannot hang the CTA), read the partner's.  Slots alternate by swap
+// parity: a slot is rewritten two swaps later, after the partner has met us
+// once more and so has read it.
 struct Pair {
   uint64_t *bar;
+  float2 (*slot)[2][128];
   uint32_t phase;
-  __device__ __forceinline__ bool sync(int lane, int *err) {
+  __device__ __forceinline__ bool swap(float2 mine, float2 &theirs, int half, int r, int lane,
+                                       int *err) {
+    const uint32_t par = phase & 1;
+    slot[par][half][r] = mine;
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(bar);
-    return tc::mbar_wait(bar, phase++ & 1, err);
+    const bool ok = tc::mbar_wait(bar, par, err);
+    theirs = slot[par][half ^ 1][r];
+    ++phase;
+    return ok;
   }
 };
 
@@ -582,8 +550,8 @@ struct Done {
 };
 
 // Epilogue of one q-tile: O_long / l_long and its RMSNorm over the 64
-// columns (the two warps of a row block exchange partial sums), O_win / l_win,
-// the mix, the store.  TMEM is read in 16-column pieces to keep registers low.
+// columns, O_win / l_win, the mix, the store.  The two warps of a row block
+// swap (l_long, l_win), then the long branch's partial sum of squares.
 __device__ __forceinline__ bool epilogue(const Params &p, Barriers &bar, uint32_t tmem,
                                          const Done &d, Pair &pr, int quarter, int half,
                                          int lane) {
@@ -594,75 +562,68 @@ __device__ __forceinline__ bool epilogue(const Params &p, Barriers &bar, uint32_
   if (!wait_nth(&bar.o_done[d.i & 1], d.i >> 1, p.err)) return false;
   tc::fence_after_sync();
   if (r == 0 && half == 0) FS_TR(10, d.i);
+  const bool have_long = p.has_long && d.nl > 0;
+  const bool use_win = !p.write_long && d.it.nw > 0;
+
+  float2 o;
+  if (!pr.swap(make_float2(d.ll, d.lw), o, half, r, lane, p.err)) return false;
+  const float ltot = d.ll + o.x, wtot = d.lw + o.y;
+  const float invl = ltot > 0.f ? 1.f / ltot : 0.f;
   float lo_scale = 0.f;
   if (p.has_long) {
-    bar.xsum[half][r] = d.ll;
-    if (!pr.sync(lane, p.err)) return false;
-    const float ltot = d.ll + bar.xsum[half ^ 1][r];
-    if (!pr.sync(lane, p.err)) return false;
-    const float invl = ltot > 0.f ? 1.f / ltot : 0.f;
-    float ss = 0.f;
-    if (d.nl > 0) {
+    float sq[4] = {0.f, 0.f, 0.f, 0.f};
+    if (have_long) {
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
-        uint32_t o[16];
-        tc::tmem_ld16(ol_addr + 16 * c16, o);
+        uint32_t o16[16];
+        tc::tmem_ld16(ol_addr + 16 * c16, o16);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float y = __uint_as_float(o[c]) * invl;
-          ss = fmaf(y, y, ss);
+          const float y = __uint_as_float(o16[c]) * invl;
+          sq[c & 3] = fmaf(y, y, sq[c & 3]);
         }
       }
     }
-    bar.xsum[half][r] = ss;
-    if (!pr.sync(lane, p.err)) return false;
-    ss += bar.xsum[half ^ 1][r];
-    if (!pr.sync(lane, p.err)) return false;
-    lo_scale = (d.nl > 0 && ltot > 0.f) ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
+    float ss = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+    if (!pr.swap(make_float2(ss, 0.f), o, half, r, lane, p.err)) return false;
+    ss += o.x;
+    lo_scale = (have_long && ltot > 0.f) ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
   }
-  float wscale = 0.f;
-  if (d.it.nw > 0) {
-    bar.xsum[half][r] = d.lw;
-    if (!pr.sync(lane, p.err)) return false;
-    wscale = 1.f / (d.lw + bar.xsum[half ^ 1][r]);
-    if (!pr.sync(lane, p.err)) return false;
-  }
+  const float wscale = d.it.nw > 0 ? 1.f / wtot : 0.f;
   const size_t row = (size_t)d.it.bh * p.N + d.it.b0 + r;
   float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD + 32 * half);
   const float mh = p.mix ? p.mix[d.it.bh % p.H] : 0.f;
   const bool use_long = lo_scale != 0.f;
-  const bool use_win = !p.write_long && d.it.nw > 0;
   const float4 *oin = (!p.write_long && !use_long && p.o_long_in)
       ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD + 32 * half) : nullptr;
   const float ls = p.write_long ? lo_scale : mh * lo_scale;
+  uint32_t ow[16], ol[16];
 #pragma unroll
-  for (int c16 = 0; c16 < 2; ++c16) {
-    uint32_t ow[16], ol[16];
-    if (use_win) tc::tmem_ld16(ow_addr + 16 * c16, ow);
-    if (use_long) tc::tmem_ld16(ol_addr + 16 * c16, ol);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (use_win)
-        v = make_float4(__uint_as_float(ow[4 * c4]) * wscale, __uint_as_float(ow[4 * c4 + 1]) * wscale,
-                        __uint_as_float(ow[4 * c4 + 2]) * wscale,
-                        __uint_as_float(ow[4 * c4 + 3]) * wscale);
-      if (use_long) {
-        v.x = fmaf(ls, __uint_as_float(ol[4 * c4]), v.x);
-        v.y = fmaf(ls, __uint_as_float(ol[4 * c4 + 1]), v.y);
-        v.z = fmaf(ls, __uint_as_float(ol[4 * c4 + 2]), v.z);
-        v.w = fmaf(ls, __uint_as_float(ol[4 * c4 + 3]), v.w);
-      } else if (oin) {
-        const float4 u4 = __ldg(oin + 4 * c16 + c4);
-        v.x = fmaf(mh, u4.x, v.x);
-        v.y = fmaf(mh, u4.y, v.y);
-        v.z = fmaf(mh, u4.z, v.z);
-        v.w = fmaf(mh, u4.w, v.w);
-      }
-      dst[4 * c16 + c4] = v;
+  for (int c4 = 0; c4 < 8; ++c4) {
+    if ((c4 & 3) == 0) {  // accumulators in 16-column pieces
+      if (use_win) tc::tmem_ld16(ow_addr + 4 * c4, ow);
+      if (use_long) tc::tmem_ld16(ol_addr + 4 * c4, ol);
+      tc::tmem_wait_ld();
     }
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int o4 = 4 * (c4 & 3);
+    if (use_win)
+      v = make_float4(__uint_as_float(ow[o4]) * wscale, __uint_as_float(ow[o4 + 1]) * wscale,
+                      __uint_as_float(ow[o4 + 2]) * wscale, __uint_as_float(ow[o4 + 3]) * wscale);
+    if (use_long) {
+      v.x = fmaf(ls, __uint_as_float(ol[o4]), v.x);
+      v.y = fmaf(ls, __uint_as_float(ol[o4 + 1]), v.y);
+      v.z = fmaf(ls, __uint_as_float(ol[o4 + 2]), v.z);
+      v.w = fmaf(ls, __uint_as_float(ol[o4 + 3]), v.w);
+    } else if (oin) {
+      const float4 u4 = __ldg(oin + c4);
+      v.x = fmaf(mh, u4.x, v.x);
+      v.y = fmaf(mh, u4.y, v.y);
+      v.z = fmaf(mh, u4.z, v.z);
+      v.w = fmaf(mh, u4.w, v.w);
+    }
+    dst[c4] = v;
   }
   tc::fence_before_sync();
   __syncwarp();
@@ -681,7 +642,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
   uint32_t T = 0, i = 0;
   Done prev;
   bool pending = false;
-  Pair pr{&bar.pair[quarter], 0u};
+  Pair pr{&bar.pair[quarter], bar.xch, 0u};
   // one pass past the last q-tile runs the final epilogue
   for (int g = blockIdx.x;; g += gridDim.x, ++i) {
     const bool real = g < p.nitems;
@@ -734,20 +695,23 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
           }
           any = __any_sync(0xffffffffu, cell[0] || cell[1]);
         }
+        // the warp's 64 score columns in one TMEM round trip
+        uint32_t xa[32], xb[32];
         float mx = -INFINITY;
+        if (r == 0 && half == 0) FS_TR(16, T);
         if (any) {
-#pragma unroll 1
-          for (int ch = 0; ch < 2; ++ch) {
-            uint32_t x[32];
-            load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
-            mx = fmaxf(mx, max_chunk(x));
-          }
+          tc::tmem_ld32(s_addr, xa);
+          tc::tmem_ld32(s_addr + 32, xb);
+          tc::tmem_wait_ld();
+          if (r == 0 && half == 0) FS_TR(17, T);
+          mask_chunk(xa, is_long, lo, hi, 64 * half, cell[0]);
+          mask_chunk(xb, is_long, lo, hi, 64 * half + 32, cell[1]);
+          mx = fmaxf(max_chunk(xa), max_chunk(xb));
         }
-        bar.xmax[half][r] = mx;
         if (r == 0 && half == 0) FS_TR(11, T);
-        if (!pr.sync(lane, p.err)) return;
-        mx = fmaxf(mx, bar.xmax[half ^ 1][r]);
-        if (!pr.sync(lane, p.err)) return;  // the slot is rewritten next tile
+        float2 o;
+        if (!pr.swap(make_float2(mx, 0.f), o, half, r, lane, p.err)) return;
+        mx = fmaxf(mx, o.x);
         if (r == 0 && half == 0) FS_TR(12, T);
         const float m = is_long ? ml : mw;
         float l = is_long ? ll : lw;
@@ -760,12 +724,16 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         const float muse = mnew == -INFINITY ? 0.f : mnew;
         l = l * alpha;
         if (any) {
+          // chunk 0 from xa, then chunk 1 moved into xa (one copy of the code)
 #pragma unroll 1
           for (int ch = 0; ch < 2; ++ch) {
-            uint32_t x[32];
-            load_chunk(s_addr, ch, is_long, lo, hi, 64 * half, cell[ch], x);
-            l += is_long ? exp_chunk<true>(x, s_addr + 32 * ch, s_addr + 32 * ch + 16, sl2, muse)
-                         : exp_chunk<false>(x, s_addr + 32 * ch, s_addr + 32 * ch + 16, sl2, muse);
+            const uint32_t pa = s_addr + 32 * ch;
+            l += is_long ? exp_chunk<true>(xa, pa, pa + 16, sl2, muse)
+                         : exp_chunk<false>(xa, pa, pa + 16, sl2, muse);
+            if (ch == 0) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) xa[c] = xb[c];
+            }
           }
         } else {
           uint32_t z[16];
@@ -816,7 +784,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
 }
 
 __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
-    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+    const __grid_constant__ CUtensorMap tmap_kt, const __grid_constant__ CUtensorMap tmap_v16,
     const __grid_constant__ CUtensorMap cmap_k, const __grid_constant__ CUtensorMap cmap_v,
     const Params p) {
   extern __shared__ unsigned char smem_raw[];
@@ -830,7 +798,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     tc::mbar_init(&bar.q_empty, 1);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&bar.raw_full[i], 1);
-      tc::mbar_init(&bar.kt_full[i], kRotThreads);
       tc::mbar_init(&bar.k_empty[i], 1);
       tc::mbar_init(&bar.v_empty[i], 1);
     }
@@ -846,28 +813,21 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     tc::mbar_init(&bar.pv_done, 1);
     tc::mbar_init(&bar.u_full, 1);
     // the union may be rebuilt once every role has read it: 8 softmax warps,
-    // 4 rotation warps, the two issuers and the TMA thread
-    tc::mbar_init(&bar.u_free, 15);
+    // the two issuers and the TMA thread
+    tc::mbar_init(&bar.u_free, 11);
     tc::mbar_fence_init();
   }
   if (warp == 8) {
     tc::tmem_alloc(&bar.tmem, kTmemCols);
     tc::tmem_relinquish();
   }
-  // angle tables, staged once per CTA by the rotation warps (window only)
+  // rows r*theta (r < 64) of the angle table, staged once per CTA (window only)
   if (threadIdx.x >= kRotBase && p.has_window) {
-    const int r = threadIdx.x - kRotBase;
-    const float4 *rel = reinterpret_cast<const float4 *>(p.rel);
-    for (int i = r; i < 64 * 16; i += kRotThreads) {
+    const float4 *tab = reinterpret_cast<const float4 *>(p.tab);
+    for (int i = threadIdx.x - kRotBase; i < 64 * 16; i += kRotThreads) {
       const int row = i >> 4, part = i & 15;
       *reinterpret_cast<float4 *>(smem + kOffT64 + row * kT64Stride + part * 16) =
-          __ldg(rel + (size_t)(row + p.rel_off) * 16 + part);
-    }
-    float4 *tu = reinterpret_cast<float4 *>(smem + kOffTU);
-    const int nu = 3 - p.umin;  // u in [umin, 2]
-    for (int i = r; i < nu * 16; i += kRotThreads) {
-      const int row = i >> 4, part = i & 15;
-      tu[i] = __ldg(rel + (size_t)(64 * (row + p.umin) + p.rel_off) * 16 + part);
+          __ldg(tab + (size_t)row * 16 + part);
     }
   }
   tc::fence_before_sync();
@@ -876,13 +836,14 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   const uint32_t tmem = bar.tmem;
   const uint32_t sbase = smem_u32(smem);
 
-  // registers: the issuer / TMA / union warpgroup (warps 8-11) gives up 48 per
-  // thread, the softmax (0-7) and rotation (12-15) warpgroups take 16 more:
-  // 4*32*80 + 12*32*144 = 65536, the block's launch allotment of 512 x 128
-  if (warp >= 8 && warp < 12)
-    tc::regs_dec<80>();
+  // registers: the issuer / TMA / union warpgroup (warps 8-11) and the query
+  // staging warpgroup (12-15) give up 56 per thread, the two softmax
+  // warpgroups (0-7) take 56 more: 8*32*72 + 8*32*184 = 65536, the block's
+  // launch allotment of 512 x 128
+  if (warp >= 8)
+    tc::regs_dec<72>();
   else
-    tc::regs_inc<144>();
+    tc::regs_inc<184>();
   if (warp < 8) {
     role_softmax(p, bar, tmem, smem);
   } else if (warp == 8 || warp == 9) {
@@ -895,11 +856,11 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
       tc::mbar_wait(&bar.fin[warp - 8], 0, p.err);
     }
   } else if (warp == 10) {
-    if (lane == 0) role_tma(p, bar, smem, &tmap_k, &tmap_v, &cmap_k, &cmap_v);
+    if (lane == 0) role_tma(p, bar, smem, &tmap_kt, &tmap_v16, &cmap_k, &cmap_v);
   } else if (warp == 11) {
     role_union(p, bar, smem);
   } else {
-    role_rotate(p, bar, smem, threadIdx.x - kRotBase);
+    role_qprep(p, bar, smem, threadIdx.x - kRotBase);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -907,16 +868,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-__global__ void rel_rope_table_kernel(float2 *__restrict__ tab, int rows, int off, double base) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= rows * (kD / 2)) return;
-  const int row = idx / (kD / 2), i = idx % (kD / 2);
-  const double theta = pow(base, -2.0 * (double)i / (double)kD);
-  double s, c;
-  sincos((double)(row - off) * theta, &s, &c);
-  tab[idx] = make_float2((float)c, (float)s);
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -937,18 +888,20 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// [rows, 64] bf16 row-major, boxes of box_rows x 64 with the 128-byte swizzle;
-// rows past the end read as zeros.
-bool make_rows_map(CUtensorMap *map, const void *ptr, size_t rows, int box_rows) {
+// [rows, cols] 16-bit row-major (bf16 or fp16), boxes of box_rows x 64 with
+// the 128-byte swizzle; rows past the end read as zeros.
+bool make_rows_map(CUtensorMap *map, const void *ptr, size_t rows, int cols, int box_rows,
+                   bool f16) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {
@@ -959,40 +912,29 @@ int sm_count() {
   return n;
 }
 
-int rel_offset(int w) { return (w + 127 + 63) / 64 * 64; }
-
 }  // namespace
-
-// Relative-angle table rows: offsets o in [-rel_offset, kBq + 64); the kernel
-// needs o*theta for o = 64*u (u >= umin) and o in [0, 64).
-size_t attn_table_bytes(int w) {
-  return (size_t)(rel_offset(w) + kBq + 64) * (kD / 2) * sizeof(float2);
-}
 
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   const Shape &sh = a.sh;
-  const int off = rel_offset(a.w);
-  const int rows = off + kBq + 64;
-  float2 *tab = static_cast<float2 *>(a.table);
-  if (a.window) {  // the angle table is used (and written) by the window branch only
-    if (!tab) return cudaErrorInvalidValue;
-    rel_rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(tab, rows, off,
-                                                                        (double)a.rope_base);
-  }
   if (!a.window && !a.sel) return cudaErrorInvalidValue;
-  CUtensorMap mk, mv, ck, cv;
+  // the window branch reads the prepared operands and the angle table
+  if (a.window && (!a.kt || !a.v16 || !a.tab)) return cudaErrorInvalidValue;
+  CUtensorMap mkt, mv16, ck, cv;
   const size_t nrows = (size_t)sh.BH() * sh.N;
-  if (!make_rows_map(&mk, a.k, nrows, kKT) || !make_rows_map(&mv, a.v, nrows, kKT) ||
-      !make_rows_map(&ck, a.k, nrows, kS) || !make_rows_map(&cv, a.v, nrows, kS))
+  memset(&mkt, 0, sizeof(mkt));
+  memset(&mv16, 0, sizeof(mv16));
+  if (a.window && (!make_rows_map(&mkt, a.kt, nrows, 2 * kD, kKT, false) ||
+                   !make_rows_map(&mv16, a.v16, nrows, kD, kKT, true)))
+    return cudaErrorInvalidValue;
+  if (!make_rows_map(&ck, a.k, nrows, kD, kS, false) ||
+      !make_rows_map(&cv, a.v, nrows, kD, kS, false))
     return cudaErrorInvalidValue;
   Params p;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.sel = a.sel;
   p.o_long_in = a.o_long_in;
   p.mix = a.mix;
-  p.rel = tab;
-  p.rel_off = off;
-  p.umin = -(off / 64);
+  p.tab = static_cast<const float2 *>(a.tab);
   p.H = sh.H;
   p.N = sh.N;
   p.w = a.w;
@@ -1006,12 +948,11 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   p.nrows = nrows;
   p.out = a.out;
   p.err = a.err;
-  const uint32_t smem = kOffTU + (3 - p.umin) * 256 + 1024;
   cudaError_t e = cudaFuncSetAttribute(fs_attn_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.nitems < sm_count() ? p.nitems : sm_count();
-  fs_attn_tc_kernel<<<grid, kThreads, smem, st>>>(mk, mv, ck, cv, p);
+  fs_attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mkt, mv16, ck, cv, p);
   return cudaGetLastError();
 }
 

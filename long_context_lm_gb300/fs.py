@@ -83,7 +83,7 @@ def load(build_if_stale: bool = True):
         L.fs_workspace_bytes.restype = Z
         L.fs_prune_workspace_bytes.argtypes = [I, I, I, PP]
         L.fs_prune_workspace_bytes.restype = Z
-        L.fs_window_workspace_bytes.argtypes = [I, PP]
+        L.fs_window_workspace_bytes.argtypes = [I, I, I, I, PP]
         L.fs_window_workspace_bytes.restype = Z
         L.fs_cell_summarize.argtypes = [P, I, I, I, I, I, I, P, P, P]
         L.fs_prune_cells.argtypes = [P, I, I, I, PP, P, P, P, Z, P]
@@ -240,7 +240,7 @@ def fs_window_attn(q, k, v, o_long=None, mix=None, params=None, out=None, stream
         _dev(o_long, "o_long", (torch.float32,))
         _dev(mix, "mix", (torch.float32,))
     out = out if out is not None else torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
-    wsb = L.fs_window_workspace_bytes(N, ctypes.byref(p))
+    wsb = L.fs_window_workspace_bytes(B, H, N, d, ctypes.byref(p))
     if wsb == 0:
         raise FSError(FS_ERR_INVALID_ARG, "fs_window_workspace_bytes")
     ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
