@@ -45,8 +45,10 @@ typedef enum {
   FS_ERR_UNSUPPORTED = 2,
   FS_ERR_CUDA = 3,
   FS_ERR_TIMEOUT = 4,
-  FS_ERR_RANGE = 5 /* a finite value of v read by the window branch has
-                      |v| >= 65520: past the fp16 range of its P.V product */
+  FS_ERR_RANGE = 5, /* a finite value of v read by the window branch has
+                       |v| >= 65520: past the fp16 range of its P.V product */
+  FS_ERR_SCRATCH_LIMIT = 6 /* fs_prune_cells_static: the shape needs more
+                              than its fixed scratch array */
 } fs_status;
 
 typedef enum { FS_BF16 = 0, FS_FP32 = 1 } fs_dtype;
@@ -111,6 +113,25 @@ int fs_cell_summarize(const void *k, int dtype, int batch, int H, int N, int d,
 int fs_prune_cells(const float *amax, int batch, int H, int N,
                    const fs_params *p, int32_t *pool, int32_t *pool_count,
                    void *ws, size_t ws_bytes, void *stream);
+
+/* fs_prune_cells for callers that can neither allocate device memory nor
+ * lend a workspace (no counterpart on the pages: a library convenience).
+ * Same arguments, same pools and counts, bit for bit, as fs_prune_cells; the
+ * scratch is a fixed array inside the library instead of `ws`.
+ *  - Limit: fs_prune_static_scratch_bytes() (4 MiB per device), enough for
+ *    batch*H*ceil(N/2048) <= 4096; a larger shape returns
+ *    FS_ERR_SCRATCH_LIMIT and launches nothing.
+ *  - The array needs no initial contents (nothing in it must start at zero).
+ *  - Every call on a device uses the same array: calls that overlap in time
+ *    (other streams, or host threads without ordering) race on it.
+ *  - The first call on each device looks up the array's address (once, for
+ *    the device current at that call); make that first call before any
+ *    stream capture begins.
+ * Allocates nothing: no device or host memory is obtained. */
+size_t fs_prune_static_scratch_bytes(void);
+int fs_prune_cells_static(const float *amax, int batch, int H, int N,
+                          const fs_params *p, int32_t *pool,
+                          int32_t *pool_count, void *stream);
 
 /* Cell scoring and top-K (paper.rainbus.top summary, 核心方法 and
  * 方法步骤详情 ⑤; 局限与改进 for the erf factor; ai.info "Methodology in

@@ -3,6 +3,7 @@
 #include <stdio.h>
 
 #include <functional>
+#include <mutex>
 
 #include "fs_common.cuh"
 #include "fs_internal.h"
@@ -170,6 +171,9 @@ const char *fs_status_string(int status) {
     case FS_ERR_CUDA: return "CUDA error";
     case FS_ERR_TIMEOUT: return "device wait timed out";
     case FS_ERR_RANGE: return "a value of v is outside the fp16 range of the window product";
+    case FS_ERR_SCRATCH_LIMIT:
+      return "shape needs more scratch than the static array holds "
+             "(4 MiB: batch*H*ceil(N/2048) <= 4096)";
     default: return "unknown status";
   }
 }
@@ -385,6 +389,81 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   a.err = err;
   FS_TRY(status_of(launch_attn_tc(a, st)));
   return mark(4);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// fs_prune_cells_static: the pool construction without a caller workspace.
+//
+// Some callers have no device memory to hand over and may not obtain any:
+// code that runs where allocating is forbidden or impossible, such as a
+// memory allocator's own callbacks or out-of-memory handling, or a serving
+// loop whose device memory was fully reserved before it started, and that
+// owns no spare buffer it could lend as scratch.  For them this entry point
+// runs the same three pruning kernels on a fixed array compiled into the
+// library, so the call allocates nothing.
+//
+// Limit: kStaticScratchBytes (4 MiB per device) holds the two banks of
+// per-chunk lists the kernels ping-pong between, 2 * batch*H*ceil(C/64)
+// lists of 64 eight-byte keys; it serves batch*H*ceil(N/2048) <= 4096 (for
+// example 16 heads up to N = 512k).  Larger shapes are rejected with
+// FS_ERR_SCRATCH_LIMIT before anything is launched.  No byte of the array
+// needs to start at zero: every call writes each list before it reads it.
+// All calls on a device share the one array, so calls that overlap in time
+// (on different streams, or from host threads without ordering between
+// them) race on it.
+//
+// Set-up: the first call on each device (the device current at that call)
+// looks up the array's device address once with cudaGetSymbolAddress and
+// keeps it; make that first call before any stream capture begins.
+// ---------------------------------------------------------------------------
+namespace fs {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_prune_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_prune_scratch on the current device (looked up once).
+cudaError_t static_scratch(void **addr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_prune_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *addr = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" {
+
+size_t fs_prune_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+int fs_prune_cells_static(const float *amax, int batch, int H, int N, const fs_params *p,
+                          int32_t *pool, int32_t *pool_count, void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, kD));
+  if (!amax || !pool || !pool_count) return FS_ERR_INVALID_ARG;
+  if (p->mode != FS_MODE_FSL) return FS_ERR_INVALID_ARG;
+  const Shape sh{batch, H, N, kD};
+  if (prune_workspace_bytes(sh) > kStaticScratchBytes) return FS_ERR_SCRATCH_LIMIT;
+  void *scratch = nullptr;
+  FS_TRY(status_of(static_scratch(&scratch)));
+  return status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, scratch,
+                                static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

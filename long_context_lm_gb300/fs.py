@@ -20,14 +20,16 @@ import torch
 
 from . import build as _build
 
-FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_RANGE = range(6)
+(FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_RANGE,
+ FS_ERR_SCRATCH_LIMIT) = range(7)
 FS_BF16, FS_FP32 = 0, 1
 FS_MODE_FSL, FS_MODE_FS = 0, 1
 
 SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_workspace_bytes",
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
-           "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status"]
+           "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
+           "fs_prune_static_scratch_bytes", "fs_prune_cells_static"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cell_summary", "prune", "select", "attention"]
 
@@ -94,9 +96,12 @@ def load(build_if_stale: bool = True):
         L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
         L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 5
         L.fs_check_status.argtypes = [P, P]
+        L.fs_prune_static_scratch_bytes.argtypes = []
+        L.fs_prune_static_scratch_bytes.restype = Z
+        L.fs_prune_cells_static.argtypes = [P, I, I, I, PP, P, P, P]
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
-                            "fs_workspace_bytes",
+                            "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
@@ -194,6 +199,23 @@ def fs_prune_cells(amax, N, params=None, stream=None):
     ws = torch.empty(wsb, device=amax.device, dtype=torch.uint8)
     _check(L.fs_prune_cells(_ptr(amax), B, H, N, ctypes.byref(p), _ptr(pool), _ptr(count),
                             _ptr(ws), wsb, _stream(stream)), "fs_prune_cells")
+    return pool, count
+
+
+def fs_prune_cells_static(amax, N, params=None, pool=None, count=None, stream=None):
+    """fs_prune_cells on the library's fixed scratch array (no workspace).
+    ``pool`` / ``count`` may be given to avoid allocating outputs here."""
+    L = load()
+    p = _params(params)
+    _dev(amax, "amax", (torch.float32,))
+    B, H, C = amax.shape
+    nblk = N // p.Bq
+    if pool is None:
+        pool = torch.empty((B, H, nblk, p.P + p.W), device=amax.device, dtype=torch.int32)
+    if count is None:
+        count = torch.empty((B, H, nblk), device=amax.device, dtype=torch.int32)
+    _check(L.fs_prune_cells_static(_ptr(amax), B, H, N, ctypes.byref(p), _ptr(pool),
+                                   _ptr(count), _stream(stream)), "fs_prune_cells_static")
     return pool, count
 
 
