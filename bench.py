@@ -271,7 +271,73 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_extras:
+        res["decode"] = time_decode(q, k, v, lam, sigma, mix, params, stream)
+        res["fs_mode"] = time_fs_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
     return res
+
+
+def time_decode(q, k, v, lam, sigma, mix, params, stream, iters=200):
+    """One decode step at t = N (the token after the prefix) against the FS-L
+    state the prefix leaves: history caches, cell summaries, the pool of the
+    last block.  t = N starts a block, so every step also advances the pool;
+    the pool is restored (one small device copy, inside the timing) before
+    each step so that every step does the same work."""
+    from long_context_lm_gb300 import fs
+    B, H, N, d = q.shape
+    n_cap = N + 128
+    kc = torch.zeros((B, H, n_cap, d), device=q.device, dtype=q.dtype)
+    vc = torch.zeros_like(kc)
+    kc[:, :, :N] = k
+    vc[:, :, :N] = v
+    kbar, amax = fs.fs_cell_summarize(kc)
+    pool_all, count_all = fs.fs_prune_cells(amax, n_cap, params)
+    blk = (N - 1) // 128
+    cap = pool_all.shape[-1]
+    # pool and count share one buffer, so that one copy restores both
+    buf0 = torch.cat([pool_all[:, :, blk].reshape(-1), count_all[:, :, blk].reshape(-1)])
+    buf = buf0.clone()
+    st = dict(k_cache=kc, v_cache=vc, kbar=kbar, amax=amax,
+              pool=buf[:B * H * cap].view(B, H, cap), pool_count=buf[B * H * cap:].view(B, H))
+    qt, kt, vt = (x[:, :, N - 1].contiguous() for x in (q, k, v))
+    out = torch.empty((B, H, d), device=q.device, dtype=torch.float32)
+    for _ in range(5):
+        buf.copy_(buf0)
+        fs.fs_decode_step(qt, kt, vt, N, st, lam, sigma, mix, params, out=out)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        buf.copy_(buf0)
+        fs.fs_decode_step(qt, kt, vt, N, st, lam, sigma, mix, params, out=out)
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / iters * 1e3
+    return {"t": N, "us_per_token": us, "heads": B * H, "steps": iters,
+            "note": "per step: pool restore (1 copy) + fs_decode_step, all (batch, head) at once"}
+
+
+def time_fs_mode(q, k, v, lam, sigma, mix, params, stream, tokens, steps=3):
+    """Base FS (every available cell is a candidate, no pruning) on the same
+    inputs: the quadratic comparator of FS-L."""
+    from long_context_lm_gb300 import fs
+    from long_context_lm_gb300.fs import FS_N_STAGES
+    d = {f: getattr(params, f) for f, _ in params._fields_}  # a copy: params stays FS-L
+    d["mode"] = fs.FS_MODE_FS
+    B, H, N, hd = q.shape
+    ws = torch.empty(fs.fs_workspace_bytes(B, H, N, hd, d, fs.FS_BF16), device=q.device,
+                     dtype=torch.uint8)
+    out = torch.empty((B, H, N, hd), device=q.device, dtype=torch.float32)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(FS_N_STAGES + 1)]
+              for _ in range(steps + 1)]
+    for i in range(steps + 1):  # the first is a warm-up
+        fs.fs_attention_fwd_traced(q, k, v, lam, sigma, mix, events[i], d, out=out, ws=ws)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events[1:])
+    sel_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in events[1:])
+    return {"ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3), "select_ms": sel_ms,
+            "steps": steps}
 
 
 # ---------------------------------------------------------------------------
@@ -349,6 +415,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the decode-step and base-FS timings")
     ap.add_argument("--extra-lengths", default="fsl_16k_b2,fsl_256k",
                     help="other workloads timed briefly for the per-length figures ('none' = skip)")
     args = ap.parse_args()

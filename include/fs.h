@@ -114,6 +114,34 @@ int fs_prune_cells(const float *amax, int batch, int H, int N,
                    const fs_params *p, int32_t *pool, int32_t *pool_count,
                    void *ws, size_t ws_bytes, void *stream);
 
+/* One decode step of FS-L for token t of every (batch, head), against the
+ * bounded state the caller owns (paper.rainbus.top summary, 核心方法: linear
+ * prefill, constant-size decode state; 方法步骤详情 ②-⑥).  Per (batch, head):
+ *   q_t, k_t, v_t   [batch,H,d] bf16: the new token
+ *   k_cache,v_cache [batch,H,n_cap,d] bf16: rows < t hold the history; the
+ *                   step writes row t
+ *   kbar, amax      [batch,H,n_cap/s,d], [batch,H,n_cap/s] f32: cells
+ *                   < floor(t/s) hold their summaries; the step writes cell
+ *                   t/s when row t closes it ((t+1) % s == 0), bit-identical
+ *                   to fs_cell_summarize
+ *   pool, pool_count [batch,H,P+W] int32, [batch,H] int32: the pool of block
+ *                   floor((t-1)/Bq) in fs_prune_cells' row layout (count 0
+ *                   for t = 0); at a block start (t % Bq == 0, t > 0) the
+ *                   step advances it in place to block t/Bq, exactly as
+ *                   fs_prune_cells would compute that block
+ *   lambda, sigma, mix [H] f32
+ *   out_t           [batch,H,d] f32: row t of fs_attention_fwd's output
+ *   sel_t           [batch,H,K] int32 (nullable): the selected cells
+ * n_cap is a multiple of Bq and 0 <= t < n_cap; FS-L mode only; P + W <= 72.
+ * A step reads about (w + K*s) key/value rows and the pool's summaries per
+ * (batch, head); one CTA per (batch, head). */
+int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
+                   int batch, int H, int d, int t, int n_cap, void *k_cache,
+                   void *v_cache, float *kbar, float *amax, int32_t *pool,
+                   int32_t *pool_count, const float *lambda, const float *sigma,
+                   const float *mix, const fs_params *p, float *out_t,
+                   int32_t *sel_t, void *stream);
+
 /* fs_prune_cells for callers that can neither allocate device memory nor
  * lend a workspace (no counterpart on the pages: a library convenience).
  * Same arguments, same pools and counts, bit for bit, as fs_prune_cells; the

@@ -393,6 +393,50 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
 
 }  // extern "C"
 
+extern "C" int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
+                              int batch, int H, int d, int t, int n_cap, void *k_cache,
+                              void *v_cache, float *kbar, float *amax, int32_t *pool,
+                              int32_t *pool_count, const float *lambda, const float *sigma,
+                              const float *mix, const fs_params *p, float *out_t,
+                              int32_t *sel_t, void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, n_cap, d));
+  FS_TRY(check_dtype(dtype));
+  if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+  if (p->mode != FS_MODE_FSL) return FS_ERR_INVALID_ARG;
+  if (p->P + p->W > kMaxP + 8) return FS_ERR_UNSUPPORTED;
+  if (t < 0 || t >= n_cap) return FS_ERR_INVALID_ARG;
+  if (!q_t || !k_t || !v_t || !k_cache || !v_cache || !kbar || !amax || !pool || !pool_count ||
+      !lambda || !sigma || !mix || !out_t)
+    return FS_ERR_INVALID_ARG;
+  DecodeArgs a{};
+  a.q_t = q_t;
+  a.k_t = k_t;
+  a.v_t = v_t;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.kbar = kbar;
+  a.amax = amax;
+  a.pool = pool;
+  a.pool_count = pool_count;
+  a.lambda = lambda;
+  a.sigma = sigma;
+  a.mix = mix;
+  a.batch = batch;
+  a.H = H;
+  a.t = t;
+  a.n_cap = n_cap;
+  a.P = p->P;
+  a.W = p->W;
+  a.K = p->K;
+  a.w = p->w;
+  a.rope_base = p->rope_base;
+  a.rms_eps = p->rms_eps;
+  a.out = out_t;
+  a.sel_out = sel_t;
+  return status_of(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
 // ---------------------------------------------------------------------------
 // fs_prune_cells_static: the pool construction without a caller workspace.
 //

@@ -51,5 +51,19 @@ struct AttnArgs {
   int *err;
 };
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
+// One decode step for token t of every (batch, head) (see k6_decode.cu for
+// the state layout and what the step updates).
+struct DecodeArgs {
+  const void *q_t, *k_t, *v_t;
+  void *k_cache, *v_cache;
+  float *kbar, *amax;
+  int32_t *pool, *pool_count;
+  const float *lambda, *sigma, *mix;
+  int batch, H, t, n_cap, P, W, K, w;
+  float rope_base, rms_eps;
+  float *out;
+  int32_t *sel_out;
+};
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
 }  // namespace fs

@@ -10,6 +10,7 @@
 // warp reads 512 contiguous bytes per load instruction, and the CTA's eight
 // warps cover eight consecutive cells (32 KB).  Per token-head it reads 128 B
 // and writes 8 B (kbar fp32 and a_c, amortised over the 32 tokens).
+#include "cell_summary.cuh"
 #include "fs_common.cuh"
 #include "fs_internal.h"
 
@@ -22,25 +23,11 @@ __global__ void __launch_bounds__(256) k1_cell_summary_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long cell = (long long)blockIdx.x * 8 + warp;
   if (cell >= ncells) return;
-  const int g = lane & 7;      // dims 8g .. 8g+7
-  const int t0 = lane >> 3;    // tokens t0 + 4i
-
   float x[8][8];
   if constexpr (!kF32) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(k) + cell * (kS * kD / 8);
-    uint4 raw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) raw[i] = __ldg(src + (t0 + 4 * i) * 8 + g);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[i][2 * j] = bf16_lo(w[j]);
-        x[i][2 * j + 1] = bf16_hi(w[j]);
-      }
-    }
+    load_cell_bf16<true>(reinterpret_cast<const uint4 *>(k) + cell * (kS * kD / 8), lane, x);
   } else {
+    const int g = lane & 7, t0 = lane >> 3;
     const float4 *src = reinterpret_cast<const float4 *>(k) + cell * (kS * kD / 4);
     float4 raw[8][2];
 #pragma unroll
@@ -56,39 +43,7 @@ __global__ void __launch_bounds__(256) k1_cell_summary_kernel(
       for (int j = 0; j < 8; ++j) x[i][j] = __bfloat162float(__float2bfloat16_rn(f[j]));
     }
   }
-
-  float acc[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  float best = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float sq = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      acc[j] += x[i][j];
-      sq = fmaf(x[i][j], x[i][j], sq);
-    }
-    // the eight lanes holding token t0+4i: full squared norm
-    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 4);
-    best = fmaxf(best, sq);
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 8);
-    acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 16);
-  }
-  best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 8));
-  best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 16));
-  if (lane < 8) {
-    const float inv = 1.0f / kS;
-    float4 *dst = reinterpret_cast<float4 *>(kbar + cell * kD) + 2 * g;
-    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-  }
-  if (lane == 0) amax[cell] = sqrtf(best);
+  cell_summary_warp(x, lane, kbar + cell * kD, amax + cell);
 }
 
 cudaError_t launch_cell_summary(const void *k, bool f32, const Shape &sh, float *kbar,

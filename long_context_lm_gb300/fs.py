@@ -29,7 +29,7 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
-           "fs_prune_static_scratch_bytes", "fs_prune_cells_static"]
+           "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cell_summary", "prune", "select", "attention"]
 
@@ -99,6 +99,8 @@ def load(build_if_stale: bool = True):
         L.fs_prune_static_scratch_bytes.argtypes = []
         L.fs_prune_static_scratch_bytes.restype = Z
         L.fs_prune_cells_static.argtypes = [P, I, I, I, PP, P, P, P]
+        L.fs_decode_step.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, PP, P,
+                                     P, P]
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
                             "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
@@ -217,6 +219,30 @@ def fs_prune_cells_static(amax, N, params=None, pool=None, count=None, stream=No
     _check(L.fs_prune_cells_static(_ptr(amax), B, H, N, ctypes.byref(p), _ptr(pool),
                                    _ptr(count), _stream(stream)), "fs_prune_cells_static")
     return pool, count
+
+
+def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=None,
+                   sel=None, stream=None):
+    """One decode step for token t.  ``state`` is a dict of caller-owned device
+    tensors: k_cache, v_cache [B,H,n_cap,d] bf16; kbar [B,H,n_cap/32,d] and
+    amax [B,H,n_cap/32] f32; pool [B,H,P+W] and pool_count [B,H] int32 (all
+    updated in place as the step prescribes).  Returns out_t [B,H,d] f32."""
+    L = load()
+    p = _params(params)
+    for t_, n in ((q_t, "q_t"), (k_t, "k_t"), (v_t, "v_t")):
+        _dev(t_, n, (torch.bfloat16,))
+    B, H, d = q_t.shape
+    kc, vc = state["k_cache"], state["v_cache"]
+    _dev(kc, "k_cache", (torch.bfloat16,))
+    _dev(vc, "v_cache", (torch.bfloat16,))
+    n_cap = kc.shape[2]
+    out = out if out is not None else torch.empty((B, H, d), device=q_t.device, dtype=torch.float32)
+    _check(L.fs_decode_step(_ptr(q_t), _ptr(k_t), _ptr(v_t), FS_BF16, B, H, d, int(t), n_cap,
+                            _ptr(kc), _ptr(vc), _ptr(state["kbar"]), _ptr(state["amax"]),
+                            _ptr(state["pool"]), _ptr(state["pool_count"]), _ptr(lam),
+                            _ptr(sigma), _ptr(mix), ctypes.byref(p), _ptr(out), _ptr(sel),
+                            _stream(stream)), "fs_decode_step")
+    return out
 
 
 def fs_select_cells(q, kbar, amax, pool, pool_count, lam, sigma, params=None,
