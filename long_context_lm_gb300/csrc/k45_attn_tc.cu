@@ -836,30 +836,32 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   const uint32_t tmem = bar.tmem;
   const uint32_t sbase = smem_u32(smem);
 
-  // registers: the issuer / TMA / union warpgroup (warps 8-11) and the query
+  // Registers: the issuer / TMA / union warpgroup (warps 8-11) and the query
   // staging warpgroup (12-15) give up 56 per thread, the two softmax
   // warpgroups (0-7) take 56 more: 8*32*72 + 8*32*184 = 65536, the block's
-  // launch allotment of 512 x 128
-  if (warp >= 8)
-    tc::regs_dec<72>();
-  else
-    tc::regs_inc<184>();
+  // launch allotment of 512 x 128.  Each change sits inside its role's
+  // branch, so that the compiler sizes every role's code by its own count.
   if (warp < 8) {
+    tc::regs_inc<184>();
     role_softmax(p, bar, tmem, smem);
-  } else if (warp == 8 || warp == 9) {
-    if (lane == 0) {
-      if (warp == 8)
-        role_qk(p, bar, tmem, sbase);
-      else
-        role_pv(p, bar, tmem, sbase);
-      tc::mma_commit(&bar.fin[warp - 8]);  // every MMA this thread issued has completed
-      tc::mbar_wait(&bar.fin[warp - 8], 0, p.err);
+  } else if (warp < 12) {
+    tc::regs_dec<72>();
+    if (warp == 8 || warp == 9) {
+      if (lane == 0) {
+        if (warp == 8)
+          role_qk(p, bar, tmem, sbase);
+        else
+          role_pv(p, bar, tmem, sbase);
+        tc::mma_commit(&bar.fin[warp - 8]);  // every MMA this thread issued has completed
+        tc::mbar_wait(&bar.fin[warp - 8], 0, p.err);
+      }
+    } else if (warp == 10) {
+      if (lane == 0) role_tma(p, bar, smem, &tmap_kt, &tmap_v16, &cmap_k, &cmap_v);
+    } else {
+      role_union(p, bar, smem);
     }
-  } else if (warp == 10) {
-    if (lane == 0) role_tma(p, bar, smem, &tmap_kt, &tmap_v16, &cmap_k, &cmap_v);
-  } else if (warp == 11) {
-    role_union(p, bar, smem);
   } else {
+    tc::regs_dec<72>();
     role_qprep(p, bar, smem, threadIdx.x - kRotBase);
   }
   tc::fence_before_sync();
