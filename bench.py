@@ -35,6 +35,9 @@ from long_context_lm_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
 METRIC = "FS-L attn fwd tokens/s at 16k/64k/256k (H=16,d=64,bf16); % of roofline"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
+# dram__bytes_read.sum + dram__bytes_write.sum of fs_attn_tc_kernel in one ncu
+# capture (fsl_16k_b2: 288.83 + 103.62 MB over 2*16*16384 token-heads)
+ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (288.828928e6 + 103.619840e6) / (2 * 16 * 16384)
 
 
 # ---------------------------------------------------------------------------
@@ -246,17 +249,24 @@ def run_ours(args, rank, world, local_rank):
     wk = work[dom]
     if wk["bound"] == "tensor":
         ach = wk["flops"] / (stage_ms[dom] / 1e3) / 1e12
+        traffic = None
+        if dom == "attention" and params.mode == fs.FS_MODE_FSL:
+            # DRAM bytes per launch: the per-token figure of one ncu capture of
+            # the attention kernel (profiles/fs_attn_tc_kernel_fsl_16k_b2.md),
+            # scaled by the tokens one launch processes
+            traffic = ATTN_DRAM_BYTES_PER_TOKEN_HEAD * B * H * N
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
-                "unit": "TFLOP/s", "frac": ach / pk["bf16"], "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / pk["bf16"], "traffic": traffic,
                 "peak_source": pk["source"] + " (bf16 burst)"}
     else:
         ach = wk["bytes"] / (stage_ms[dom] / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
                 "frac": ach / pk["hbm"], "traffic": None, "peak_source": pk["source"]}
-    # our kernels per step: cells 1, prune (sort, scan when >1 chunk, emit),
-    # select 1, RoPE angle table 1, attention 1 (+3 roundings for fp32)
+    # our kernels per step: cell summaries 1, RoPE angle table 1, window operand
+    # preparation 1, prune (sort, scan when >1 chunk, emit), select 1,
+    # attention 1 (+3 roundings for fp32 inputs)
     prune_launches = 0 if params.mode == fs.FS_MODE_FS else 2 + (1 if N // 32 > 64 else 0)
-    launches_per_step = 1 + prune_launches + 1 + 2 + (3 if code == fs.FS_FP32 else 0)
+    launches_per_step = 3 + prune_launches + 1 + 1 + (3 if code == fs.FS_FP32 else 0)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

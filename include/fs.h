@@ -248,6 +248,14 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v,
  * or the synchronisation fails). */
 int fs_check_status(const void *ws, void *stream);
 
+/* Self-test of the bounded device waits (no counterpart on the pages): one
+ * CTA waits on an mbarrier that nothing completes; the wait gives up after
+ * its limit (about two seconds of SM clock) and records FS_ERR_TIMEOUT in the
+ * error word at the start of `ws` (cleared first), exactly as a stalled
+ * pipeline stage of the attention kernels would.  fs_check_status(ws) then
+ * returns FS_ERR_TIMEOUT.  No GPU fault is involved. */
+int fs_selftest_wait_timeout(void *ws, void *stream);
+
 /* Byte offsets of the intermediates inside an fs_attention_fwd workspace,
  * for inspection: kbar, amax, pool, pool_count, sel (any may be NULL).  The
  * long-branch output is never materialised: the attention kernel mixes it

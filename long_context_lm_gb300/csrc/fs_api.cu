@@ -7,6 +7,7 @@
 
 #include "fs_common.cuh"
 #include "fs_internal.h"
+#include "tc05.cuh"
 
 namespace fs {
 
@@ -435,6 +436,32 @@ extern "C" int fs_decode_step(const void *q_t, const void *k_t, const void *v_t,
   a.out = out_t;
   a.sel_out = sel_t;
   return status_of(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+namespace fs {
+namespace {
+// One CTA waits on an mbarrier that nothing ever completes: the bounded wait
+// gives up after its limit and records FS_ERR_TIMEOUT, as a stalled pipeline
+// stage would, and the kernel returns normally.
+__global__ void selftest_timeout_kernel(int *err) {
+  __shared__ __align__(8) uint64_t never;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&never, 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) tc::mbar_wait(&never, 0, err);
+}
+}  // namespace
+}  // namespace fs
+
+extern "C" int fs_selftest_wait_timeout(void *ws, void *stream) {
+  if (!ws) return FS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int *err = static_cast<int *>(ws);
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(err);
+  return status_of(cudaGetLastError());
 }
 
 // ---------------------------------------------------------------------------

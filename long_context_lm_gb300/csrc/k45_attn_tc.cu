@@ -315,6 +315,14 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
   }
 }
 
+// Before the CTA exits, every tile load this thread issued has landed (the
+// normal path consumed them all; after a wait gave up, this bounds the
+// wait for the ones still in flight by time only).
+__device__ void drain_tma(Barriers &bar, uint32_t issued) {
+  for (uint32_t T = issued > kRing ? issued - kRing : 0; T < issued; ++T)
+    tc::mbar_wait(&bar.raw_full[T % kRing], T / kRing, nullptr);
+}
+
 __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
                          const CUtensorMap *tkt, const CUtensorMap *tv16, const CUtensorMap *ck,
                          const CUtensorMap *cv) {
@@ -326,15 +334,15 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
     int nl = 0;
     for (int t = 0;; ++t, ++T) {
       if (t == it.nw) {
-        if (!wait_nth(&bar.u_full, i, p.err)) return;
+        if (!wait_nth(&bar.u_full, i, p.err)) return drain_tma(bar, T);
         nl = long_tiles(bar, p);
       }
       if (t >= it.nw + nl) break;
       const int slot = T % kRing;
       FS_TR(0, T);
       if (T >= kRing) {
-        if (!wait_nth(&bar.k_empty[slot], T / kRing - 1, p.err)) return;
-        if (!wait_nth(&bar.v_empty[slot], T / kRing - 1, p.err)) return;
+        if (!wait_nth(&bar.k_empty[slot], T / kRing - 1, p.err)) return drain_tma(bar, T);
+        if (!wait_nth(&bar.v_empty[slot], T / kRing - 1, p.err)) return drain_tma(bar, T);
       }
       unsigned char *kd = smem + kOffK + slot * 32768, *vd = smem + kOffV + slot * 16384;
       if (t < it.nw) {  // rotated keys (hi, lo) and fp16 values: 48 KB
@@ -359,6 +367,7 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
     }
     tc::mbar_arrive(&bar.u_free);  // the union list is no longer read
   }
+  drain_tma(bar, T);
 }
 
 // Union of the q-tile's selected cells, sorted ascending, by repeated
@@ -852,8 +861,10 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
           role_qk(p, bar, tmem, sbase);
         else
           role_pv(p, bar, tmem, sbase);
-        tc::mma_commit(&bar.fin[warp - 8]);  // every MMA this thread issued has completed
-        tc::mbar_wait(&bar.fin[warp - 8], 0, p.err);
+        // every MMA this thread issued has completed before TMEM is released
+        // (bounded by time only, even after an error was recorded)
+        tc::mma_commit(&bar.fin[warp - 8]);
+        tc::mbar_wait(&bar.fin[warp - 8], 0, nullptr);
       }
     } else if (warp == 10) {
       if (lane == 0) role_tma(p, bar, smem, &tmap_kt, &tmap_v16, &cmap_k, &cmap_v);

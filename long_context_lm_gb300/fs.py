@@ -29,7 +29,8 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
-           "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step"]
+           "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
+           "fs_selftest_wait_timeout"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cell_summary", "prune", "select", "attention"]
 
@@ -96,6 +97,7 @@ def load(build_if_stale: bool = True):
         L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
         L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 5
         L.fs_check_status.argtypes = [P, P]
+        L.fs_selftest_wait_timeout.argtypes = [P, P]
         L.fs_prune_static_scratch_bytes.argtypes = []
         L.fs_prune_static_scratch_bytes.restype = Z
         L.fs_prune_cells_static.argtypes = [P, I, I, I, PP, P, P, P]
@@ -219,6 +221,12 @@ def fs_prune_cells_static(amax, N, params=None, pool=None, count=None, stream=No
     _check(L.fs_prune_cells_static(_ptr(amax), B, H, N, ctypes.byref(p), _ptr(pool),
                                    _ptr(count), _stream(stream)), "fs_prune_cells_static")
     return pool, count
+
+
+def fs_selftest_wait_timeout(ws, stream=None):
+    """Launch the bounded-wait self-test into workspace ``ws`` (device uint8,
+    >= 256 bytes); read the outcome with fs_check_status(ws)."""
+    _check(load().fs_selftest_wait_timeout(_ptr(ws), _stream(stream)), "fs_selftest_wait_timeout")
 
 
 def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=None,
