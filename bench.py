@@ -44,6 +44,17 @@ ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (288.828928e6 + 103.619840e6) / (2 * 16 * 16384
 # helpers
 # ---------------------------------------------------------------------------
 
+def combine_ranks(ms, tokens_per_rank, world, device):
+    """Whole-job figure of a weak-scaling run: every rank processed
+    `tokens_per_rank` in `ms`; the job time is the slowest rank's (max over
+    ranks) and the throughput counts the tokens of all ranks."""
+    if world > 1:
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, tokens_per_rank * world / (ms / 1e3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -126,19 +137,23 @@ def stage_work(wl, distinct_cells, sel_counts):
     K, cap = p["K"], p["P"] + p["W"]
     tok = BH * N
     work = {}
-    # cell summaries: read k (bf16), write kbar (fp32) and amax
-    work["cell_summary"] = dict(bound="hbm", bytes=tok * d * 2 + BH * C * (d * 4 + 4))
+    # cell summaries (read k, write kbar fp32 and amax) and window operands
+    # (read k, v; write the rotated keys as bf16 hi | lo and v as fp16)
+    work["cells_prep"] = dict(bound="hbm", bytes=tok * d * 2 + BH * C * (d * 4 + 4)
+                              + tok * d * 2 * 2 + tok * d * 2 * 3)
     # prune: read amax (chunk sort + per block), write pools
     work["prune"] = dict(bound="latency", bytes=BH * C * 4 * 2 + BH * nblk * (cap + 1) * 4)
     # select: q (bf16), pool ids, mean keys of the pool cells once per block
     # (fp32), sel out; flops: q.kbar for every candidate of every query
     work["select"] = dict(bound="tensor", bytes=tok * d * 2 + BH * nblk * cap * (d * 4 + 8) + tok * K * 4,
                           flops=2.0 * d * float(sel_counts["cands"]))
-    # attention (both branches + mix): q, k, v (bf16), sel, out (fp32), the k/v
-    # of every distinct selected cell once; flops: QK^T and PV over the window
-    # keys of every query plus the tokens of its selected cells
+    # attention (both branches + mix): q (bf16), rotated keys (bf16 hi | lo),
+    # fp16 values, sel, out (fp32), the raw k/v of every distinct selected
+    # cell once; flops: QK^T and PV over the window keys of every query plus
+    # the tokens of its selected cells
     work["attention"] = dict(bound="tensor",
-                             bytes=tok * d * (2 * 3 + 4) + tok * K * 4 + distinct_cells * 32 * d * 2 * 2,
+                             bytes=tok * d * (2 + 4 + 2 + 4) + tok * K * 4
+                             + distinct_cells * 32 * d * 2 * 2,
                              flops=window_flops(BH, N, p["w"], d) + 4.0 * d * float(sel_counts["tokens_read"]))
     return work
 
@@ -201,13 +216,7 @@ def run_ours(args, rank, world, local_rank):
         total_ms = t0.elapsed_time(t1)
     stage_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
                 for j, name in enumerate(STAGE_NAMES)}
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = B * N * world
-    value = tokens / (ms / 1e3)
+    ms, value = combine_ranks(total_ms / args.steps, B * N, world, dev)
 
     # end to end through the public API with host buffers
     e2e = None

@@ -219,7 +219,8 @@ int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype,
                      const float *lambda, const float *sigma, const float *mix,
                      float *out, void *ws, size_t ws_bytes, void *stream);
 
-/* Number of timed stages of fs_attention_fwd_traced: cell summaries,
+/* Number of timed stages of fs_attention_fwd_traced: cell summaries and
+ * window-operand preparation (RoPE angle table, rotated keys, fp16 values),
  * pruning, selection, attention (window branch, NoPE readout of the selected
  * cells and the mix, in one kernel). */
 #define FS_N_STAGES 4

@@ -32,7 +32,7 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
            "fs_selftest_wait_timeout"]
 FS_N_STAGES = 4
-STAGE_NAMES = ["cell_summary", "prune", "select", "attention"]
+STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
 
 class fs_params(ctypes.Structure):
