@@ -27,6 +27,32 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Three-input maximum (one instruction on this architecture).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed fp32 pairs: (a.x*b.x + c.x, a.y*b.y + c.y) and (a.x+b.x, a.y+b.y),
+// each element rounded exactly as the scalar fmaf / add would round it.
+__device__ __forceinline__ unsigned long long f2_bits(float x, float y) {
+  return (unsigned long long)__float_as_uint(x) | ((unsigned long long)__float_as_uint(y) << 32);
+}
+__device__ __forceinline__ void fma2(float &rx, float &ry, float ax, float ay, float b, float c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(ax, ay)), "l"(f2_bits(b, b)),
+      "l"(f2_bits(c, c)));
+  rx = __uint_as_float((uint32_t)r);
+  ry = __uint_as_float((uint32_t)(r >> 32));
+}
+__device__ __forceinline__ void add2(float &ax, float &ay, float bx, float by) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(ax, ay)), "l"(f2_bits(bx, by)));
+  ax = __uint_as_float((uint32_t)r);
+  ay = __uint_as_float((uint32_t)(r >> 32));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half)
   return *reinterpret_cast<uint32_t *>(&h);

@@ -483,12 +483,14 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], bool is_long, int 
 }
 
 __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
+  // four running maxima, two new elements per three-input max
   float mx[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) mx[j] = __uint_as_float(x[j]);
 #pragma unroll
-  for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(x[c]));
-  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  for (int c = 4; c < 32; c += 2)
+    mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
+  return max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
 }
 
 // 2^(s*sl2 - m) for one chunk, written as pairs into 16 P columns: fp16 for a
@@ -497,15 +499,19 @@ __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
 template <bool kSplit>
 __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_addr,
                                            uint32_t pl_addr, float sl2, float m) {
+  // two pairs of partial sums (packed adds), arguments by packed FMA
   float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int h16 = 0; h16 < 2; ++h16) {
     uint32_t pk[8], pl[8];
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
-      const float e0 = tc::ex2(fmaf(__uint_as_float(x[16 * h16 + c]), sl2, -m));
-      const float e1 = tc::ex2(fmaf(__uint_as_float(x[16 * h16 + c + 1]), sl2, -m));
-      part[(c >> 1) & 3] += e0 + e1;
+      float a0, a1;
+      fma2(a0, a1, __uint_as_float(x[16 * h16 + c]), __uint_as_float(x[16 * h16 + c + 1]), sl2, -m);
+      const float e0 = tc::ex2(a0);
+      const float e1 = tc::ex2(a1);
+      const int q = (c >> 1) & 1;
+      add2(part[2 * q], part[2 * q + 1], e0, e1);
       if (kSplit) {  // long tile: bf16 hi + lo
         pk[c / 2] = pack_bf16(e0, e1);
         pl[c / 2] = pack_bf16(e0 - bf16_lo(pk[c / 2]), e1 - bf16_hi(pk[c / 2]));
