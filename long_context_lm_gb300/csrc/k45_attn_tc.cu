@@ -39,7 +39,7 @@
 // fp64 table) are split into bf16 hi + lo halves and S takes three MMA
 // chains (hi.hi + hi.lo + lo.hi): a single bf16 rounding of the rotated
 // vectors exceeds the output tolerance on lognormal keys.  The window P.V
-// product runs in fp16 (P below 256, V re-encoded exactly from bf16): with a
+// product runs in fp16 (P below 2^14, V re-encoded exactly from bf16): with a
 // lagging maximum the dominant probability is not exactly 1, and bf16's
 // 8-bit significand on it alone reaches the tolerance on peaked rows.  Long
 // branch: q and k are exact bf16, so S is one chain; P is split into bf16
@@ -99,9 +99,12 @@ constexpr uint32_t kSmemBytes = kOffRS + kMaxSel * 2 + 1024;  // + alignment sla
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint32_t kTmemCols = 512;
 // The running maximum is raised only when a tile's maximum exceeds it by more
-// than 2^8 (log2 units): probabilities stay below 256, and the accumulators
-// are rescaled (which waits for the previous P.V) only on such a jump.
-constexpr float kLazyMax = 8.f;
+// than 2^kLazy (log2 units); below that, probabilities are taken against the
+// old maximum and the accumulator is left alone (a raise rescales it, which
+// waits for the previous P.V).  The bound is what the formats hold: window P
+// is fp16 (values up to 2^14 < 65504), long-branch P is bf16 hi + lo with fp32
+// sums and accumulators (2^30 leaves room for 128 keys times |v|).
+constexpr float kLazyWin = 14.f, kLazyLong = 30.f;
 
 __device__ __forceinline__ uint32_t p_col(int k) {  // P of key group k (16 keys)
   return 32 * (k >> 1) + 8 * (k & 1);
@@ -731,7 +734,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         const float m = is_long ? ml : mw;
         float l = is_long ? ll : lw;
         const float mt = mx * sl2;
-        const float mnew = mt > m + kLazyMax ? mt : m;
+        const float mnew = mt > m + (is_long ? kLazyLong : kLazyWin) ? mt : m;
         const bool first = is_long ? t == it.nw : t == 0;
         // the accumulator holds exact zeros while m is -inf: nothing to rescale
         const bool resc = !first && m != -INFINITY && mnew != m;
