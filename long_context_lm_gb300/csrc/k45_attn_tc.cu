@@ -60,11 +60,13 @@ namespace {
 // [e*64 + t].
 #ifdef FS_TRACE
 __device__ long long *g_trace = nullptr;
-#define FS_TR(e, t)                                                                   \
-  do {                                                                                \
-    if (g_trace && blockIdx.x == 0 && (t) < 64) g_trace[(e) * 64 + (t)] = clock64(); \
+__shared__ long long *s_trace;  // CTA 0's copy of g_trace (null elsewhere)
+#define FS_TR(e, t)                                                  \
+  do {                                                               \
+    long long *tp_ = s_trace;                                        \
+    if (tp_ && (t) < 64) tp_[(e) * 64 + (t)] = clock64();            \
   } while (0)
-__device__ __forceinline__ bool g_trace_nu_enabled() { return g_trace && blockIdx.x == 0; }
+__device__ __forceinline__ bool g_trace_nu_enabled() { return s_trace != nullptr; }
 __device__ __forceinline__ void g_trace_nu(int i, int nu) { g_trace[9 * 64 + i] = nu; }
 #else
 __device__ __forceinline__ bool g_trace_nu_enabled() { return false; }
@@ -466,11 +468,14 @@ __device__ __forceinline__ void mask_window(uint32_t (&x)[32], int lo, int hi, i
     for (int c = 0; c < 32; ++c) x[c] = kNegInf;
     return;
   }
+  // bit c set iff column c0 + c lies in [lo, hi]; then one select per element
+  // (no per-element branches)
+  const int a = min(max(lo - c0, 0), 32), b = min(max(hi - c0 + 1, 0), 32);
+  const uint32_t below_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
+  const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+  const uint32_t valid = below_b & ~below_a;
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const int col = c0 + c;
-    if (col < lo || col > hi) x[c] = kNegInf;
-  }
+  for (int c = 0; c < 32; ++c) x[c] = (valid & (1u << c)) ? x[c] : kNegInf;
 }
 
 // Mask a 32-column chunk starting at tile column c0: window band [lo, hi],
@@ -479,9 +484,10 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], bool is_long, int 
                                            int c0, bool keep) {
   if (!is_long) {
     mask_window(x, lo, hi, c0);
-  } else if (!keep) {
+  } else {
+    if (__all_sync(0xffffffffu, keep)) return;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) x[c] = kNegInf;
+    for (int c = 0; c < 32; ++c) x[c] = keep ? x[c] : kNegInf;  // selects, not a branch
   }
 }
 
@@ -811,6 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   __shared__ Barriers bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+#ifdef FS_TRACE
+  if (threadIdx.x == 0) s_trace = blockIdx.x == 0 ? g_trace : nullptr;
+#endif
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar.q_full, kRotThreads);
     tc::mbar_init(&bar.q_empty, 1);
