@@ -121,11 +121,14 @@ struct Barriers {
   uint64_t p_full[2], pv_done;     // p_full per score buffer: the softmax may run a
                                   // tile ahead of the P.V issuer
   uint64_t o_done[2], o_free[2];  // per accumulator set
+  uint64_t stats_full[2], stat_free[2];  // per q-tile parity: row sums published / read
   uint64_t pair[4];               // the two softmax warps of a row block meet here
   uint64_t u_full, u_free;   // union of the q-tile's cells built / consumed
   uint64_t fin[2];
   uint32_t tmem;
   int nu;                    // cells in the current union
+  float2 stat[2][2][128];    // [q-tile parity][warp half][row]: (l_win, l_long) partial sums
+  int item_nl[2];            // [q-tile parity]: long tiles of that q-tile
   float2 xch[2][2][128];     // row values the two softmax warps of a row block
                              // exchange: [exchange parity][warp half][row]
 };
@@ -425,30 +428,44 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   }
 }
 
-// Query staging: row r of each q-tile, raw (NoPE long branch) and, for the
-// window, rotated by its absolute position and split into bf16 hi / lo.
-__device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, int r) {
+__device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int g, uint32_t i,
+                              int r);
+
+// Query staging and epilogue: row r of each q-tile, raw (NoPE long branch)
+// and, for the window, rotated by its absolute position and split into bf16
+// hi / lo; after staging q-tile i, the epilogue of q-tile i-1.  One pass
+// past the last q-tile runs the last epilogue.
+__device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, uint32_t tmem,
+                           int r) {
   uint32_t i = 0;
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
-    // fetch the row first, then wait until the previous q-tile's S MMAs no
-    // longer read the query tiles
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + r) * kD);
-    uint4 raw[8];
+  int g_prev = -1;
+  for (int g = blockIdx.x;; g += gridDim.x, ++i) {
+    const bool real = g < p.nitems;
+    if (real) {
+      const Item it = item_of(p, g);
+      // fetch the row first, then wait until the previous q-tile's S MMAs no
+      // longer read the query tiles
+      const uint4 *src =
+          reinterpret_cast<const uint4 *>(p.q + ((size_t)it.bh * p.N + it.b0 + r) * kD);
+      uint4 raw[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) raw[c] = __ldg(src + c);
-    if (i > 0 && !wait_nth(&bar.q_empty, i - 1, p.err)) return;
-    unsigned char *qh = smem + kOffQ, *qr = smem + kOffQR;
+      for (int c = 0; c < 8; ++c) raw[c] = __ldg(src + c);
+      if (i > 0 && !wait_nth(&bar.q_empty, i - 1, p.err)) return;
+      unsigned char *qh = smem + kOffQ, *qr = smem + kOffQR;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qr + swz128(r, c)) = raw[c];
-    if (p.has_window) {
+      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qr + swz128(r, c)) = raw[c];
+      if (p.has_window) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
-      rotate_row(qh, qh + 16384, r, it.b0 + r, smem, p.tab);
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
+        rotate_row(qh, qh + 16384, r, it.b0 + r, smem, p.tab);
+      }
+      tc::fence_async_smem();
+      tc::mbar_arrive(&bar.q_full);
+      if (r == 0) FS_TR(1, i);
     }
-    tc::fence_async_smem();
-    tc::mbar_arrive(&bar.q_full);
-    if (r == 0) FS_TR(1, i);
+    if (g_prev >= 0 && !epilogue_rows(p, bar, tmem, g_prev, i - 1, r)) return;
+    if (!real) break;
+    g_prev = g;
   }
 }
 
@@ -565,94 +582,87 @@ __device__ __forceinline__ void rescale(uint32_t addr, float alpha) {
   tc::tmem_st32(addr, o);
 }
 
-// Per-row state of a finished q-tile, kept until its epilogue runs.
-struct Done {
-  Item it;
-  uint32_t i;  // q-tile index of this CTA (accumulator set i & 1)
-  int nl;
-  float ll, lw;
-};
-
-// Epilogue of one q-tile: O_long / l_long and its RMSNorm over the 64
-// columns, O_win / l_win, the mix, the store.  The two warps of a row block
-// swap (l_long, l_win), then the long branch's partial sum of squares.
-__device__ __forceinline__ bool epilogue(const Params &p, Barriers &bar, uint32_t tmem,
-                                         const Done &d, Pair &pr, int quarter, int half,
-                                         int lane) {
-  const int r = quarter * 32 + lane;
-  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-  const uint32_t ow_addr = tmem + kColO + 128 * (d.i & 1) + 32 * half + lane_base;
-  const uint32_t ol_addr = ow_addr + 64;
-  if (!wait_nth(&bar.o_done[d.i & 1], d.i >> 1, p.err)) return false;
+// Epilogue of one q-tile, run by the query-staging warpgroup (warp 12 + q
+// reads TMEM lanes 32q..32q+31), one thread per query row and all 64 output
+// columns: O_long / l_long and its RMSNorm, O_win / l_win, the mix, the
+// store.  The softmax warps have moved on to the next q-tile; the P.V
+// issuer reuses this accumulator set only for the q-tile after that.
+__device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int g, uint32_t i,
+                              int r) {
+  const Item it = item_of(p, g);
+  const int lane = r & 31, par = i & 1;
+  const uint32_t lane_base = (uint32_t)(r & ~31) << 16;
+  if (!wait_nth(&bar.o_done[par], i >> 1, p.err)) return false;
+  if (!wait_nth(&bar.stats_full[par], i >> 1, p.err)) return false;
   tc::fence_after_sync();
-  if (r == 0 && half == 0) FS_TR(10, d.i);
-  const bool have_long = p.has_long && d.nl > 0;
-  const bool use_win = !p.write_long && d.it.nw > 0;
-
-  float2 o;
-  if (!pr.swap(make_float2(d.ll, d.lw), o, half, r, lane, p.err)) return false;
-  const float ltot = d.ll + o.x, wtot = d.lw + o.y;
-  const float invl = ltot > 0.f ? 1.f / ltot : 0.f;
+  if (r == 0) FS_TR(10, i);
+  const float2 s0 = bar.stat[par][0][r], s1 = bar.stat[par][1][r];
+  const int nl = bar.item_nl[par];
+  const float lw = s0.x + s1.x, ll = s0.y + s1.y;
+  const uint32_t ow = tmem + kColO + 128 * par + lane_base, ol = ow + 64;
+  const bool load_long = p.has_long && nl > 0;      // the whole warp (same q-tile)
+  const bool use_win = !p.write_long && it.nw > 0;  // the whole warp
+  const float invl = ll > 0.f ? 1.f / ll : 0.f;
   float lo_scale = 0.f;
-  if (p.has_long) {
+  if (load_long) {
     float sq[4] = {0.f, 0.f, 0.f, 0.f};
-    if (have_long) {
+#pragma unroll 1
+    for (int c32 = 0; c32 < 2; ++c32) {
+      uint32_t o[32];
+      tc::tmem_ld32(ol + 32 * c32, o);
+      tc::tmem_wait_ld();
 #pragma unroll
-      for (int c16 = 0; c16 < 2; ++c16) {
-        uint32_t o16[16];
-        tc::tmem_ld16(ol_addr + 16 * c16, o16);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float y = __uint_as_float(o16[c]) * invl;
-          sq[c & 3] = fmaf(y, y, sq[c & 3]);
-        }
+      for (int c = 0; c < 32; ++c) {
+        const float y = __uint_as_float(o[c]) * invl;
+        sq[c & 3] = fmaf(y, y, sq[c & 3]);
       }
     }
-    float ss = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-    if (!pr.swap(make_float2(ss, 0.f), o, half, r, lane, p.err)) return false;
-    ss += o.x;
-    lo_scale = (have_long && ltot > 0.f) ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
+    const float ss = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+    lo_scale = ll > 0.f ? invl * rsqrtf(ss / kD + p.rms_eps) : 0.f;
   }
-  const float wscale = d.it.nw > 0 ? 1.f / wtot : 0.f;
-  const size_t row = (size_t)d.it.bh * p.N + d.it.b0 + r;
-  float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD + 32 * half);
-  const float mh = p.mix ? p.mix[d.it.bh % p.H] : 0.f;
-  const bool use_long = lo_scale != 0.f;
+  const float wscale = it.nw > 0 ? 1.f / lw : 0.f;
+  const size_t row = (size_t)it.bh * p.N + it.b0 + r;
+  float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD);
+  const float mh = p.mix ? p.mix[it.bh % p.H] : 0.f;
+  const bool use_long = lo_scale != 0.f;  // this row
   const float4 *oin = (!p.write_long && !use_long && p.o_long_in)
-      ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD + 32 * half) : nullptr;
+      ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD) : nullptr;
   const float ls = p.write_long ? lo_scale : mh * lo_scale;
-  uint32_t ow[16], ol[16];
+#pragma unroll 1
+  for (int c16 = 0; c16 < kD / 16; ++c16) {
+    uint32_t w[16], l16[16];
+    if (use_win) tc::tmem_ld16(ow + 16 * c16, w);
+    if (load_long) tc::tmem_ld16(ol + 16 * c16, l16);
+    tc::tmem_wait_ld();
 #pragma unroll
-  for (int c4 = 0; c4 < 8; ++c4) {
-    if ((c4 & 3) == 0) {  // accumulators in 16-column pieces
-      if (use_win) tc::tmem_ld16(ow_addr + 4 * c4, ow);
-      if (use_long) tc::tmem_ld16(ol_addr + 4 * c4, ol);
-      tc::tmem_wait_ld();
+    for (int c4 = 0; c4 < 4; ++c4) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * c4 + e;
+        float y = use_win ? __uint_as_float(w[c]) * wscale : 0.f;
+        if (load_long) y = fmaf(ls, __uint_as_float(l16[c]), y);
+        v[e] = y;
+      }
+      float4 o4 = make_float4(v[0], v[1], v[2], v[3]);
+      if (oin) {
+        const float4 u4 = __ldg(oin + 4 * c16 + c4);
+        o4.x = fmaf(mh, u4.x, o4.x);
+        o4.y = fmaf(mh, u4.y, o4.y);
+        o4.z = fmaf(mh, u4.z, o4.z);
+        o4.w = fmaf(mh, u4.w, o4.w);
+      }
+      dst[4 * c16 + c4] = o4;
     }
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int o4 = 4 * (c4 & 3);
-    if (use_win)
-      v = make_float4(__uint_as_float(ow[o4]) * wscale, __uint_as_float(ow[o4 + 1]) * wscale,
-                      __uint_as_float(ow[o4 + 2]) * wscale, __uint_as_float(ow[o4 + 3]) * wscale);
-    if (use_long) {
-      v.x = fmaf(ls, __uint_as_float(ol[o4]), v.x);
-      v.y = fmaf(ls, __uint_as_float(ol[o4 + 1]), v.y);
-      v.z = fmaf(ls, __uint_as_float(ol[o4 + 2]), v.z);
-      v.w = fmaf(ls, __uint_as_float(ol[o4 + 3]), v.w);
-    } else if (oin) {
-      const float4 u4 = __ldg(oin + c4);
-      v.x = fmaf(mh, u4.x, v.x);
-      v.y = fmaf(mh, u4.y, v.y);
-      v.z = fmaf(mh, u4.z, v.z);
-      v.w = fmaf(mh, u4.w, v.w);
-    }
-    dst[c4] = v;
   }
+  // accumulator set and row-sum slot may be reused
   tc::fence_before_sync();
   __syncwarp();
-  if (lane == 0) tc::mbar_arrive(&bar.o_free[d.i & 1]);
-  if (r == 0 && half == 0) FS_TR(6, d.i);
+  if (lane == 0) {
+    tc::mbar_arrive(&bar.o_free[par]);
+    tc::mbar_arrive(&bar.stat_free[par]);
+  }
+  if (r == 0) FS_TR(6, i);
   return true;
 }
 
@@ -664,25 +674,16 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
   const uint16_t *rs = reinterpret_cast<const uint16_t *>(smem + kOffRS);
   const float sl2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
   uint32_t T = 0, i = 0;
-  Done prev;
-  bool pending = false;
   Pair pr{&bar.pair[quarter], bar.xch, 0u};
-  // one pass past the last q-tile runs the final epilogue
-  for (int g = blockIdx.x;; g += gridDim.x, ++i) {
-    const bool real = g < p.nitems;
-    Item it;
-    if (real) {
-      it = item_of(p, g);
-    } else {
-      it.bh = it.b0 = it.kt0 = it.nw = 0;
-    }
+  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+    const Item it = item_of(p, g);
     const int n = it.b0 + r;
     const uint32_t ow_addr = tmem + kColO + 128 * (i & 1) + 32 * half + lane_base;
     float mw = -INFINITY, lw = 0.f, ml = -INFINITY, ll = 0.f;
     int nl = 0;
     uint32_t pick[kMaxK / 2];  // this row's union slots, two 16-bit slots per word
     for (int t = 0;; ++t, ++T) {
-      if (real && t == it.nw) {
+      if (t == it.nw) {
         if (!wait_nth(&bar.u_full, i, p.err)) return;
         nl = long_tiles(bar, p);
 #pragma unroll
@@ -694,7 +695,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bar.u_free);  // union data read
       }
-      const bool done = !real || t >= it.nw + nl;
+      const bool done = t >= it.nw + nl;
       if (!done) {
         const bool is_long = t >= it.nw;
         const int b = T & 1;
@@ -791,19 +792,16 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         if (lane == 0) tc::mbar_arrive(&bar.p_full[b]);
         if (r == 0 && half == 0) FS_TR(4, T);
       }
-      if (pending && t == 0) {  // the previous q-tile's epilogue, off the MMA path
-        if (!epilogue(p, bar, tmem, prev, pr, quarter, half, lane)) return;
-        pending = false;
-      }
       if (done) break;
     }
-    if (!real) break;
-    prev.it = it;
-    prev.i = i;
-    prev.nl = nl;
-    prev.ll = ll;
-    prev.lw = lw;
-    pending = true;
+    // hand this half-row's sums to the epilogue warpgroup (slot of the
+    // q-tile's parity; it was read two q-tiles ago)
+    const int par = i & 1;
+    if (i >= 2 && !wait_nth(&bar.stat_free[par], (i >> 1) - 1, p.err)) return;
+    bar.stat[par][half][r] = make_float2(lw, ll);
+    if (warp == 0 && lane == 0) bar.item_nl[par] = nl;
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bar.stats_full[par]);
   }
 }
 
@@ -833,7 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
       tc::mbar_init(&bar.s_free[b], 1);
       tc::mbar_init(&bar.fin[b], 1);
       tc::mbar_init(&bar.o_done[b], 1);
-      tc::mbar_init(&bar.o_free[b], 8);
+      tc::mbar_init(&bar.o_free[b], 4);      // the epilogue (query-staging) warps
+      tc::mbar_init(&bar.stats_full[b], 8);  // the softmax warps
+      tc::mbar_init(&bar.stat_free[b], 4);
     }
     for (int b = 0; b < 2; ++b) tc::mbar_init(&bar.p_full[b], 8);
     for (int q4 = 0; q4 < 4; ++q4) tc::mbar_init(&bar.pair[q4], 2);
@@ -863,13 +863,14 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   const uint32_t tmem = bar.tmem;
   const uint32_t sbase = smem_u32(smem);
 
-  // Registers: the issuer / TMA / union warpgroup (warps 8-11) and the query
-  // staging warpgroup (12-15) give up 56 per thread, the two softmax
-  // warpgroups (0-7) take 56 more: 8*32*72 + 8*32*184 = 65536, the block's
-  // launch allotment of 512 x 128.  Each change sits inside its role's
-  // branch, so that the compiler sizes every role's code by its own count.
+  // Registers: the issuer / TMA / union warpgroup (warps 8-11) gives up 56
+  // per thread, the query-staging / epilogue warpgroup (12-15) 24, the two
+  // softmax warpgroups (0-7) take 40 more: 8*32*168 + 4*32*72 + 4*32*104 =
+  // 65536, the block's launch allotment of 512 x 128.  Each change sits
+  // inside its role's branch, so that the compiler sizes every role's code by
+  // its own count.
   if (warp < 8) {
-    tc::regs_inc<184>();
+    tc::regs_inc<168>();
     role_softmax(p, bar, tmem, smem);
   } else if (warp < 12) {
     tc::regs_dec<72>();
@@ -890,8 +891,8 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
       role_union(p, bar, smem);
     }
   } else {
-    tc::regs_dec<72>();
-    role_qprep(p, bar, smem, threadIdx.x - kRotBase);
+    tc::regs_dec<104>();
+    role_qprep(p, bar, smem, tmem, threadIdx.x - kRotBase);
   }
   tc::fence_before_sync();
   __syncthreads();
