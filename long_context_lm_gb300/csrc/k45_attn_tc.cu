@@ -495,19 +495,6 @@ __device__ __forceinline__ void mask_window(uint32_t (&x)[32], int lo, int hi, i
   for (int c = 0; c < 32; ++c) x[c] = (valid & (1u << c)) ? x[c] : kNegInf;
 }
 
-// Mask a 32-column chunk starting at tile column c0: window band [lo, hi],
-// or (long tile) the whole chunk is one cell the row picked or not.
-__device__ __forceinline__ void mask_chunk(uint32_t (&x)[32], bool is_long, int lo, int hi,
-                                           int c0, bool keep) {
-  if (!is_long) {
-    mask_window(x, lo, hi, c0);
-  } else {
-    if (__all_sync(0xffffffffu, keep)) return;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) x[c] = keep ? x[c] : kNegInf;  // selects, not a branch
-  }
-}
-
 __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
   // four running maxima, two new elements per three-input max
   float mx[4];
@@ -729,9 +716,17 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
           tc::tmem_ld32(s_addr + 32, xb);
           tc::tmem_wait_ld();
           if (r == 0 && half == 0) FS_TR(17, T);
-          mask_chunk(xa, is_long, lo, hi, 64 * half, cell[0]);
-          mask_chunk(xb, is_long, lo, hi, 64 * half + 32, cell[1]);
-          mx = fmaxf(max_chunk(xa), max_chunk(xb));
+          if (!is_long) {
+            mask_window(xa, lo, hi, 64 * half);
+            mask_window(xb, lo, hi, 64 * half + 32);
+            mx = fmaxf(max_chunk(xa), max_chunk(xb));
+          } else {
+            // a long tile's chunk is one cell, picked by the row or not: its
+            // scores are left as they are and the pick enters the maximum
+            // here and the probabilities below (through their reference)
+            const float ma = max_chunk(xa), mb = max_chunk(xb);
+            mx = fmaxf(cell[0] ? ma : -INFINITY, cell[1] ? mb : -INFINITY);
+          }
         }
         if (r == 0 && half == 0) FS_TR(11, T);
         float2 o;
@@ -753,8 +748,10 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
 #pragma unroll 1
           for (int ch = 0; ch < 2; ++ch) {
             const uint32_t pa = s_addr + 32 * ch;
-            l += is_long ? exp_chunk<true>(xa, pa, pa + 16, sl2, muse)
-                         : exp_chunk<false>(xa, pa, pa + 16, sl2, muse);
+            // an unpicked cell gets reference +inf: 2^(x - inf) = 0 exactly
+            const float mref = (is_long && !(ch ? cell[1] : cell[0])) ? INFINITY : muse;
+            l += is_long ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
+                         : exp_chunk<false>(xa, pa, pa + 16, sl2, mref);
             if (ch == 0) {
 #pragma unroll
               for (int c = 0; c < 32; ++c) xa[c] = xb[c];
