@@ -46,6 +46,13 @@ __device__ __forceinline__ void fma2(float &rx, float &ry, float ax, float ay, f
   rx = __uint_as_float((uint32_t)r);
   ry = __uint_as_float((uint32_t)(r >> 32));
 }
+// (a - b) on the two fp32 halves packed in 64-bit words (as bits).
+__device__ __forceinline__ unsigned long long sub2_bits(unsigned long long a,
+                                                       unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ void add2(float &ax, float &ay, float bx, float by) {
   unsigned long long r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(ax, ay)), "l"(f2_bits(bx, by)));

@@ -525,9 +525,12 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&x)[32], uint32_t p_a
       const float e1 = tc::ex2(a1);
       const int q = (c >> 1) & 1;
       add2(part[2 * q], part[2 * q + 1], e0, e1);
-      if (kSplit) {  // long tile: bf16 hi + lo
+      if (kSplit) {  // long tile: bf16 hi + lo (remainders by one packed subtract)
         pk[c / 2] = pack_bf16(e0, e1);
-        pl[c / 2] = pack_bf16(e0 - bf16_lo(pk[c / 2]), e1 - bf16_hi(pk[c / 2]));
+        const unsigned long long hi2 =
+            (unsigned long long)(pk[c / 2] << 16) | ((unsigned long long)(pk[c / 2] & 0xffff0000u) << 32);
+        const unsigned long long rem = sub2_bits(f2_bits(e0, e1), hi2);
+        pl[c / 2] = pack_bf16(__uint_as_float((uint32_t)rem), __uint_as_float((uint32_t)(rem >> 32)));
       } else {  // window tile: fp16
         pk[c / 2] = pack_f16(e0, e1);
       }
