@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kChunk = 128;       // candidates per MMA (N <= 128)
 constexpr int kThreads = 192;     // warps 0-3 score, warp 4 MMA, all stage operands
+constexpr int kGather = 4;        // 16-byte key chunks a thread gathers per pass
 constexpr uint32_t kOffQ = 0, kOffK = 16384;  // then 3 split tiles of `rows` x 128 B
 
 // candidate rows a chunk holds: the pool capacity (FS-L) or a full chunk (FS)
@@ -44,7 +45,7 @@ __device__ __forceinline__ bool ranks_before(float u, int c, float u2, int c2) {
 __device__ __noinline__ float erf_bias(float x) { return erff(x); }
 
 template <int K>
-__global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
+__global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
     const float *__restrict__ amax, const int32_t *__restrict__ pool,
     const int32_t *__restrict__ pool_count, const float *__restrict__ lambda,
@@ -75,12 +76,13 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
     tc::tmem_alloc(&s_tmem, 128);
     tc::tmem_relinquish();
   }
-  // query tile -> shared (K-major SW128)
+  // query tile -> shared (K-major SW128) by asynchronous copies, so that it
+  // lands while the candidate gathers below are in flight
   for (int p = tid; p < kBq * 8; p += kThreads) {
     const int r = p >> 3, ch = p & 7;
-    *reinterpret_cast<uint4 *>(smem + kOffQ + swz128(r, ch)) =
-        __ldg(reinterpret_cast<const uint4 *>(q + (head + b0 + r) * kD) + ch);
+    cp_async16(smem + kOffQ + swz128(r, ch), q + (head + b0 + r) * kD + ch * 8);
   }
+  cp_async_commit();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -107,44 +109,60 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
   for (int base = 0, chunk = 0; base < count; base += kChunk, ++chunk) {
     const int nc = min(kChunk, count - base);
     const int np = (nc + 15) / 16 * 16;
-    for (int j = tid; j < np; j += kThreads) {
-      int c = -1;
-      if (j < nc) {
-        c = fs_mode ? base + j : pl[base + j];
-        if (c < 0 || c >= A) c = -1;  // not a cell this block may read: skipped
-      }
-      s_c[j] = c;
-      s_a[j] = c >= 0 ? amax[(size_t)bh * C + c] : 0.f;
-    }
-    __syncthreads();
-    // mean keys -> three bf16 split tiles (rows beyond nc or skipped: zero)
+    // candidate ids, norms and mean keys in one pass: eight threads share a
+    // candidate (one 16-byte output chunk each), and the id is the only load
+    // ahead of the gathers.  Rows beyond nc or skipped cells stay zero.
     const uint32_t tile = (uint32_t)chunk_rows(fs_mode, cap) * 128;
-    for (int p = tid; p < np * 8; p += kThreads) {
-      const int j = p >> 3, ch = p & 7;
-      const int c = s_c[j];
-      float x[8];
-      if (c >= 0) {
-        const float4 *src = reinterpret_cast<const float4 *>(kbar + ((size_t)bh * C + c) * kD) + 2 * ch;
-        const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
-        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
-        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-      } else {
+    for (int p0 = 0; p0 < np * 8; p0 += kGather * kThreads) {
+      int cj[kGather];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      for (int it = 0; it < kGather; ++it) {
+        const int j = (p0 + tid + it * kThreads) >> 3;
+        int c = -1;
+        if (j < nc) {
+          c = fs_mode ? base + j : __ldg(pl + base + j);
+          if (c < 0 || c >= A) c = -1;  // not a cell this block may read: skipped
+        }
+        cj[it] = c;
       }
-      uint32_t hw[4], mw[4], lw[4];
+      float x[kGather][8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        hw[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
-        const float r0 = x[2 * e] - bf16_lo(hw[e]), r1 = x[2 * e + 1] - bf16_hi(hw[e]);
-        mw[e] = pack_bf16(r0, r1);
-        lw[e] = pack_bf16(r0 - bf16_lo(mw[e]), r1 - bf16_hi(mw[e]));
+      for (int it = 0; it < kGather; ++it) {
+        const int p = p0 + tid + it * kThreads, j = p >> 3, ch = p & 7;
+        const int c = cj[it];
+        if (c >= 0) {
+          const float4 *src = reinterpret_cast<const float4 *>(kbar + ((size_t)bh * C + c) * kD) + 2 * ch;
+          const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
+          x[it][0] = u0.x; x[it][1] = u0.y; x[it][2] = u0.z; x[it][3] = u0.w;
+          x[it][4] = u1.x; x[it][5] = u1.y; x[it][6] = u1.z; x[it][7] = u1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[it][e] = 0.f;
+        }
+        if (ch == 0 && j < np) {
+          s_c[j] = c;
+          s_a[j] = c >= 0 ? __ldg(amax + (size_t)bh * C + c) : 0.f;
+        }
       }
-      const uint32_t off = swz128(j, ch);
-      *reinterpret_cast<uint4 *>(smem + kOffK + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4 *>(smem + kOffK + tile + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-      *reinterpret_cast<uint4 *>(smem + kOffK + 2 * tile + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+      for (int it = 0; it < kGather; ++it) {
+        const int p = p0 + tid + it * kThreads, j = p >> 3, ch = p & 7;
+        if (j >= np) break;
+        uint32_t hw[4], mw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hw[e] = pack_bf16(x[it][2 * e], x[it][2 * e + 1]);
+          const float r0 = x[it][2 * e] - bf16_lo(hw[e]), r1 = x[it][2 * e + 1] - bf16_hi(hw[e]);
+          mw[e] = pack_bf16(r0, r1);
+          lw[e] = pack_bf16(r0 - bf16_lo(mw[e]), r1 - bf16_hi(mw[e]));
+        }
+        const uint32_t off = swz128(j, ch);
+        *reinterpret_cast<uint4 *>(smem + kOffK + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(smem + kOffK + tile + off) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+        *reinterpret_cast<uint4 *>(smem + kOffK + 2 * tile + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     }
+    cp_async_wait<0>();  // the query tile (first chunk; a no-op afterwards)
     tc::fence_async_smem();
     __syncthreads();
     if (tid == 128) {  // warp 4, one thread: D = Q.(hi + mid + lo)^T
@@ -200,6 +218,7 @@ __global__ void __launch_bounds__(kThreads) k3_select_tc_kernel(
     tc::fence_before_sync();
     __syncthreads();  // shared tiles and TMEM are reused by the next chunk
   }
+  cp_async_wait<0>();  // a block with no candidates never waited above
   if (warp < 4 && ok) {
 #pragma unroll
     for (int i = 0; i < K; ++i) {
