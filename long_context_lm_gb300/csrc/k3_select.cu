@@ -29,6 +29,8 @@ namespace {
 constexpr int kChunk = 128;       // candidates per MMA (N <= 128)
 constexpr int kThreads = 192;     // warps 0-3 score, warp 4 MMA, all stage operands
 constexpr int kGather = 4;        // 16-byte key chunks a thread gathers per pass
+constexpr int kInvalid = 0x7fffffff;          // candidate slot holding no cell
+constexpr int kNeedsErf = int(0x80000000u);   // flag bit on a candidate's cell id
 constexpr uint32_t kOffQ = 0, kOffK = 16384;  // then 3 split tiles of `rows` x 128 B
 
 // candidate rows a chunk holds: the pool capacity (FS-L) or a full chunk (FS)
@@ -45,7 +47,7 @@ __device__ __forceinline__ bool ranks_before(float u, int c, float u2, int c2) {
 __device__ __noinline__ float erf_bias(float x) { return erff(x); }
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
+__global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
     const float *__restrict__ amax, const int32_t *__restrict__ pool,
     const int32_t *__restrict__ pool_count, const float *__restrict__ lambda,
@@ -54,8 +56,11 @@ __global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ int s_c[kChunk];
-  __shared__ float s_a[kChunk];
+  // per candidate, what every row shares: (cell id, lambda_h * a_c).  The id
+  // is kInvalid for an empty or skipped slot (lambda * a then -inf, so it never
+  // ranks), and carries kNeedsErf when the bias factor can fall below 1 for
+  // some row of the block.
+  __shared__ int2 s_ca[kChunk];
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t s_tmem;
 
@@ -99,11 +104,10 @@ __global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
 #pragma unroll
   for (int i = 0; i < K; ++i) {
     bu[i] = -INFINITY;
-    bc[i] = 0x7fffffff;
+    bc[i] = kInvalid;
   }
   float wu = -INFINITY;
-  int wc = 0x7fffffff;
-  int nvalid = 0;
+  int wc = kInvalid;
   bool ok = true;
 
   for (int base = 0, chunk = 0; base < count; base += kChunk, ++chunk) {
@@ -140,8 +144,15 @@ __global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
           for (int e = 0; e < 8; ++e) x[it][e] = 0.f;
         }
         if (ch == 0 && j < np) {
-          s_c[j] = c;
-          s_a[j] = c >= 0 ? __ldg(amax + (size_t)bh * C + c) : 0.f;
+          int cf = kInvalid;
+          float la = -INFINITY;
+          if (c >= 0) {
+            la = lam * __ldg(amax + (size_t)bh * C + c);
+            // x grows with n, so the block's first row has the smallest one
+            const float x0 = sig_s * ((float)(b0 - c * kS) - 0.5f * kS);
+            cf = x0 < 4.0f ? (c | kNeedsErf) : c;
+          }
+          s_ca[j] = make_int2(cf, __float_as_int(la));
         }
       }
 #pragma unroll
@@ -183,20 +194,25 @@ __global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
       ok = tc::mbar_wait(&bar, chunk & 1, err) && ok;
       tc::fence_after_sync();
       const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-      for (int j0 = 0; j0 < nc; j0 += 32) {
+      for (int j0 = 0; j0 < np; j0 += 32) {
         uint32_t d[32];
-        tc::tmem_ld32(taddr + j0, d);
+        tc::tmem_ld32(taddr + j0, d);  // columns past np are read, never used
         tc::tmem_wait_ld();
-        const int jn = min(32, nc - j0);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
-          if (jj >= jn) break;
-          const int c = s_c[j0 + jj];
-          if (c < 0) continue;
-          ++nvalid;
-          const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
-          const float g = x < 4.0f ? erf_bias(x) : 1.0f;
-          float u = __uint_as_float(d[jj]) + lam * s_a[j0 + jj] * g;
+          if (jj == 16 && j0 + 16 >= np) break;  // np is a multiple of 16
+          const int2 ca = s_ca[j0 + jj];
+          const float la = __int_as_float(ca.y);
+          int c = ca.x;
+          float u;
+          if (c < 0) {  // kNeedsErf (the same for every lane of the warp)
+            c &= ~kNeedsErf;
+            const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
+            const float g = x < 4.0f ? erf_bias(x) : 1.0f;
+            u = __uint_as_float(d[jj]) + la * g;
+          } else {
+            u = __uint_as_float(d[jj]) + la;  // g = 1 exactly
+          }
           if (!ranks_before(u, c, wu, wc)) continue;
           int cu = c;
 #pragma unroll
@@ -222,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 4) k3_select_tc_kernel(
   if (warp < 4 && ok) {
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      const bool valid = i < nvalid;
+      const bool valid = bc[i] != kInvalid;  // fewer than K readable cells
       sel[(head + n) * K + i] = valid ? bc[i] : -1;
       if (sel_score) sel_score[(head + n) * K + i] = valid ? bu[i] : 0.f;
     }
