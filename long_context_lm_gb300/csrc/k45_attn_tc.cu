@@ -42,9 +42,12 @@
 // product runs in fp16 (P below 2^14, V re-encoded exactly from bf16): with a
 // lagging maximum the dominant probability is not exactly 1, and bf16's
 // 8-bit significand on it alone reaches the tolerance on peaked rows.  Long
-// branch: q and k are exact bf16, so S is one chain; P is split into bf16
-// hi + lo halves (two P.V chains) because RMSNorm rescales the branch output
-// and would amplify a plain bf16 rounding of P.
+// branch: q and k are exact bf16, so S is one chain.  RMSNorm rescales the
+// branch output, which amplifies the rounding of P: a plain bf16 P reaches
+// about 5e-3 after the norm, fp16 P about 6e-4.  So next to the window
+// branch (whose fp16 values exist) the long P is fp16 with one P.V chain;
+// the long branch alone splits P into bf16 hi + lo (two chains) against the
+// raw bf16 values.
 #include <cuda.h>
 #include <string.h>
 
@@ -96,16 +99,17 @@ constexpr uint32_t kSmemBytes = kOffRS + kMaxSel * 2 + 1024;  // + alignment sla
 
 // TMEM columns: S / P buffers at 0 and 128; accumulator sets at 256 and 384
 // (O_win at +0, O_long at +64).  Inside a score buffer, key chunk c (32 keys)
-// keeps its P in columns 32c..32c+15 and P_lo in 32c+16..32c+31, so each
-// softmax warp writes only the columns it has already read.
+// keeps its P in columns 32c..32c+15 (and, for a bf16 hi + lo long tile, P_lo
+// in 32c+16..32c+31), so each softmax warp writes only the columns it has
+// already read.
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint32_t kTmemCols = 512;
 // The running maximum is raised only when a tile's maximum exceeds it by more
 // than 2^kLazy (log2 units); below that, probabilities are taken against the
 // old maximum and the accumulator is left alone (a raise rescales it, which
-// waits for the previous P.V).  The bound is what the formats hold: window P
-// is fp16 (values up to 2^14 < 65504), long-branch P is bf16 hi + lo with fp32
-// sums and accumulators (2^30 leaves room for 128 keys times |v|).
+// waits for the previous P.V).  The bound is what the formats hold: fp16 P
+// (values up to 2^14 < 65504); bf16 hi + lo long-branch P with fp32 sums and
+// accumulators (2^30 leaves room for 128 keys times |v|).
 constexpr float kLazyWin = 14.f, kLazyLong = 30.f;
 
 __device__ __forceinline__ uint32_t p_col(int k) {  // P of key group k (16 keys)
@@ -141,6 +145,8 @@ struct Params {
   const float2 *tab;       // (cos, sin) of r*theta_i (rows r < 64), 64*u*theta_i (row 64 + u)
   int H, N, w, K, nblk, nitems;
   int has_window, has_long, write_long;  // write_long: output RMSNorm(o_long) only
+  int long16;              // long-branch P in fp16 against the fp16 values (the
+                           // window's encoding); else bf16 hi + lo against raw v
   float rms_eps;
   size_t nrows;            // BH * N (first out-of-range key row: zero fill)
   float *out;
@@ -278,7 +284,7 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
 
 __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t base) {
   const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);  // long: bf16 P hi / lo, bf16 V
-  const uint32_t id_pv_h = tc::idesc_f16(128, kD, 1);  // window: fp16 P, fp16 V
+  const uint32_t id_pv_h = tc::idesc_f16(128, kD, 1);  // window (and long16): fp16 P, V
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
@@ -305,6 +311,12 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
         for (int k = 0; k < kKT / 16; ++k)
           tc::mma_ts(ob, sp + p_col(k), dv + (uint64_t)(k * 128), id_pv_h,
                      (t > 0 || k > 0) ? 1u : 0u);
+      } else if (p.long16) {
+        const bool first = t == it.nw;
+#pragma unroll
+        for (int k = 0; k < kKT / 16; ++k)
+          tc::mma_ts(ob + 64, sp + p_col(k), dv + (uint64_t)(k * 128), id_pv_h,
+                     (!first || k > 0) ? 1u : 0u);
       } else {
         const bool first = t == it.nw;
 #pragma unroll
@@ -359,7 +371,7 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
         tc::tma_load_2d(kd, tkt, &bar.raw_full[slot], 0, y);
         tc::tma_load_2d(kd + 16384, tkt, &bar.raw_full[slot], kD, y);
         tc::tma_load_2d(vd, tv16, &bar.raw_full[slot], 0, y);
-      } else {  // raw keys and values of four cells: 32 KB
+      } else {  // raw keys and values (fp16 copy under long16) of four cells: 32 KB
         tc::mbar_arrive_expect_tx(&bar.raw_full[slot], 2 * kKT * kD * 2);
         // four cells of the union; a missing cell reads zeros from past the
         // last row, so stale data never meets a zero probability
@@ -688,6 +700,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
       const bool done = t >= it.nw + nl;
       if (!done) {
         const bool is_long = t >= it.nw;
+        const bool split = is_long && !p.long16;  // bf16 hi + lo P
         const int b = T & 1;
         const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
         if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
@@ -739,7 +752,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         const float m = is_long ? ml : mw;
         float l = is_long ? ll : lw;
         const float mt = mx * sl2;
-        const float mnew = mt > m + (is_long ? kLazyLong : kLazyWin) ? mt : m;
+        const float mnew = mt > m + (split ? kLazyLong : kLazyWin) ? mt : m;
         const bool first = is_long ? t == it.nw : t == 0;
         // the accumulator holds exact zeros while m is -inf: nothing to rescale
         const bool resc = !first && m != -INFINITY && mnew != m;
@@ -753,8 +766,8 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
             const uint32_t pa = s_addr + 32 * ch;
             // an unpicked cell gets reference +inf: 2^(x - inf) = 0 exactly
             const float mref = (is_long && !(ch ? cell[1] : cell[0])) ? INFINITY : muse;
-            l += is_long ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
-                         : exp_chunk<false>(xa, pa, pa + 16, sl2, mref);
+            l += split ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
+                       : exp_chunk<false>(xa, pa, pa + 16, sl2, mref);
             if (ch == 0) {
 #pragma unroll
               for (int c = 0; c < 32; ++c) xa[c] = xb[c];
@@ -766,7 +779,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
           for (int c = 0; c < 16; ++c) z[c] = 0u;
           tc::tmem_st16(s_addr, z);
           tc::tmem_st16(s_addr + 32, z);
-          if (is_long) {
+          if (split) {
             tc::tmem_st16(s_addr + 16, z);
             tc::tmem_st16(s_addr + 48, z);
           }
@@ -958,8 +971,11 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   if (a.window && (!make_rows_map(&mkt, a.kt, nrows, 2 * kD, kKT, false) ||
                    !make_rows_map(&mv16, a.v16, nrows, kD, kKT, true)))
     return cudaErrorInvalidValue;
+  // with the window branch the fp16 values exist, and the long branch reads
+  // its cells from them too
+  const bool long16 = a.window && a.sel != nullptr;
   if (!make_rows_map(&ck, a.k, nrows, kD, kS, false) ||
-      !make_rows_map(&cv, a.v, nrows, kD, kS, false))
+      !make_rows_map(&cv, long16 ? a.v16 : a.v, nrows, kD, kS, long16))
     return cudaErrorInvalidValue;
   Params p;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -976,6 +992,7 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   p.has_window = a.window ? 1 : 0;
   p.has_long = a.sel ? 1 : 0;
   p.write_long = a.write_long ? 1 : 0;
+  p.long16 = long16 ? 1 : 0;
   p.rms_eps = a.rms_eps;
   p.nrows = nrows;
   p.out = a.out;
