@@ -228,8 +228,11 @@ __device__ __forceinline__ void rotate_row(unsigned char *hi, unsigned char *lo,
                                            const unsigned char *smem, const float2 *tab) {
   const float2 *t64r = reinterpret_cast<const float2 *>(smem + kOffT64 + (n & 63) * kT64Stride);
   const float2 *tur = tab + (size_t)(64 + (n >> 6)) * (kD / 2);
-  rotate_half_row(hi, lo, r, 0, t64r, tur);
-  rotate_half_row(hi, lo, r, 1, t64r, tur);
+  // one copy of the half-row code: the staging warps also run the epilogue,
+  // and straight-line code here competes with the softmax loop for the
+  // instruction cache
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) rotate_half_row(hi, lo, r, half, t64r, tur);
 }
 
 // --------------------------------------------------------------------------
@@ -256,6 +259,7 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
       if (T >= 2 && !wait_nth(&bar.s_free[b], T / 2 - 1, p.err)) return;
       tc::fence_after_sync();
+      FS_TR(18, T);
       const uint32_t kh = base + kOffK + slot * 32768;
       const uint64_t dkh = tc::desc_sw128(kh), dkl = tc::desc_sw128(kh + 16384);
       const uint32_t s_col = tmem + kColS + 128 * b;
@@ -301,8 +305,10 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       if (t >= it.nw + nl) break;
       const int slot = T % kRing, b = T & 1;
       if (!wait_nth(&bar.p_full[b], T / 2, p.err)) return;
+      FS_TR(19, T);
       // the value tile is read by this thread's MMAs: observe its arrival here too
       if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
+      FS_TR(20, T);
       tc::fence_after_sync();
       const uint64_t dv = tc::desc_sw128(base + kOffV + slot * 16384);
       const uint32_t sp = tmem + kColS + 128 * b;
@@ -668,6 +674,31 @@ __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int
   return true;
 }
 
+// Which of the warp's 64 columns of key tile t its rows read: the window
+// bounds [lo, hi] of the row, or which of the long tile's two cells the row
+// picked.  Returns whether any lane of the warp reads a column.
+__device__ __forceinline__ bool tile_cols(const Params &p, const Item &it, int t, int n, int half,
+                                          const uint32_t (&pick)[kMaxK / 2], int &lo, int &hi,
+                                          bool (&cell)[2]) {
+  cell[0] = cell[1] = false;
+  lo = 0;
+  hi = -1;
+  if (t < it.nw) {
+    const int kt = it.kt0 + t * kKT;
+    lo = max(0, n - p.w + 1 - kt);
+    hi = min(kKT - 1, n - kt);
+    return __any_sync(0xffffffffu, lo <= hi && hi >= 64 * half && lo <= 64 * half + 63);
+  }
+  const uint32_t u0 = 4 * (t - it.nw) + 2 * half;
+#pragma unroll
+  for (int k = 0; k < kMaxK / 2; ++k) {
+    const uint32_t a = pick[k] & 0xffffu, bb = pick[k] >> 16;
+    cell[0] |= (a == u0) || (bb == u0);
+    cell[1] |= (a == u0 + 1) || (bb == u0 + 1);
+  }
+  return __any_sync(0xffffffffu, cell[0] || cell[1]);
+}
+
 __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsigned char *smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, half = warp >> 2;
@@ -706,23 +737,9 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
         tc::fence_after_sync();
         if (r == 0 && half == 0) FS_TR(3, T);
-        bool any, cell[2] = {false, false};
-        int lo = 0, hi = -1;
-        if (!is_long) {
-          const int kt = it.kt0 + t * kKT;
-          lo = max(0, n - p.w + 1 - kt);
-          hi = min(kKT - 1, n - kt);
-          any = __any_sync(0xffffffffu, lo <= hi && hi >= 64 * half && lo <= 64 * half + 63);
-        } else {
-          const uint32_t u0 = 4 * (t - it.nw) + 2 * half;
-#pragma unroll
-          for (int k = 0; k < kMaxK / 2; ++k) {
-            const uint32_t a = pick[k] & 0xffffu, bb = pick[k] >> 16;
-            cell[0] |= (a == u0) || (bb == u0);
-            cell[1] |= (a == u0 + 1) || (bb == u0 + 1);
-          }
-          any = __any_sync(0xffffffffu, cell[0] || cell[1]);
-        }
+        bool cell[2];
+        int lo, hi;
+        const bool any = tile_cols(p, it, t, n, half, pick, lo, hi, cell);
         // the warp's 64 score columns in one TMEM round trip
         uint32_t xa[32], xb[32];
         float mx = -INFINITY;
