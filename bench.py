@@ -36,8 +36,8 @@ METRIC = "FS-L attn fwd tokens/s at 16k/64k/256k (H=16,d=64,bf16); % of roofline
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of fs_attn_tc_kernel in one ncu
-# capture (fsl_16k_b2: 288.83 + 103.62 MB over 2*16*16384 token-heads)
-ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (288.828928e6 + 103.619840e6) / (2 * 16 * 16384)
+# capture (fsl_16k_b2: 281.90 + 102.60 MB over 2*16*16384 token-heads)
+ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (281.901568e6 + 102.599936e6) / (2 * 16 * 16384)
 
 
 # ---------------------------------------------------------------------------
