@@ -35,6 +35,7 @@ from long_context_lm_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
 METRIC = "FS-L attn fwd tokens/s at 16k/64k/256k (H=16,d=64,bf16); % of roofline"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
+E2E_HEADS = 4  # heads per group of the host-buffer pipeline (2.43 ms vs 2.50 for 2, 2.46 for 8)
 # dram__bytes_read.sum + dram__bytes_write.sum of fs_attn_tc_kernel in one ncu
 # capture (fsl_16k_b2: 281.90 + 102.60 MB over 2*16*16384 token-heads)
 ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (281.901568e6 + 102.599936e6) / (2 * 16 * 16384)
@@ -218,28 +219,33 @@ def run_ours(args, rank, world, local_rank):
                 for j, name in enumerate(STAGE_NAMES)}
     ms, value = combine_ranks(total_ms / args.steps, B * N, world, dev)
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: fs_attention_fwd_host
+    # takes pinned host q, k, v and returns out in pinned host memory, its
+    # copies pipelined with the compute over groups of E2E_HEADS heads
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
         hout = torch.empty((B, H, N, d), dtype=torch.float32).pin_memory()
+        ws_h = torch.empty(fs.fs_host_workspace_bytes(B, H, N, d, params, code, E2E_HEADS),
+                           device=dev, dtype=torch.uint8)
         e2e_steps = max(2, min(args.steps, 5))
+        fs.fs_attention_fwd_host(hq, hk, hv, lam, sigma, mix, params, out=hout, ws=ws_h,
+                                 heads_per_chunk=E2E_HEADS)  # first call: copy streams
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(e2e_steps):
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            fs.fs_attention_fwd(q, k, v, lam, sigma, mix, params, out=out, ws=ws)
-            hout.copy_(out, non_blocking=True)
+            fs.fs_attention_fwd_host(hq, hk, hv, lam, sigma, mix, params, out=hout, ws=ws_h,
+                                     heads_per_chunk=E2E_HEADS)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(b) / e2e_steps
         e2e = {"value": B * N * world / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out.numel() * 4,
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms,
+               "path": f"fs_attention_fwd_host, pinned host buffers, groups of {E2E_HEADS} heads"}
+        del ws_h
 
     pk = peaks()
     kernels = {}

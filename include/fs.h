@@ -238,6 +238,41 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v,
                             void *ws, size_t ws_bytes, void *stream,
                             void *const *stage_events);
 
+/* Device workspace bytes fs_attention_fwd_host needs: two staging slots,
+ * each with q, k, v and out of `heads_per_chunk` heads and a forward
+ * workspace for them.  0 on bad args. */
+size_t fs_host_workspace_bytes(int batch, int H, int N, int d,
+                               const fs_params *p, int dtype,
+                               int heads_per_chunk);
+
+/* fs_attention_fwd on HOST buffers, with the copies inside the call.  This
+ * entry point has no counterpart on the pages: it serves callers whose
+ * activations live in host memory.  The op is independent per (batch,
+ * head), so the call walks groups of `heads_per_chunk` heads of one batch
+ * row through two device staging slots.  The load of the next group, the
+ * forward of this one and the store of the previous one overlap: loads on
+ * one copy stream, forwards on `stream`, stores on a second copy stream,
+ * ordered by events.  Results are bit-identical to fs_attention_fwd.
+ *   q, k, v   [batch,H,N,d] HOST memory, dtype as in fs_attention_fwd
+ *             (page-locked memory lets the copies overlap; pageable memory
+ *             works, with copies that do not)
+ *   lambda, sigma, mix   [H] f32 DEVICE memory
+ *   out       [batch,H,N,d] f32 HOST memory
+ *   ws        device workspace of at least fs_host_workspace_bytes() bytes;
+ *             its header holds the error word of the whole call
+ * `stream` completes only after every copy of the call, so a stream
+ * synchronise makes `out` readable; the host buffers must stay valid until
+ * then.  The two copy streams and their six events are created on the first
+ * call of each host thread on each device and kept for the thread's life
+ * (driver objects, not memory: the call allocates no memory).  A CUDA failure
+ * while creating them gives FS_ERR_CUDA. */
+int fs_attention_fwd_host(const void *q, const void *k, const void *v,
+                          int dtype, int batch, int H, int N, int d,
+                          const fs_params *p, const float *lambda,
+                          const float *sigma, const float *mix, float *out,
+                          int heads_per_chunk, void *ws, size_t ws_bytes,
+                          void *stream);
+
 /* Every workspace begins with a 256-byte header whose first int is a device
  * error word, cleared at the start of each call.  Kernels that wait on
  * mbarriers give up after a bounded number of polls (seconds) and record

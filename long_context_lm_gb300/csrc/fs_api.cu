@@ -144,6 +144,11 @@ int prepare_window(const Shape &sh, const void *k, const void *v, float rope_bas
   return status_of(launch_prep(k, v, base + W.tab, sh, base + W.kt, base + W.v16, err, st));
 }
 
+int forward(const void *q, const void *k, const void *v, int dtype, const Shape &sh,
+            const fs_params *p, const float *lambda, const float *sigma, const float *mix,
+            float *out, char *base, const Layout &L, int *err, cudaStream_t st,
+            void *const *stage_events);
+
 }  // namespace
 }  // namespace fs
 
@@ -337,8 +342,24 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   const Shape sh{batch, H, N, d};
   const Layout L = make_layout(sh, *p, dtype);
   if (ws_bytes < L.total) return FS_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  char *base = static_cast<char *>(ws);
+  int *err = reinterpret_cast<int *>(ws);
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), static_cast<cudaStream_t>(stream))));
+  return forward(q, k, v, dtype, sh, p, lambda, sigma, mix, out, static_cast<char *>(ws), L, err,
+                 static_cast<cudaStream_t>(stream), stage_events);
+}
+
+}  // extern "C"
+
+namespace fs {
+namespace {
+
+// The forward on validated arguments: workspace `base` laid out as `L`;
+// device errors are recorded in `err` (not cleared here).
+int forward(const void *q, const void *k, const void *v, int dtype, const Shape &sh,
+            const fs_params *p, const float *lambda, const float *sigma, const float *mix,
+            float *out, char *base, const Layout &L, int *err, cudaStream_t st,
+            void *const *stage_events) {
+  const int N = sh.N, d = sh.d;
   const void *qb = q, *kb = k, *vb = v;
   if (dtype == FS_FP32) {
     const size_t elems = (size_t)sh.BH() * N * d;
@@ -354,9 +375,7 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   int32_t *pool = reinterpret_cast<int32_t *>(base + L.pool);
   int32_t *pool_count = reinterpret_cast<int32_t *>(base + L.pool_count);
   int32_t *sel = reinterpret_cast<int32_t *>(base + L.sel);
-  int *err = reinterpret_cast<int *>(base);
   const bool fs_mode = p->mode == FS_MODE_FS;
-  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
 
   auto mark = [&](int i) -> int {
     if (!stage_events || !stage_events[i]) return FS_OK;
@@ -390,6 +409,143 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   a.err = err;
   FS_TRY(status_of(launch_attn_tc(a, st)));
   return mark(4);
+}
+
+// Two copy streams and the events of the host-buffer pipeline, per (host
+// thread, device): created on first use and kept for the thread's life.  Per
+// host thread, so that two callers never share an event between its record
+// and its wait.
+constexpr int kPipeDevices = 64;
+struct CopyPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t loaded[2] = {}, computed[2] = {}, stored[2] = {};
+};
+
+CopyPipe *copy_pipe() {
+  thread_local CopyPipe per_device[kPipeDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kPipeDevices) return nullptr;
+  CopyPipe &c = per_device[dev];
+  if (!c.h2d) {
+    CopyPipe n;
+    bool ok = cudaStreamCreateWithFlags(&n.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&n.d2h, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+      ok = cudaEventCreateWithFlags(&n.loaded[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&n.computed[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&n.stored[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      for (int i = 0; i < 2; ++i) {
+        if (n.loaded[i]) cudaEventDestroy(n.loaded[i]);
+        if (n.computed[i]) cudaEventDestroy(n.computed[i]);
+        if (n.stored[i]) cudaEventDestroy(n.stored[i]);
+      }
+      if (n.h2d) cudaStreamDestroy(n.h2d);
+      if (n.d2h) cudaStreamDestroy(n.d2h);
+      return nullptr;
+    }
+    c = n;
+  }
+  return &c;
+}
+
+// Staging slot of the host-buffer pipeline: q, k, v and out of `hc` heads,
+// then a forward workspace for them.
+struct HostLayout {
+  size_t qkv_bytes, out_bytes, fwd_bytes, slot_bytes, total;
+};
+
+HostLayout host_layout(int H, int N, int d, const fs_params &p, int dtype, int hc) {
+  HostLayout h{};
+  const size_t elem = dtype == FS_FP32 ? 4 : 2;
+  const size_t n = (size_t)hc * N * d;
+  h.qkv_bytes = align_up(n * elem);
+  h.out_bytes = align_up(n * 4);
+  h.fwd_bytes = align_up(make_layout(Shape{1, hc, N, d}, p, dtype).total);
+  h.slot_bytes = 3 * h.qkv_bytes + h.out_bytes + h.fwd_bytes;
+  h.total = kHeader + 2 * h.slot_bytes;
+  return h;
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" {
+
+size_t fs_host_workspace_bytes(int batch, int H, int N, int d, const fs_params *p, int dtype,
+                               int heads_per_chunk) {
+  if (check_params(p) != FS_OK || check_shape(batch, H, N, d) != FS_OK ||
+      check_dtype(dtype) != FS_OK || heads_per_chunk < 1)
+    return 0;
+  return host_layout(H, N, d, *p, dtype, heads_per_chunk < H ? heads_per_chunk : H).total;
+}
+
+int fs_attention_fwd_host(const void *q, const void *k, const void *v, int dtype, int batch,
+                          int H, int N, int d, const fs_params *p, const float *lambda,
+                          const float *sigma, const float *mix, float *out, int heads_per_chunk,
+                          void *ws, size_t ws_bytes, void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (!q || !k || !v || !lambda || !sigma || !mix || !out || !ws || heads_per_chunk < 1)
+    return FS_ERR_INVALID_ARG;
+  const int hc = heads_per_chunk < H ? heads_per_chunk : H;
+  const HostLayout HL = host_layout(H, N, d, *p, dtype, hc);
+  if (ws_bytes < HL.total) return FS_ERR_INVALID_ARG;
+  CopyPipe *cp = copy_pipe();
+  if (!cp) return FS_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *base = static_cast<char *>(ws);
+  int *err = reinterpret_cast<int *>(base);
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  const size_t elem = dtype == FS_FP32 ? 4 : 2;
+  int rc = FS_OK;
+  int chunk = 0;
+  for (int b = 0; b < batch && rc == FS_OK; ++b) {
+    for (int h0 = 0; h0 < H && rc == FS_OK; h0 += hc, ++chunk) {
+      const int hn = H - h0 < hc ? H - h0 : hc;
+      const int s = chunk & 1;
+      char *slot = base + kHeader + s * HL.slot_bytes;
+      char *qd = slot, *kd = qd + HL.qkv_bytes, *vd = kd + HL.qkv_bytes;
+      float *od = reinterpret_cast<float *>(vd + HL.qkv_bytes);
+      char *fws = vd + HL.qkv_bytes + HL.out_bytes;
+      const size_t first = ((size_t)b * H + h0) * N * d;  // first element of the chunk
+      const size_t n = (size_t)hn * N * d;
+      // load: the slot's previous forward must have finished reading it
+      if (chunk >= 2) rc = status_of(cudaStreamWaitEvent(cp->h2d, cp->computed[s], 0));
+      const char *srcs[3] = {static_cast<const char *>(q), static_cast<const char *>(k),
+                             static_cast<const char *>(v)};
+      char *dsts[3] = {qd, kd, vd};
+      for (int i = 0; i < 3 && rc == FS_OK; ++i)
+        rc = status_of(cudaMemcpyAsync(dsts[i], srcs[i] + first * elem, n * elem,
+                                       cudaMemcpyHostToDevice, cp->h2d));
+      if (rc == FS_OK) rc = status_of(cudaEventRecord(cp->loaded[s], cp->h2d));
+      // compute on the caller's stream: after the load, and after the slot's
+      // previous output has been stored
+      if (rc == FS_OK) rc = status_of(cudaStreamWaitEvent(st, cp->loaded[s], 0));
+      if (rc == FS_OK && chunk >= 2) rc = status_of(cudaStreamWaitEvent(st, cp->stored[s], 0));
+      if (rc == FS_OK) {
+        const Shape sh{1, hn, N, d};
+        rc = forward(qd, kd, vd, dtype, sh, p, lambda + h0, sigma + h0, mix + h0, od, fws,
+                     make_layout(sh, *p, dtype), err, st, nullptr);
+      }
+      if (rc == FS_OK) rc = status_of(cudaEventRecord(cp->computed[s], st));
+      // store
+      if (rc == FS_OK) rc = status_of(cudaStreamWaitEvent(cp->d2h, cp->computed[s], 0));
+      if (rc == FS_OK)
+        rc = status_of(cudaMemcpyAsync(out + first, od, n * 4, cudaMemcpyDeviceToHost, cp->d2h));
+      if (rc == FS_OK) rc = status_of(cudaEventRecord(cp->stored[s], cp->d2h));
+    }
+  }
+  // the caller's stream completes only after every copy this call issued (also
+  // after a failure, so that no copy outlives the caller's view of the buffers)
+  for (int s = 0; s < 2 && s < chunk; ++s) {
+    cudaEventRecord(cp->loaded[s], cp->h2d);
+    cudaStreamWaitEvent(st, cp->loaded[s], 0);
+    cudaEventRecord(cp->stored[s], cp->d2h);
+    cudaStreamWaitEvent(st, cp->stored[s], 0);
+  }
+  return rc;
 }
 
 }  // extern "C"

@@ -30,7 +30,7 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
            "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
-           "fs_selftest_wait_timeout"]
+           "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
@@ -88,6 +88,8 @@ def load(build_if_stale: bool = True):
         L.fs_prune_workspace_bytes.restype = Z
         L.fs_window_workspace_bytes.argtypes = [I, I, I, I, PP]
         L.fs_window_workspace_bytes.restype = Z
+        L.fs_host_workspace_bytes.argtypes = [I, I, I, I, PP, I, I]
+        L.fs_host_workspace_bytes.restype = Z
         L.fs_cell_summarize.argtypes = [P, I, I, I, I, I, I, P, P, P]
         L.fs_prune_cells.argtypes = [P, I, I, I, PP, P, P, P, Z, P]
         L.fs_select_cells.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, PP, P, P, P]
@@ -95,6 +97,7 @@ def load(build_if_stale: bool = True):
         L.fs_window_attn.argtypes = [P, P, P, I, P, P, I, I, I, I, PP, P, P, Z, P]
         L.fs_attention_fwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, Z, P]
         L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
+        L.fs_attention_fwd_host.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, I, P, Z, P]
         L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 5
         L.fs_check_status.argtypes = [P, P]
         L.fs_selftest_wait_timeout.argtypes = [P, P]
@@ -106,7 +109,8 @@ def load(build_if_stale: bool = True):
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
                             "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
-                            "fs_prune_workspace_bytes", "fs_window_workspace_bytes"):
+                            "fs_prune_workspace_bytes", "fs_window_workspace_bytes",
+                            "fs_host_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -330,6 +334,54 @@ def fs_attention_fwd(q, k, v, lam, sigma, mix, params=None, out=None, ws=None, s
     _check(L.fs_attention_fwd(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, d, ctypes.byref(p),
                               _ptr(lam), _ptr(sigma), _ptr(mix), _ptr(out), _ptr(ws), wsb,
                               _stream(stream)), "fs_attention_fwd")
+    return out
+
+
+def fs_host_workspace_bytes(batch, H, N, d, params=None, dtype=FS_BF16, heads_per_chunk=2) -> int:
+    p = _params(params)
+    return load().fs_host_workspace_bytes(batch, H, N, d, ctypes.byref(p), dtype, heads_per_chunk)
+
+
+def _host(t, name, dtypes):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fs_attention_fwd_host(q, k, v, lam, sigma, mix, params=None, out=None, ws=None,
+                          heads_per_chunk=2, stream=None):
+    """fs_attention_fwd on host tensors q, k, v [batch, H, N, d] (pinned memory
+    lets the copies overlap the compute); lam, sigma, mix are device tensors.
+    Returns ``out`` [batch, H, N, d] fp32 on the host, readable after the
+    stream is synchronised."""
+    L = load()
+    p = _params(params)
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _host(t, nm, (torch.bfloat16, torch.float32))
+    if not (q.dtype == k.dtype == v.dtype) or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share dtype and shape")
+    for t, nm in ((lam, "lam"), (sigma, "sigma"), (mix, "mix")):
+        _dev(t, nm, (torch.float32,))
+    B, H, N, d = _qkv_shape(q)
+    code = FS_FP32 if q.dtype == torch.float32 else FS_BF16
+    wsb = L.fs_host_workspace_bytes(B, H, N, d, ctypes.byref(p), code, heads_per_chunk)
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_host_workspace_bytes")
+    dev = lam.device
+    if ws is None:
+        ws = torch.empty(wsb, device=dev, dtype=torch.uint8)
+    elif ws.numel() * ws.element_size() < wsb:
+        raise ValueError(f"workspace too small: {ws.numel()} < {wsb} bytes")
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.float32, pin_memory=True)
+    _host(out, "out", (torch.float32,))
+    _check(L.fs_attention_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), code, B, H, N, d,
+                                   ctypes.byref(p), _ptr(lam), _ptr(sigma), _ptr(mix),
+                                   out.data_ptr(), heads_per_chunk, _ptr(ws), wsb,
+                                   _stream(stream)), "fs_attention_fwd_host")
     return out
 
 
