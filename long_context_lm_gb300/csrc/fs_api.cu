@@ -382,8 +382,11 @@ int forward(const void *q, const void *k, const void *v, int dtype, const Shape 
     return status_of(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st));
   };
   FS_TRY(mark(0));
-  FS_TRY(status_of(launch_cell_summary(kb, false, sh, kbar, amax, st)));
-  FS_TRY(prepare_window(sh, kb, vb, p->rope_base, base, L.win, err, st));
+  // angle table, then rotated keys, fp16 values and cell summaries in one
+  // pass over k and v
+  FS_TRY(status_of(launch_rope_table(base + L.win.tab, sh.N, p->rope_base, st)));
+  FS_TRY(status_of(launch_prep_summary(kb, vb, base + L.win.tab, sh, base + L.win.kt,
+                                       base + L.win.v16, kbar, amax, err, st)));
   FS_TRY(mark(1));
   if (!fs_mode)
     FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));

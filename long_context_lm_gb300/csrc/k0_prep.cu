@@ -9,12 +9,16 @@
 // once per query tile inside the attention kernel:
 //   kt[row] = [bf16 hi (64) | bf16 lo (64)] of R(n) k_n (fp32), 256 B per row
 //   v16[row] = fp16(v_n) (exact from bf16 inside the fp16 range), 128 B per row
-// Streaming, HBM-bound: per token-head it reads 256 B and writes 384 B.
+// Streaming, HBM-bound: per token-head it reads 256 B and writes 384 B.  The
+// whole forward runs k0_prep_summary_kernel instead, which also writes the
+// cell summaries of the keys it reads (8.1 B more per token-head), so that
+// the keys are read once per call.
 //
 // Angles: row r < 64 of the table holds (cos, sin)(r theta_i); row 64 + u
 // holds (cos, sin)(64 u theta_i); both are evaluated in fp64 and rounded
 // once, and an absolute angle is composed from its two rows by the angle-sum
 // identity in fp32 (error of a few fp32 ulps, independent of the position).
+#include "cell_summary.cuh"
 #include "fs_common.cuh"
 #include "fs_internal.h"
 #include "tc05.cuh"
@@ -95,6 +99,91 @@ __global__ void __launch_bounds__(256) k0_prep_kernel(
   if (!range_ok) tc::report_error(err, FS_ERR_RANGE);
 }
 
+// The same pass with the cell summaries of the keys it reads (one read of
+// the keys instead of two): one warp per 32-token cell, in the lane layout of
+// cell_summary_warp (lane = 8 * t0 + g holds 16-byte chunk g of tokens
+// t0 + 4i), so kbar and a_c are bit-identical to the summary kernel's.  A
+// lane rotates the pairs of its chunk with the other half of each pair from
+// lane ^ 4 (chunk g ^ 4 of the same tokens), by the arithmetic of
+// k0_prep_kernel, so the rotated keys are bit-identical too; values are
+// re-encoded chunk by chunk.
+__global__ void __launch_bounds__(256, 2) k0_prep_summary_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const float4 *__restrict__ tab,
+    int N, long long ncells, uint4 *__restrict__ kt, uint4 *__restrict__ v16,
+    float *__restrict__ kbar, float *__restrict__ amax, int *err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long cell = (long long)blockIdx.x * 8 + warp;
+  if (cell >= ncells) return;
+  const int g = lane & 7, t0 = lane >> 3;
+  const long long row0 = cell * kS;  // first token row of the cell (rows of all heads)
+  uint4 kr[8], vr[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) kr[i] = __ldg(k + (row0 + t0 + 4 * i) * 8 + g);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) vr[i] = __ldg(v + (row0 + t0 + 4 * i) * 8 + g);
+  {
+    float x[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {kr[i].x, kr[i].y, kr[i].z, kr[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[i][2 * j] = bf16_lo(w[j]);
+        x[i][2 * j + 1] = bf16_hi(w[j]);
+      }
+    }
+    cell_summary_warp(x, lane, kbar + cell * kD, amax + cell);
+  }
+  const bool first = g < 4;  // dims 8g.. are the first halves of their pairs
+  const int pq = g & 3;      // pairs 8pq .. 8pq+7
+  bool range_ok = true;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const long long row = row0 + t0 + 4 * i;
+    const int n = (int)(row % N);
+    const uint32_t mine[4] = {kr[i].x, kr[i].y, kr[i].z, kr[i].w};
+    uint32_t other[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) other[j] = __shfl_xor_sync(0xffffffffu, mine[j], 4);
+    const float4 *tr = tab + (size_t)(n & 63) * 16 + 4 * pq;
+    const float4 *tu = tab + (size_t)(64 + (n >> 6)) * 16 + 4 * pq;
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // pairs 8pq + 2j, 8pq + 2j + 1
+      const float4 rr = __ldg(tr + j), uu = __ldg(tu + j);
+      const uint32_t wa = first ? mine[j] : other[j], wb = first ? other[j] : mine[j];
+      float y[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float cr = e ? rr.z : rr.x, sr = e ? rr.w : rr.y;
+        const float cu = e ? uu.z : uu.x, su = e ? uu.w : uu.y;
+        const float c = fmaf(cu, cr, -su * sr), sn = fmaf(su, cr, cu * sr);
+        const float x0 = e ? bf16_hi(wa) : bf16_lo(wa);
+        const float x1 = e ? bf16_hi(wb) : bf16_lo(wb);
+        y[e] = first ? fmaf(x0, c, -x1 * sn) : fmaf(x0, sn, x1 * c);
+      }
+      hw[j] = pack_bf16(y[0], y[1]);
+      lw[j] = pack_bf16(y[0] - bf16_lo(hw[j]), y[1] - bf16_hi(hw[j]));
+    }
+    uint4 *dst = kt + row * 16;
+    dst[g] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    dst[8 + g] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    // values: bf16 -> fp16; a finite |v| >= 65520 would round to infinity
+    const uint32_t vw[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
+    uint32_t h[4];
+    float big = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = bf16_lo(vw[j]), hi = bf16_hi(vw[j]);
+      big = fmaxf(big, fmaxf(fabsf(lo), fabsf(hi)));
+      h[j] = pack_f16(lo, hi);
+    }
+    range_ok &= !(big >= 65520.f && big != INFINITY);
+    v16[row * 8 + g] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+  if (!range_ok) tc::report_error(err, FS_ERR_RANGE);
+}
+
 }  // namespace
 
 size_t rope_table_bytes(int N) { return (size_t)(64 + (N + 63) / 64) * (kD / 2) * sizeof(float2); }
@@ -103,6 +192,17 @@ cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st
   const int rows = 64 + (N + 63) / 64;
   rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(static_cast<float2 *>(tab),
                                                                   rows, (double)rope_base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_summary(const void *k, const void *v, const void *tab, const Shape &sh,
+                                void *kt, void *v16, float *kbar, float *amax, int *err,
+                                cudaStream_t st) {
+  const long long ncells = (long long)sh.BH() * sh.C();
+  k0_prep_summary_kernel<<<(unsigned)((ncells + 7) / 8), 256, 0, st>>>(
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+      static_cast<const float4 *>(tab), sh.N, ncells, static_cast<uint4 *>(kt),
+      static_cast<uint4 *>(v16), kbar, amax, err);
   return cudaGetLastError();
 }
 
