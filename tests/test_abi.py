@@ -38,6 +38,23 @@ def test_default_params_are_the_page_values():
     assert p.mode == fs.FS_MODE_FSL
 
 
+def test_host_workspace_bytes():
+    # two staging slots, each with q, k, v and out of one group of heads and a
+    # forward workspace for that group
+    one = fs.fs_host_workspace_bytes(1, 16, 65536, 64, heads_per_chunk=1)
+    four = fs.fs_host_workspace_bytes(1, 16, 65536, 64, heads_per_chunk=4)
+    grp = 4 * 65536 * 64
+    assert four >= 2 * (3 * grp * 2 + grp * 4 + fs.fs_workspace_bytes(1, 4, 65536, 64))
+    assert one < four < fs.fs_host_workspace_bytes(1, 16, 65536, 64, heads_per_chunk=16)
+    # a group never exceeds H heads; the batch does not change the slot size
+    assert fs.fs_host_workspace_bytes(1, 3, 2048, 64, heads_per_chunk=8) == \
+        fs.fs_host_workspace_bytes(4, 3, 2048, 64, heads_per_chunk=3)
+    assert fs.fs_host_workspace_bytes(1, 16, 4096, 64, heads_per_chunk=0) == 0
+    assert fs.fs_host_workspace_bytes(1, 16, 4096 + 1, 64) == 0
+    assert fs.fs_host_workspace_bytes(1, 2, 2048, 64, dtype=fs.FS_FP32) > \
+        fs.fs_host_workspace_bytes(1, 2, 2048, 64, dtype=fs.FS_BF16)
+
+
 def test_status_strings():
     assert fs.status_string(0) == "ok"
     assert "invalid" in fs.status_string(1)
