@@ -16,24 +16,26 @@
 // Sixteen warps with fixed roles and mbarrier hand-offs; every counter runs
 // across q-tiles, so producers start the next q-tile while the softmax
 // finishes the current one:
-//   warps 0-7   softmax + epilogue: warp w owns TMEM lanes / query rows
-//               32*(w%4).. and key columns 64*(w/4).. of each key tile; the
-//               two warps of a row block exchange row maxima through shared
-//               memory (one named barrier per tile)
+//   warps 0-7   softmax: warp w owns TMEM lanes / query rows 32*(w%4).. and
+//               key columns 64*(w/4).. of each key tile; the two warps of a
+//               row block exchange row maxima through shared memory (one
+//               bounded mbarrier phase per tile)
 //   warp  8     TMEM allocation; lane 0 issues the S = Q.K^T MMAs
 //   warp  9     lane 0 issues the P.V MMAs (one issuing thread sustains about
 //               one tcgen05.mma per ~100 cycles, hence two issuers)
 //   warp  10    lane 0: TMA producer (contiguous window tiles; gathered cells)
 //   warp  11    builds the union of the q-tile's selected cells
-//   warps 12-15 stage the query tile: raw (long branch) and rotated (window)
+//   warps 12-15 stage the query tile: raw (long branch) and rotated (window);
+//               then the epilogue of the previous q-tile (one thread per row)
 // Window key tiles arrive already rotated (absolute positions, bf16 hi | lo)
 // with fp16 values, from the preparation pass; the query tile is rotated
 // here by the same absolute angles, so q_n . k_j carries R(n - j).
 // TMEM: two 128-column score buffers S; the softmax overwrites each with
-// its tile's probabilities (bf16 pairs, the A operand of P.V) in place, so
-// P is double-buffered with S.  Two accumulator sets (O_win, O_long; 64
-// columns each) alternate between q-tiles, and the epilogue of a q-tile runs
-// after the softmax of the next q-tile's first key tile, off the MMA path.
+// its tile's probabilities (fp16 pairs, or bf16 hi / lo pairs for the long
+// branch alone; the A operand of P.V) in place, so P is double-buffered with
+// S.  Two accumulator sets (O_win, O_long; 64 columns each) alternate between
+// q-tiles, so the epilogue of a q-tile has the whole next q-tile to run in,
+// off the softmax and MMA paths.
 //
 // Precision.  Window: the rotated q and k (fp32, absolute angles from an
 // fp64 table) are split into bf16 hi + lo halves and S takes three MMA
