@@ -1,6 +1,6 @@
 /*
  * fs_oracle.c -- plain, slow fp64 CPU oracle of the FreeSolo FS-L attention
- * forward pass.
+ * forward pass, and of its backward pass with the hard indices held fixed.
  *
  * TEST INFRASTRUCTURE ONLY.  The test-suite, the package smoke check and the
  * benchmark's CPU-baseline leg load this library; the product path (the CUDA
@@ -501,5 +501,227 @@ int fso_forward(const float *q, const float *k, const float *v, int BH, int H,
     free(pcount);
     free(pgap);
   }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass.  [rainbus] 方法步骤详情 (training: the hard top-P / top-K
+ * indices carry no gradient), 核心方法 (the per-head mixing coefficient is
+ * learned), 局限与改进 (sigma_h and lambda_h are fixed, without gradient);
+ * [ai.info] "Methodology in Plain English" (training paragraph: hard top-P
+ * and top-K indices receive no gradient, routing scalars stay fixed).
+ *
+ * Given g = dL/dout for a scalar loss L, the pool and the selection of every
+ * row are held fixed, so the gradient reaches q, k and v only through the two
+ * softmax reads (and the RMSNorm of the long branch), plus the mix weight
+ * m_h; kbar_c, a_c, lambda_h and sigma_h receive none.  Per row n, with the
+ * window probabilities p_j over the rotated q~ = R(n) q_n, k~_j = R(j) k_j
+ * and the long probabilities p_t over the selected tokens (unrotated):
+ *   window  dv_j += p_j g;  ds_j = p_j (g.v_j - g.o_win);
+ *           dq~ = sum_j ds_j k~_j / sqrt(d);  dk~_j += ds_j q~ / sqrt(d);
+ *           dq_n += R(n)^T dq~;  dk_j += R(j)^T dk~_j
+ *   long    dm_h += g.o^;  do^ = m_h g;  rho = (mean(o^2) + eps)^(-1/2),
+ *           o^ = rho o, so do = rho do^ - rho^3 (o.do^) o / d;
+ *           dv_t += p_t do;  dl_t = p_t (do.v_t - do.o);
+ *           dq_n += sum_t dl_t k_t / sqrt(d);  dk_t += dl_t q_n / sqrt(d)
+ * (the softmax rule ds = p (dp - p.dp) with dp_j = g.v_j and p.dp = g.o).  */
+/* ------------------------------------------------------------------------ */
+
+/* out = R(pos)^T y: the inverse rotation of one vector (pairs i, i + d/2). */
+static void rope_rotate_t(const double *y, double pos, int d, double base,
+                          double *out) {
+  int h = d / 2;
+  for (int i = 0; i < h; ++i) {
+    double theta = pow(base, -2.0 * (double)i / (double)d);
+    double ang = pos * theta;
+    double cs = cos(ang), sn = sin(ang);
+    double y0 = y[i], y1 = y[i + h];
+    out[i] = y0 * cs + y1 * sn;
+    out[i + h] = -y0 * sn + y1 * cs;
+  }
+}
+
+/* Gradients of one head slice.  dq, dk, dv [N, d] are accumulated into
+ * (zeroed by the caller); returns g . o^ summed over the rows (dm_h). */
+static double backward_head(const float *q, const float *k, const float *v,
+                            const double *g, int N, int d, int w, int s, int K,
+                            int P, int W, int Bq, double base, double eps,
+                            int mode, double lambda, double sigma, double mix,
+                            double *dq, double *dk, double *dv) {
+  int C = N / s, nblk = N / Bq;
+  int cap = mode == 1 ? C : P + W;
+  double scale = 1.0 / sqrt((double)d);
+  double *kbar = (double *)malloc(sizeof(double) * (size_t)C * d);
+  double *amax = (double *)malloc(sizeof(double) * (size_t)C);
+  double *krot = (double *)malloc(sizeof(double) * (size_t)N * d);
+  double *dkrot = (double *)calloc((size_t)N * d, sizeof(double));
+  int32_t *pools = (int32_t *)malloc(sizeof(int32_t) * (size_t)nblk * cap);
+  int32_t *pcount = (int32_t *)malloc(sizeof(int32_t) * (size_t)nblk);
+  cell_key *scratch = (cell_key *)malloc(sizeof(cell_key) * (size_t)(C + 1));
+  scored_cell *sc = (scored_cell *)malloc(sizeof(scored_cell) * (size_t)(cap + 1));
+  double *pw = (double *)malloc(sizeof(double) * (size_t)w);
+  double *pt = (double *)malloc(sizeof(double) * (size_t)K * s + 1);
+  double dmix = 0.0;
+  cell_summaries(k, N, d, s, kbar, amax);
+  for (int j = 0; j < N; ++j)
+    rope_rotate(k + (size_t)j * d, (double)j, d, base, krot + (size_t)j * d);
+  for (int beta = 0; beta < nblk; ++beta) {
+    double gap;
+    pcount[beta] = pool_definition(amax, beta * Bq / s, P, W, mode,
+                                   pools + (size_t)beta * cap, &gap, scratch);
+  }
+  for (int n = 0; n < N; ++n) {
+    const float *qn = q + (size_t)n * d;
+    const double *gn = g + (size_t)n * d;
+    double qr[256], dqr[256], dqn[256], ow[256], ol[256], dol[256], tmp[256];
+    for (int i = 0; i < d; ++i) dqn[i] = 0.0;
+    /* window branch: forward again, then its backward in rotated space */
+    rope_rotate(qn, (double)n, d, base, qr);
+    int j0 = n - w + 1 < 0 ? 0 : n - w + 1;
+    double mx = -INFINITY, den = 0.0;
+    for (int j = j0; j <= n; ++j) {
+      double l = 0.0;
+      for (int i = 0; i < d; ++i) l += qr[i] * krot[(size_t)j * d + i];
+      pw[j - j0] = l * scale;
+      if (pw[j - j0] > mx) mx = pw[j - j0];
+    }
+    for (int j = j0; j <= n; ++j) {
+      pw[j - j0] = exp(pw[j - j0] - mx);
+      den += pw[j - j0];
+    }
+    for (int i = 0; i < d; ++i) ow[i] = 0.0;
+    for (int j = j0; j <= n; ++j) {
+      pw[j - j0] /= den;
+      for (int i = 0; i < d; ++i) ow[i] += pw[j - j0] * (double)v[(size_t)j * d + i];
+    }
+    double g_ow = 0.0;
+    for (int i = 0; i < d; ++i) g_ow += gn[i] * ow[i];
+    for (int i = 0; i < d; ++i) dqr[i] = 0.0;
+    for (int j = j0; j <= n; ++j) {
+      double p = pw[j - j0], g_vj = 0.0;
+      for (int i = 0; i < d; ++i) {
+        g_vj += gn[i] * (double)v[(size_t)j * d + i];
+        dv[(size_t)j * d + i] += p * gn[i];
+      }
+      double ds = p * (g_vj - g_ow) * scale;
+      for (int i = 0; i < d; ++i) {
+        dqr[i] += ds * krot[(size_t)j * d + i];
+        dkrot[(size_t)j * d + i] += ds * qr[i];
+      }
+    }
+    rope_rotate_t(dqr, (double)n, d, base, tmp);
+    for (int i = 0; i < d; ++i) dqn[i] += tmp[i];
+    /* long branch: the row's selection (held fixed), forward, backward */
+    int beta = n / Bq, np = pcount[beta];
+    const int32_t *pl = pools + (size_t)beta * cap;
+    for (int t = 0; t < np; ++t) {
+      sc[t].c = pl[t];
+      sc[t].u = cell_score(qn, kbar + (size_t)pl[t] * d, amax[pl[t]], pl[t], n,
+                           d, s, lambda, sigma);
+    }
+    qsort(sc, (size_t)np, sizeof(scored_cell), cmp_scored);
+    int nsel = np < K ? np : K;
+    if (nsel > 0) {
+      int ntok = nsel * s;
+      mx = -INFINITY;
+      den = 0.0;
+      for (int r = 0; r < nsel; ++r)
+        for (int e = 0; e < s; ++e) {
+          int tk = sc[r].c * s + e;
+          double l = 0.0;
+          for (int i = 0; i < d; ++i) l += (double)qn[i] * (double)k[(size_t)tk * d + i];
+          pt[r * s + e] = l * scale;
+          if (pt[r * s + e] > mx) mx = pt[r * s + e];
+        }
+      for (int x = 0; x < ntok; ++x) {
+        pt[x] = exp(pt[x] - mx);
+        den += pt[x];
+      }
+      for (int i = 0; i < d; ++i) ol[i] = 0.0;
+      for (int r = 0; r < nsel; ++r)
+        for (int e = 0; e < s; ++e) {
+          int tk = sc[r].c * s + e;
+          pt[r * s + e] /= den;
+          for (int i = 0; i < d; ++i) ol[i] += pt[r * s + e] * (double)v[(size_t)tk * d + i];
+        }
+      double ms = 0.0;
+      for (int i = 0; i < d; ++i) ms += ol[i] * ol[i];
+      double rho = 1.0 / sqrt(ms / (double)d + eps);
+      /* mix weight and RMSNorm */
+      double o_dohat = 0.0;
+      for (int i = 0; i < d; ++i) {
+        dmix += gn[i] * ol[i] * rho;
+        o_dohat += ol[i] * mix * gn[i];
+      }
+      for (int i = 0; i < d; ++i)
+        dol[i] = rho * mix * gn[i] - rho * rho * rho * o_dohat * ol[i] / (double)d;
+      /* softmax read */
+      double do_o = 0.0;
+      for (int i = 0; i < d; ++i) do_o += dol[i] * ol[i];
+      for (int r = 0; r < nsel; ++r)
+        for (int e = 0; e < s; ++e) {
+          int tk = sc[r].c * s + e;
+          double p = pt[r * s + e], do_v = 0.0;
+          for (int i = 0; i < d; ++i) {
+            do_v += dol[i] * (double)v[(size_t)tk * d + i];
+            dv[(size_t)tk * d + i] += p * dol[i];
+          }
+          double dl = p * (do_v - do_o) * scale;
+          for (int i = 0; i < d; ++i) {
+            dqn[i] += dl * (double)k[(size_t)tk * d + i];
+            dk[(size_t)tk * d + i] += dl * (double)qn[i];
+          }
+        }
+    }
+    for (int i = 0; i < d; ++i) dq[(size_t)n * d + i] += dqn[i];
+  }
+  /* rotated-key gradients back to the unrotated keys */
+  for (int j = 0; j < N; ++j) {
+    double tmp[256];
+    rope_rotate_t(dkrot + (size_t)j * d, (double)j, d, base, tmp);
+    for (int i = 0; i < d; ++i) dk[(size_t)j * d + i] += tmp[i];
+  }
+  free(kbar);
+  free(amax);
+  free(krot);
+  free(dkrot);
+  free(pools);
+  free(pcount);
+  free(scratch);
+  free(sc);
+  free(pw);
+  free(pt);
+  return dmix;
+}
+
+/* Gradients of L = sum(g * out) for every head slice.
+ *   g                [BH, N, d] upstream gradient dL/dout
+ *   dq, dk, dv       [BH, N, d] (written)
+ *   dmix             [H] (written): summed over the batch
+ * Same parameters as fso_forward (all rows, no position offset). */
+int fso_backward(const float *q, const float *k, const float *v, int BH, int H,
+                 int N, int d, int w, int s, int K, int P, int W, int Bq,
+                 double rope_base, double rms_eps, int mode,
+                 const double *lambda, const double *sigma, const double *mix,
+                 const double *g, double *dq, double *dk, double *dv,
+                 double *dmix, int nthreads) {
+  if (N % Bq || Bq % s || d > 256 || d % 2 || K < 0 || K > 64 || w < 1) return 1;
+  if (BH % H) return 1;
+  double *part = (double *)malloc(sizeof(double) * (size_t)BH);
+  memset(dq, 0, sizeof(double) * (size_t)BH * N * d);
+  memset(dk, 0, sizeof(double) * (size_t)BH * N * d);
+  memset(dv, 0, sizeof(double) * (size_t)BH * N * d);
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int bh = 0; bh < BH; ++bh) {
+    size_t o = (size_t)bh * N * d;
+    int h = bh % H;
+    part[bh] = backward_head(q + o, k + o, v + o, g + o, N, d, w, s, K, P, W, Bq,
+                             rope_base, rms_eps, mode, lambda[h], sigma[h], mix[h],
+                             dq + o, dk + o, dv + o);
+  }
+  for (int h = 0; h < H; ++h) dmix[h] = 0.0;
+  for (int bh = 0; bh < BH; ++bh) dmix[bh % H] += part[bh];  /* fixed order */
+  free(part);
   return 0;
 }

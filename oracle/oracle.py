@@ -1,4 +1,5 @@
-"""ctypes front end of the fp64 CPU oracle in ``fs_oracle.c``.
+"""ctypes front end of the fp64 CPU oracle in ``fs_oracle.c`` (forward, and the
+backward with the hard indices held fixed).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline / reference leg call this module.  The product path
@@ -55,6 +56,8 @@ def lib():
             L.fso_forward.argtypes = ([P, P, P, i, i, i, i, i, i, i, i, i, i,
                                        dbl, dbl, i, dbl, P, P, P, P, i]
                                       + [P] * 7 + [i])
+            L.fso_backward.argtypes = ([P, P, P, i, i, i, i, i, i, i, i, i, i,
+                                        dbl, dbl, i, P, P, P, P, P, P, P, P, i])
             L.fso_max_threads.restype = i
             _lib = L
     return _lib
@@ -161,5 +164,32 @@ def forward(q, k, v, H, lam, sigma, mix, rows=None, params=None, pos_offset=0.0,
         _ptr(res["out"]), _ptr(res.get("o_win")), _ptr(res.get("o_long")),
         _ptr(res["sel"]), _ptr(res["sel_score"]), _ptr(res["gap_rel"]),
         _ptr(res["pool_gap"]), nthreads)
+    assert rc == 0, rc
+    return res
+
+
+def backward(q, k, v, H, lam, sigma, mix, g, params=None, nthreads=0):
+    """Gradients of L = sum(g * out) for the forward of every [BH, N, d] head
+    slice, with the pools and selections held fixed (the pages: hard top-P /
+    top-K indices carry no gradient; sigma_h, lambda_h fixed).  Returns a dict
+    with ``dq``, ``dk``, ``dv`` [BH, N, d] and ``dmix`` [H] (float64)."""
+    p = dict(DEFAULT_PARAMS)
+    if params:
+        p.update(params)
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    BH, N, d = q.shape
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    assert g.shape == q.shape
+    lam = np.ascontiguousarray(lam, dtype=np.float64).reshape(-1)
+    sigma = np.ascontiguousarray(sigma, dtype=np.float64).reshape(-1)
+    mix = np.ascontiguousarray(mix, dtype=np.float64).reshape(-1)
+    assert lam.size == H and sigma.size == H and mix.size == H and BH % H == 0
+    res = dict(dq=np.zeros((BH, N, d)), dk=np.zeros((BH, N, d)), dv=np.zeros((BH, N, d)),
+               dmix=np.zeros(H))
+    rc = lib().fso_backward(
+        _ptr(q), _ptr(k), _ptr(v), BH, H, N, d, p["w"], p["s"], p["K"], p["P"], p["W"],
+        p["Bq"], float(p["rope_base"]), float(p["rms_eps"]), int(p["mode"]),
+        _ptr(lam), _ptr(sigma), _ptr(mix), _ptr(g), _ptr(res["dq"]), _ptr(res["dk"]),
+        _ptr(res["dv"]), _ptr(res["dmix"]), nthreads)
     assert rc == 0, rc
     return res
