@@ -267,8 +267,8 @@ def run_ours(args, rank, world, local_rank):
         traffic = None
         if dom == "attention" and params.mode == fs.FS_MODE_FSL:
             # DRAM bytes per launch: the per-token figure of one ncu capture of
-            # the attention kernel (profiles/fs_attn_tc_kernel_fsl_16k_b2.md),
-            # scaled by the tokens one launch processes
+            # the attention kernel on fsl_16k_b2, scaled by the tokens one
+            # launch processes
             traffic = ATTN_DRAM_BYTES_PER_TOKEN_HEAD * B * H * N
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16"], "traffic": traffic,
@@ -297,8 +297,76 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     if not args.no_extras:
+        res["branches"] = time_branches(q, k, v, mix, view["sel"], params, stream, distinct,
+                                        counts, pk)
         res["decode"] = time_decode(q, k, v, lam, sigma, mix, params, stream)
         res["fs_mode"] = time_fs_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
+    return res
+
+
+def _timed(fn, stream, iters):
+    """Mean device time (ms) of fn() over `iters` back-to-back calls on `stream`
+    after two warm-up calls (CUDA events on the launching stream)."""
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def _entry(ms, nbytes, flops, pk, bound):
+    e = {"ms": ms, "bound": bound, "GB/s": nbytes / (ms / 1e3) / 1e9}
+    e["hbm_frac"] = e["GB/s"] / pk["hbm"]
+    if flops is not None:
+        e["TFLOP/s"] = flops / (ms / 1e3) / 1e12
+        e["tensor_frac"] = e["TFLOP/s"] / pk["bf16"]
+    return e
+
+
+def time_branches(q, k, v, mix, sel, params, stream, distinct_cells, counts, pk, iters=20):
+    """Each kernel of the path on its own, on the benchmark's inputs, against its
+    own roofline: the cell summary (HBM), the window branch alone (prep pass +
+    tensor-core kernel, no long branch), and the NoPE readout of the forward's
+    own selection alone (the gathered long branch)."""
+    from long_context_lm_gb300 import fs
+    B, H, N, d = q.shape
+    tok = B * H * N
+    C = N // 32
+    res = {}
+    # cell summary: read k (128 B), write kbar (d fp32) and amax per cell
+    kbar = torch.empty((B, H, C, d), device=q.device, dtype=torch.float32)
+    amax = torch.empty((B, H, C), device=q.device, dtype=torch.float32)
+    ms = _timed(lambda: fs.fs_cell_summarize(k, kbar=kbar, amax=amax), stream, iters)
+    res["cell_summary"] = _entry(ms, tok * d * 2 + B * H * C * (d * 4 + 4), None, pk, "hbm")
+    res["cell_summary"]["bytes_per_token_head"] = (tok * d * 2 + B * H * C * (d * 4 + 4)) / tok
+    # window branch alone (o_long = NULL): events around the prep pass and the kernel
+    wsb = fs.fs_window_workspace_bytes(B, H, N, d, params)
+    ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    out = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters + 2)]
+    for ev in evs:
+        fs.fs_window_attn(q, k, v, None, None, params, out=out, ws=ws, events=ev)
+    torch.cuda.synchronize()
+    prep_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs[2:])
+    win_ms = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs[2:])
+    # prep: angle table + read k, v (bf16), write rotated keys (bf16 hi | lo) and fp16 v
+    res["window_prep"] = _entry(prep_ms, tok * d * 2 * 2 + tok * d * 2 * 3, None, pk, "hbm")
+    # window kernel: q, rotated keys, fp16 values read once, out written (fp32)
+    res["window_attn"] = _entry(win_ms, tok * (d * 2 + d * 4 + d * 2 + d * 4),
+                                window_flops(B * H, N, params.w, d), pk, "tensor")
+    # long branch alone: q, sel, the raw k/v rows of every distinct selected
+    # cell once, o_long written (fp32); flops over the selected tokens
+    o_long = torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
+    ms = _timed(lambda: fs.fs_sparse_readout(q, k, v, sel, params, o_long=o_long), stream, iters)
+    nbytes = tok * (d * 2 + params.K * 4 + d * 4) + distinct_cells * 32 * d * 2 * 2
+    res["sparse_readout"] = _entry(ms, nbytes, 4.0 * d * float(counts["tokens_read"]), pk, "hbm")
+    del ws, out, o_long
     return res
 
 

@@ -152,9 +152,11 @@ int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
  *  - The array needs no initial contents (nothing in it must start at zero).
  *  - Every call on a device uses the same array: calls that overlap in time
  *    (other streams, or host threads without ordering) race on it.
- *  - The first call on each device looks up the array's address (once, for
- *    the device current at that call); make that first call before any
- *    stream capture begins.
+ *  - The first call on each device looks up the array's address (for the
+ *    device current at that call) and keeps it with the device's context; a
+ *    device reset (cudaDeviceReset) changes the address, and the next call
+ *    looks it up again.  Make the first call on a device, and the first
+ *    after a reset, before any stream capture begins.
  * Allocates nothing: no device or host memory is obtained. */
 size_t fs_prune_static_scratch_bytes(void);
 int fs_prune_cells_static(const float *amax, int batch, int H, int N,
@@ -206,6 +208,18 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype,
                    const float *o_long, const float *mix, int batch, int H,
                    int N, int d, const fs_params *p, float *out, void *ws,
                    size_t ws_bytes, void *stream);
+
+/* fs_window_attn that also records CUDA events on `stream` (no counterpart
+ * on the pages: per-kernel timing).  stage_events: NULL, or an array of 3
+ * cudaEvent_t (as void*) created by the caller; event 0 is recorded before
+ * the operand preparation (angle table, rotated keys, fp16 values), event 1
+ * before the attention kernel and event 2 after it.  Same arguments and
+ * results otherwise. */
+int fs_window_attn_traced(const void *q, const void *k, const void *v,
+                          int dtype, const float *o_long, const float *mix,
+                          int batch, int H, int N, int d, const fs_params *p,
+                          float *out, void *ws, size_t ws_bytes, void *stream,
+                          void *const *stage_events);
 
 /* Whole FS-L (or FS) attention forward: cell summaries, pools, selection,
  * then both attention branches and the mix in one kernel, all on `stream`.

@@ -292,6 +292,14 @@ int fs_sparse_readout(const void *q, const void *k, const void *v, int dtype,
 int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const float *o_long,
                    const float *mix, int batch, int H, int N, int d, const fs_params *p,
                    float *out, void *ws, size_t ws_bytes, void *stream) {
+  return fs_window_attn_traced(q, k, v, dtype, o_long, mix, batch, H, N, d, p, out, ws, ws_bytes,
+                               stream, nullptr);
+}
+
+int fs_window_attn_traced(const void *q, const void *k, const void *v, int dtype,
+                          const float *o_long, const float *mix, int batch, int H, int N, int d,
+                          const fs_params *p, float *out, void *ws, size_t ws_bytes, void *stream,
+                          void *const *stage_events) {
   FS_TRY(check_params(p));
   FS_TRY(check_shape(batch, H, N, d));
   FS_TRY(check_dtype(dtype));
@@ -303,8 +311,14 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *base = static_cast<char *>(ws);
   int *err = reinterpret_cast<int *>(base);
+  auto mark = [&](int i) -> int {
+    if (!stage_events || !stage_events[i]) return FS_OK;
+    return status_of(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st));
+  };
   FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  FS_TRY(mark(0));
   FS_TRY(prepare_window(sh, k, v, p->rope_base, base, W, err, st));
+  FS_TRY(mark(1));
   AttnArgs a{};
   a.sh = sh;
   a.q = q;
@@ -321,7 +335,8 @@ int fs_window_attn(const void *q, const void *k, const void *v, int dtype, const
   a.window = true;
   a.out = out;
   a.err = err;
-  return status_of(launch_attn_tc(a, st));
+  FS_TRY(status_of(launch_attn_tc(a, st)));
+  return mark(2);
 }
 
 int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype, int batch, int H,
@@ -421,6 +436,7 @@ int forward(const void *q, const void *k, const void *v, int dtype, const Shape 
 constexpr int kPipeDevices = 64;
 struct CopyPipe {
   cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t entry = nullptr;  // the caller's stream at the start of a call
   cudaEvent_t loaded[2] = {}, computed[2] = {}, stored[2] = {};
 };
 
@@ -433,11 +449,13 @@ CopyPipe *copy_pipe() {
     CopyPipe n;
     bool ok = cudaStreamCreateWithFlags(&n.h2d, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&n.d2h, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&n.entry, cudaEventDisableTiming) == cudaSuccess;
     for (int i = 0; ok && i < 2; ++i)
       ok = cudaEventCreateWithFlags(&n.loaded[i], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&n.computed[i], cudaEventDisableTiming) == cudaSuccess &&
            cudaEventCreateWithFlags(&n.stored[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
+      if (n.entry) cudaEventDestroy(n.entry);
       for (int i = 0; i < 2; ++i) {
         if (n.loaded[i]) cudaEventDestroy(n.loaded[i]);
         if (n.computed[i]) cudaEventDestroy(n.computed[i]);
@@ -501,6 +519,11 @@ int fs_attention_fwd_host(const void *q, const void *k, const void *v, int dtype
   char *base = static_cast<char *>(ws);
   int *err = reinterpret_cast<int *>(base);
   FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  // The loads begin only after everything already on the caller's stream:
+  // an earlier call's forwards and stores that still read the staging slots,
+  // and any work that writes the host inputs.
+  FS_TRY(status_of(cudaEventRecord(cp->entry, st)));
+  FS_TRY(status_of(cudaStreamWaitEvent(cp->h2d, cp->entry, 0)));
   const size_t elem = dtype == FS_FP32 ? 4 : 2;
   int rc = FS_OK;
   int chunk = 0;
@@ -645,8 +668,10 @@ extern "C" int fs_selftest_wait_timeout(void *ws, void *stream) {
 // them) race on it.
 //
 // Set-up: the first call on each device (the device current at that call)
-// looks up the array's device address once with cudaGetSymbolAddress and
-// keeps it; make that first call before any stream capture begins.
+// looks up the array's device address with cudaGetSymbolAddress and keeps it
+// with the device's context; after a device reset the next call looks it up
+// again.  Make the first call on a device (and the first after a reset)
+// before any stream capture begins.
 // ---------------------------------------------------------------------------
 namespace fs {
 namespace {
@@ -656,22 +681,50 @@ static __device__ __align__(256) unsigned char g_prune_scratch[kStaticScratchByt
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  void *ctx = nullptr;   // the device's context when the address was taken
+  void *addr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 
-// Device address of g_prune_scratch on the current device (looked up once).
+// The current context (cuCtxGetCurrent through the runtime's driver entry
+// point); null when it cannot be read.
+void *current_context() {
+  using GetCurrent = int (*)(void **);
+  static GetCurrent fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<GetCurrent>(ptr);
+    return static_cast<GetCurrent>(nullptr);
+  }();
+  void *ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// Device address of g_prune_scratch on the current device.  It is looked up
+// once per device and context: a device reset (cudaDeviceReset) replaces the
+// context and with it the array's address, so a changed context (or one that
+// cannot be read) makes the lookup run again.
 cudaError_t static_scratch(void **addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void *ctx = current_context();  // null before the runtime's first use of the device
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr &c = g_scratch_addr[dev];
+  if (!c.addr || !ctx || c.ctx != ctx) {
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_prune_scratch);
+    e = cudaGetSymbolAddress(&p, g_prune_scratch);  // also makes the context current
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx = current_context();
   }
-  *addr = g_scratch_addr[dev];
+  *addr = c.addr;
   return cudaSuccess;
 }
 

@@ -15,9 +15,10 @@
 // the keys are read once per call.
 //
 // Angles: row r < 64 of the table holds (cos, sin)(r theta_i); row 64 + u
-// holds (cos, sin)(64 u theta_i); both are evaluated in fp64 and rounded
-// once, and an absolute angle is composed from its two rows by the angle-sum
-// identity in fp32 (error of a few fp32 ulps, independent of the position).
+// holds (cos, sin)(64 u theta_i), each from the angle reduced modulo 2 pi in
+// fp64 and an fp32 sincospi; an absolute angle is composed from its two rows
+// by the angle-sum identity in fp32 (error of a few fp32 ulps, independent of
+// the position).
 #include "cell_summary.cuh"
 #include "fs_common.cuh"
 #include "fs_internal.h"
@@ -26,15 +27,27 @@
 namespace fs {
 namespace {
 
-__global__ void rope_table_kernel(float2 *__restrict__ tab, int rows, double base) {
+// theta_i / pi per block in fp64 (32 pow calls), then per entry one fp64
+// product reduced modulo 2 exactly and an fp32 sincospi of the remainder: the
+// fp64 work is a multiply and a floor, not a trigonometric evaluation (fp64
+// throughput is small on this chip).  Entry error: the fp32 rounding of the
+// reduced angle (<= 2^-24 * pi rad) plus sincospif's ulp, against the fp64
+// reference values.
+__global__ void __launch_bounds__(256) rope_table_kernel(float2 *__restrict__ tab, int rows,
+                                                         double base) {
+  __shared__ double s_th[kD / 2];
+  if (threadIdx.x < kD / 2)
+    s_th[threadIdx.x] = pow(base, -2.0 * (double)threadIdx.x / (double)kD) / 3.14159265358979323846;
+  __syncthreads();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * (kD / 2)) return;
   const int row = idx / (kD / 2), i = idx % (kD / 2);
-  const double theta = pow(base, -2.0 * (double)i / (double)kD);
   const double pos = row < 64 ? (double)row : 64.0 * (double)(row - 64);
-  double s, c;
-  sincos(pos * theta, &s, &c);
-  tab[idx] = make_float2((float)c, (float)s);
+  const double x = pos * s_th[i];                // angle / pi
+  const double r = x - 2.0 * floor(0.5 * x);     // in [0, 2), exact
+  float sn, cs;
+  sincospif((float)r, &sn, &cs);
+  tab[idx] = make_float2(cs, sn);
 }
 
 // Four threads per token row; thread part p rotates pairs 8p .. 8p+7 (dims

@@ -37,8 +37,8 @@
 // q-tiles, so the epilogue of a q-tile has the whole next q-tile to run in,
 // off the softmax and MMA paths.
 //
-// Precision.  Window: the rotated q and k (fp32, absolute angles from an
-// fp64 table) are split into bf16 hi + lo halves and S takes three MMA
+// Precision.  Window: the rotated q and k (fp32, absolute angles from the
+// angle table) are split into bf16 hi + lo halves and S takes three MMA
 // chains (hi.hi + hi.lo + lo.hi): a single bf16 rounding of the rotated
 // vectors exceeds the output tolerance on lognormal keys.  The window P.V
 // product runs in fp16 (P below 2^14, V re-encoded exactly from bf16): with a
@@ -59,27 +59,6 @@
 
 namespace fs {
 namespace {
-
-// Pipeline timeline probe (builds with -DFS_TRACE only): clock64() stamps of
-// each role's hand-offs in CTA 0, event e of global tile / q-tile t at
-// [e*64 + t].
-#ifdef FS_TRACE
-__device__ long long *g_trace = nullptr;
-__shared__ long long *s_trace;  // CTA 0's copy of g_trace (null elsewhere)
-#define FS_TR(e, t)                                                  \
-  do {                                                               \
-    long long *tp_ = s_trace;                                        \
-    if (tp_ && (t) < 64) tp_[(e) * 64 + (t)] = clock64();            \
-  } while (0)
-__device__ __forceinline__ bool g_trace_nu_enabled() { return s_trace != nullptr; }
-__device__ __forceinline__ void g_trace_nu(int i, int nu) { g_trace[9 * 64 + i] = nu; }
-#else
-__device__ __forceinline__ bool g_trace_nu_enabled() { return false; }
-__device__ __forceinline__ void g_trace_nu(int, int) {}
-#define FS_TR(e, t) \
-  do {              \
-  } while (0)
-#endif
 
 constexpr int kKT = 128;          // keys per tile
 constexpr int kRing = 3;          // key / value ring depth
@@ -261,7 +240,6 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
       if (T >= 2 && !wait_nth(&bar.s_free[b], T / 2 - 1, p.err)) return;
       tc::fence_after_sync();
-      FS_TR(18, T);
       const uint32_t kh = base + kOffK + slot * 32768;
       const uint64_t dkh = tc::desc_sw128(kh), dkl = tc::desc_sw128(kh + 16384);
       const uint32_t s_col = tmem + kColS + 128 * b;
@@ -282,7 +260,6 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       }
       tc::mma_commit(&bar.s_full[b]);
       tc::mma_commit(&bar.k_empty[slot]);
-      FS_TR(2, T);
     }
     tc::mma_commit(&bar.q_empty);
   }
@@ -310,10 +287,8 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       if (t >= it.nw + nl) break;
       const int slot = T % kRing, b = T & 1;
       if (!wait_nth(&bar.p_full[b], T / 2, p.err)) return;
-      FS_TR(19, T);
       // the value tile is read by this thread's MMAs: observe its arrival here too
       if (!wait_nth(&bar.raw_full[slot], T / kRing, p.err)) return;
-      FS_TR(20, T);
       tc::fence_after_sync();
       const uint64_t dv = tc::desc_sw128(base + kOffV + slot * 16384);
       const uint32_t sp = tmem + kColS + 128 * b;
@@ -340,7 +315,6 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
       tc::mma_commit(&bar.pv_done);
       tc::mma_commit(&bar.v_empty[slot]);
       tc::mma_commit(&bar.s_free[b]);
-      FS_TR(5, T);
     }
     tc::mma_commit(&bar.o_done[i & 1]);
   }
@@ -370,7 +344,6 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
       }
       if (t >= it.nw + nl) break;
       const int slot = T % kRing;
-      FS_TR(0, T);
       if (T >= kRing) {
         if (!wait_nth(&bar.k_empty[slot], T / kRing - 1, p.err)) return drain_tma(bar, T);
         if (!wait_nth(&bar.v_empty[slot], T / kRing - 1, p.err)) return drain_tma(bar, T);
@@ -412,7 +385,6 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of(p, g);
     if (i > 0 && !wait_nth(&bar.u_free, i - 1, p.err)) return;
-    if (lane == 0) FS_TR(8, i);
     int nu = 0;
     if (p.has_long) {
       const int A = it.b0 / kS;  // cells ending at or before the block start
@@ -446,8 +418,6 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
     if (lane == 0) bar.nu = nu;
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&bar.u_full);
-    if (lane == 0) FS_TR(7, i);
-    if (lane == 0 && i < 64 && g_trace_nu_enabled()) g_trace_nu(i, nu);
   }
 }
 
@@ -484,7 +454,6 @@ __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, 
       }
       tc::fence_async_smem();
       tc::mbar_arrive(&bar.q_full);
-      if (r == 0) FS_TR(1, i);
     }
     if (g_prev >= 0 && !epilogue_rows(p, bar, tmem, g_prev, i - 1, r)) return;
     if (!real) break;
@@ -498,15 +467,16 @@ __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, 
 constexpr uint32_t kNegInf = 0xff800000u;
 
 // window: columns outside [lo, hi] (tile columns) become -inf; the test is
-// uniform across the warp except in a chunk a triangular edge crosses
-__device__ __forceinline__ void mask_window(uint32_t (&x)[32], int lo, int hi, int c0) {
+// uniform across the warp except in a chunk a triangular edge crosses.
+// Returns whether any row of the warp reads a column of the chunk.
+__device__ __forceinline__ bool mask_window(uint32_t (&x)[32], int lo, int hi, int c0) {
   const bool full = lo <= c0 && hi >= c0 + 31;
   const bool empty = hi < c0 || lo > c0 + 31;
-  if (__all_sync(0xffffffffu, full)) return;
+  if (__all_sync(0xffffffffu, full)) return true;
   if (__all_sync(0xffffffffu, empty)) {
 #pragma unroll
     for (int c = 0; c < 32; ++c) x[c] = kNegInf;
-    return;
+    return false;
   }
   // bit c set iff column c0 + c lies in [lo, hi]; then one select per element
   // (no per-element branches)
@@ -516,6 +486,7 @@ __device__ __forceinline__ void mask_window(uint32_t (&x)[32], int lo, int hi, i
   const uint32_t valid = below_b & ~below_a;
 #pragma unroll
   for (int c = 0; c < 32; ++c) x[c] = (valid & (1u << c)) ? x[c] : kNegInf;
+  return true;
 }
 
 __device__ __forceinline__ float max_chunk(const uint32_t (&x)[32]) {
@@ -608,7 +579,6 @@ __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int
   if (!wait_nth(&bar.o_done[par], i >> 1, p.err)) return false;
   if (!wait_nth(&bar.stats_full[par], i >> 1, p.err)) return false;
   tc::fence_after_sync();
-  if (r == 0) FS_TR(10, i);
   const float2 s0 = bar.stat[par][0][r], s1 = bar.stat[par][1][r];
   const int nl = bar.item_nl[par];
   const float lw = s0.x + s1.x, ll = s0.y + s1.y;
@@ -675,7 +645,6 @@ __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int
     tc::mbar_arrive(&bar.o_free[par]);
     tc::mbar_arrive(&bar.stat_free[par]);
   }
-  if (r == 0) FS_TR(6, i);
   return true;
 }
 
@@ -741,24 +710,26 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
         if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
         tc::fence_after_sync();
-        if (r == 0 && half == 0) FS_TR(3, T);
         bool cell[2];
         int lo, hi;
         const bool any = tile_cols(p, it, t, n, half, pick, lo, hi, cell);
         // the warp's 64 score columns in one TMEM round trip
         uint32_t xa[32], xb[32];
         float mx = -INFINITY;
-        if (r == 0 && half == 0) FS_TR(16, T);
+        // per 32-key chunk: does any row of the warp read it (else its
+        // probabilities are zeros, written without exponentials)
+        bool live0 = false, live1 = false;
         if (any) {
           tc::tmem_ld32(s_addr, xa);
           tc::tmem_ld32(s_addr + 32, xb);
           tc::tmem_wait_ld();
-          if (r == 0 && half == 0) FS_TR(17, T);
           if (!is_long) {
-            mask_window(xa, lo, hi, 64 * half);
-            mask_window(xb, lo, hi, 64 * half + 32);
+            live0 = mask_window(xa, lo, hi, 64 * half);
+            live1 = mask_window(xb, lo, hi, 64 * half + 32);
             mx = fmaxf(max_chunk(xa), max_chunk(xb));
           } else {
+            live0 = __any_sync(0xffffffffu, cell[0]);
+            live1 = __any_sync(0xffffffffu, cell[1]);
             // a long tile's chunk is one cell, picked by the row or not: its
             // scores are left as they are and the pick enters the maximum
             // here and the probabilities below (through their reference)
@@ -766,11 +737,9 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
             mx = fmaxf(cell[0] ? ma : -INFINITY, cell[1] ? mb : -INFINITY);
           }
         }
-        if (r == 0 && half == 0) FS_TR(11, T);
         float2 o;
         if (!pr.swap(make_float2(mx, 0.f), o, half, r, lane, p.err)) return;
         mx = fmaxf(mx, o.x);
-        if (r == 0 && half == 0) FS_TR(12, T);
         const float m = is_long ? ml : mw;
         float l = is_long ? ll : lw;
         const float mt = mx * sl2;
@@ -786,10 +755,18 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
 #pragma unroll 1
           for (int ch = 0; ch < 2; ++ch) {
             const uint32_t pa = s_addr + 32 * ch;
-            // an unpicked cell gets reference +inf: 2^(x - inf) = 0 exactly
-            const float mref = (is_long && !(ch ? cell[1] : cell[0])) ? INFINITY : muse;
-            l += split ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
-                       : exp_chunk<false>(xa, pa, pa + 16, sl2, mref);
+            if (ch ? live1 : live0) {
+              // an unpicked cell gets reference +inf: 2^(x - inf) = 0 exactly
+              const float mref = (is_long && !(ch ? cell[1] : cell[0])) ? INFINITY : muse;
+              l += split ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
+                         : exp_chunk<false>(xa, pa, pa + 16, sl2, mref);
+            } else {
+              uint32_t z[16];
+#pragma unroll
+              for (int c = 0; c < 16; ++c) z[c] = 0u;
+              tc::tmem_st16(pa, z);
+              if (split) tc::tmem_st16(pa + 16, z);
+            }
             if (ch == 0) {
 #pragma unroll
               for (int c = 0; c < 32; ++c) xa[c] = xb[c];
@@ -813,9 +790,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
           mw = mnew;
           lw = l;
         }
-        if (r == 0 && half == 0) FS_TR(13, T);
         if (__any_sync(0xffffffffu, resc)) {
-          if (lane == 0 && half == 0) FS_TR(14 + (quarter >> 1), T);
           // the previous P.V accumulates into the same set: let it finish
           if (!wait_nth(&bar.pv_done, T - 1, p.err)) return;
           tc::fence_after_sync();
@@ -825,7 +800,6 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bar.p_full[b]);
-        if (r == 0 && half == 0) FS_TR(4, T);
       }
       if (done) break;
     }
@@ -850,9 +824,6 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   __shared__ Barriers bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-#ifdef FS_TRACE
-  if (threadIdx.x == 0) s_trace = blockIdx.x == 0 ? g_trace : nullptr;
-#endif
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar.q_full, kRotThreads);
     tc::mbar_init(&bar.q_empty, 1);
@@ -1028,9 +999,3 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
 }
 
 }  // namespace fs
-
-#ifdef FS_TRACE
-extern "C" int fs_trace_set(long long *buf) {
-  return (int)cudaMemcpyToSymbol(fs::g_trace, &buf, sizeof(buf));
-}
-#endif

@@ -30,7 +30,8 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
            "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
-           "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host"]
+           "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host",
+           "fs_window_attn_traced"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
@@ -95,6 +96,7 @@ def load(build_if_stale: bool = True):
         L.fs_select_cells.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, PP, P, P, P]
         L.fs_sparse_readout.argtypes = [P, P, P, I, P, I, I, I, I, PP, P, P]
         L.fs_window_attn.argtypes = [P, P, P, I, P, P, I, I, I, I, PP, P, P, Z, P]
+        L.fs_window_attn_traced.argtypes = L.fs_window_attn.argtypes + [P]
         L.fs_attention_fwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, Z, P]
         L.fs_attention_fwd_traced.argtypes = L.fs_attention_fwd.argtypes + [P]
         L.fs_attention_fwd_host.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, I, P, Z, P]
@@ -290,7 +292,11 @@ def fs_sparse_readout(q, k, v, sel, params=None, o_long=None, stream=None):
     return o_long
 
 
-def fs_window_attn(q, k, v, o_long=None, mix=None, params=None, out=None, stream=None):
+def fs_window_attn(q, k, v, o_long=None, mix=None, params=None, out=None, stream=None,
+                   ws=None, events=None):
+    """Window branch (and mix with ``o_long`` when given).  ``events``: None,
+    or 3 torch.cuda.Event objects (enable_timing) recorded before the operand
+    preparation, before the attention kernel and after it."""
     L = load()
     p = _params(params)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -303,11 +309,26 @@ def fs_window_attn(q, k, v, o_long=None, mix=None, params=None, out=None, stream
     wsb = L.fs_window_workspace_bytes(B, H, N, d, ctypes.byref(p))
     if wsb == 0:
         raise FSError(FS_ERR_INVALID_ARG, "fs_window_workspace_bytes")
-    ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
-    _check(L.fs_window_attn(_ptr(q), _ptr(k), _ptr(v), FS_BF16, _ptr(o_long), _ptr(mix), B, H,
-                            N, d, ctypes.byref(p), _ptr(out), _ptr(ws), wsb, _stream(stream)),
-           "fs_window_attn")
+    if ws is None:
+        ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    elif ws.numel() * ws.element_size() < wsb:
+        raise ValueError(f"workspace too small: {ws.numel()} < {wsb} bytes")
+    args = [_ptr(q), _ptr(k), _ptr(v), FS_BF16, _ptr(o_long), _ptr(mix), B, H, N, d,
+            ctypes.byref(p), _ptr(out), _ptr(ws), wsb, _stream(stream)]
+    if events is None:
+        _check(L.fs_window_attn(*args), "fs_window_attn")
+    else:
+        if len(events) != 3:
+            raise ValueError("need 3 events")
+        _check(L.fs_window_attn_traced(*args, _event_array(events)), "fs_window_attn_traced")
     return out
+
+
+def _event_array(events):
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event lazily
+            e.record()
+    return (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
 
 
 def fs_attention_fwd(q, k, v, lam, sigma, mix, params=None, out=None, ws=None, stream=None):
@@ -403,10 +424,7 @@ def fs_attention_fwd_traced(q, k, v, lam, sigma, mix, events, params=None, out=N
     elif ws.numel() * ws.element_size() < wsb:
         raise ValueError("workspace too small")
     out = out if out is not None else torch.empty((B, H, N, d), device=q.device, dtype=torch.float32)
-    for e in events:
-        if e.cuda_event == 0:  # torch creates the CUDA event lazily
-            e.record()
-    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    arr = _event_array(events)
     _check(L.fs_attention_fwd_traced(_ptr(q), _ptr(k), _ptr(v), code, B, H, N, d,
                                      ctypes.byref(p), _ptr(lam), _ptr(sigma), _ptr(mix),
                                      _ptr(out), _ptr(ws), wsb, _stream(stream), arr),

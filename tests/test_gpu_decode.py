@@ -59,11 +59,17 @@ def _run(inp, t0, t1, params):
     return d, st, out, sel
 
 
-@pytest.mark.parametrize("N,t0,t1,H", [(4352, 4096 - 40, 4096 + 40, 3), (384, 0, 300, 2)])
-def test_decode_rows_match_oracle_and_state(N, t0, t1, H):
+@pytest.mark.parametrize("N,t0,t1,H,sigma_ln", [
+    (4352, 4096 - 40, 4096 + 40, 3, 0.8),
+    (384, 0, 300, 2, 0.8),
+    # the benchmark's decode context: 16 heads, t around 65536 (a block start,
+    # where the pool advances), lognormal spread of the 64k workload
+    (65536 + 128, 65536 - 40, 65536 + 40, 16, 0.5),
+])
+def test_decode_rows_match_oracle_and_state(N, t0, t1, H, sigma_ln):
     params = dict(PAGE)
-    inp = make_inputs(1, H, N, seed=N + t0, sigma_ln=0.8, needles="uniform" if N > 2048 else "none",
-                      n_needles=4)
+    inp = make_inputs(1, H, N, seed=N + t0, sigma_ln=sigma_ln,
+                      needles="uniform" if N > 2048 else "none", n_needles=4)
     d, st, out, sel = _run(inp, t0, t1, params)
     rows = np.arange(t0, t1)
     compare_forward(inp, params, rows, out, sel)

@@ -86,3 +86,19 @@ def test_explicit_stream_and_repeat_calls_are_deterministic():
         b = fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], PAGE)
     s.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("N,H", [(16384, 4), (65536, 16)])
+def test_fs_mode_across_candidate_chunks(N, H):
+    # Base FS scores every available cell: the last blocks have up to
+    # N/32 - 4 candidates, taken by the selection kernel in chunks of 128
+    # with the running top-K carried from chunk to chunk.  N = 65536 with 16
+    # heads is the benchmark's base-FS comparator (up to 2044 candidates, 16
+    # chunks).  Rows: sampled blocks plus every row of the last block.
+    params = dict(PAGE, mode=1)
+    inp = make_inputs(1, H, N, seed=N // 1024 + H, sigma_ln=0.5 if N > 16384 else 0.8)
+    out, sel, _ = run_fwd(inp, params)
+    rows = sample_rows(N, n_blocks=12, per_block=8, seed=N)
+    rows = np.unique(np.concatenate([rows, np.arange(N - 128, N)]))
+    stats = compare_forward(inp, params, rows, out, sel)
+    print(N, H, stats)

@@ -48,6 +48,35 @@ def test_host_forward_matches_device_forward(B, H, N, hc, dtype, pinned):
         assert torch.equal(out, ref)
 
 
+def test_host_forward_back_to_back_calls_with_different_inputs():
+    # Two calls on one workspace and stream with no synchronisation between
+    # them: the second call's loads into the staging slots wait for the first
+    # call's forwards and stores, so each output matches its own inputs.
+    B, H, N, hc = 1, 4, 2048, 1
+    params = fs.fs_default_params(**PAGE)
+    inps = [make_inputs(B, H, N, seed=90 + i, sigma_ln=0.8) for i in range(2)]
+    refs = [_device_ref(inp, params) for inp in inps]
+    assert not torch.equal(refs[0], refs[1])
+    lam, sigma, mix = inps[0].lam.cuda(), inps[0].sigma.cuda(), inps[0].mix.cuda()
+    host = [[t.contiguous().pin_memory() for t in (inp.q, inp.k, inp.v)] for inp in inps]
+    # the second call runs on the first call's per-head parameters
+    refs[1] = fs.fs_attention_fwd(*[t.cuda() for t in (inps[1].q, inps[1].k, inps[1].v)],
+                                  lam, sigma, mix, params).cpu()
+    outs = [torch.full((B, H, N, 64), float("nan")).pin_memory() for _ in range(2)]
+    ws = torch.empty(fs.fs_host_workspace_bytes(B, H, N, 64, params, fs.FS_BF16, hc),
+                     device="cuda", dtype=torch.uint8)
+    torch.cuda.synchronize()
+    for rep in range(2):
+        for o in outs:
+            o.fill_(float("nan"))
+        for i in range(2):
+            fs.fs_attention_fwd_host(*host[i], lam, sigma, mix, params, out=outs[i], ws=ws,
+                                     heads_per_chunk=hc)
+        fs.fs_check_status(ws)
+        assert torch.equal(outs[0], refs[0])
+        assert torch.equal(outs[1], refs[1])
+
+
 def test_host_forward_reports_a_range_error_of_any_group():
     B, H, N = 1, 3, 1024
     inp = make_inputs(B, H, N, seed=4)

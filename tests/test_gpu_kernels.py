@@ -68,6 +68,7 @@ def _select(inp, params, with_scores=False):
 @pytest.mark.parametrize("params,N,lam0", [
     (PAGE, 8192, False),
     (dict(PAGE, mode=1), 4096, False),
+    (dict(PAGE, mode=1), 16384, False),   # up to 508 candidates: four 128-cell chunks
     (PAGE, 4096, True),
     (dict(PAGE, K=1), 4096, False),
     (dict(PAGE, K=8, P=16, W=2), 8192, False),
