@@ -181,6 +181,11 @@ def fs_workspace_bytes(batch, H, N, d, params=None, dtype=FS_BF16) -> int:
     return load().fs_workspace_bytes(batch, H, N, d, ctypes.byref(p), dtype)
 
 
+def fs_window_workspace_bytes(batch, H, N, d, params=None) -> int:
+    p = _params(params)
+    return load().fs_window_workspace_bytes(batch, H, N, d, ctypes.byref(p))
+
+
 def fs_cell_summarize(k, s=32, kbar=None, amax=None, stream=None):
     L = load()
     _dev(k, "k", (torch.bfloat16, torch.float32))
