@@ -299,7 +299,9 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extras:
         res["branches"] = time_branches(q, k, v, mix, view["sel"], params, stream, distinct,
                                         counts, pk)
+    if not args.no_extras or getattr(args, "decode_only", False):
         res["decode"] = time_decode(q, k, v, lam, sigma, mix, params, stream)
+    if not args.no_extras:
         res["fs_mode"] = time_fs_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
     return res
 
@@ -370,45 +372,44 @@ def time_branches(q, k, v, mix, sel, params, stream, distinct_cells, counts, pk,
     return res
 
 
-def time_decode(q, k, v, lam, sigma, mix, params, stream, iters=200):
-    """One decode step at t = N (the token after the prefix) against the FS-L
-    state the prefix leaves: history caches, cell summaries, the pool of the
-    last block.  t = N starts a block, so every step also advances the pool;
-    the pool is restored (one small device copy, inside the timing) before
-    each step so that every step does the same work."""
+def time_decode(q, k, v, lam, sigma, mix, params, stream, steps=256, warm=8):
+    """Decode steps right after the whole prefix: the bounded state is built
+    from the prefill (cell summaries, pools, fs_decode_state_init at N0 = N),
+    then tokens t = N, N+1, ... are decoded (the new tokens are rows of the
+    prefix's last block).  `steps` consecutive steps (two block starts, where
+    the pool advances, and eight cell closes) are captured in a CUDA graph
+    and replayed once, so the time is the device's, not the host's launch
+    rate; the state has the same size at any t."""
     from long_context_lm_gb300 import fs
     B, H, N, d = q.shape
-    n_cap = N + 128
-    kc = torch.zeros((B, H, n_cap, d), device=q.device, dtype=q.dtype)
-    vc = torch.zeros_like(kc)
-    kc[:, :, :N] = k
-    vc[:, :, :N] = v
-    kbar, amax = fs.fs_cell_summarize(kc)
-    pool_all, count_all = fs.fs_prune_cells(amax, n_cap, params)
-    blk = (N - 1) // 128
-    cap = pool_all.shape[-1]
-    # pool and count share one buffer, so that one copy restores both
-    buf0 = torch.cat([pool_all[:, :, blk].reshape(-1), count_all[:, :, blk].reshape(-1)])
-    buf = buf0.clone()
-    st = dict(k_cache=kc, v_cache=vc, kbar=kbar, amax=amax,
-              pool=buf[:B * H * cap].view(B, H, cap), pool_count=buf[B * H * cap:].view(B, H))
-    qt, kt, vt = (x[:, :, N - 1].contiguous() for x in (q, k, v))
+    kbar, amax = fs.fs_cell_summarize(k)
+    pool, count = fs.fs_prune_cells(amax, N, params)
+    state = fs.fs_decode_state_init(B, H, params, k=k, v=v, kbar=kbar, amax=amax, pool=pool,
+                                    pool_count=count, N0=N)
+    rows = [N - 128 + (i % 128) for i in range(warm + steps)]
+    toks = [tuple(x[:, :, r].contiguous() for x in (q, k, v)) for r in rows]
     out = torch.empty((B, H, d), device=q.device, dtype=torch.float32)
-    for _ in range(5):
-        buf.copy_(buf0)
-        fs.fs_decode_step(qt, kt, vt, N, st, lam, sigma, mix, params, out=out)
+    for i in range(warm):
+        fs.fs_decode_step(*toks[i], N + i, state, lam, sigma, mix, params, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    with torch.cuda.stream(s2):
+        with torch.cuda.graph(g, stream=s2):
+            for i in range(warm, warm + steps):
+                fs.fs_decode_step(*toks[i], N + i, state, lam, sigma, mix, params, out=out)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(iters):
-        buf.copy_(buf0)
-        fs.fs_decode_step(qt, kt, vt, N, st, lam, sigma, mix, params, out=out)
+    g.replay()
     b.record(stream)
     torch.cuda.synchronize()
-    us = a.elapsed_time(b) / iters * 1e3
-    return {"t": N, "us_per_token": us, "heads": B * H, "steps": iters,
-            "note": "per step: pool restore (1 copy) + fs_decode_step, all (batch, head) at once"}
+    fs.fs_check_status(state)
+    us = a.elapsed_time(b) / steps * 1e3
+    return {"t0": N + warm, "us_per_token": us, "heads": B * H, "steps": steps,
+            "state_bytes": state.numel(), "state_bytes_per_head": state.numel() / (B * H),
+            "note": "bounded state from the prefill; graph of consecutive steps, all (batch, head)"}
 
 
 def time_fs_mode(q, k, v, lam, sigma, mix, params, stream, tokens, steps=3):
@@ -533,8 +534,11 @@ def main():
         for name in [n for n in args.extra_lengths.split(",") if n and n != args.workload]:
             sub = argparse.Namespace(**vars(args))
             sub.workload, sub.steps, sub.warmup, sub.no_e2e = name, 5, 3, True
+            sub.no_extras, sub.decode_only = True, name == "fsl_256k"
             r = run_ours(sub, rank, world, local_rank)
             per_len[name] = r["value"]
+            if "decode" in r:
+                res["decode_256k"] = r["decode"]
             res.setdefault("other_lengths", {})[name] = {
                 "value": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
                 "kernels": {k_: {"ms": v_["ms"], "share": v_["share"]} for k_, v_ in r["kernels"].items()}}

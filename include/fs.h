@@ -47,8 +47,10 @@ typedef enum {
   FS_ERR_TIMEOUT = 4,
   FS_ERR_RANGE = 5, /* a finite value of v read by the window branch has
                        |v| >= 65520: past the fp16 range of its P.V product */
-  FS_ERR_SCRATCH_LIMIT = 6 /* fs_prune_cells_static: the shape needs more
-                              than its fixed scratch array */
+  FS_ERR_SCRATCH_LIMIT = 6, /* fs_prune_cells_static: the shape needs more
+                               than its fixed scratch array */
+  FS_ERR_STATE = 7 /* fs_decode_step: the decode state is not at the step's
+                      position t */
 } fs_status;
 
 typedef enum { FS_BF16 = 0, FS_FP32 = 1 } fs_dtype;
@@ -114,32 +116,64 @@ int fs_prune_cells(const float *amax, int batch, int H, int N,
                    const fs_params *p, int32_t *pool, int32_t *pool_count,
                    void *ws, size_t ws_bytes, void *stream);
 
-/* One decode step of FS-L for token t of every (batch, head), against the
- * bounded state the caller owns (paper.rainbus.top summary, 核心方法: linear
- * prefill, constant-size decode state; 方法步骤详情 ②-⑥).  Per (batch, head):
+/* Decoding from a bounded state (paper.rainbus.top summary, 核心方法: linear
+ * prefill, constant-size decode state; 实验结果: constant attention buffer
+ * from 4k to 256k; ai.info "Methodology in Plain English": a bounded pool of
+ * 8 recent plus 64 highest-norm cells, updated at block boundaries, and a
+ * small streaming cache).  The state is one caller-owned device buffer of
+ * fs_decode_state_bytes() bytes whose size does not depend on the position:
+ *  - a 256-byte header whose first int is the error word (fs_check_status
+ *    reads it) and the relative-angle tables of the window branch;
+ *  - per (batch, head): a w-row ring of the last keys and values, P + W +
+ *    Bq/s + 1 cell slots (raw keys and values of one cell, its mean key and
+ *    largest key norm), and the lists that place the slots: the W recent
+ *    cells, the running top-P older cells (a_c desc, c asc), the closed cells
+ *    not yet available, the open cell, the free slots.
+ * A cell stays in its slot from its first token until it leaves the pool; a
+ * cell dropped from the top P is never needed again (the threshold only
+ * rises), so its slot is reused.  Decoding supports w <= 512 (the window is
+ * staged in shared memory), FS-L mode only, P + W <= 72, K <= 8. */
+size_t fs_decode_state_bytes(int batch, int H, int d, const fs_params *p);
+
+/* Layout of a decode state, for inspection: offs receives 7 values --
+ * the global part's bytes, one (batch, head)'s bytes, then inside a head's
+ * block the offsets of the slot cell ids (int32), slot a_c (f32), slot mean
+ * keys (f32 x d), and the number of slots and of header ints.  Head bh's
+ * block starts at offs[0] + bh * offs[1]. */
+int fs_decode_state_view(int batch, int H, int d, const fs_params *p,
+                         size_t *offs);
+
+/* Fill `state` as it stands after the first N0 tokens of a sequence.
+ *   k, v        [batch,H,N,d] bf16 DEVICE: rows < N0 are the prefix (N0 <= N,
+ *               N a multiple of Bq); NULL when N0 == 0
+ *   kbar, amax  fs_cell_summarize of k (cells < floor(N0/s) are read)
+ *   pool, pool_count  fs_prune_cells of amax (the row of block
+ *               floor((N0-1)/Bq) is read); NULL when N0 == 0
+ * The next fs_decode_step must be for t = N0. */
+int fs_decode_state_init(const void *k, const void *v, int dtype,
+                         const float *kbar, const float *amax,
+                         const int32_t *pool, const int32_t *pool_count,
+                         int batch, int H, int N, int N0, int d,
+                         const fs_params *p, void *state, size_t state_bytes,
+                         void *stream);
+
+/* One decode step of FS-L for token t of every (batch, head): row t of
+ * fs_attention_fwd's output, from the bounded state alone (paper.rainbus.top
+ * summary, 方法步骤详情 ②-⑥).  It also advances the state: at a block start
+ * (t % Bq == 0, t > 0) the pool moves to block t/Bq; k_t, v_t enter the ring
+ * and the open cell; a cell that row t closes gets its summary, bit-identical
+ * to fs_cell_summarize.
  *   q_t, k_t, v_t   [batch,H,d] bf16: the new token
- *   k_cache,v_cache [batch,H,n_cap,d] bf16: rows < t hold the history; the
- *                   step writes row t
- *   kbar, amax      [batch,H,n_cap/s,d], [batch,H,n_cap/s] f32: cells
- *                   < floor(t/s) hold their summaries; the step writes cell
- *                   t/s when row t closes it ((t+1) % s == 0), bit-identical
- *                   to fs_cell_summarize
- *   pool, pool_count [batch,H,P+W] int32, [batch,H] int32: the pool of block
- *                   floor((t-1)/Bq) in fs_prune_cells' row layout (count 0
- *                   for t = 0); at a block start (t % Bq == 0, t > 0) the
- *                   step advances it in place to block t/Bq, exactly as
- *                   fs_prune_cells would compute that block
  *   lambda, sigma, mix [H] f32
- *   out_t           [batch,H,d] f32: row t of fs_attention_fwd's output
+ *   out_t           [batch,H,d] f32
  *   sel_t           [batch,H,K] int32 (nullable): the selected cells
- * n_cap is a multiple of Bq and 0 <= t < n_cap; FS-L mode only; P + W <= 72.
- * A step reads about (w + K*s) key/value rows and the pool's summaries per
- * (batch, head); one CTA per (batch, head). */
+ * The state must be at position t (after t tokens); otherwise the step
+ * changes nothing and records FS_ERR_STATE in the state's error word.
+ * One CTA per (batch, head); the state stays the same size at any t. */
 int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
-                   int batch, int H, int d, int t, int n_cap, void *k_cache,
-                   void *v_cache, float *kbar, float *amax, int32_t *pool,
-                   int32_t *pool_count, const float *lambda, const float *sigma,
-                   const float *mix, const fs_params *p, float *out_t,
+                   int batch, int H, int d, int t, const float *lambda,
+                   const float *sigma, const float *mix, const fs_params *p,
+                   void *state, size_t state_bytes, float *out_t,
                    int32_t *sel_t, void *stream);
 
 /* fs_prune_cells for callers that can neither allocate device memory nor

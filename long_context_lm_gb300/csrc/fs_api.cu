@@ -180,6 +180,7 @@ const char *fs_status_string(int status) {
     case FS_ERR_SCRATCH_LIMIT:
       return "shape needs more scratch than the static array holds "
              "(4 MiB: batch*H*ceil(N/2048) <= 4096)";
+    case FS_ERR_STATE: return "the decode state is not at the step's position";
     default: return "unknown status";
   }
 }
@@ -576,44 +577,86 @@ int fs_attention_fwd_host(const void *q, const void *k, const void *v, int dtype
 
 }  // extern "C"
 
-extern "C" int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
-                              int batch, int H, int d, int t, int n_cap, void *k_cache,
-                              void *v_cache, float *kbar, float *amax, int32_t *pool,
-                              int32_t *pool_count, const float *lambda, const float *sigma,
-                              const float *mix, const fs_params *p, float *out_t,
-                              int32_t *sel_t, void *stream) {
+namespace fs {
+namespace {
+int check_decode(const fs_params *p, int d) {
   FS_TRY(check_params(p));
-  FS_TRY(check_shape(batch, H, n_cap, d));
+  if (d != kD) return FS_ERR_UNSUPPORTED;
+  if (p->mode != FS_MODE_FSL) return FS_ERR_INVALID_ARG;
+  if (p->P + p->W > kMaxP + 8 || p->W > 8 || p->w > 512) return FS_ERR_UNSUPPORTED;
+  return FS_OK;
+}
+}  // namespace
+}  // namespace fs
+
+extern "C" size_t fs_decode_state_bytes(int batch, int H, int d, const fs_params *p) {
+  if (check_decode(p, d) != FS_OK || check_shape(batch, H, kBq, d) != FS_OK) return 0;
+  return decode_layout(p->w, p->P, p->W, p->K).total(batch * H);
+}
+
+extern "C" int fs_decode_state_view(int batch, int H, int d, const fs_params *p, size_t *offs) {
+  FS_TRY(check_decode(p, d));
+  FS_TRY(check_shape(batch, H, kBq, d));
+  if (!offs) return FS_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(p->w, p->P, p->W, p->K);
+  offs[0] = L.global_bytes;
+  offs[1] = L.head_bytes;
+  offs[2] = L.slot_cell;
+  offs[3] = L.slot_amax;
+  offs[4] = L.slot_kbar;
+  offs[5] = (size_t)L.nslots;
+  offs[6] = (size_t)kDecodeHeaderInts;
+  return FS_OK;
+}
+
+extern "C" int fs_decode_state_init(const void *k, const void *v, int dtype, const float *kbar,
+                                    const float *amax, const int32_t *pool,
+                                    const int32_t *pool_count, int batch, int H, int N, int N0,
+                                    int d, const fs_params *p, void *state, size_t state_bytes,
+                                    void *stream) {
+  FS_TRY(check_decode(p, d));
   FS_TRY(check_dtype(dtype));
   if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
-  if (p->mode != FS_MODE_FSL) return FS_ERR_INVALID_ARG;
-  if (p->P + p->W > kMaxP + 8) return FS_ERR_UNSUPPORTED;
-  if (t < 0 || t >= n_cap) return FS_ERR_INVALID_ARG;
-  if (!q_t || !k_t || !v_t || !k_cache || !v_cache || !kbar || !amax || !pool || !pool_count ||
-      !lambda || !sigma || !mix || !out_t)
+  if (N0 < 0 || !state) return FS_ERR_INVALID_ARG;
+  if (N0 > 0) {
+    FS_TRY(check_shape(batch, H, N, d));
+    if (N0 > N || !k || !v || !kbar || !amax || !pool || !pool_count) return FS_ERR_INVALID_ARG;
+  } else {
+    FS_TRY(check_shape(batch, H, kBq, d));
+    N = kBq;
+  }
+  const DecodeLayout L = decode_layout(p->w, p->P, p->W, p->K);
+  if (state_bytes < L.total(batch * H)) return FS_ERR_INVALID_ARG;
+  return status_of(launch_decode_init(k, v, kbar, amax, pool, pool_count, batch * H, N, N0,
+                                      p->rope_base, L, state, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
+                              int batch, int H, int d, int t, const float *lambda,
+                              const float *sigma, const float *mix, const fs_params *p,
+                              void *state, size_t state_bytes, float *out_t, int32_t *sel_t,
+                              void *stream) {
+  FS_TRY(check_decode(p, d));
+  FS_TRY(check_shape(batch, H, kBq, d));
+  FS_TRY(check_dtype(dtype));
+  if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+  if (t < 0) return FS_ERR_INVALID_ARG;
+  if (!q_t || !k_t || !v_t || !lambda || !sigma || !mix || !state || !out_t)
     return FS_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(p->w, p->P, p->W, p->K);
+  if (state_bytes < L.total(batch * H)) return FS_ERR_INVALID_ARG;
   DecodeArgs a{};
   a.q_t = q_t;
   a.k_t = k_t;
   a.v_t = v_t;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.kbar = kbar;
-  a.amax = amax;
-  a.pool = pool;
-  a.pool_count = pool_count;
+  a.state = state;
   a.lambda = lambda;
   a.sigma = sigma;
   a.mix = mix;
+  a.L = L;
   a.batch = batch;
   a.H = H;
   a.t = t;
-  a.n_cap = n_cap;
-  a.P = p->P;
-  a.W = p->W;
-  a.K = p->K;
-  a.w = p->w;
-  a.rope_base = p->rope_base;
   a.rms_eps = p->rms_eps;
   a.out = out_t;
   a.sel_out = sel_t;

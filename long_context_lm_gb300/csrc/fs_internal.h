@@ -55,16 +55,32 @@ struct AttnArgs {
   int *err;
 };
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
-// One decode step for token t of every (batch, head) (see k6_decode.cu for
-// the state layout and what the step updates).
+// Bounded decode state (see k6_decode.cu): a global part (256-byte header
+// whose first int is the error word, then the relative-angle tables), then
+// one fixed-size block per (batch, head).  Offsets inside a head's block.
+constexpr int kDecodeHeaderInts = 192;  // counts and slot lists of one head
+constexpr int kDecodeTabRows = 64 + 16;  // (cos, sin)(o theta): o = r < 64, o = 64a, a < 16
+struct DecodeLayout {
+  int w, P, W, K, pend, nslots;
+  size_t hdr, slot_cell, slot_amax, slot_kbar, slot_k, slot_v, ring_k, ring_v;
+  size_t head_bytes;              // one (batch, head)
+  size_t tab, global_bytes;       // angle tables inside the global part; its size
+  size_t total(int BH) const { return global_bytes + (size_t)BH * head_bytes; }
+};
+DecodeLayout decode_layout(int w, int P, int W, int K);
+size_t decode_smem_bytes(const DecodeLayout &L);
+cudaError_t launch_decode_init(const void *k, const void *v, const float *kbar, const float *amax,
+                               const int32_t *pool, const int32_t *pool_count, int BH, int N,
+                               int N0, float rope_base, const DecodeLayout &L, void *state,
+                               cudaStream_t st);
+// One decode step for token t of every (batch, head).
 struct DecodeArgs {
   const void *q_t, *k_t, *v_t;
-  void *k_cache, *v_cache;
-  float *kbar, *amax;
-  int32_t *pool, *pool_count;
+  void *state;
   const float *lambda, *sigma, *mix;
-  int batch, H, t, n_cap, P, W, K, w;
-  float rope_base, rms_eps;
+  DecodeLayout L;
+  int batch, H, t;
+  float rms_eps;
   float *out;
   int32_t *sel_out;
 };

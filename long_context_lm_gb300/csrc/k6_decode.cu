@@ -1,62 +1,105 @@
-// k6_decode.cu -- one decode step of FS-L attention against its bounded state.
+// k6_decode.cu -- FS-L decoding from a bounded per-head state.
 //
-// FreeSolo (paper.rainbus.top summary, 核心方法 (prefill linear in N, decode
-// state of constant size), 方法步骤详情 ②-⑥; ai.info summary, "Methodology
-// in Plain English"): at decode time a head keeps the key/value history, the
-// summaries (kbar_c, a_c) of its closed cells and the pool of its current
-// query block; token t is answered from the w newest keys (RoPE window) and
-// the K pool cells its query selects (NoPE readout + RMSNorm), mixed by m_h.
+// FreeSolo (ai.info summary, "Methodology in Plain English": the FS-L pool
+// holds at most 72 cells -- the 8 most recent plus the 64 with the largest key
+// norm -- and changes only at query-block boundaries, so the streaming cache
+// stays small; "Why This Matters": a bounded state; paper.rainbus.top summary,
+// 核心方法: linear prefill and a decode state of constant size, 实验结果: the
+// attention buffer stays constant from 4k to 256k, 局限与改进: repeated buffer
+// copies are the weakness of the reference streaming cache).
 //
-// State of one (batch, head), owned by the caller:
-//   k_cache, v_cache [n_cap, d] bf16   rows < t hold the history
-//   kbar [n_cap/s, d], amax [n_cap/s]  cells < floor(t/s) hold their summaries
-//   pool [P+W], pool_count             the pool of block floor((t-1)/Bq), laid
-//                                      out as fs_prune_cells writes a block's
-//                                      row (recent cells, then the older cells
-//                                      by rank); for t = 0 a count of 0
-// One step for token t:
-//   1. writes k_t, v_t into row t of the caches;
-//   2. at a block start (t % Bq == 0, t > 0) advances the pool to block
-//      t/Bq: the cells that leave the W-cell recency window join the ranked
-//      older list, which keeps its best P by (a_c desc, c asc) -- the top P
-//      of a growing set is the top P of the old top P plus the newcomers;
-//   3. scores the pool with q_t (a3), reads the K best cells out with
-//      RMSNorm (a4), attends over rows [t-w+1, t] with RoPE and mixes (a5);
-//   4. when row t closes a cell ((t+1) % s == 0), writes that cell's kbar
-//      and a_c, bit-identical to the prefill's cell summaries.
-// One CTA of 256 threads per (batch, head); a step is launch-latency bound.
+// State of one (batch, head), fixed in size whatever the position t:
+//   window ring    the last w keys and values (raw bf16), row j at j mod w;
+//   cell slots     P + W + Bq/s + 1 slots of one cell each: raw keys and
+//                  values (s rows), mean key kbar_c (fp32), largest key norm
+//                  a_c and the cell id;
+//   lists          the W recent available cells, the running top-P older
+//                  cells in rank order (a_c desc, c asc), the closed cells
+//                  not yet available (at most Bq/s), the open cell, and the
+//                  free slots.
+// A cell lives in one slot from its first token until it leaves the pool:
+// nothing is ever moved between slots.  One step for token t:
+//   1. at a block start (t % Bq == 0, t > 0) the pending cells become
+//      recent; the cells leaving the W-cell recency window join the ranked
+//      older list, which keeps its best P (a dropped cell frees its slot:
+//      the top-P threshold only rises, so it is never needed again);
+//   2. writes k_t, v_t into the ring and the open cell's slot (opening one
+//      from the free list when t starts a cell);
+//   3. scores the pool with q_t (a3), reads the K best cells' raw rows out
+//      with RMSNorm (a4), attends over the ring with RoPE and mixes (a5);
+//   4. when row t closes its cell ((t+1) % s == 0), writes the cell's kbar
+//      and a_c, bit-identical to the prefill's cell summaries, and queues it.
+// The step stages the ring and the pool's summaries in shared memory with
+// bulk asynchronous copies, then the selected cells' rows while the window
+// branch computes.  One CTA of 256 threads per (batch, head).
 //
-// Angles: RoPE enters as q_t . R(j - t) k_j.  cos / sin of o*theta_i for
-// o = -(64a + r) come from two per-CTA tables (r < 64, a < 16) joined by the
-// angle-sum identity; the table entries are sincospi of o*theta_i/pi with
-// theta_i/pi carried as a 13-bit head (exact products with o) plus a 24-bit
-// tail, reduced modulo 2 exactly before the call.
+// Angles: RoPE enters the window as q_t . R(j - t) k_j.  cos / sin of o*theta_i
+// for o = 64a + r (r < 64, a < 16) are two tables built once with the state
+// (fp64 reduction, fp32 sincospi) and joined by the angle-sum identity.
 #include "cell_summary.cuh"
 #include "fs_common.cuh"
 #include "fs_internal.h"
+#include "tc05.cuh"
 
 namespace fs {
+
+DecodeLayout decode_layout(int w, int P, int W, int K) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  DecodeLayout L;
+  L.w = w;
+  L.P = P;
+  L.W = W;
+  L.K = K;
+  L.pend = kBq / kS;
+  L.nslots = P + W + L.pend + 1;
+  size_t off = 0;
+  L.hdr = off;
+  off = up(off + kDecodeHeaderInts * 4);
+  L.slot_cell = off;
+  off = up(off + (size_t)(L.nslots + 3) / 4 * 16);
+  L.slot_amax = off;
+  off = up(off + (size_t)(L.nslots + 3) / 4 * 16);
+  L.slot_kbar = off;
+  off = up(off + (size_t)L.nslots * kD * 4);
+  L.slot_k = off;
+  off = up(off + (size_t)L.nslots * kS * kD * 2);
+  L.slot_v = off;
+  off = up(off + (size_t)L.nslots * kS * kD * 2);
+  L.ring_k = off;
+  off = up(off + (size_t)w * kD * 2);
+  L.ring_v = off;
+  off = up(off + (size_t)w * kD * 2);
+  L.head_bytes = off;
+  L.tab = 256;  // after the error word's 256-byte header
+  L.global_bytes = up(L.tab + (size_t)kDecodeTabRows * (kD / 2) * 8);
+  return L;
+}
+
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxWin = 1024;
-constexpr int kMaxPool = kMaxP + 8;  // P + W with W <= 8 in practice; checked on the host
-constexpr int kMaxTok = kMaxK * kS;
+constexpr int kMaxSlots = kMaxP + 8 + kBq / kS + 1;
+// header ints of one head: counts, then the lists
+enum { kHT = 0, kHRecent = 1, kHTop = 2, kHPend = 3, kHOpen = 4, kHFree = 5 };
+constexpr int kLRecent = 8, kLTop = kLRecent + 8, kLPend = kLTop + kMaxP, kLFree = kLPend + 4;
+static_assert(kLFree + kMaxSlots <= kDecodeHeaderInts, "decode header too small");
 
-struct DecodeParams {
+struct StepParams {
   const uint16_t *q_t, *k_t, *v_t;  // [BH, d] bf16
-  uint16_t *k_cache, *v_cache;      // [BH, n_cap, d] bf16
-  float *kbar, *amax;               // [BH, n_cap/s, d], [BH, n_cap/s]
-  int32_t *pool, *pool_count;       // [BH, P+W], [BH]
+  unsigned char *state;             // global part, then one head after another
   const float *lambda, *sigma, *mix;
-  int H, t, n_cap, P, W, K, w;
-  double rope_base;
+  DecodeLayout L;
+  int H, t;
   float rms_eps;
   float *out;                       // [BH, d] f32
   int32_t *sel_out;                 // [BH, K] (nullable)
 };
 
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+__device__ __forceinline__ bool ranks_before(float a, int c, float a2, int c2) {
+  return a > a2 || (a == a2 && c < c2);
+}
 
 // block-wide max / sum over 256 threads (red: 8 floats of shared scratch)
 __device__ __forceinline__ float block_max(float v, float *red) {
@@ -81,174 +124,253 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   return s;
 }
 
-// sum_i wgt[i] * v[row(i)] for i < n: warp w takes i = w, w+8, ...; lane l
-// owns dims 2l, 2l+1 (one 32-bit load per row), sixteen rows in flight per
-// warp; the eight warp partials go to part[w] for the caller to add up.
+// sum_i wgt[i] * v(row_of(i)) for i < n, rows in shared memory (64 bf16 each):
+// warp w takes i = w, w+8, ...; lane l owns dims 2l, 2l+1; the eight warp
+// partials go to part[w] for the caller to add up.
 template <typename RowOf>
-__device__ __forceinline__ void weighted_rows(const uint16_t *__restrict__ vbase, const float *wgt,
-                                              int n, RowOf row_of, const float *vt_row,
+__device__ __forceinline__ void weighted_rows(const float *wgt, int n, RowOf row_of,
                                               float2 (*part)[kD / 2]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float ax = 0.f, ay = 0.f;
-  for (int i0 = warp; i0 < n; i0 += 16 * (kThreads / 32)) {
-    uint32_t x[16];
-    float wv[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = i0 + u * (kThreads / 32);
-      wv[u] = 0.f;
-      x[u] = 0u;
-      if (i < n) {
-        const long long r = row_of(i);
-        wv[u] = wgt[i];
-        if (r >= 0)
-          x[u] = reinterpret_cast<const uint32_t *>(vbase + (size_t)r * kD)[lane];
-        else  // the new token's row, from shared memory
-          x[u] = pack_bf16(vt_row[2 * lane], vt_row[2 * lane + 1]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      ax = fmaf(wv[u], bf16_lo(x[u]), ax);
-      ay = fmaf(wv[u], bf16_hi(x[u]), ay);
-    }
+#pragma unroll 4
+  for (int i = warp; i < n; i += kThreads / 32) {
+    const uint32_t x = reinterpret_cast<const uint32_t *>(row_of(i))[lane];
+    const float wv = wgt[i];
+    ax = fmaf(wv, bf16_lo(x), ax);
+    ay = fmaf(wv, bf16_hi(x), ay);
   }
   part[warp][lane] = make_float2(ax, ay);
 }
 
-__device__ __forceinline__ bool ranks_before(float a, int c, float a2, int c2) {
-  return a > a2 || (a == a2 && c < c2);
+__device__ __forceinline__ float sum_parts(const float2 (*part)[kD / 2], int dim) {
+  float o = 0.f;
+#pragma unroll
+  for (int w8 = 0; w8 < kThreads / 32; ++w8) {
+    const float2 pp = part[w8][dim >> 1];
+    o += (dim & 1) ? pp.y : pp.x;
+  }
+  return o;
 }
 
-__global__ void __launch_bounds__(kThreads) k6_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p) {
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  const DecodeLayout &L = p.L;
+  // dynamic shared memory: ring keys, ring values, slot summaries, the
+  // selected cells' keys and values
+  unsigned char *s_rk = dsm;
+  unsigned char *s_rv = s_rk + (size_t)L.w * kD * 2;
+  float *s_kbar = reinterpret_cast<float *>(s_rv + (size_t)L.w * kD * 2);
+  float *s_amax = s_kbar + (size_t)L.nslots * kD;
+  int *s_cell = reinterpret_cast<int *>(s_amax + (L.nslots + 3) / 4 * 4);
+  unsigned char *s_ck = reinterpret_cast<unsigned char *>(s_cell + (L.nslots + 3) / 4 * 4);
+  unsigned char *s_cv = s_ck + (size_t)L.K * kS * kD * 2;
+
+  __shared__ __align__(8) uint64_t barA, barB;
+  __shared__ int s_hdr[kDecodeHeaderInts];
   __shared__ float s_q[kD], s_k[kD], s_v[kD];
-  __shared__ int s_pool[kMaxPool];
-  __shared__ int s_cand_c[kMaxPool];
-  __shared__ float s_cand_a[kMaxPool];
-  __shared__ int s_count;
-  __shared__ float s_u[kMaxPool];
-  __shared__ int s_sel[kMaxK];
-  __shared__ float s_lg[kMaxWin];
+  __shared__ int s_pool[kMaxP + 8];
+  __shared__ float s_u[kMaxP + 8];
+  __shared__ int s_sel[kMaxK], s_selc[kMaxK];
+  __shared__ float s_w[1024];
   __shared__ float2 s_part[kThreads / 32][kD / 2];
   __shared__ float s_olong[kD];
   __shared__ float s_red[8];
-  __shared__ float s_th_hi[kD / 2], s_th_lo[kD / 2];
-  __shared__ float2 s_tr[64][kD / 2], s_ta[kMaxWin / 64][kD / 2];
+  __shared__ int s_ok;
 
   const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = bh % p.H, t = p.t;
-  const int C = p.n_cap / kS;
-  const size_t row0 = (size_t)bh * p.n_cap;
-  const int cap = p.P + p.W;
+  int *err = reinterpret_cast<int *>(p.state);
+  const float2 *tab = reinterpret_cast<const float2 *>(p.state + L.tab);
+  unsigned char *hs = p.state + L.global_bytes + (size_t)bh * L.head_bytes;
+  int *g_hdr = reinterpret_cast<int *>(hs + L.hdr);
+  int *g_cell = reinterpret_cast<int *>(hs + L.slot_cell);
+  float *g_amax = reinterpret_cast<float *>(hs + L.slot_amax);
+  float *g_kbar = reinterpret_cast<float *>(hs + L.slot_kbar);
+  uint16_t *g_sk = reinterpret_cast<uint16_t *>(hs + L.slot_k);
+  uint16_t *g_sv = reinterpret_cast<uint16_t *>(hs + L.slot_v);
+  uint16_t *g_rk = reinterpret_cast<uint16_t *>(hs + L.ring_k);
+  uint16_t *g_rv = reinterpret_cast<uint16_t *>(hs + L.ring_v);
+  const size_t cell_bytes = (size_t)kS * kD * 2;
 
-  // ---- 1. the new token: registers of the CTA, and row t of the caches
+  // ---- stage the ring and the slot summaries (bulk copies, one barrier)
+  if (tid == 0) {
+    tc::mbar_init(&barA, 1);
+    tc::mbar_init(&barB, 1);
+    tc::mbar_fence_init();
+    const uint32_t ring = (uint32_t)L.w * kD * 2;
+    const uint32_t sums = (uint32_t)L.nslots * kD * 4;
+    const uint32_t small = (uint32_t)(L.nslots + 3) / 4 * 16;
+    tc::mbar_arrive_expect_tx(&barA, 2 * ring + sums + 2 * small);
+    for (uint32_t o = 0; o < ring; o += 32768) {
+      const uint32_t n = ring - o < 32768 ? ring - o : 32768;
+      tc::bulk_load(s_rk + o, reinterpret_cast<const unsigned char *>(g_rk) + o, n, &barA);
+      tc::bulk_load(s_rv + o, reinterpret_cast<const unsigned char *>(g_rv) + o, n, &barA);
+    }
+    tc::bulk_load(s_kbar, g_kbar, sums, &barA);
+    tc::bulk_load(s_amax, g_amax, small, &barA);
+    tc::bulk_load(s_cell, g_cell, small, &barA);
+  }
+  for (int i = tid; i < kDecodeHeaderInts; i += kThreads) s_hdr[i] = g_hdr[i];
   if (tid < kD) {
     s_q[tid] = bf16f(p.q_t[(size_t)bh * kD + tid]);
     s_k[tid] = bf16f(p.k_t[(size_t)bh * kD + tid]);
     s_v[tid] = bf16f(p.v_t[(size_t)bh * kD + tid]);
-  } else if (tid < kD + 8) {
-    const int c = tid - kD;
-    reinterpret_cast<uint4 *>(p.k_cache + (row0 + t) * kD)[c] =
-        reinterpret_cast<const uint4 *>(p.k_t + (size_t)bh * kD)[c];
-  } else if (tid < kD + 16) {
-    const int c = tid - kD - 8;
-    reinterpret_cast<uint4 *>(p.v_cache + (row0 + t) * kD)[c] =
-        reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[c];
-  }
-  // theta_i / pi as a 13-bit head and a tail (products with |o| < 2^11 exact)
-  if (tid < kD / 2) {
-    const double x = pow(p.rope_base, -2.0 * tid / kD) / 3.14159265358979323846;
-    const float hi = __uint_as_float(__float_as_uint((float)x) & 0xfffff800u);
-    s_th_hi[tid] = hi;
-    s_th_lo[tid] = (float)(x - (double)hi);
-  }
-  // ---- 2. the pool of block t / Bq
-  const int beta = t / kBq, A = beta * (kBq / kS);
-  int32_t *gpool = p.pool + (size_t)bh * cap;
-  const float *am = p.amax + (size_t)bh * C;
-  const bool advance = t > 0 && t % kBq == 0;
-  const int cnt_prev = p.pool_count[bh];
-  for (int i = tid; i < cap; i += kThreads) s_pool[i] = gpool[i];
-  if (tid == 0) s_count = cnt_prev;
-  if (advance) {
-    // candidates: the previous ranked older cells, then the cells [Lp, L)
-    // leaving the recency window; each one's rank among all of them is the
-    // number that rank before it, so the kept P land in order in one pass
-    const int Ap = A - kBq / kS;
-    const int nrec_p = min(p.W, Ap), Lp = Ap - nrec_p;
-    const int nrec = min(p.W, A), L = A - nrec;
-    const int keep_p = cnt_prev - nrec_p;
-    const int ncand = keep_p + (L - Lp);
-    const int keep = min(p.P, L);
-    __syncthreads();  // s_pool holds the previous pool
-    if (tid < ncand) {
-      s_cand_c[tid] = tid < keep_p ? s_pool[nrec_p + tid] : Lp + (tid - keep_p);
-      s_cand_a[tid] = am[s_cand_c[tid]];
-    }
-    __syncthreads();
-    int rank = 0, my_c = -1;
-    if (tid < ncand) {
-      my_c = s_cand_c[tid];
-      const float my_a = s_cand_a[tid];
-      for (int j = 0; j < ncand; ++j) rank += ranks_before(s_cand_a[j], s_cand_c[j], my_a, my_c);
-    }
-    __syncthreads();  // every candidate has been read before s_pool is rewritten
-    for (int i = tid; i < cap; i += kThreads) s_pool[i] = i < nrec ? L + i : -1;
-    __syncthreads();
-    if (tid < ncand && rank < keep) s_pool[nrec + rank] = my_c;
-    if (tid == 0) s_count = nrec + min(keep, ncand);
-    __syncthreads();
-    for (int i = tid; i < cap; i += kThreads) gpool[i] = s_pool[i];
-    if (tid == 0) p.pool_count[bh] = s_count;
   }
   __syncthreads();
-  // angle tables: rows r*theta (r < 64) and 64a*theta (a < 16), sign of o applied later
-  for (int i = tid; i < (64 + kMaxWin / 64) * (kD / 2); i += kThreads) {
-    const int row = i / (kD / 2), k = i % (kD / 2);
-    const int o = row < 64 ? row : 64 * (row - 64);
-    const float head = fmodf((float)o * s_th_hi[k], 2.f);  // exact: o < 2^11, head has 13 bits
-    float sn, cs;
-    sincospif(head + (float)o * s_th_lo[k], &sn, &cs);
-    if (row < 64)
-      s_tr[row][k] = make_float2(cs, sn);
-    else
-      s_ta[row - 64][k] = make_float2(cs, sn);
+  // the state must be at position t (every copy is awaited before an exit)
+  const bool in_step = s_hdr[kHT] == t;
+  const bool staged = tc::mbar_wait(&barA, 0, err);
+  if (!in_step || !staged) {
+    if (tid == 0 && !in_step) tc::report_error(err, FS_ERR_STATE);
+    return;
   }
 
-  // ---- 3a. score the pool (a3): u = q . kbar_c + lambda * a_c * erf(sigma (t - p_c) / s)
-  const int nc = s_count;
+  // ---- 1. block start: pending cells become recent, leavers join the top list
+  if (tid == 0) {
+    int *recent = s_hdr + kLRecent, *top = s_hdr + kLTop, *pend = s_hdr + kLPend;
+    int *freel = s_hdr + kLFree;
+    if (t > 0 && t % kBq == 0) {
+      for (int k = 0; k < s_hdr[kHPend]; ++k) recent[s_hdr[kHRecent]++] = pend[k];
+      s_hdr[kHPend] = 0;
+      while (s_hdr[kHRecent] > L.W) {
+        const int slot = recent[0];
+        for (int k = 1; k < s_hdr[kHRecent]; ++k) recent[k - 1] = recent[k];
+        --s_hdr[kHRecent];
+        // insert by (a desc, c asc) into the ranked older list of at most P
+        const float a = s_amax[slot];
+        const int c = s_cell[slot];
+        int n = s_hdr[kHTop], pos = n;
+        while (pos > 0 && ranks_before(a, c, s_amax[top[pos - 1]], s_cell[top[pos - 1]])) --pos;
+        if (pos >= L.P) {
+          freel[s_hdr[kHFree]++] = slot;  // ranks past the top P: dropped
+        } else {
+          int dropped = -1;
+          if (n == L.P) dropped = top[--n];  // the list was full: its last cell leaves
+          for (int q = n; q > pos; --q) top[q] = top[q - 1];
+          top[pos] = slot;
+          s_hdr[kHTop] = n + 1;
+          if (dropped >= 0) freel[s_hdr[kHFree]++] = dropped;
+        }
+      }
+    }
+    // 2. a new cell opens
+    if (t % kS == 0) s_hdr[kHOpen] = freel[--s_hdr[kHFree]];
+  }
+  __syncthreads();
+  const int open = s_hdr[kHOpen];
+  // ---- 2. the new token: ring row t mod w and the open slot's row t mod s
+  if (tid < 8) {
+    const uint4 kv = reinterpret_cast<const uint4 *>(p.k_t + (size_t)bh * kD)[tid];
+    reinterpret_cast<uint4 *>(g_rk + (size_t)(t % L.w) * kD)[tid] = kv;
+    reinterpret_cast<uint4 *>(g_sk + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[tid] = kv;
+    reinterpret_cast<uint4 *>(s_rk + (size_t)(t % L.w) * kD * 2)[tid] = kv;
+  } else if (tid < 16) {
+    const int c = tid - 8;
+    const uint4 vv = reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[c];
+    reinterpret_cast<uint4 *>(g_rv + (size_t)(t % L.w) * kD)[c] = vv;
+    reinterpret_cast<uint4 *>(g_sv + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[c] = vv;
+    reinterpret_cast<uint4 *>(s_rv + (size_t)(t % L.w) * kD * 2)[c] = vv;
+  }
+
+  // ---- 3a. score the pool: u = q . kbar_c + lambda * a_c * erf(sigma (t - p_c) / s)
+  const int nrec = s_hdr[kHRecent], nc = nrec + s_hdr[kHTop];
+  if (tid < nc) s_pool[tid] = tid < nrec ? s_hdr[kLRecent + tid] : s_hdr[kLTop + tid - nrec];
+  __syncthreads();
   const float lam = p.lambda[h], sig = p.sigma[h];
   for (int i = warp; i < nc; i += kThreads / 32) {
-    const int c = s_pool[i];
-    const float2 kb = reinterpret_cast<const float2 *>(p.kbar + ((size_t)bh * C + c) * kD)[lane];
+    const int slot = s_pool[i];
+    const float2 kb = reinterpret_cast<const float2 *>(s_kbar + (size_t)slot * kD)[lane];
     const float dot = warp_sum(fmaf(s_q[2 * lane], kb.x, s_q[2 * lane + 1] * kb.y));
     if (lane == 0) {
-      const float pc = (float)(c * kS) + 0.5f * kS;
-      s_u[i] = dot + lam * p.amax[(size_t)bh * C + c] * erff(sig * ((float)t - pc) / kS);
+      const float pc = (float)(s_cell[slot] * kS) + 0.5f * kS;
+      s_u[i] = dot + lam * s_amax[slot] * erff(sig * ((float)t - pc) / kS);
     }
   }
-  __syncthreads();
-  // top K by (u desc, c asc): rank of each candidate by counting
   if (tid < kMaxK) s_sel[tid] = -1;
   __syncthreads();
+  // top K by (u desc, c asc): rank of each candidate by counting
   if (tid < nc) {
     const float u = s_u[tid];
-    const int c = s_pool[tid];
+    const int c = s_cell[s_pool[tid]];
     int rank = 0;
-    for (int j = 0; j < nc; ++j) rank += ranks_before(s_u[j], s_pool[j], u, c);
-    if (rank < p.K) s_sel[rank] = c;
+    for (int j = 0; j < nc; ++j) rank += ranks_before(s_u[j], s_cell[s_pool[j]], u, c);
+    if (rank < L.K) s_sel[rank] = s_pool[tid];
   }
   __syncthreads();
-  if (p.sel_out && tid < p.K) p.sel_out[(size_t)bh * p.K + tid] = s_sel[tid];
+  int nsel = 0;
+  for (int k = 0; k < L.K; ++k) nsel += s_sel[k] >= 0;
+  if (tid < L.K) {
+    s_selc[tid] = s_sel[tid] >= 0 ? s_cell[s_sel[tid]] : -1;
+    if (p.sel_out) p.sel_out[(size_t)bh * L.K + tid] = s_selc[tid];
+  }
+  // the selected cells' rows, in rank order
+  if (tid == 0 && nsel > 0) {
+    tc::mbar_arrive_expect_tx(&barB, (uint32_t)(2 * nsel * cell_bytes));
+    for (int k = 0; k < nsel; ++k) {
+      tc::bulk_load(s_ck + k * cell_bytes, g_sk + (size_t)s_sel[k] * kS * kD, (uint32_t)cell_bytes,
+                    &barB);
+      tc::bulk_load(s_cv + k * cell_bytes, g_sv + (size_t)s_sel[k] * kS * kD, (uint32_t)cell_bytes,
+                    &barB);
+    }
+  }
+
+  // ---- 3c. RoPE window over rows [t - w + 1, t] (a5), while the cells land
+  const int j0 = max(0, t - L.w + 1), nwin = t - j0 + 1;
+  float mloc = -INFINITY;
+  for (int i = tid; i < nwin; i += kThreads) {
+    const int j = j0 + i, o = t - j;  // R(j - t) = R(-o)
+    const uint4 *kr = reinterpret_cast<const uint4 *>(s_rk + (size_t)(j % L.w) * kD * 2);
+    float kx[kD];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 x = kr[c];
+      const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        kx[8 * c + 2 * jj] = bf16_lo(wv[jj]);
+        kx[8 * c + 2 * jj + 1] = bf16_hi(wv[jj]);
+      }
+    }
+    const float2 *tr = tab + (size_t)(o & 63) * (kD / 2);
+    const float2 *ta = tab + (size_t)(64 + (o >> 6)) * (kD / 2);
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < kD / 2; ++k) {
+      // cos / sin of o*theta by the angle sum, then of -o*theta
+      const float2 a = __ldg(tr + k), b = __ldg(ta + k);
+      const float c = fmaf(a.x, b.x, -a.y * b.y), s = -fmaf(a.y, b.x, a.x * b.y);
+      const float y0 = fmaf(kx[k], c, -kx[k + kD / 2] * s);
+      const float y1 = fmaf(kx[k], s, kx[k + kD / 2] * c);
+      dot = fmaf(s_q[k], y0, fmaf(s_q[k + kD / 2], y1, dot));
+    }
+    s_w[i] = dot * 0.125f;
+    mloc = fmaxf(mloc, dot * 0.125f);
+  }
+  const float mwin = block_max(mloc, s_red);  // its barriers also order the s_w writes
+  float lsum = 0.f;
+  for (int i = tid; i < nwin; i += kThreads) {
+    const float e = __expf(s_w[i] - mwin);
+    s_w[i] = e;
+    lsum += e;
+  }
+  const float lwin = block_sum(lsum, s_red);
+  weighted_rows(s_w, nwin,
+                [&](int i) { return s_rv + (size_t)((j0 + i) % L.w) * kD * 2; }, s_part);
+  __syncthreads();
+  float owin = 0.f;
+  if (tid < kD) owin = sum_parts(s_part, tid) / lwin;
+  __syncthreads();  // s_part and s_w are reused below
 
   // ---- 3b. NoPE readout over the selected cells' tokens (a4), then RMSNorm
-  int nsel = 0;
-  for (int k = 0; k < p.K; ++k) nsel += s_sel[k] >= 0;
-  const int ntok = nsel * kS;  // selected ids are packed first, -1 after
+  const int ntok = nsel * kS;
+  bool cells_ok = true;
+  if (nsel > 0) cells_ok = tc::mbar_wait(&barB, 0, err);
+  if (tid == 0) s_ok = cells_ok;
+  __syncthreads();
+  if (!s_ok) return;
   float lg = -INFINITY;
   if (tid < ntok) {
-    const int tok = s_sel[tid / kS] * kS + tid % kS;
-    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k_cache + (row0 + tok) * kD);
+    const uint4 *kr = reinterpret_cast<const uint4 *>(s_ck + (size_t)tid * kD * 2);
     float dot = 0.f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -264,121 +386,172 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const DecodeParams 
   }
   const float mlong = block_max(lg, s_red);
   const float pl = tid < ntok ? __expf(lg - mlong) : 0.f;
-  if (tid < kMaxTok) s_lg[tid] = pl;
-  const float llong = block_sum(pl, s_red);  // also orders the s_lg writes
-  weighted_rows(p.v_cache + row0 * kD, s_lg, ntok,
-                [&](int i) { return (long long)(s_sel[i / kS] * kS + i % kS); }, s_v, s_part);
+  if (tid < kMaxK * kS) s_w[tid] = pl;
+  const float llong = block_sum(pl, s_red);  // also orders the s_w writes
+  weighted_rows(s_w, ntok, [&](int i) { return s_cv + (size_t)i * kD * 2; }, s_part);
   __syncthreads();
-  if (tid < kD) {
-    float o = 0.f;
-#pragma unroll
-    for (int w8 = 0; w8 < kThreads / 32; ++w8) {
-      const float2 pp = s_part[w8][tid >> 1];
-      o += (tid & 1) ? pp.y : pp.x;
-    }
-    s_olong[tid] = ntok > 0 ? o / llong : 0.f;
-  }
+  if (tid < kD) s_olong[tid] = ntok > 0 ? sum_parts(s_part, tid) / llong : 0.f;
   __syncthreads();
   float ss = tid < kD ? s_olong[tid] * s_olong[tid] : 0.f;
   ss = block_sum(ss, s_red);
   const float rms_scale = ntok > 0 ? rsqrtf(ss / kD + p.rms_eps) : 0.f;
+  if (tid < kD) p.out[(size_t)bh * kD + tid] = owin + p.mix[h] * s_olong[tid] * rms_scale;
 
-  // ---- 3c. RoPE window over rows [t - w + 1, t] (a5)
-  const int j0 = max(0, t - p.w + 1), nwin = t - j0 + 1;
-  float mloc = -INFINITY;
-  for (int i = tid; i < nwin; i += kThreads) {
-    const int j = j0 + i, o = t - j;  // R(j - t) = R(-o)
-    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k_cache + (row0 + j) * kD);
-    float kx[kD];
-    if (j == t) {
-#pragma unroll
-      for (int c = 0; c < kD; ++c) kx[c] = s_k[c];
-    } else {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 x = kr[c];
-        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          kx[8 * c + 2 * jj] = bf16_lo(wv[jj]);
-          kx[8 * c + 2 * jj + 1] = bf16_hi(wv[jj]);
-        }
+  // ---- 4. row t closes its cell: summary, as the prefill computes it; the
+  // cell waits in the pending list for the next block start
+  if ((t + 1) % kS == 0 && warp == 0) {
+    float x[8][8];
+    load_cell_bf16<false>(reinterpret_cast<const uint4 *>(g_sk + (size_t)open * kS * kD), lane, x);
+    cell_summary_warp(x, lane, g_kbar + (size_t)open * kD, g_amax + open);
+    if (lane == 0) g_cell[open] = t / kS;
+  }
+  if (tid == 0) {
+    if ((t + 1) % kS == 0) {
+      s_hdr[kLPend + s_hdr[kHPend]++] = open;
+      s_hdr[kHOpen] = -1;
+    }
+    s_hdr[kHT] = t + 1;
+  }
+  __syncthreads();
+  for (int i = tid; i < kDecodeHeaderInts; i += kThreads) g_hdr[i] = s_hdr[i];
+}
+
+// Build the state after the first N0 tokens from the prefix's keys, values,
+// cell summaries and the pool of block (N0-1)/Bq: recent then ranked older
+// cells in slots 0.., the pending cells after them, the open cell's rows, the
+// ring, the free list.  CTA 0 also writes the angle tables.
+__global__ void __launch_bounds__(kThreads) k6_init_kernel(
+    const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, const float *__restrict__ kbar,
+    const float *__restrict__ amax, const int32_t *__restrict__ pool,
+    const int32_t *__restrict__ pool_count, int N, int N0, double rope_base, DecodeLayout L,
+    unsigned char *state) {
+  __shared__ int s_hdr[kDecodeHeaderInts];
+  __shared__ int s_slot_cell[kMaxSlots];
+  const int bh = blockIdx.x, tid = threadIdx.x;
+  const int C = N / kS, nblk = N / kBq, cap = L.P + L.W;
+  unsigned char *hs = state + L.global_bytes + (size_t)bh * L.head_bytes;
+  if (bh == 0) {
+    // angle tables: rows o = r (r < 64) and o = 64a (a < 16) of (cos, sin)(o theta_i)
+    if (tid == 0) *reinterpret_cast<int *>(state) = 0;
+    float2 *tab = reinterpret_cast<float2 *>(state + L.tab);
+    for (int idx = tid; idx < kDecodeTabRows * (kD / 2); idx += kThreads) {
+      const int row = idx / (kD / 2), i = idx % (kD / 2);
+      const double o = row < 64 ? (double)row : 64.0 * (double)(row - 64);
+      const double x = o * (pow(rope_base, -2.0 * i / kD) / 3.14159265358979323846);
+      const double red = x - 2.0 * floor(0.5 * x);
+      float sn, cs;
+      sincospif((float)red, &sn, &cs);
+      tab[idx] = make_float2(cs, sn);
+    }
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kDecodeHeaderInts; ++i) s_hdr[i] = 0;
+    for (int i = 0; i < kMaxSlots; ++i) s_slot_cell[i] = -1;
+    int nslot = 0;
+    s_hdr[kHT] = N0;
+    s_hdr[kHOpen] = -1;
+    if (N0 > 0) {
+      const int beta = (N0 - 1) / kBq, A = beta * (kBq / kS);
+      const int cnt = min(max(pool_count[(size_t)bh * nblk + beta], 0), cap);
+      const int nrec = min(L.W, A);
+      const int32_t *row = pool + ((size_t)bh * nblk + beta) * cap;
+      for (int i = 0; i < cnt; ++i) {
+        s_slot_cell[nslot] = row[i];
+        if (i < nrec)
+          s_hdr[kLRecent + s_hdr[kHRecent]++] = nslot;
+        else
+          s_hdr[kLTop + s_hdr[kHTop]++] = nslot;
+        ++nslot;
+      }
+      for (int c = beta * (kBq / kS); c < N0 / kS; ++c) {  // closed, not yet available
+        s_slot_cell[nslot] = c;
+        s_hdr[kLPend + s_hdr[kHPend]++] = nslot++;
+      }
+      if (N0 % kS) {  // the open cell
+        s_slot_cell[nslot] = N0 / kS;
+        s_hdr[kHOpen] = nslot++;
       }
     }
-    const float2 *tr = s_tr[o & 63], *ta = s_ta[o >> 6];
-    float dot = 0.f;
-#pragma unroll
-    for (int k = 0; k < kD / 2; ++k) {
-      // cos / sin of o*theta by the angle sum, then of -o*theta
-      const float2 a = tr[k], b = ta[k];
-      const float c = fmaf(a.x, b.x, -a.y * b.y), s = -fmaf(a.y, b.x, a.x * b.y);
-      const float y0 = fmaf(kx[k], c, -kx[k + kD / 2] * s);
-      const float y1 = fmaf(kx[k], s, kx[k + kD / 2] * c);
-      dot = fmaf(s_q[k], y0, fmaf(s_q[k + kD / 2], y1, dot));
-    }
-    s_lg[i] = dot * 0.125f;
-    mloc = fmaxf(mloc, dot * 0.125f);
+    // free slots, handed out from the end of the list
+    for (int i = L.nslots - 1; i >= nslot; --i) s_hdr[kLFree + s_hdr[kHFree]++] = i;
   }
-  const float mwin = block_max(mloc, s_red);  // its barriers also order the s_lg writes
-  float lsum = 0.f;
-  for (int i = tid; i < nwin; i += kThreads) {
-    const float e = __expf(s_lg[i] - mwin);
-    s_lg[i] = e;
-    lsum += e;
-  }
-  const float lwin = block_sum(lsum, s_red);
-  weighted_rows(p.v_cache + row0 * kD, s_lg, nwin,
-                [&](int i) { return j0 + i == t ? -1ll : (long long)(j0 + i); }, s_v, s_part);
   __syncthreads();
-  if (tid < kD) {
-    float owin = 0.f;
-#pragma unroll
-    for (int w8 = 0; w8 < kThreads / 32; ++w8) {
-      const float2 pp = s_part[w8][tid >> 1];
-      owin += (tid & 1) ? pp.y : pp.x;
+  int *g_hdr = reinterpret_cast<int *>(hs + L.hdr);
+  int *g_cell = reinterpret_cast<int *>(hs + L.slot_cell);
+  float *g_amax = reinterpret_cast<float *>(hs + L.slot_amax);
+  float *g_kbar = reinterpret_cast<float *>(hs + L.slot_kbar);
+  uint4 *g_sk = reinterpret_cast<uint4 *>(hs + L.slot_k);
+  uint4 *g_sv = reinterpret_cast<uint4 *>(hs + L.slot_v);
+  for (int i = tid; i < kDecodeHeaderInts; i += kThreads) g_hdr[i] = s_hdr[i];
+  const size_t head = (size_t)bh * N;
+  const int full_cells = N0 / kS;
+  for (int sl = 0; sl < L.nslots; ++sl) {
+    const int c = s_slot_cell[sl];
+    if (tid == 0) {
+      const bool closed = c >= 0 && c < full_cells;
+      g_cell[sl] = closed ? c : -1;
+      g_amax[sl] = closed ? amax[(size_t)bh * C + c] : 0.f;
     }
-    owin /= lwin;
-    p.out[(size_t)bh * kD + tid] = owin + p.mix[h] * s_olong[tid] * rms_scale;
+    if (c < 0) continue;
+    const bool closed = c < full_cells;
+    if (closed && tid < kD) g_kbar[(size_t)sl * kD + tid] = kbar[((size_t)bh * C + c) * kD + tid];
+    // the cell's rows below N0 (all of them for a closed cell)
+    const int rows = min(kS, N0 - c * kS);
+    for (int e = tid; e < rows * 8; e += kThreads) {
+      const size_t src = (head + (size_t)c * kS) * 8 + e;
+      g_sk[(size_t)sl * kS * 8 + e] = reinterpret_cast<const uint4 *>(k)[src];
+      g_sv[(size_t)sl * kS * 8 + e] = reinterpret_cast<const uint4 *>(v)[src];
+    }
   }
-
-  // ---- 4. row t closes cell t / s: its summary, as the prefill computes it
-  if ((t + 1) % kS == 0 && warp == 0) {
-    const int c = t / kS;
-    float x[8][8];
-    load_cell_bf16<false>(reinterpret_cast<const uint4 *>(p.k_cache + (row0 + (size_t)c * kS) * kD),
-                          lane, x);
-    cell_summary_warp(x, lane, p.kbar + ((size_t)bh * C + c) * kD, p.amax + (size_t)bh * C + c);
+  // the ring: rows [max(0, N0 - w), N0) at j mod w
+  uint4 *g_rk = reinterpret_cast<uint4 *>(hs + L.ring_k);
+  uint4 *g_rv = reinterpret_cast<uint4 *>(hs + L.ring_v);
+  const int r0 = max(0, N0 - L.w);
+  for (int e = tid; e < (N0 - r0) * 8; e += kThreads) {
+    const int j = r0 + e / 8;
+    const size_t dst = (size_t)(j % L.w) * 8 + e % 8;
+    g_rk[dst] = reinterpret_cast<const uint4 *>(k)[(head + j) * 8 + e % 8];
+    g_rv[dst] = reinterpret_cast<const uint4 *>(v)[(head + j) * 8 + e % 8];
   }
 }
 
 }  // namespace
 
+size_t decode_smem_bytes(const DecodeLayout &L) {
+  return 2 * (size_t)L.w * kD * 2 + (size_t)L.nslots * kD * 4 + 2 * (size_t)(L.nslots + 3) / 4 * 16 +
+         2 * (size_t)L.K * kS * kD * 2;
+}
+
+cudaError_t launch_decode_init(const void *k, const void *v, const float *kbar, const float *amax,
+                               const int32_t *pool, const int32_t *pool_count, int BH, int N,
+                               int N0, float rope_base, const DecodeLayout &L, void *state,
+                               cudaStream_t st) {
+  k6_init_kernel<<<BH, kThreads, 0, st>>>(
+      static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), kbar, amax, pool,
+      pool_count, N, N0, (double)rope_base, L, static_cast<unsigned char *>(state));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
-  DecodeParams p;
+  StepParams p;
   p.q_t = static_cast<const uint16_t *>(a.q_t);
   p.k_t = static_cast<const uint16_t *>(a.k_t);
   p.v_t = static_cast<const uint16_t *>(a.v_t);
-  p.k_cache = static_cast<uint16_t *>(a.k_cache);
-  p.v_cache = static_cast<uint16_t *>(a.v_cache);
-  p.kbar = a.kbar;
-  p.amax = a.amax;
-  p.pool = a.pool;
-  p.pool_count = a.pool_count;
+  p.state = static_cast<unsigned char *>(a.state);
   p.lambda = a.lambda;
   p.sigma = a.sigma;
   p.mix = a.mix;
+  p.L = a.L;
   p.H = a.H;
   p.t = a.t;
-  p.n_cap = a.n_cap;
-  p.P = a.P;
-  p.W = a.W;
-  p.K = a.K;
-  p.w = a.w;
-  p.rope_base = a.rope_base;
   p.rms_eps = a.rms_eps;
   p.out = a.out;
   p.sel_out = a.sel_out;
-  k6_decode_kernel<<<a.batch * a.H, kThreads, 0, st>>>(p);
+  const size_t smem = decode_smem_bytes(a.L);
+  cudaError_t e =
+      cudaFuncSetAttribute(k6_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k6_decode_kernel<<<a.batch * a.H, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -267,5 +267,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` from global memory into shared memory,
+// completion counted on `bar` (both addresses 16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 }  // namespace tc
 }  // namespace fs

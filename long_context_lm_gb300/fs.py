@@ -21,7 +21,7 @@ import torch
 from . import build as _build
 
 (FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_RANGE,
- FS_ERR_SCRATCH_LIMIT) = range(7)
+ FS_ERR_SCRATCH_LIMIT, FS_ERR_STATE) = range(8)
 FS_BF16, FS_FP32 = 0, 1
 FS_MODE_FSL, FS_MODE_FS = 0, 1
 
@@ -31,7 +31,8 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
            "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
            "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host",
-           "fs_window_attn_traced"]
+           "fs_window_attn_traced", "fs_decode_state_bytes", "fs_decode_state_init",
+           "fs_decode_state_view"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
@@ -106,13 +107,16 @@ def load(build_if_stale: bool = True):
         L.fs_prune_static_scratch_bytes.argtypes = []
         L.fs_prune_static_scratch_bytes.restype = Z
         L.fs_prune_cells_static.argtypes = [P, I, I, I, PP, P, P, P]
-        L.fs_decode_step.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, PP, P,
-                                     P, P]
+        L.fs_decode_state_bytes.argtypes = [I, I, I, PP]
+        L.fs_decode_state_bytes.restype = Z
+        L.fs_decode_state_view.argtypes = [I, I, I, PP, ctypes.POINTER(Z)]
+        L.fs_decode_state_init.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, PP, P, Z, P]
+        L.fs_decode_step.argtypes = [P, P, P, I, I, I, I, I, P, P, P, PP, P, Z, P, P, P]
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
                             "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes",
-                            "fs_host_workspace_bytes"):
+                            "fs_host_workspace_bytes", "fs_decode_state_bytes"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -240,26 +244,73 @@ def fs_selftest_wait_timeout(ws, stream=None):
     _check(load().fs_selftest_wait_timeout(_ptr(ws), _stream(stream)), "fs_selftest_wait_timeout")
 
 
+def fs_decode_state_bytes(batch, H, d=64, params=None) -> int:
+    p = _params(params)
+    return load().fs_decode_state_bytes(batch, H, d, ctypes.byref(p))
+
+
+def fs_decode_state_view(state, batch, H, params=None):
+    """Views into a decode state: per (batch, head) slot cell ids [BH, nslots]
+    int32, slot a_c [BH, nslots] f32, slot mean keys [BH, nslots, 64] f32,
+    and the header ints [BH, n] (position, list counts, lists)."""
+    L = load()
+    p = _params(params)
+    offs = (ctypes.c_size_t * 7)()
+    _check(L.fs_decode_state_view(batch, H, 64, ctypes.byref(p), offs), "fs_decode_state_view")
+    g, hb, oc, oa, ok, ns, nh = (int(x) for x in offs)
+    heads = state[g:g + batch * H * hb].view(batch * H, hb)
+    return dict(cell=heads[:, oc:oc + 4 * ns].contiguous().view(torch.int32),
+                amax=heads[:, oa:oa + 4 * ns].contiguous().view(torch.float32),
+                kbar=heads[:, ok:ok + 4 * 64 * ns].contiguous().view(torch.float32).view(-1, ns, 64),
+                header=heads[:, :4 * nh].contiguous().view(torch.int32))
+
+
+def fs_decode_state_init(batch, H, params=None, k=None, v=None, kbar=None, amax=None, pool=None,
+                         pool_count=None, N0=0, state=None, device=None, stream=None):
+    """Bounded decode state after the first N0 tokens (N0 = 0: an empty state).
+    For N0 > 0, k, v [B,H,N,d] bf16 hold the prefix in rows < N0, and kbar,
+    amax, pool, pool_count are fs_cell_summarize / fs_prune_cells of k.
+    Returns the state (a device uint8 tensor of fs_decode_state_bytes)."""
+    L = load()
+    p = _params(params)
+    nb = L.fs_decode_state_bytes(batch, H, 64, ctypes.byref(p))
+    if nb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_decode_state_bytes")
+    if N0 > 0:
+        for t_, n in ((k, "k"), (v, "v")):
+            _dev(t_, n, (torch.bfloat16,))
+        for t_, n in ((kbar, "kbar"), (amax, "amax")):
+            _dev(t_, n, (torch.float32,))
+        for t_, n in ((pool, "pool"), (pool_count, "pool_count")):
+            _dev(t_, n, (torch.int32,))
+        N = k.shape[2]
+        device = k.device
+    else:
+        N = 128
+        device = device or torch.device("cuda")
+    if state is None:
+        state = torch.empty(nb, device=device, dtype=torch.uint8)
+    elif state.numel() * state.element_size() < nb:
+        raise ValueError(f"state too small: {state.numel()} < {nb} bytes")
+    _check(L.fs_decode_state_init(_ptr(k), _ptr(v), FS_BF16, _ptr(kbar), _ptr(amax), _ptr(pool),
+                                  _ptr(pool_count), batch, H, N, int(N0), 64, ctypes.byref(p),
+                                  _ptr(state), nb, _stream(stream)), "fs_decode_state_init")
+    return state
+
+
 def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=None,
                    sel=None, stream=None):
-    """One decode step for token t.  ``state`` is a dict of caller-owned device
-    tensors: k_cache, v_cache [B,H,n_cap,d] bf16; kbar [B,H,n_cap/32,d] and
-    amax [B,H,n_cap/32] f32; pool [B,H,P+W] and pool_count [B,H] int32 (all
-    updated in place as the step prescribes).  Returns out_t [B,H,d] f32."""
+    """One decode step for token t from the bounded ``state`` (advanced in
+    place).  q_t, k_t, v_t [B,H,d] bf16.  Returns out_t [B,H,d] f32."""
     L = load()
     p = _params(params)
     for t_, n in ((q_t, "q_t"), (k_t, "k_t"), (v_t, "v_t")):
         _dev(t_, n, (torch.bfloat16,))
     B, H, d = q_t.shape
-    kc, vc = state["k_cache"], state["v_cache"]
-    _dev(kc, "k_cache", (torch.bfloat16,))
-    _dev(vc, "v_cache", (torch.bfloat16,))
-    n_cap = kc.shape[2]
     out = out if out is not None else torch.empty((B, H, d), device=q_t.device, dtype=torch.float32)
-    _check(L.fs_decode_step(_ptr(q_t), _ptr(k_t), _ptr(v_t), FS_BF16, B, H, d, int(t), n_cap,
-                            _ptr(kc), _ptr(vc), _ptr(state["kbar"]), _ptr(state["amax"]),
-                            _ptr(state["pool"]), _ptr(state["pool_count"]), _ptr(lam),
-                            _ptr(sigma), _ptr(mix), ctypes.byref(p), _ptr(out), _ptr(sel),
+    _check(L.fs_decode_step(_ptr(q_t), _ptr(k_t), _ptr(v_t), FS_BF16, B, H, d, int(t), _ptr(lam),
+                            _ptr(sigma), _ptr(mix), ctypes.byref(p), _ptr(state),
+                            state.numel() * state.element_size(), _ptr(out), _ptr(sel),
                             _stream(stream)), "fs_decode_step")
     return out
 
