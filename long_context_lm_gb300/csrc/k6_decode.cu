@@ -81,7 +81,10 @@ constexpr int kThreads = 256;
 constexpr int kMaxSlots = kMaxP + 8 + kBq / kS + 1;
 // header ints of one head: counts, then the lists
 enum { kHT = 0, kHRecent = 1, kHTop = 2, kHPend = 3, kHOpen = 4, kHFree = 5 };
-constexpr int kLRecent = 8, kLTop = kLRecent + 8, kLPend = kLTop + kMaxP, kLFree = kLPend + 4;
+// the recent list briefly holds W + Bq/s cells at a block start, before the
+// leavers move on
+constexpr int kLRecent = 8, kLTop = kLRecent + 8 + kBq / kS, kLPend = kLTop + kMaxP,
+              kLFree = kLPend + kBq / kS;
 static_assert(kLFree + kMaxSlots <= kDecodeHeaderInts, "decode header too small");
 
 struct StepParams {
@@ -253,10 +256,20 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
         }
       }
     }
-    // 2. a new cell opens
-    if (t % kS == 0) s_hdr[kHOpen] = freel[--s_hdr[kHFree]];
+    // 2. a new cell opens (a slot is always free: at most W + P + Bq/s cells
+    // are held when one opens, of P + W + Bq/s + 1 slots)
+    if (t % kS == 0) {
+      if (s_hdr[kHFree] > 0) {
+        s_hdr[kHOpen] = freel[--s_hdr[kHFree]];
+      } else {
+        s_hdr[kHOpen] = -1;
+        tc::report_error(err, FS_ERR_STATE);
+      }
+    }
+    s_ok = s_hdr[kHOpen] >= 0;
   }
   __syncthreads();
+  if (!s_ok) return;  // a state that lost track of its slots is left as it was
   const int open = s_hdr[kHOpen];
   // ---- 2. the new token: ring row t mod w and the open slot's row t mod s
   if (tid < 8) {
