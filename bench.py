@@ -303,6 +303,7 @@ def run_ours(args, rank, world, local_rank):
         res["decode"] = time_decode(q, k, v, lam, sigma, mix, params, stream)
     if not args.no_extras:
         res["fs_mode"] = time_fs_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
+        res["prologue"] = time_prologue(B, N, H, stream)
     return res
 
 
@@ -370,6 +371,25 @@ def time_branches(q, k, v, mix, sel, params, stream, distinct_cells, counts, pk,
     res["sparse_readout"] = _entry(ms, nbytes, 4.0 * d * float(counts["tokens_read"]), pk, "hbm")
     del ws, out, o_long
     return res
+
+
+def time_prologue(B, N, H, stream, D=1024, iters=10):
+    """The shared q / k / v projection of a layer with d_model = D feeding the
+    benchmark's attention shape (random-init weights, gain folded): one call
+    = row-scale pass + gain fold + tcgen05 GEMM, timed with CUDA events."""
+    from long_context_lm_gb300 import fs
+    from long_context_lm_gb300.inputs import make_prologue_inputs
+    inp = make_prologue_inputs(B, N, D, H, seed=11)
+    x, w, g = inp.x.cuda(), inp.w_qkv.cuda(), inp.gain.cuda()
+    outs = [torch.empty((B, H, N, 64), device=x.device, dtype=torch.bfloat16) for _ in range(3)]
+    ws = torch.empty(fs.fs_qkv_workspace_bytes(B, N, D, H), device=x.device, dtype=torch.uint8)
+    ms = _timed(lambda: fs.fs_qkv_prologue(x, w, H, gain=g, q=outs[0], k=outs[1], v=outs[2],
+                                           ws=ws), stream, iters)
+    flops = 2.0 * B * N * D * 3 * H * 64
+    pk = peaks()
+    return {"ms": ms, "d_model": D, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+            "tensor_frac": flops / (ms / 1e3) / 1e12 / pk["bf16"],
+            "note": "RMSNorm row scales + gain fold + GEMM [B*N, D] x [D, 3*H*64] bf16 -> q, k, v"}
 
 
 def time_decode(q, k, v, lam, sigma, mix, params, stream, steps=256, warm=8):

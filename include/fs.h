@@ -197,6 +197,27 @@ int fs_prune_cells_static(const float *amax, int batch, int H, int N,
                           const fs_params *p, int32_t *pool,
                           int32_t *pool_count, void *stream);
 
+/* Shared q / k / v projection (paper.rainbus.top summary, 方法步骤详情 ①:
+ * the hidden state goes through RMSNorm and W_q, W_k, W_v, and both branches
+ * of every head use the result):
+ *   RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gain      (per row of D)
+ *   [q | k | v] = RMSNorm(x) . w_qkv^T, split into heads of d = 64
+ *   x        [batch, N, D] bf16 DEVICE (N a multiple of 128, D of 64)
+ *   gain     [D] f32, or NULL for ones; it is folded into the weights once
+ *            per call as bf16(w * gain)
+ *   w_qkv    [3*H*64, D] bf16: rows of q, then k, then v (head h of each
+ *            holds rows h*64 .. h*64+63), the [out, in] layout
+ *   q, k, v  [batch, H, N, 64] bf16 (the layout every attention call reads)
+ *   ws       device workspace of fs_qkv_workspace_bytes() bytes (row
+ *            scales, folded weights; the first 256 bytes are the error word)
+ * One tcgen05 GEMM with the row scale in its epilogue, after a streaming
+ * pass for the row scales. */
+size_t fs_qkv_workspace_bytes(int batch, int N, int D, int H);
+int fs_qkv_prologue(const void *x, const float *gain, const void *w_qkv,
+                    int batch, int N, int D, int H, float eps, void *q,
+                    void *k, void *v, void *ws, size_t ws_bytes,
+                    void *stream);
+
 /* Cell scoring and top-K (paper.rainbus.top summary, 核心方法 and
  * 方法步骤详情 ⑤; 局限与改进 for the erf factor; ai.info "Methodology in
  * Plain English").  For query n of block beta and candidate c

@@ -594,6 +594,50 @@ extern "C" size_t fs_decode_state_bytes(int batch, int H, int d, const fs_params
   return decode_layout(p->w, p->P, p->W, p->K).total(batch * H);
 }
 
+namespace fs {
+namespace {
+int check_qkv(int batch, int N, int D, int H) {
+  if (batch < 1 || N < 1 || D < 1 || H < 1) return FS_ERR_INVALID_ARG;
+  if (N % kBq || D % 64) return FS_ERR_INVALID_ARG;
+  if ((long long)batch * N >= (1ll << 31) || (long long)3 * H * kD >= (1ll << 20) ||
+      D > (1 << 16))
+    return FS_ERR_UNSUPPORTED;
+  return FS_OK;
+}
+}  // namespace
+}  // namespace fs
+
+extern "C" size_t fs_qkv_workspace_bytes(int batch, int N, int D, int H) {
+  if (check_qkv(batch, N, D, H) != FS_OK) return 0;
+  return kHeader + qkv_workspace_bytes(batch * N, D, H);
+}
+
+extern "C" int fs_qkv_prologue(const void *x, const float *gain, const void *w_qkv, int batch,
+                               int N, int D, int H, float eps, void *q, void *k, void *v, void *ws,
+                               size_t ws_bytes, void *stream) {
+  FS_TRY(check_qkv(batch, N, D, H));
+  if (!x || !w_qkv || !q || !k || !v || !ws || !(eps >= 0.f)) return FS_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader + qkv_workspace_bytes(batch * N, D, H)) return FS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int *err = static_cast<int *>(ws);
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  QkvArgs a{};
+  a.x = x;
+  a.gain = gain;
+  a.w = w_qkv;
+  a.batch = batch;
+  a.N = N;
+  a.D = D;
+  a.H = H;
+  a.eps = eps;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.ws = static_cast<char *>(ws) + kHeader;
+  a.err = err;
+  return status_of(launch_qkv(a, st));
+}
+
 extern "C" int fs_decode_state_view(int batch, int H, int d, const fs_params *p, size_t *offs) {
   FS_TRY(check_decode(p, d));
   FS_TRY(check_shape(batch, H, kBq, d));

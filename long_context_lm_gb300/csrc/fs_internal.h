@@ -86,4 +86,19 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
+// Shared q / k / v projection (k7_qkv.cu): RMSNorm row scale, gain folded
+// into the weights, one tcgen05 GEMM writing q, k, v [batch, H, N, 64] bf16.
+struct QkvArgs {
+  const void *x;      // [batch, N, D] bf16
+  const float *gain;  // [D] or null (ones)
+  const void *w;      // [3*H*64, D] bf16
+  int batch, N, D, H;
+  float eps;
+  void *q, *k, *v;
+  void *ws;           // qkv_workspace_bytes
+  int *err;
+};
+size_t qkv_workspace_bytes(int M, int D, int H);
+cudaError_t launch_qkv(const QkvArgs &a, cudaStream_t st);
+
 }  // namespace fs

@@ -32,7 +32,7 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
            "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host",
            "fs_window_attn_traced", "fs_decode_state_bytes", "fs_decode_state_init",
-           "fs_decode_state_view"]
+           "fs_decode_state_view", "fs_qkv_workspace_bytes", "fs_qkv_prologue"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
@@ -110,13 +110,17 @@ def load(build_if_stale: bool = True):
         L.fs_decode_state_bytes.argtypes = [I, I, I, PP]
         L.fs_decode_state_bytes.restype = Z
         L.fs_decode_state_view.argtypes = [I, I, I, PP, ctypes.POINTER(Z)]
+        L.fs_qkv_workspace_bytes.argtypes = [I, I, I, I]
+        L.fs_qkv_workspace_bytes.restype = Z
+        L.fs_qkv_prologue.argtypes = [P, P, P, I, I, I, I, F, P, P, P, P, Z, P]
         L.fs_decode_state_init.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, PP, P, Z, P]
         L.fs_decode_step.argtypes = [P, P, P, I, I, I, I, I, P, P, P, PP, P, Z, P, P, P]
         for name in SYMBOLS:
             if name not in ("fs_default_params", "fs_status_string", "fs_last_cuda_error",
                             "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes",
-                            "fs_host_workspace_bytes", "fs_decode_state_bytes"):
+                            "fs_host_workspace_bytes", "fs_decode_state_bytes",
+                            "fs_qkv_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -313,6 +317,39 @@ def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=No
                             state.numel() * state.element_size(), _ptr(out), _ptr(sel),
                             _stream(stream)), "fs_decode_step")
     return out
+
+
+def fs_qkv_workspace_bytes(batch, N, D, H) -> int:
+    return load().fs_qkv_workspace_bytes(batch, N, D, H)
+
+
+def fs_qkv_prologue(x, w_qkv, H, gain=None, eps=1e-6, q=None, k=None, v=None, ws=None,
+                    stream=None):
+    """RMSNorm(x) . w_qkv^T split into q, k, v [batch, H, N, 64] bf16.
+    x [batch, N, D] bf16, w_qkv [3*H*64, D] bf16, gain [D] f32 or None."""
+    L = load()
+    _dev(x, "x", (torch.bfloat16,))
+    _dev(w_qkv, "w_qkv", (torch.bfloat16,))
+    if gain is not None:
+        _dev(gain, "gain", (torch.float32,))
+    B, N, D = x.shape
+    if tuple(w_qkv.shape) != (3 * H * 64, D):
+        raise ValueError(f"w_qkv must be [{3 * H * 64}, {D}]")
+    outs = []
+    for t_ in (q, k, v):
+        t_ = t_ if t_ is not None else torch.empty((B, H, N, 64), device=x.device,
+                                                   dtype=torch.bfloat16)
+        _dev(t_, "q/k/v", (torch.bfloat16,))
+        outs.append(t_)
+    wsb = L.fs_qkv_workspace_bytes(B, N, D, H)
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_qkv_workspace_bytes")
+    if ws is None:
+        ws = torch.empty(wsb, device=x.device, dtype=torch.uint8)
+    _check(L.fs_qkv_prologue(_ptr(x), _ptr(gain), _ptr(w_qkv), B, N, D, H, float(eps),
+                             _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(ws), wsb,
+                             _stream(stream)), "fs_qkv_prologue")
+    return tuple(outs)
 
 
 def fs_select_cells(q, kbar, amax, pool, pool_count, lam, sigma, params=None,

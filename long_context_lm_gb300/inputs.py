@@ -126,3 +126,29 @@ def workload_inputs(name: str) -> Inputs:
 def bf16_values(x: torch.Tensor) -> torch.Tensor:
     """The bf16-rounded values of x as float32 (what both sides compute on)."""
     return x.to(torch.bfloat16).to(torch.float32)
+
+
+@dataclass
+class PrologueInputs:
+    x: torch.Tensor      # [B, N, D] bf16 hidden states
+    gain: torch.Tensor   # [D] float32 RMSNorm gain
+    w_qkv: torch.Tensor  # [3*H*d, D] bf16 projection weights (rows: q, k, v heads)
+
+
+def make_prologue_inputs(batch, seq_len, d_model, heads, head_dim=64, seed=0,
+                         gain="random") -> PrologueInputs:
+    """Random-init projection inputs: hidden states N(0,1) scaled per token by
+    a lognormal(0, 0.5) factor, weights N(0, 1/D) (random initialisation; no
+    trained weights exist here), gain U[0.5, 1.5] or ones.  Draw order: x
+    directions, token scales, weights, gain."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = torch.randn((batch, seq_len, d_model), generator=g, dtype=torch.float32)
+    x.mul_(torch.exp(0.5 * torch.randn((batch, seq_len, 1), generator=g, dtype=torch.float32)))
+    w = torch.randn((3 * heads * head_dim, d_model), generator=g, dtype=torch.float32)
+    w.mul_(d_model ** -0.5)
+    if gain == "ones":
+        gn = torch.ones(d_model, dtype=torch.float32)
+    else:
+        gn = 0.5 + torch.rand(d_model, generator=g, dtype=torch.float32)
+    return PrologueInputs(x.to(torch.bfloat16), gn, w.to(torch.bfloat16))
