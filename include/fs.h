@@ -288,6 +288,28 @@ int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype,
                      const float *lambda, const float *sigma, const float *mix,
                      float *out, void *ws, size_t ws_bytes, void *stream);
 
+/* Gradients of the forward (paper.rainbus.top summary, 方法步骤详情: the
+ * hard top-P / top-K indices carry no gradient; sigma_h and lambda_h are
+ * fixed, 局限与改进; ai.info "Methodology in Plain English", training).  For
+ * L = sum(dout * out) with out = fs_attention_fwd(q, k, v, ...), the pools and
+ * selections held at the forward's:
+ *   dout        [batch,H,N,d] f32 DEVICE (dL/dout)
+ *   dq, dk, dv  [batch,H,N,d] f32 (written)
+ *   dmix        [H] f32 (written): summed over the batch
+ * q, k, v bf16 (FS_BF16 only); the other arguments as fs_attention_fwd.
+ *   ws          device workspace of fs_backward_workspace_bytes() bytes
+ * The forward's selection stages run again inside the call (cell summaries,
+ * pools, scores and top-K, bit-identical to the forward's).  dk and dv of the
+ * long branch are accumulated with fp32 atomic additions, so their last bits
+ * can differ between runs; everything else is deterministic. */
+size_t fs_backward_workspace_bytes(int batch, int H, int N, int d,
+                                   const fs_params *p);
+int fs_attention_bwd(const void *q, const void *k, const void *v, int dtype,
+                     int batch, int H, int N, int d, const fs_params *p,
+                     const float *lambda, const float *sigma, const float *mix,
+                     const float *dout, float *dq, float *dk, float *dv,
+                     float *dmix, void *ws, size_t ws_bytes, void *stream);
+
 /* Number of timed stages of fs_attention_fwd_traced: cell summaries and
  * window-operand preparation (RoPE angle table, rotated keys, fp16 values),
  * pruning, selection, attention (window branch, NoPE readout of the selected

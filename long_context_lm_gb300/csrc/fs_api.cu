@@ -607,6 +607,63 @@ int check_qkv(int batch, int N, int D, int H) {
 }  // namespace
 }  // namespace fs
 
+extern "C" size_t fs_backward_workspace_bytes(int batch, int H, int N, int d,
+                                              const fs_params *p) {
+  if (check_params(p) != FS_OK || check_shape(batch, H, N, d) != FS_OK) return 0;
+  const Shape sh{batch, H, N, d};
+  return make_layout(sh, *p, FS_BF16).total + backward_workspace_bytes(sh);
+}
+
+extern "C" int fs_attention_bwd(const void *q, const void *k, const void *v, int dtype, int batch,
+                                int H, int N, int d, const fs_params *p, const float *lambda,
+                                const float *sigma, const float *mix, const float *dout, float *dq,
+                                float *dk, float *dv, float *dmix, void *ws, size_t ws_bytes,
+                                void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  FS_TRY(check_dtype(dtype));
+  if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !lambda || !sigma || !mix || !dout || !dq || !dk || !dv || !dmix || !ws)
+    return FS_ERR_INVALID_ARG;
+  const Shape sh{batch, H, N, d};
+  const Layout L = make_layout(sh, *p, FS_BF16);
+  if (ws_bytes < L.total + backward_workspace_bytes(sh)) return FS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *base = static_cast<char *>(ws);
+  int *err = reinterpret_cast<int *>(base);
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  float *kbar = reinterpret_cast<float *>(base + L.kbar);
+  float *amax = reinterpret_cast<float *>(base + L.amax);
+  int32_t *pool = reinterpret_cast<int32_t *>(base + L.pool);
+  int32_t *pool_count = reinterpret_cast<int32_t *>(base + L.pool_count);
+  int32_t *sel = reinterpret_cast<int32_t *>(base + L.sel);
+  const bool fs_mode = p->mode == FS_MODE_FS;
+  // the forward's selection, by the forward's kernels
+  FS_TRY(status_of(launch_cell_summary(k, false, sh, kbar, amax, st)));
+  if (!fs_mode)
+    FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));
+  FS_TRY(status_of(launch_select(q, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
+                                 p->P + p->W, fs_mode, sel, nullptr, err, st)));
+  BwdArgs a{};
+  a.sh = sh;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = dout;
+  a.sel = sel;
+  a.mix = mix;
+  a.w = p->w;
+  a.K = p->K;
+  a.rope_base = p->rope_base;
+  a.rms_eps = p->rms_eps;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dmix = dmix;
+  a.ws = base + L.total;
+  return status_of(launch_backward(a, st));
+}
+
 extern "C" size_t fs_qkv_workspace_bytes(int batch, int N, int D, int H) {
   if (check_qkv(batch, N, D, H) != FS_OK) return 0;
   return kHeader + qkv_workspace_bytes(batch * N, D, H);

@@ -99,6 +99,20 @@ struct QkvArgs {
   int *err;
 };
 size_t qkv_workspace_bytes(int M, int D, int H);
+// Gradients of the forward (k8_backward.cu), from the forward's selection.
+struct BwdArgs {
+  Shape sh;
+  const void *q, *k, *v;   // bf16
+  const float *g;          // dL/dout
+  const int32_t *sel;      // the forward's selection [BH, N, K]
+  const float *mix;
+  int w, K;
+  float rope_base, rms_eps;
+  float *dq, *dk, *dv, *dmix;
+  void *ws;                // backward_workspace_bytes
+};
+size_t backward_workspace_bytes(const Shape &sh);
+cudaError_t launch_backward(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_qkv(const QkvArgs &a, cudaStream_t st);
 
 }  // namespace fs

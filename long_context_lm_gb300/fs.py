@@ -32,7 +32,8 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_prune_static_scratch_bytes", "fs_prune_cells_static", "fs_decode_step",
            "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host",
            "fs_window_attn_traced", "fs_decode_state_bytes", "fs_decode_state_init",
-           "fs_decode_state_view", "fs_qkv_workspace_bytes", "fs_qkv_prologue"]
+           "fs_decode_state_view", "fs_qkv_workspace_bytes", "fs_qkv_prologue",
+           "fs_backward_workspace_bytes", "fs_attention_bwd"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
@@ -111,6 +112,9 @@ def load(build_if_stale: bool = True):
         L.fs_decode_state_bytes.restype = Z
         L.fs_decode_state_view.argtypes = [I, I, I, PP, ctypes.POINTER(Z)]
         L.fs_qkv_workspace_bytes.argtypes = [I, I, I, I]
+        L.fs_backward_workspace_bytes.argtypes = [I, I, I, I, PP]
+        L.fs_backward_workspace_bytes.restype = Z
+        L.fs_attention_bwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, P, P, P, P, Z, P]
         L.fs_qkv_workspace_bytes.restype = Z
         L.fs_qkv_prologue.argtypes = [P, P, P, I, I, I, I, F, P, P, P, P, Z, P]
         L.fs_decode_state_init.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, PP, P, Z, P]
@@ -120,7 +124,7 @@ def load(build_if_stale: bool = True):
                             "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes",
                             "fs_host_workspace_bytes", "fs_decode_state_bytes",
-                            "fs_qkv_workspace_bytes"):
+                            "fs_qkv_workspace_bytes", "fs_backward_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -317,6 +321,32 @@ def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=No
                             state.numel() * state.element_size(), _ptr(out), _ptr(sel),
                             _stream(stream)), "fs_decode_step")
     return out
+
+
+def fs_attention_bwd(q, k, v, lam, sigma, mix, dout, params=None, ws=None, stream=None):
+    """Gradients of L = sum(dout * fs_attention_fwd(q, k, v, ...)) with the
+    forward's selections held fixed.  Returns dq, dk, dv [B,H,N,d] f32 and
+    dmix [H] f32."""
+    L = load()
+    p = _params(params)
+    for t_, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t_, n, (torch.bfloat16,))
+    _dev(dout, "dout", (torch.float32,))
+    for t_, n in ((lam, "lam"), (sigma, "sigma"), (mix, "mix")):
+        _dev(t_, n, (torch.float32,))
+    B, H, N, d = _qkv_shape(q)
+    wsb = L.fs_backward_workspace_bytes(B, H, N, d, ctypes.byref(p))
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_backward_workspace_bytes")
+    if ws is None:
+        ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    dq, dk, dv = (torch.empty((B, H, N, d), device=q.device, dtype=torch.float32) for _ in range(3))
+    dmix = torch.empty(H, device=q.device, dtype=torch.float32)
+    _check(L.fs_attention_bwd(_ptr(q), _ptr(k), _ptr(v), FS_BF16, B, H, N, d, ctypes.byref(p),
+                              _ptr(lam), _ptr(sigma), _ptr(mix), _ptr(dout), _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(dmix), _ptr(ws), wsb, _stream(stream)),
+           "fs_attention_bwd")
+    return dq, dk, dv, dmix
 
 
 def fs_qkv_workspace_bytes(batch, N, D, H) -> int:
