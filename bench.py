@@ -304,6 +304,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extras:
         res["fs_mode"] = time_fs_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
         res["prologue"] = time_prologue(B, N, H, stream)
+        res["backward"] = time_backward(q, k, v, lam, sigma, mix, params, stream, counts)
     return res
 
 
@@ -390,6 +391,30 @@ def time_prologue(B, N, H, stream, D=1024, iters=10):
     return {"ms": ms, "d_model": D, "TFLOP/s": flops / (ms / 1e3) / 1e12,
             "tensor_frac": flops / (ms / 1e3) / 1e12 / pk["bf16"],
             "note": "RMSNorm row scales + gain fold + GEMM [B*N, D] x [D, 3*H*64] bf16 -> q, k, v"}
+
+
+def time_backward(q, k, v, lam, sigma, mix, params, stream, counts, iters=3):
+    """fs_attention_bwd on the benchmark's inputs with a random upstream
+    gradient (the forward's selection recomputed inside the call).  Its
+    kernels work in fp32 on the CUDA cores: the roofline is the fp32 FMA rate
+    (152 SMs x 128 FMA per clock x 2.07 GHz), the work the executed FMA of
+    the design: 576 per (query, window key) pair (query side 320, key side
+    256) and 576 per (query, selected token) pair of the long branch."""
+    from long_context_lm_gb300 import fs
+    B, H, N, d = q.shape
+    g = torch.randn((B, H, N, d), device=q.device, dtype=torch.float32)
+    ws = torch.empty(fs.fs_backward_workspace_bytes(B, H, N, d, params), device=q.device,
+                     dtype=torch.uint8)
+    ms = _timed(lambda: fs.fs_attention_bwd(q, k, v, lam, sigma, mix, g, params, ws=ws), stream,
+                iters)
+    n = np.arange(N, dtype=np.float64)
+    win_pairs = B * H * float(np.minimum(n + 1, params.w).sum())
+    fma = 576.0 * win_pairs + 576.0 * float(counts["tokens_read"])
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12  # TFLOP/s, fp32 FMA
+    ach = 2 * fma / (ms / 1e3) / 1e12
+    return {"ms": ms, "tokens_per_s": B * N / (ms / 1e3), "bound": "alu",
+            "achieved_TFLOP/s": ach, "peak_TFLOP/s": peak, "frac": ach / peak,
+            "note": "fp32 CUDA-core kernels; includes recomputing the forward's selection"}
 
 
 def time_decode(q, k, v, lam, sigma, mix, params, stream, steps=256, warm=8):
