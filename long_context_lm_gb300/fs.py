@@ -323,6 +323,11 @@ def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=No
     return out
 
 
+def fs_backward_workspace_bytes(batch, H, N, d=64, params=None) -> int:
+    p = _params(params)
+    return load().fs_backward_workspace_bytes(batch, H, N, d, ctypes.byref(p))
+
+
 def fs_attention_bwd(q, k, v, lam, sigma, mix, dout, params=None, ws=None, stream=None):
     """Gradients of L = sum(dout * fs_attention_fwd(q, k, v, ...)) with the
     forward's selections held fixed.  Returns dq, dk, dv [B,H,N,d] f32 and
