@@ -36,11 +36,39 @@ namespace {
 constexpr int kQT = 128;  // query tile
 constexpr int kKT = 64;   // key tile
 constexpr float kScale = 0.125f;  // 1 / sqrt(64)
-// shared-memory rows of 64 floats keep dims 32..63 one word further (column
-// c at c + c / 32): the two threads of a row read the same element index of
-// their halves at the same time, which then sit in different banks
-constexpr int kRow = kD + 2;
-__device__ __forceinline__ int col(int c) { return c + (c >> 5); }
+// shared-memory rows of 64 floats keep dims 32..63 four words further (column
+// c at c + 4 * (c / 32)): the two threads of a row read the same element
+// index of their halves at the same time, which then sit in different banks,
+// and both halves stay 16-byte aligned for vector loads
+constexpr int kRow = kD + 4;
+constexpr int kH1 = 36;  // first column of the second half
+__device__ __forceinline__ int col(int c) { return c + 4 * (c >> 5); }
+
+// dot of 32 register values with 32 consecutive shared floats (16-byte
+// aligned), four independent partial sums
+__device__ __forceinline__ float dot32(const float (&a)[32], const float *s) {
+  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 b = *reinterpret_cast<const float4 *>(s + e);
+    p0 = fmaf(a[e], b.x, p0);
+    p1 = fmaf(a[e + 1], b.y, p1);
+    p2 = fmaf(a[e + 2], b.z, p2);
+    p3 = fmaf(a[e + 3], b.w, p3);
+  }
+  return (p0 + p1) + (p2 + p3);
+}
+// acc += f * s[0..32)
+__device__ __forceinline__ void axpy32(float (&acc)[32], float f, const float *s) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 b = *reinterpret_cast<const float4 *>(s + e);
+    acc[e] = fmaf(f, b.x, acc[e]);
+    acc[e + 1] = fmaf(f, b.y, acc[e + 1]);
+    acc[e + 2] = fmaf(f, b.z, acc[e + 2]);
+    acc[e + 3] = fmaf(f, b.w, acc[e + 3]);
+  }
+}
 
 // x~ = R(n) x in fp32 for rows of bf16 x: one thread per (row, pair i), the
 // angle n*theta_i composed from table rows n mod 64 and 64 * (n / 64)
@@ -99,8 +127,8 @@ struct BwdParams {
 // window, query side
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k8_win_q_kernel(const BwdParams p) {
-  __shared__ float s_k[kKT][kRow];
-  __shared__ float s_v[kKT][kRow];
+  __shared__ __align__(16) float s_k[kKT][kRow];
+  __shared__ __align__(16) float s_v[kKT][kRow];
   const int tid = threadIdx.x, half = tid & 1, r = tid >> 1;
   const int nblk = p.N / kQT;
   const int bh = blockIdx.x / nblk, b0 = (blockIdx.x % nblk) * kQT;
@@ -126,9 +154,7 @@ __global__ void __launch_bounds__(256) k8_win_q_kernel(const BwdParams p) {
     __syncthreads();
     const int ja = max(lo, j0) - j0, jb = min(n, j0 + kKT - 1) - j0;
     for (int jj = 0; jj <= 63; ++jj) {
-      float part = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) part = fmaf(qh[e], s_k[jj][33 * half + e], part);
+      const float part = dot32(qh, &s_k[jj][kH1 * half]);
       const float sc = part + __shfl_xor_sync(0xffffffffu, part, 1);
       if (jj < ja || jj > jb) continue;
       if (sc > m) {
@@ -140,8 +166,7 @@ __global__ void __launch_bounds__(256) k8_win_q_kernel(const BwdParams p) {
       }
       const float pe = __expf(sc - m);
       l += pe;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = fmaf(pe, s_v[jj][33 * half + e], acc[e]);
+      axpy32(acc, pe, &s_v[jj][kH1 * half]);
     }
   }
   float gh[32];
@@ -171,19 +196,14 @@ __global__ void __launch_bounds__(256) k8_win_q_kernel(const BwdParams p) {
     __syncthreads();
     const int ja = max(lo, j0) - j0, jb = min(n, j0 + kKT - 1) - j0;
     for (int jj = 0; jj <= 63; ++jj) {
-      float ps = 0.f, pd = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        ps = fmaf(qh[e], s_k[jj][33 * half + e], ps);
-        pd = fmaf(gh[e], s_v[jj][33 * half + e], pd);
-      }
+      const float ps = dot32(qh, &s_k[jj][kH1 * half]);
+      const float pd = dot32(gh, &s_v[jj][kH1 * half]);
       const float sc = ps + __shfl_xor_sync(0xffffffffu, ps, 1);
       const float dp = pd + __shfl_xor_sync(0xffffffffu, pd, 1);
       if (jj < ja || jj > jb) continue;
       const float pr = __expf(sc - lse);
       const float ds = pr * (dp - gdo) * kScale;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = fmaf(ds, s_k[jj][33 * half + e], acc[e]);
+      axpy32(acc, ds, &s_k[jj][kH1 * half]);
     }
   }
   rotate_back_pair(acc, n, half, p.tab);
@@ -195,8 +215,8 @@ __global__ void __launch_bounds__(256) k8_win_q_kernel(const BwdParams p) {
 // window, key side
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) k8_win_kv_kernel(const BwdParams p) {
-  __shared__ float s_q[kKT][kRow];  // rotated q / 8
-  __shared__ float s_g[kKT][kRow];
+  __shared__ __align__(16) float s_q[kKT][kRow];  // rotated q / 8
+  __shared__ __align__(16) float s_g[kKT][kRow];
   __shared__ float s_lse[kKT], s_gdo[kKT];
   const int tid = threadIdx.x, half = tid & 1, jr = tid >> 1;
   const int ntile = p.N / kKT;
@@ -229,22 +249,15 @@ __global__ void __launch_bounds__(128) k8_win_kv_kernel(const BwdParams p) {
     __syncthreads();
     for (int rr = 0; rr < kKT; ++rr) {
       const int nn = n0 + rr;
-      float ps = 0.f, pd = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        ps = fmaf(s_q[rr][33 * half + e], kh[e], ps);
-        pd = fmaf(s_g[rr][33 * half + e], vh[e], pd);
-      }
+      const float ps = dot32(kh, &s_q[rr][kH1 * half]);
+      const float pd = dot32(vh, &s_g[rr][kH1 * half]);
       const float sc = ps + __shfl_xor_sync(0xffffffffu, ps, 1);
       const float dp = pd + __shfl_xor_sync(0xffffffffu, pd, 1);
       if (nn >= p.N || j > nn || j < nn - p.w + 1) continue;  // this key is not in n's window
       const float pr = __expf(sc - s_lse[rr]);
       const float ds = pr * (dp - s_gdo[rr]);  // the 1/8 is in s_q
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        dv[e] = fmaf(pr, s_g[rr][33 * half + e], dv[e]);
-        dk[e] = fmaf(ds, s_q[rr][33 * half + e], dk[e]);
-      }
+      axpy32(dv, pr, &s_g[rr][kH1 * half]);
+      axpy32(dk, ds, &s_q[rr][kH1 * half]);
     }
   }
   rotate_back_pair(dk, j, half, p.tab);
@@ -261,8 +274,8 @@ __global__ void __launch_bounds__(128) k8_win_kv_kernel(const BwdParams p) {
 constexpr int kMaxU = kBq * kMaxK;
 
 __global__ void __launch_bounds__(256) k8_long_kernel(const BwdParams p) {
-  __shared__ float s_k[kS][kRow];
-  __shared__ float s_v[kS][kRow];
+  __shared__ __align__(16) float s_k[kS][kRow];
+  __shared__ __align__(16) float s_v[kS][kRow];
   __shared__ int s_ul[kMaxU];
   __shared__ int s_nu;
   __shared__ float s_red[8];
@@ -323,9 +336,7 @@ __global__ void __launch_bounds__(256) k8_long_kernel(const BwdParams p) {
     for (int k = 0; k < kMaxK; ++k) mine |= pick[k] == c;
     if (!mine) continue;  // both threads of the row agree
     for (int t = 0; t < kS; ++t) {
-      float part = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) part = fmaf(qh[e], s_k[t][33 * half + e], part);
+      const float part = dot32(qh, &s_k[t][kH1 * half]);
       const float sc = part + __shfl_xor_sync(0x3u << (tid & 30), part, 1);
       if (sc > m) {
         const float f = __expf(m - sc);
@@ -336,8 +347,7 @@ __global__ void __launch_bounds__(256) k8_long_kernel(const BwdParams p) {
       }
       const float pe = __expf(sc - m);
       l += pe;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = fmaf(pe, s_v[t][33 * half + e], acc[e]);
+      axpy32(acc, pe, &s_v[t][kH1 * half]);
     }
   }
   const bool has = l > 0.f;
@@ -402,17 +412,12 @@ __global__ void __launch_bounds__(256) k8_long_kernel(const BwdParams p) {
     for (int k = 0; k < kMaxK; ++k) mine |= pick[k] == c;
     if (mine) {
       for (int t = 0; t < kS; ++t) {
-        float ps = 0.f, pd = 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          ps = fmaf(qh[e], s_k[t][33 * half + e], ps);
-          pd = fmaf(doh[e], s_v[t][33 * half + e], pd);
-        }
+        const float ps = dot32(qh, &s_k[t][kH1 * half]);
+        const float pd = dot32(doh, &s_v[t][kH1 * half]);
         const float sc = ps + __shfl_xor_sync(0x3u << (tid & 30), ps, 1);
         const float dp = pd + __shfl_xor_sync(0x3u << (tid & 30), pd, 1);
         const float ds = __expf(sc - lse) * (dp - dodo) * kScale;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = fmaf(ds, s_k[t][33 * half + e], acc[e]);
+        axpy32(acc, ds, &s_k[t][kH1 * half]);
       }
     }
     // scatter: dk, dv of cell c from the tile's rows that picked it; thread
