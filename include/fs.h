@@ -56,8 +56,10 @@ typedef enum {
 typedef enum { FS_BF16 = 0, FS_FP32 = 1 } fs_dtype;
 
 /* FS-L prunes the prefix to P + W cells per block; FS scores the whole
- * available prefix (quadratic).  paper.rainbus.top summary, 核心方法. */
-typedef enum { FS_MODE_FSL = 0, FS_MODE_FS = 1 } fs_mode;
+ * available prefix (quadratic); FS-B keeps every cell and selects by beam
+ * search over two causal forests (paper.rainbus.top summary, 核心方法 and
+ * 方法步骤详情 ⑤; ai.info "Methodology in Plain English"). */
+typedef enum { FS_MODE_FSL = 0, FS_MODE_FS = 1, FS_MODE_FSB = 2 } fs_mode;
 
 /* Method parameters.  Page values: w=512, s=32, K=4, P=64, W=8, Bq=128
  * (paper.rainbus.top summary, 核心方法); rope_base=10000 and rms_eps=1e-6 are
@@ -72,9 +74,12 @@ typedef struct {
   float rope_base; /* theta_i = rope_base^(-2i/d), half-split pairing    */
   float rms_eps;   /* RMSNorm epsilon of the long-branch output          */
   int mode;        /* fs_mode                                            */
+  int beam;        /* FS-B: nodes kept per level of each forest (1..16)  */
+  float tau;       /* FS-B: the second forest holds the cells a_c > tau  */
 } fs_params;
 
-/* Fills the page values above. */
+/* Fills the page values above (FS-B: beam 16; tau 0, an input the pages
+ * calibrate per model as a median cell norm). */
 void fs_default_params(fs_params *p);
 
 /* Human-readable name of a status code (static string). */
@@ -217,6 +222,27 @@ int fs_qkv_prologue(const void *x, const float *gain, const void *w_qkv,
                     int batch, int N, int D, int H, float eps, void *q,
                     void *k, void *v, void *ws, size_t ws_bytes,
                     void *stream);
+
+/* FS-B selection (ai.info summary, "Methodology in Plain English", FS-B;
+ * paper.rainbus.top summary, 方法步骤详情 ⑤ and 技术新颖性): two causal
+ * forests per (batch, head) over the cells in position order -- all cells, and
+ * the cells with amax > tau -- whose nodes (aligned runs of 2^j cells) keep
+ * the mean of their mean keys, a radius bounding their children, the largest
+ * amax and the first cell; for query n of block beta, a beam of p->beam nodes
+ * per level descends the runs tiling each forest's cells below beta*Bq/s,
+ * ranked by the bound
+ *   q . mean + |q| radius + lambda amax erf(sigma (n - p_first) / s),
+ * and the union of both beams' cells is reranked by the log-sum-exp of their
+ * s token logits q . k_t / sqrt(d); the top K are kept (LSE desc, c asc).
+ *   q, k        [batch,H,N,d] bf16 (k unrotated, for the rerank)
+ *   kbar, amax  fs_cell_summarize of k
+ *   sel         [batch,H,N,K] int32 ranked, -1 padded
+ *   ws          device scratch of fs_fsb_workspace_bytes() bytes (forests) */
+size_t fs_fsb_workspace_bytes(int batch, int H, int N, const fs_params *p);
+int fs_fsb_select(const void *q, const void *k, const float *kbar,
+                  const float *amax, const float *lambda, const float *sigma,
+                  int batch, int H, int N, int d, const fs_params *p,
+                  int32_t *sel, void *ws, size_t ws_bytes, void *stream);
 
 /* Cell scoring and top-K (paper.rainbus.top summary, 核心方法 and
  * 方法步骤详情 ⑤; 局限与改进 for the erf factor; ai.info "Methodology in

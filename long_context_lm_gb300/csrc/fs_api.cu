@@ -39,7 +39,10 @@ int check_params(const fs_params *p) {
     return FS_ERR_INVALID_ARG;
   if (p->Bq % p->s) return FS_ERR_INVALID_ARG;
   if (!(p->rms_eps >= 0.f) || !(p->rope_base > 0.f)) return FS_ERR_INVALID_ARG;
-  if (p->mode != FS_MODE_FSL && p->mode != FS_MODE_FS) return FS_ERR_INVALID_ARG;
+  if (p->mode != FS_MODE_FSL && p->mode != FS_MODE_FS && p->mode != FS_MODE_FSB)
+    return FS_ERR_INVALID_ARG;
+  if (p->mode == FS_MODE_FSB && (p->beam < 1 || !(p->tau == p->tau))) return FS_ERR_INVALID_ARG;
+  if (p->mode == FS_MODE_FSB && p->beam > 16) return FS_ERR_UNSUPPORTED;
   if (p->s != kS || p->Bq != kBq || p->P > kMaxP || p->K > kMaxK || p->w > 1024)
     return FS_ERR_UNSUPPORTED;
   return FS_OK;
@@ -95,7 +98,7 @@ WindowLayout take_window(const Shape &sh, const std::function<size_t(size_t)> &t
 // Layout of the fs_attention_fwd workspace.
 struct Layout {
   size_t qb, kb, vb;       // bf16 copies (fp32 inputs only)
-  size_t kbar, amax, pool, pool_count, sel, prune;
+  size_t kbar, amax, pool, pool_count, sel, prune, fsb;
   WindowLayout win;
   size_t total;
 };
@@ -119,6 +122,7 @@ Layout make_layout(const Shape &sh, const fs_params &p, int dtype) {
   L.pool_count = take((size_t)sh.BH() * sh.nblk() * sizeof(int32_t));
   L.sel = take((size_t)sh.BH() * sh.N * p.K * sizeof(int32_t));
   L.prune = take(prune_workspace_bytes(sh));
+  L.fsb = take(p.mode == FS_MODE_FSB ? (size_t)sh.BH() * fsb_layout(sh.C()).head_bytes : 0);
   L.win = take_window(sh, take);
   L.total = off;
   return L;
@@ -167,6 +171,8 @@ void fs_default_params(fs_params *p) {
   p->rope_base = 10000.f;
   p->rms_eps = 1e-6f;
   p->mode = FS_MODE_FSL;
+  p->beam = 16;
+  p->tau = 0.f;
 }
 
 const char *fs_status_string(int status) {
@@ -260,6 +266,7 @@ int fs_select_cells(const void *q, int dtype, const float *kbar, const float *am
   FS_TRY(check_dtype(dtype));
   if (dtype != FS_BF16) return FS_ERR_UNSUPPORTED;
   if (!q || !kbar || !amax || !lambda || !sigma || !sel) return FS_ERR_INVALID_ARG;
+  if (p->mode == FS_MODE_FSB) return FS_ERR_INVALID_ARG;  // fs_fsb_select
   const bool fs_mode = p->mode == FS_MODE_FS;
   if (!fs_mode && (!pool || !pool_count)) return FS_ERR_INVALID_ARG;
   return status_of(launch_select(q, kbar, amax, pool, pool_count, lambda, sigma,
@@ -404,11 +411,16 @@ int forward(const void *q, const void *k, const void *v, int dtype, const Shape 
   FS_TRY(status_of(launch_prep_summary(kb, vb, base + L.win.tab, sh, base + L.win.kt,
                                        base + L.win.v16, kbar, amax, err, st)));
   FS_TRY(mark(1));
-  if (!fs_mode)
+  const bool fsb = p->mode == FS_MODE_FSB;
+  if (!fs_mode && !fsb)
     FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));
   FS_TRY(mark(2));
-  FS_TRY(status_of(launch_select(qb, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
-                                 p->P + p->W, fs_mode, sel, nullptr, err, st)));
+  if (fsb)
+    FS_TRY(status_of(launch_fsb(qb, kb, kbar, amax, lambda, sigma, sh, p->K, p->beam, p->tau,
+                                base + L.fsb, sel, st)));
+  else
+    FS_TRY(status_of(launch_select(qb, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
+                                   p->P + p->W, fs_mode, sel, nullptr, err, st)));
   FS_TRY(mark(3));
   AttnArgs a{};
   a.sh = sh;
@@ -606,6 +618,25 @@ int check_qkv(int batch, int N, int D, int H) {
 }
 }  // namespace
 }  // namespace fs
+
+extern "C" size_t fs_fsb_workspace_bytes(int batch, int H, int N, const fs_params *p) {
+  if (check_params(p) != FS_OK || check_shape(batch, H, N, kD) != FS_OK) return 0;
+  if (p->mode != FS_MODE_FSB) return 0;
+  return (size_t)batch * H * fsb_layout(N / kS).head_bytes;
+}
+
+extern "C" int fs_fsb_select(const void *q, const void *k, const float *kbar, const float *amax,
+                             const float *lambda, const float *sigma, int batch, int H, int N,
+                             int d, const fs_params *p, int32_t *sel, void *ws, size_t ws_bytes,
+                             void *stream) {
+  FS_TRY(check_params(p));
+  FS_TRY(check_shape(batch, H, N, d));
+  if (p->mode != FS_MODE_FSB) return FS_ERR_INVALID_ARG;
+  if (!q || !k || !kbar || !amax || !lambda || !sigma || !sel || !ws) return FS_ERR_INVALID_ARG;
+  if (ws_bytes < (size_t)batch * H * fsb_layout(N / kS).head_bytes) return FS_ERR_INVALID_ARG;
+  return status_of(launch_fsb(q, k, kbar, amax, lambda, sigma, Shape{batch, H, N, d}, p->K,
+                              p->beam, p->tau, ws, sel, static_cast<cudaStream_t>(stream)));
+}
 
 extern "C" size_t fs_backward_workspace_bytes(int batch, int H, int N, int d,
                                               const fs_params *p) {

@@ -99,6 +99,19 @@ struct QkvArgs {
   int *err;
 };
 size_t qkv_workspace_bytes(int M, int D, int H);
+// FS-B forests (k9_fsb.cu): per (batch, head) two leaf lists (all cells;
+// cells with a_c > tau), the tau forest's prefix count, then per forest the
+// node means [nodes, 64] and (radius, a_max, first cell, -) [nodes].
+constexpr int kFsbMaxLevels = 24;
+struct FsbLayout {
+  int C, levels, nodes;
+  int level_off[kFsbMaxLevels];
+  size_t list, hcount, mean, meta, head_bytes;
+};
+FsbLayout fsb_layout(int C);
+cudaError_t launch_fsb(const void *q, const void *k, const float *kbar, const float *amax,
+                       const float *lambda, const float *sigma, const Shape &sh, int K, int beam,
+                       float tau, void *ws, int32_t *sel, cudaStream_t st);
 // Gradients of the forward (k8_backward.cu), from the forward's selection.
 struct BwdArgs {
   Shape sh;

@@ -1,0 +1,385 @@
+// k9_fsb.cu -- FS-B cell selection: beam search over two causal forests per
+// head, then a token-level rerank.
+//
+// FreeSolo (ai.info summary, "Methodology in Plain English", FS-B: two
+// balanced trees per head, over the full prefix and over the cells whose
+// largest key norm exceeds a threshold tau; every node stores a mean key, a
+// radius bounding its children, the largest cell norm and the earliest
+// position; a beam of 16 nodes per level descends each tree by a provable
+// upper bound on the cell scores beneath a node; the union of both beams is
+// reranked by token-level log-sum-exp and the top K cells are read;
+// paper.rainbus.top summary, 方法步骤详情 ⑤, 技术新颖性).
+//
+// Forest: the leaves are the forest's cells in position order (all cells, or
+// the cells with a_c > tau); level j node i covers leaves [i 2^j, (i+1) 2^j)
+// and stores the mean of their mean keys, a radius r (max over children of
+// |mean_child - mean| + r_child), the largest a_c and its first cell.  A
+// query of block beta searches the maximal aligned runs tiling the forest's
+// leaves below A = beta Bq / s (the binary decomposition of their count), so
+// no node it visits holds an unavailable cell.  Node bound for query n:
+//   q . mean + |q| r + lambda a_max erf(sigma (n - p_first) / s),
+// p_first = first * s + s / 2, above the score u_c of every cell beneath.
+//
+//   k9_build_kernel   one CTA per (batch, head, forest): the leaf list (a
+//                     block scan over the cells for the tau forest, with a
+//                     prefix count for the queries), then the levels
+//   k9_search_kernel  one warp per query: the beam descent of both forests
+//                     (a lane per candidate node), then the rerank (a lane per
+//                     token) and the top K by (LSE desc, c asc)
+#include "fs_common.cuh"
+#include "fs_internal.h"
+
+namespace fs {
+
+FsbLayout fsb_layout(int C) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  FsbLayout L;
+  L.C = C;
+  L.levels = 1;
+  size_t nodes = 0;
+  for (int m = C;; m = (m + 1) / 2, ++L.levels) {
+    L.level_off[L.levels - 1] = (int)nodes;
+    nodes += (size_t)m;
+    if (m <= 1) break;
+  }
+  L.nodes = (int)nodes;
+  // per (batch, head): leaf lists (two), the tau forest's prefix count, then
+  // per forest the node means and (radius, amax, first)
+  L.list = 0;
+  L.hcount = up(2 * (size_t)C * 4);
+  L.mean = L.hcount + up(((size_t)C + 1) * 4);
+  L.meta = L.mean + up(2 * nodes * kD * 4);
+  L.head_bytes = L.meta + up(2 * nodes * 16);
+  return L;
+}
+
+namespace {
+
+constexpr int kBuildThreads = 256;
+
+__global__ void __launch_bounds__(kBuildThreads) k9_build_kernel(const float *__restrict__ kbar,
+                                                                 const float *__restrict__ amax,
+                                                                 float tau, FsbLayout L,
+                                                                 unsigned char *ws) {
+  __shared__ int s_scan[kBuildThreads];
+  const int bh = blockIdx.x >> 1, f = blockIdx.x & 1;  // forest 0: all cells, 1: a_c > tau
+  const int tid = threadIdx.x, C = L.C;
+  unsigned char *hs = ws + (size_t)bh * L.head_bytes;
+  int *list = reinterpret_cast<int *>(hs + L.list) + (size_t)f * C;
+  int *hcount = reinterpret_cast<int *>(hs + L.hcount);
+  float *mean = reinterpret_cast<float *>(hs + L.mean) + (size_t)f * L.nodes * kD;
+  float4 *meta = reinterpret_cast<float4 *>(hs + L.meta) + (size_t)f * L.nodes;
+  const float *kb = kbar + (size_t)bh * C * kD;
+  const float *am = amax + (size_t)bh * C;
+  // leaf list in position order (tau forest: a block scan of the keep flags)
+  int M = C;
+  if (f == 0) {
+    for (int c = tid; c < C; c += kBuildThreads) list[c] = c;
+  } else {
+    int base = 0;
+    for (int c0 = 0; c0 < C; c0 += kBuildThreads) {
+      const int c = c0 + tid;
+      const int keep = c < C && am[c] > tau;
+      s_scan[tid] = keep;
+      __syncthreads();
+      for (int o = 1; o < kBuildThreads; o <<= 1) {  // inclusive scan
+        const int x = tid >= o ? s_scan[tid - o] : 0;
+        __syncthreads();
+        s_scan[tid] += x;
+        __syncthreads();
+      }
+      const int excl = base + s_scan[tid] - keep;
+      if (c < C) hcount[c] = excl;  // leaves of the tau forest below cell c
+      if (keep) list[excl] = c;
+      base += s_scan[kBuildThreads - 1];
+      __syncthreads();
+    }
+    if (tid == 0) hcount[C] = base;
+    M = base;
+  }
+  __syncthreads();
+  // level 0: one leaf per cell of the list
+  for (int e = tid; e < M * kD; e += kBuildThreads) {
+    const int i = e / kD, dd = e % kD;
+    mean[(size_t)i * kD + dd] = kb[(size_t)list[i] * kD + dd];
+  }
+  for (int i = tid; i < M; i += kBuildThreads)
+    meta[i] = make_float4(0.f, am[list[i]], __int_as_float(list[i]), 0.f);
+  __syncthreads();
+  // levels 1.. from their children, one warp per node
+  const int warp = tid >> 5, lane = tid & 31;
+  int m = M;
+  for (int j = 1; j < L.levels && m > 1; ++j) {
+    const int mc = m;
+    m = (m + 1) / 2;
+    const float *cmean = mean + (size_t)L.level_off[j - 1] * kD;
+    const float4 *cmeta = meta + L.level_off[j - 1];
+    float *pmean = mean + (size_t)L.level_off[j] * kD;
+    float4 *pmeta = meta + L.level_off[j];
+    const int half = 1 << (j - 1);  // leaves under a full child
+    for (int i = warp; i < m; i += kBuildThreads / 32) {
+      const int c0 = 2 * i, c1 = 2 * i + 1;
+      const bool two = c1 < mc;
+      const float w0 = (float)min(half, M - c0 * half);
+      const float w1 = two ? (float)min(half, M - c1 * half) : 0.f;
+      const float inv = 1.f / (w0 + w1);
+      float mu[2], a0[2], a1[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int dd = 2 * lane + e;
+        a0[e] = cmean[(size_t)c0 * kD + dd];
+        a1[e] = two ? cmean[(size_t)c1 * kD + dd] : 0.f;
+        mu[e] = (w0 * a0[e] + w1 * a1[e]) * inv;
+        pmean[(size_t)i * kD + dd] = mu[e];
+      }
+      float d0 = (a0[0] - mu[0]) * (a0[0] - mu[0]) + (a0[1] - mu[1]) * (a0[1] - mu[1]);
+      float d1 = (a1[0] - mu[0]) * (a1[0] - mu[0]) + (a1[1] - mu[1]) * (a1[1] - mu[1]);
+      d0 = warp_sum(d0);
+      d1 = warp_sum(d1);
+      if (lane == 0) {
+        const float4 m0 = cmeta[c0];
+        float r = sqrtf(d0) + m0.x, a = m0.y;
+        if (two) {
+          const float4 m1 = cmeta[c1];
+          r = fmaxf(r, sqrtf(d1) + m1.x);
+          a = fmaxf(a, m1.y);
+        }
+        // the bound needs r to cover every leaf: round up by a relative ulp
+        pmeta[i] = make_float4(r * (1.f + 4e-7f), a, m0.z, 0.f);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+struct SearchParams {
+  const uint16_t *q, *k;           // [BH, N, 64] bf16
+  const unsigned char *ws;
+  FsbLayout L;
+  const float *lambda, *sigma;
+  int H, N, K, beam;
+  long long nq;                    // BH * N
+  int32_t *sel;                    // [BH, N, K]
+};
+
+// element e (< 64) of a two-per-lane array: lane e % 32, slot e / 32
+__device__ __forceinline__ int lane_get(const int (&a)[2], int e) {
+  return __shfl_sync(0xffffffffu, e < 32 ? a[0] : a[1], e & 31);
+}
+__device__ __forceinline__ float lane_getf(const float (&a)[2], int e) {
+  return __shfl_sync(0xffffffffu, e < 32 ? a[0] : a[1], e & 31);
+}
+
+__device__ __forceinline__ float bfv(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+// ranks_before on (bound, first leaf) pairs: higher bound first, ties by the
+// lower first leaf
+__device__ __forceinline__ bool node_before(float u, int f, float u2, int f2) {
+  return u > u2 || (u == u2 && f < f2);
+}
+
+constexpr int kMaxCand = 64;
+
+__global__ void __launch_bounds__(256) k9_search_kernel(const SearchParams p) {
+  __shared__ float s_q[8][kD];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gq = (long long)blockIdx.x * 8 + warp;  // query (bh, n)
+  if (gq >= p.nq) return;  // the whole warp
+  const int bh = (int)(gq / p.N), n = (int)(gq % p.N);
+  const int h = bh % p.H;
+  const FsbLayout &L = p.L;
+  const int C = L.C;
+  const size_t row = (size_t)bh * p.N + n;
+  for (int dd = lane; dd < kD; dd += 32) s_q[warp][dd] = bfv(p.q[row * kD + dd]);
+  __syncwarp();
+  float qn2 = s_q[warp][lane] * s_q[warp][lane] + s_q[warp][lane + 32] * s_q[warp][lane + 32];
+  const float qnorm = sqrtf(warp_sum(qn2));
+  const float lam = p.lambda[h], sig = p.sigma[h];
+  const int A = (n / kBq) * (kBq / kS);
+  const unsigned char *hs = p.ws + (size_t)bh * L.head_bytes;
+  const int *hcount = reinterpret_cast<const int *>(hs + L.hcount);
+  // candidates of the union, one per lane (-1: none)
+  int cand = -1, ncand = 0;
+  for (int f = 0; f < 2; ++f) {
+    const int m = f == 0 ? A : (A > 0 ? hcount[A] : 0);
+    if (m == 0) continue;
+    const int *list = reinterpret_cast<const int *>(hs + L.list) + (size_t)f * C;
+    const float *mean = reinterpret_cast<const float *>(hs + L.mean) + (size_t)f * L.nodes * kD;
+    const float4 *meta = reinterpret_cast<const float4 *>(hs + L.meta) + (size_t)f * L.nodes;
+    // the beam: up to kMaxCand (level, index) nodes, two per lane
+    int bj[2] = {-1, -1}, bi[2] = {0, 0};
+    int nb = 0;
+    {
+      int start = 0;
+      for (int j = 31 - __clz(m); j >= 0; --j)
+        if (m & (1 << j)) {
+          if (nb % 32 == lane) {
+            if (nb < 32) {
+              bj[0] = j;
+              bi[0] = start >> j;
+            } else {
+              bj[1] = j;
+              bi[1] = start >> j;
+            }
+          }
+          ++nb;
+          start += 1 << j;
+        }
+    }
+    while (true) {
+      // any inner node left?
+      bool inner = (bj[0] > 0) || (bj[1] > 0);
+      if (!__any_sync(0xffffffffu, inner)) break;
+      // children of every beam node (a leaf stays): up to 2 nb <= kMaxCand
+      int cj[2] = {-1, -1}, ci[2] = {0, 0};
+      float cu[2] = {-INFINITY, -INFINITY};
+      int cf[2] = {0x7fffffff, 0x7fffffff};
+      int nc = 0;
+      for (int b = 0; b < nb; ++b) {
+        const int j = lane_get(bj, b);
+        const int i = lane_get(bi, b);
+        const int kids = j == 0 ? 1 : 2;
+        for (int c = 0; c < kids; ++c) {
+          if (nc % 32 == lane) {
+            const int cjj = j == 0 ? 0 : j - 1, cii = j == 0 ? i : 2 * i + c;
+            if (nc < 32) {
+              cj[0] = cjj;
+              ci[0] = cii;
+            } else {
+              cj[1] = cjj;
+              ci[1] = cii;
+            }
+          }
+          ++nc;
+        }
+      }
+      // bounds, a lane per candidate
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (cj[e] < 0) continue;
+        const int node = L.level_off[cj[e]] + ci[e];
+        const float4 *mu = reinterpret_cast<const float4 *>(mean + (size_t)node * kD);
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < kD / 4; v += 2) {
+          const float4 a = __ldg(mu + v), b4 = __ldg(mu + v + 1);
+          d0 = fmaf(s_q[warp][4 * v], a.x, d0);
+          d0 = fmaf(s_q[warp][4 * v + 1], a.y, d0);
+          d0 = fmaf(s_q[warp][4 * v + 2], a.z, d0);
+          d0 = fmaf(s_q[warp][4 * v + 3], a.w, d0);
+          d1 = fmaf(s_q[warp][4 * v + 4], b4.x, d1);
+          d1 = fmaf(s_q[warp][4 * v + 5], b4.y, d1);
+          d1 = fmaf(s_q[warp][4 * v + 6], b4.z, d1);
+          d1 = fmaf(s_q[warp][4 * v + 7], b4.w, d1);
+        }
+        const float4 mt = __ldg(meta + node);
+        const int first = __float_as_int(mt.z);
+        const float pf = (float)(first * kS) + 0.5f * kS;
+        cu[e] = (d0 + d1) + qnorm * mt.x + lam * mt.y * erff(sig * ((float)n - pf) / kS);
+        cf[e] = ci[e] << cj[e];  // first leaf of the node
+      }
+      // keep the best `beam` by (bound desc, first leaf asc): rank by counting
+      int rank[2] = {0, 0};
+      for (int b = 0; b < nc; ++b) {
+        const float u = lane_getf(cu, b);
+        const int f2 = lane_get(cf, b);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) rank[e] += node_before(u, f2, cu[e], cf[e]);
+      }
+      // the kept nodes, in rank order, two per lane again
+      nb = min(nc, p.beam);
+      int nj[2] = {-1, -1}, ni[2] = {0, 0};
+      for (int b = 0; b < nc; ++b) {
+        const int r = lane_get(rank, b);
+        const int j = lane_get(cj, b);
+        const int i = lane_get(ci, b);
+        if (r < nb && r % 32 == lane) {
+          if (r < 32) {
+            nj[0] = j;
+            ni[0] = i;
+          } else {
+            nj[1] = j;
+            ni[1] = i;
+          }
+        }
+      }
+      bj[0] = nj[0];
+      bj[1] = nj[1];
+      bi[0] = ni[0];
+      bi[1] = ni[1];
+    }
+    // the beam's leaves join the union (cells, deduplicated; two beams of at
+    // most 16 fit a lane each)
+    for (int b = 0; b < nb; ++b) {
+      const int i = lane_get(bi, b);
+      const int c = list[i];
+      const bool dup = __any_sync(0xffffffffu, lane < ncand && cand == c);
+      if (!dup) {
+        if (lane == ncand) cand = c;
+        ++ncand;
+      }
+    }
+  }
+  // rerank: LSE of the 32 token logits of each union cell (a lane per token)
+  float lse_mine = -INFINITY;
+  for (int u = 0; u < ncand; ++u) {
+    const int c = __shfl_sync(0xffffffffu, cand, u);
+    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k + ((size_t)bh * p.N + (size_t)c * kS + lane) * kD);
+    float dot = 0.f;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const uint4 x = __ldg(kr + v);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dot = fmaf(s_q[warp][8 * v + 2 * e], bf16_lo(w[e]), dot);
+        dot = fmaf(s_q[warp][8 * v + 2 * e + 1], bf16_hi(w[e]), dot);
+      }
+    }
+    const float lg = dot * 0.125f;
+    float mx = lg;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float sum = warp_sum(__expf(lg - mx));
+    if (lane == u) lse_mine = mx + __logf(sum);
+  }
+  // top K by (LSE desc, c asc)
+  int rank = 0;
+  for (int u = 0; u < ncand; ++u) {
+    const float x = __shfl_sync(0xffffffffu, lse_mine, u);
+    const int c = __shfl_sync(0xffffffffu, cand, u);
+    rank += lane < ncand && (x > lse_mine || (x == lse_mine && c < cand));
+  }
+  int32_t *dst = p.sel + row * p.K;
+  if (lane < p.K) dst[lane] = -1;
+  __syncwarp();
+  if (lane < ncand && rank < p.K) dst[rank] = cand;
+}
+
+}  // namespace
+
+cudaError_t launch_fsb(const void *q, const void *k, const float *kbar, const float *amax,
+                       const float *lambda, const float *sigma, const Shape &sh, int K, int beam,
+                       float tau, void *ws, int32_t *sel, cudaStream_t st) {
+  const FsbLayout L = fsb_layout(sh.C());
+  unsigned char *w = static_cast<unsigned char *>(ws);
+  k9_build_kernel<<<sh.BH() * 2, kBuildThreads, 0, st>>>(kbar, amax, tau, L, w);
+  SearchParams p;
+  p.q = static_cast<const uint16_t *>(q);
+  p.k = static_cast<const uint16_t *>(k);
+  p.ws = w;
+  p.L = L;
+  p.lambda = lambda;
+  p.sigma = sigma;
+  p.H = sh.H;
+  p.N = sh.N;
+  p.K = K;
+  p.beam = beam;
+  p.sel = sel;
+  const long long nq = (long long)sh.BH() * sh.N;
+  p.nq = nq;
+  k9_search_kernel<<<(unsigned)((nq + 7) / 8), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fs

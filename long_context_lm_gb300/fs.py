@@ -23,7 +23,7 @@ from . import build as _build
 (FS_OK, FS_ERR_INVALID_ARG, FS_ERR_UNSUPPORTED, FS_ERR_CUDA, FS_ERR_TIMEOUT, FS_ERR_RANGE,
  FS_ERR_SCRATCH_LIMIT, FS_ERR_STATE) = range(8)
 FS_BF16, FS_FP32 = 0, 1
-FS_MODE_FSL, FS_MODE_FS = 0, 1
+FS_MODE_FSL, FS_MODE_FS, FS_MODE_FSB = 0, 1, 2
 
 SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_workspace_bytes",
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
@@ -33,7 +33,8 @@ SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_wo
            "fs_selftest_wait_timeout", "fs_host_workspace_bytes", "fs_attention_fwd_host",
            "fs_window_attn_traced", "fs_decode_state_bytes", "fs_decode_state_init",
            "fs_decode_state_view", "fs_qkv_workspace_bytes", "fs_qkv_prologue",
-           "fs_backward_workspace_bytes", "fs_attention_bwd"]
+           "fs_backward_workspace_bytes", "fs_attention_bwd",
+           "fs_fsb_workspace_bytes", "fs_fsb_select"]
 FS_N_STAGES = 4
 STAGE_NAMES = ["cells_prep", "prune", "select", "attention"]
 
@@ -42,7 +43,7 @@ class fs_params(ctypes.Structure):
     _fields_ = [("w", ctypes.c_int), ("s", ctypes.c_int), ("K", ctypes.c_int),
                 ("P", ctypes.c_int), ("W", ctypes.c_int), ("Bq", ctypes.c_int),
                 ("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("mode", ctypes.c_int)]
+                ("mode", ctypes.c_int), ("beam", ctypes.c_int), ("tau", ctypes.c_float)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -113,6 +114,9 @@ def load(build_if_stale: bool = True):
         L.fs_decode_state_view.argtypes = [I, I, I, PP, ctypes.POINTER(Z)]
         L.fs_qkv_workspace_bytes.argtypes = [I, I, I, I]
         L.fs_backward_workspace_bytes.argtypes = [I, I, I, I, PP]
+        L.fs_fsb_workspace_bytes.argtypes = [I, I, I, PP]
+        L.fs_fsb_workspace_bytes.restype = Z
+        L.fs_fsb_select.argtypes = [P, P, P, P, P, P, I, I, I, I, PP, P, P, Z, P]
         L.fs_backward_workspace_bytes.restype = Z
         L.fs_attention_bwd.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, P, P, P, P, P, Z, P]
         L.fs_qkv_workspace_bytes.restype = Z
@@ -124,7 +128,8 @@ def load(build_if_stale: bool = True):
                             "fs_workspace_bytes", "fs_prune_static_scratch_bytes",
                             "fs_prune_workspace_bytes", "fs_window_workspace_bytes",
                             "fs_host_workspace_bytes", "fs_decode_state_bytes",
-                            "fs_qkv_workspace_bytes", "fs_backward_workspace_bytes"):
+                            "fs_qkv_workspace_bytes", "fs_backward_workspace_bytes",
+                            "fs_fsb_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -321,6 +326,27 @@ def fs_decode_step(q_t, k_t, v_t, t, state, lam, sigma, mix, params=None, out=No
                             state.numel() * state.element_size(), _ptr(out), _ptr(sel),
                             _stream(stream)), "fs_decode_step")
     return out
+
+
+def fs_fsb_select(q, k, kbar, amax, lam, sigma, params=None, stream=None):
+    """FS-B selection (beam search over the two forests, token rerank):
+    sel [B,H,N,K] int32.  params.mode must be FS_MODE_FSB."""
+    L = load()
+    p = _params(params)
+    for t_, n in ((q, "q"), (k, "k")):
+        _dev(t_, n, (torch.bfloat16,))
+    for t_, n in ((kbar, "kbar"), (amax, "amax"), (lam, "lam"), (sigma, "sigma")):
+        _dev(t_, n, (torch.float32,))
+    B, H, N, d = _qkv_shape(q)
+    wsb = L.fs_fsb_workspace_bytes(B, H, N, ctypes.byref(p))
+    if wsb == 0:
+        raise FSError(FS_ERR_INVALID_ARG, "fs_fsb_workspace_bytes")
+    ws = torch.empty(wsb, device=q.device, dtype=torch.uint8)
+    sel = torch.empty((B, H, N, p.K), device=q.device, dtype=torch.int32)
+    _check(L.fs_fsb_select(_ptr(q), _ptr(k), _ptr(kbar), _ptr(amax), _ptr(lam), _ptr(sigma), B, H,
+                           N, d, ctypes.byref(p), _ptr(sel), _ptr(ws), wsb, _stream(stream)),
+           "fs_fsb_select")
+    return sel
 
 
 def fs_backward_workspace_bytes(batch, H, N, d=64, params=None) -> int:

@@ -68,7 +68,11 @@ def test_workspace_bytes_validation():
     assert fs.fs_workspace_bytes(0, 16, 65536, 64) == 0
     assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(P=65)) == 0
     assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(K=9)) == 0
-    assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(mode=2)) == 0
+    assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(mode=3)) == 0
+    # FS-B: its forests take workspace; beam 1..16
+    assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(mode=2)) > fs.fs_workspace_bytes(1, 16, 4096, 64)
+    assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(mode=2, beam=17)) == 0
+    assert fs.fs_workspace_bytes(1, 16, 4096, 64, dict(mode=2, beam=0)) == 0
     small = fs.fs_workspace_bytes(1, 2, 2048, 64, dtype=fs.FS_BF16)
     big = fs.fs_workspace_bytes(1, 2, 2048, 64, dtype=fs.FS_FP32)
     assert big - small >= 3 * 2 * 2048 * 64 * 2
