@@ -289,7 +289,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; lognormal key norms)",
         "config": {"workload": wl.name, "batch": B, "heads": H, "seq_len": N, "head_dim": d,
                    "w": params.w, "s": params.s, "K": params.K, "P": params.P, "W": params.W,
-                   "Bq": params.Bq, "mode": "FS-L" if params.mode == 0 else "FS",
+                   "Bq": params.Bq, "mode": ["FS-L", "FS", "FS-B"][params.mode],
                    "parallelism": f"replica x{world} (independent (batch, head) slices)",
                    "l2": "inputs larger than L2 (%.0f MB vs 129 MB)" % (in_bytes / 2**20)},
         "roofline": roof, "kernels": kernels, "e2e": e2e,
@@ -303,6 +303,7 @@ def run_ours(args, rank, world, local_rank):
         res["decode"] = time_decode(q, k, v, lam, sigma, mix, params, stream)
     if not args.no_extras:
         res["fs_mode"] = time_fs_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
+        res["fsb_mode"] = time_fsb_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
         res["prologue"] = time_prologue(B, N, H, stream)
         res["backward"] = time_backward(q, k, v, lam, sigma, mix, params, stream, counts)
     return res
@@ -372,6 +373,31 @@ def time_branches(q, k, v, mix, sel, params, stream, distinct_cells, counts, pk,
     res["sparse_readout"] = _entry(ms, nbytes, 4.0 * d * float(counts["tokens_read"]), pk, "hbm")
     del ws, out, o_long
     return res
+
+
+def time_fsb_mode(q, k, v, lam, sigma, mix, params, stream, tokens, steps=3):
+    """FS-B (beam search over the two forests, token rerank) on the same
+    inputs; tau = the median cell norm of the inputs (the pages calibrate it
+    once per model as a median cell norm)."""
+    from long_context_lm_gb300 import fs
+    from long_context_lm_gb300.fs import FS_N_STAGES
+    _, amax = fs.fs_cell_summarize(k)
+    d = {f: getattr(params, f) for f, _ in params._fields_}
+    d["mode"] = fs.FS_MODE_FSB
+    d["tau"] = float(amax.median().item())
+    B, H, N, hd = q.shape
+    ws = torch.empty(fs.fs_workspace_bytes(B, H, N, hd, d, fs.FS_BF16), device=q.device,
+                     dtype=torch.uint8)
+    out = torch.empty((B, H, N, hd), device=q.device, dtype=torch.float32)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(FS_N_STAGES + 1)]
+              for _ in range(steps + 1)]
+    for i in range(steps + 1):  # the first is a warm-up
+        fs.fs_attention_fwd_traced(q, k, v, lam, sigma, mix, events[i], d, out=out, ws=ws)
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events[1:])
+    sel_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in events[1:])
+    return {"ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3), "search_ms": sel_ms,
+            "tau": d["tau"], "beam": d["beam"], "steps": steps}
 
 
 def time_prologue(B, N, H, stream, D=1024, iters=10):

@@ -76,9 +76,12 @@ def test_fsb_select_matches_oracle(B, H, N, tau, beam, seed):
 
 
 def test_fsb_forward_matches_oracle_and_finds_needles():
-    B, H, N = 1, 2, 8192
+    # needles as in the 256k workload: a key 12x a later query, a norm well
+    # above the threshold tau, so its cell sits in the second forest and its
+    # node's largest norm leads the bound
+    B, H, N = 1, 4, 8192
     params = _params(tau=25.0)
-    inp, q, k, v, kbar, amax = _setup(B, H, N, 7, needles="uniform", n_needles=8)
+    inp, q, k, v, kbar, amax = _setup(B, H, N, 7, sigma_ln=0.5, needles="deep", n_needles=1)
     d = to_device(inp)
     ws = torch.empty(fs.fs_workspace_bytes(B, H, N, 64, params), device="cuda", dtype=torch.uint8)
     out = fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], params,
@@ -106,4 +109,4 @@ def test_fsb_forward_matches_oracle_and_finds_needles():
     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
     # planted needles: the needle's cell is selected by its query
     hits = [p // 32 in gsel[b * H + h, j].tolist() for (b, h, p, j) in inp.needles]
-    assert np.mean(hits) >= 0.75, hits
+    assert all(hits), (hits, inp.needles)
