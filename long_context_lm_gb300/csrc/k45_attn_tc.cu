@@ -125,9 +125,6 @@ struct Params {
   const float *mix;
   const float2 *tab;       // (cos, sin) of r*theta_i (rows r < 64), 64*u*theta_i (row 64 + u)
   int H, N, w, K, nblk, nitems;
-  int has_window, has_long, write_long;  // write_long: output RMSNorm(o_long) only
-  int long16;              // long-branch P in fp16 against the fp16 values (the
-                           // window's encoding); else bf16 hi + lo against raw v
   float rms_eps;
   size_t nrows;            // BH * N (first out-of-range key row: zero fill)
   float *out;
@@ -138,19 +135,38 @@ __device__ __forceinline__ bool wait_nth(uint64_t *bar, uint32_t k, int *err) {
   return tc::mbar_wait(bar, k & 1, err);
 }
 
+// The kernel is compiled once per configuration, so that each carries only
+// the code of its own branches:
+//   kLongOnly  the long branch alone, written as RMSNorm(o_long) (bf16 hi + lo
+//              P against the raw bf16 values)
+//   kWindow    the window branch, plus mix_h times a long-branch output read
+//              from memory if one is given
+//   kFused     both branches; the long-branch P in fp16 against the fp16
+//              values the window branch uses
+enum Mode { kLongOnly = 0, kWindow = 1, kFused = 2 };
+template <int M>
+struct Flags {
+  static constexpr bool window = M != kLongOnly;
+  static constexpr bool lng = M != kWindow;
+  static constexpr bool long16 = M == kFused;
+  static constexpr bool write_long = M == kLongOnly;
+};
+
 struct Item {
   int bh, b0, kt0, nw;  // nw: window tiles
 };
+template <int M>
 __device__ __forceinline__ Item item_of(const Params &p, int g) {
   Item it;
   it.bh = g / p.nblk;
   it.b0 = (g % p.nblk) * kBq;
   it.kt0 = max(0, it.b0 - p.w + 1) / kKT * kKT;
-  it.nw = p.has_window ? (it.b0 + kBq - it.kt0) / kKT : 0;
+  it.nw = Flags<M>::window ? (it.b0 + kBq - it.kt0) / kKT : 0;
   return it;
 }
-__device__ __forceinline__ int long_tiles(const Barriers &bar, const Params &p) {
-  return p.has_long ? (bar.nu + 3) / 4 : 0;
+template <int M>
+__device__ __forceinline__ int long_tiles(const Barriers &bar) {
+  return Flags<M>::lng ? (bar.nu + 3) / 4 : 0;
 }
 
 // --------------------------------------------------------------------------
@@ -220,19 +236,20 @@ __device__ __forceinline__ void rotate_row(unsigned char *hi, unsigned char *lo,
 // roles
 // --------------------------------------------------------------------------
 
+template <int M>
 __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t base) {
   const uint32_t id_qk = tc::idesc_bf16(128, kKT, 0);
   const uint64_t dqh = tc::desc_sw128(base + kOffQ), dql = tc::desc_sw128(base + kOffQ + 16384);
   const uint64_t dqr = tc::desc_sw128(base + kOffQR);
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
+    const Item it = item_of<M>(p, g);
     if (!wait_nth(&bar.q_full, i, p.err)) return;
     int nl = 0;
     for (int t = 0;; ++t, ++T) {
       if (t == it.nw) {  // the window tiles do not wait for the union
         if (!wait_nth(&bar.u_full, i, p.err)) return;
-        nl = long_tiles(bar, p);
+        nl = long_tiles<M>(bar);
         tc::mbar_arrive(&bar.u_free);
       }
       if (t >= it.nw + nl) break;
@@ -268,12 +285,13 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
 // The P.V MMA loops stay rolled: the issuing thread waits on the tensor pipe
 // either way, and the smaller loop body leaves more of the instruction cache
 // to the softmax warps that share its SMSP (measured: 5% faster attention).
+template <int M>
 __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t base) {
   const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);  // long: bf16 P hi / lo, bf16 V
   const uint32_t id_pv_h = tc::idesc_f16(128, kD, 1);  // window (and long16): fp16 P, V
   uint32_t T = 0, i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
+    const Item it = item_of<M>(p, g);
     const uint32_t ob = tmem + kColO + 128 * (i & 1);
     // an accumulator set is reused once the epilogue two q-tiles back has read it
     if (i >= 2 && !wait_nth(&bar.o_free[i & 1], (i - 2) >> 1, p.err)) return;
@@ -281,7 +299,7 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
     for (int t = 0;; ++t, ++T) {
       if (t == it.nw) {
         if (!wait_nth(&bar.u_full, i, p.err)) return;
-        nl = long_tiles(bar, p);
+        nl = long_tiles<M>(bar);
         tc::mbar_arrive(&bar.u_free);
       }
       if (t >= it.nw + nl) break;
@@ -297,7 +315,7 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
         for (int k = 0; k < kKT / 16; ++k)
           tc::mma_ts(ob, sp + p_col(k), dv + (uint64_t)(k * 128), id_pv_h,
                      (t > 0 || k > 0) ? 1u : 0u);
-      } else if (p.long16) {
+      } else if (Flags<M>::long16) {
         const bool first = t == it.nw;
 #pragma unroll 1
         for (int k = 0; k < kKT / 16; ++k)
@@ -328,19 +346,20 @@ __device__ void drain_tma(Barriers &bar, uint32_t issued) {
     tc::mbar_wait(&bar.raw_full[T % kRing], T / kRing, nullptr);
 }
 
+template <int M>
 __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
                          const CUtensorMap *tkt, const CUtensorMap *tv16, const CUtensorMap *ck,
                          const CUtensorMap *cv) {
   uint32_t T = 0, i = 0;
   const int *ul = reinterpret_cast<const int *>(smem + kOffUL);
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
+    const Item it = item_of<M>(p, g);
     const int row0 = it.bh * p.N;
     int nl = 0;
     for (int t = 0;; ++t, ++T) {
       if (t == it.nw) {
         if (!wait_nth(&bar.u_full, i, p.err)) return drain_tma(bar, T);
-        nl = long_tiles(bar, p);
+        nl = long_tiles<M>(bar);
       }
       if (t >= it.nw + nl) break;
       const int slot = T % kRing;
@@ -377,16 +396,17 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
 // Union of the q-tile's selected cells, sorted ascending, by repeated
 // extraction of the smallest remaining id (cheap: the union is small); each
 // selection's slot in the union is recorded for the softmax masks.
+template <int M>
 __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) {
   const int lane = threadIdx.x & 31;
   int *ul = reinterpret_cast<int *>(smem + kOffUL);
   uint16_t *rs = reinterpret_cast<uint16_t *>(smem + kOffRS);
   uint32_t i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
+    const Item it = item_of<M>(p, g);
     if (i > 0 && !wait_nth(&bar.u_free, i - 1, p.err)) return;
     int nu = 0;
-    if (p.has_long) {
+    if (Flags<M>::lng) {
       const int A = it.b0 / kS;  // cells ending at or before the block start
       const int nsel = kBq * p.K;
       const int32_t *src = p.sel + ((size_t)it.bh * p.N + it.b0) * p.K;
@@ -421,6 +441,7 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   }
 }
 
+template <int M>
 __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int g, uint32_t i,
                               int r);
 
@@ -428,6 +449,7 @@ __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int
 // and, for the window, rotated by its absolute position and split into bf16
 // hi / lo; after staging q-tile i, the epilogue of q-tile i-1.  One pass
 // past the last q-tile runs the last epilogue.
+template <int M>
 __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, uint32_t tmem,
                            int r) {
   uint32_t i = 0;
@@ -435,7 +457,7 @@ __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, 
   for (int g = blockIdx.x;; g += gridDim.x, ++i) {
     const bool real = g < p.nitems;
     if (real) {
-      const Item it = item_of(p, g);
+      const Item it = item_of<M>(p, g);
       // fetch the row first, then wait until the previous q-tile's S MMAs no
       // longer read the query tiles
       const uint4 *src =
@@ -447,7 +469,7 @@ __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, 
       unsigned char *qh = smem + kOffQ, *qr = smem + kOffQR;
 #pragma unroll
       for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qr + swz128(r, c)) = raw[c];
-      if (p.has_window) {
+      if (Flags<M>::window) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(qh + swz128(r, c)) = raw[c];
         rotate_row(qh, qh + 16384, r, it.b0 + r, smem, p.tab);
@@ -455,7 +477,7 @@ __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, 
       tc::fence_async_smem();
       tc::mbar_arrive(&bar.q_full);
     }
-    if (g_prev >= 0 && !epilogue_rows(p, bar, tmem, g_prev, i - 1, r)) return;
+    if (g_prev >= 0 && !epilogue_rows<M>(p, bar, tmem, g_prev, i - 1, r)) return;
     if (!real) break;
     g_prev = g;
   }
@@ -571,9 +593,10 @@ __device__ __forceinline__ void rescale(uint32_t addr, float alpha) {
 // columns: O_long / l_long and its RMSNorm, O_win / l_win, the mix, the
 // store.  The softmax warps have moved on to the next q-tile; the P.V
 // issuer reuses this accumulator set only for the q-tile after that.
+template <int M>
 __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int g, uint32_t i,
                               int r) {
-  const Item it = item_of(p, g);
+  const Item it = item_of<M>(p, g);
   const int lane = r & 31, par = i & 1;
   const uint32_t lane_base = (uint32_t)(r & ~31) << 16;
   if (!wait_nth(&bar.o_done[par], i >> 1, p.err)) return false;
@@ -583,8 +606,8 @@ __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int
   const int nl = bar.item_nl[par];
   const float lw = s0.x + s1.x, ll = s0.y + s1.y;
   const uint32_t ow = tmem + kColO + 128 * par + lane_base, ol = ow + 64;
-  const bool load_long = p.has_long && nl > 0;      // the whole warp (same q-tile)
-  const bool use_win = !p.write_long && it.nw > 0;  // the whole warp
+  const bool load_long = Flags<M>::lng && nl > 0;      // the whole warp (same q-tile)
+  const bool use_win = !Flags<M>::write_long && it.nw > 0;  // the whole warp
   const float invl = ll > 0.f ? 1.f / ll : 0.f;
   float lo_scale = 0.f;
   if (load_long) {
@@ -608,9 +631,9 @@ __device__ bool epilogue_rows(const Params &p, Barriers &bar, uint32_t tmem, int
   float4 *dst = reinterpret_cast<float4 *>(p.out + row * kD);
   const float mh = p.mix ? p.mix[it.bh % p.H] : 0.f;
   const bool use_long = lo_scale != 0.f;  // this row
-  const float4 *oin = (!p.write_long && !use_long && p.o_long_in)
+  const float4 *oin = (!Flags<M>::write_long && !use_long && p.o_long_in)
       ? reinterpret_cast<const float4 *>(p.o_long_in + row * kD) : nullptr;
-  const float ls = p.write_long ? lo_scale : mh * lo_scale;
+  const float ls = Flags<M>::write_long ? lo_scale : mh * lo_scale;
 #pragma unroll 1
   for (int c16 = 0; c16 < kD / 16; ++c16) {
     uint32_t w[16], l16[16];
@@ -673,6 +696,7 @@ __device__ __forceinline__ bool tile_cols(const Params &p, const Item &it, int t
   return __any_sync(0xffffffffu, cell[0] || cell[1]);
 }
 
+template <int M>
 __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsigned char *smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, half = warp >> 2;
@@ -683,7 +707,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
   uint32_t T = 0, i = 0;
   Pair pr{&bar.pair[quarter], bar.xch, 0u};
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
-    const Item it = item_of(p, g);
+    const Item it = item_of<M>(p, g);
     const int n = it.b0 + r;
     const uint32_t ow_addr = tmem + kColO + 128 * (i & 1) + 32 * half + lane_base;
     float mw = -INFINITY, lw = 0.f, ml = -INFINITY, ll = 0.f;
@@ -692,7 +716,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
     for (int t = 0;; ++t, ++T) {
       if (t == it.nw) {
         if (!wait_nth(&bar.u_full, i, p.err)) return;
-        nl = long_tiles(bar, p);
+        nl = long_tiles<M>(bar);
 #pragma unroll
         for (int k = 0; k < kMaxK / 2; ++k) {
           const uint32_t a = (2 * k < p.K) ? rs[r * p.K + 2 * k] : 0xffffu;
@@ -705,7 +729,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
       const bool done = t >= it.nw + nl;
       if (!done) {
         const bool is_long = t >= it.nw;
-        const bool split = is_long && !p.long16;  // bf16 hi + lo P
+        const bool split = is_long && !Flags<M>::long16;  // bf16 hi + lo P
         const int b = T & 1;
         const uint32_t s_addr = tmem + kColS + 128 * b + 64 * half + lane_base;
         if (!wait_nth(&bar.s_full[b], T / 2, p.err)) return;
@@ -814,6 +838,7 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
   }
 }
 
+template <int M>
 __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_kt, const __grid_constant__ CUtensorMap tmap_v16,
     const __grid_constant__ CUtensorMap cmap_k, const __grid_constant__ CUtensorMap cmap_v,
@@ -855,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     tc::tmem_relinquish();
   }
   // rows r*theta (r < 64) of the angle table, staged once per CTA (window only)
-  if (threadIdx.x >= kRotBase && p.has_window) {
+  if (threadIdx.x >= kRotBase && Flags<M>::window) {
     const float4 *tab = reinterpret_cast<const float4 *>(p.tab);
     for (int i = threadIdx.x - kRotBase; i < 64 * 16; i += kRotThreads) {
       const int row = i >> 4, part = i & 15;
@@ -877,28 +902,28 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
   // its own count.
   if (warp < 8) {
     tc::regs_inc<168>();
-    role_softmax(p, bar, tmem, smem);
+    role_softmax<M>(p, bar, tmem, smem);
   } else if (warp < 12) {
     tc::regs_dec<72>();
     if (warp == 8 || warp == 9) {
       if (lane == 0) {
         if (warp == 8)
-          role_qk(p, bar, tmem, sbase);
+          role_qk<M>(p, bar, tmem, sbase);
         else
-          role_pv(p, bar, tmem, sbase);
+          role_pv<M>(p, bar, tmem, sbase);
         // every MMA this thread issued has completed before TMEM is released
         // (bounded by time only, even after an error was recorded)
         tc::mma_commit(&bar.fin[warp - 8]);
         tc::mbar_wait(&bar.fin[warp - 8], 0, nullptr);
       }
     } else if (warp == 10) {
-      if (lane == 0) role_tma(p, bar, smem, &tmap_kt, &tmap_v16, &cmap_k, &cmap_v);
+      if (lane == 0) role_tma<M>(p, bar, smem, &tmap_kt, &tmap_v16, &cmap_k, &cmap_v);
     } else {
-      role_union(p, bar, smem);
+      role_union<M>(p, bar, smem);
     }
   } else {
     tc::regs_dec<104>();
-    role_qprep(p, bar, smem, tmem, threadIdx.x - kRotBase);
+    role_qprep<M>(p, bar, smem, tmem, threadIdx.x - kRotBase);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -982,19 +1007,25 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   p.K = a.K;
   p.nblk = sh.nblk();
   p.nitems = sh.BH() * sh.nblk();
-  p.has_window = a.window ? 1 : 0;
-  p.has_long = a.sel ? 1 : 0;
-  p.write_long = a.write_long ? 1 : 0;
-  p.long16 = long16 ? 1 : 0;
   p.rms_eps = a.rms_eps;
   p.nrows = nrows;
   p.out = a.out;
   p.err = a.err;
-  cudaError_t e = cudaFuncSetAttribute(fs_attn_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  // the three configurations the entry points use
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Params);
+  if (a.window && a.sel && !a.write_long)
+    kern = fs_attn_tc_kernel<kFused>;
+  else if (a.window && !a.sel && !a.write_long)
+    kern = fs_attn_tc_kernel<kWindow>;
+  else if (!a.window && a.sel && a.write_long)
+    kern = fs_attn_tc_kernel<kLongOnly>;
+  else
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.nitems < sm_count() ? p.nitems : sm_count();
-  fs_attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mkt, mv16, ck, cv, p);
+  kern<<<grid, kThreads, kSmemBytes, st>>>(mkt, mv16, ck, cv, p);
   return cudaGetLastError();
 }
 
