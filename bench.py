@@ -396,8 +396,32 @@ def time_fsb_mode(q, k, v, lam, sigma, mix, params, stream, tokens, steps=3):
     torch.cuda.synchronize()
     ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events[1:])
     sel_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in events[1:])
+    # the search's work at full beams and a full union (the design's maximum
+    # per query): per forest level 2 * beam node bounds (a 64-term dot with
+    # the node mean, 256 B of mean + 16 B of node data), then the token LSE of
+    # 2 * beam cells (32 x 64-term dots, 4 KB of keys each).  Forest sizes are
+    # the inputs' own: A cells before the block, and of those the ones above
+    # tau.
+    am = amax.reshape(B * H, -1).float()
+    above = torch.cumsum((am > d["tau"]).to(torch.int64), dim=1).cpu().numpy()
+    nb = N // 128
+    A = np.arange(nb) * 4
+    m1 = np.where(A > 0, above[:, np.maximum(A - 1, 0)], 0)  # [BH, nb]
+    lv = lambda m: np.where(m > 1, np.ceil(np.log2(np.maximum(m, 1))), 0.0)
+    levels = lv(A)[None, :] + lv(m1)  # per (head, block)
+    nodes = 128.0 * float((levels * 2 * d["beam"]).sum())
+    union = 128.0 * float(((A[None, :] > 0) * 2 * d["beam"]).sum())
+    fma = nodes * 64 + union * 32 * 64
+    l2 = nodes * (256 + 16) + union * 32 * 64 * 2
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12  # TFLOP/s, fp32 FMA
+    ach = 2 * fma / (sel_ms / 1e3) / 1e12
     return {"ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3), "search_ms": sel_ms,
-            "tau": d["tau"], "beam": d["beam"], "steps": steps}
+            "tau": d["tau"], "beam": d["beam"], "steps": steps,
+            "search_roofline": {"bound": "alu", "achieved_TFLOP/s": ach, "peak_TFLOP/s": peak,
+                                "frac": ach / peak, "l2_GB/s": l2 / (sel_ms / 1e3) / 1e9,
+                                "note": "work at full beams and union (an upper bound on the "
+                                        "executed work); a warp per query reading node means "
+                                        "and candidate keys through L2"}}
 
 
 def time_prologue(B, N, H, stream, D=1024, iters=10):
@@ -478,7 +502,19 @@ def time_decode(q, k, v, lam, sigma, mix, params, stream, steps=256, warm=8):
     torch.cuda.synchronize()
     fs.fs_check_status(state)
     us = a.elapsed_time(b) / steps * 1e3
-    return {"t0": N + warm, "us_per_token": us, "heads": B * H, "steps": steps,
+    # one step of one (batch, head) reads the new q, k, v (bf16), the window's
+    # keys and values (bf16), the candidates' summaries (mean key fp32 and
+    # norm) and the K selected cells' keys and values, and writes the output
+    # (fp32) and the new token's ring entry
+    cap = params.P + params.W
+    step_bytes = (3 * d * 2 + params.w * d * 2 * 2 + cap * (d * 4 + 4)
+                  + params.K * 32 * d * 2 * 2 + d * 4 + d * 2 * 2)
+    pk = peaks()
+    gbs = B * H * step_bytes / (us / 1e6) / 1e9
+    roof = {"bound": "hbm", "bytes_per_head_step": step_bytes, "GB/s": gbs,
+            "hbm_frac": gbs / pk["hbm"],
+            "note": "one CTA per (batch, head): latency-bound, not bandwidth-bound"}
+    return {"t0": N + warm, "us_per_token": us, "heads": B * H, "steps": steps, "roofline": roof,
             "state_bytes": state.numel(), "state_bytes_per_head": state.numel() / (B * H),
             "note": "bounded state from the prefill; graph of consecutive steps, all (batch, head)"}
 
@@ -501,8 +537,17 @@ def time_fs_mode(q, k, v, lam, sigma, mix, params, stream, tokens, steps=3):
     torch.cuda.synchronize()
     ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events[1:])
     sel_ms = statistics.mean(ev[2].elapsed_time(ev[3]) for ev in events[1:])
+    # select with every available cell a candidate: each query scores the
+    # A = 4 * block cells before its block (flops: q . kbar per candidate);
+    # bytes: q, every head's mean keys once, sel out
+    nb = N // 128
+    cands = B * H * 128.0 * float((np.arange(nb) * 4).sum())
+    pk = peaks()
+    sel = _entry(sel_ms, B * H * N * hd * 2 + B * H * (N // 32) * (hd * 4 + 4) + B * H * N * d["K"] * 4,
+                 2.0 * hd * cands, pk, "tensor")
+    sel["candidates"] = cands
     return {"ms_per_step": ms, "tokens_per_s": tokens / (ms / 1e3), "select_ms": sel_ms,
-            "steps": steps}
+            "select": sel, "steps": steps}
 
 
 # ---------------------------------------------------------------------------
