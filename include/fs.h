@@ -128,16 +128,18 @@ int fs_prune_cells(const float *amax, int batch, int H, int N,
  * small streaming cache).  The state is one caller-owned device buffer of
  * fs_decode_state_bytes() bytes whose size does not depend on the position:
  *  - a 256-byte header whose first int is the error word (fs_check_status
- *    reads it) and the relative-angle tables of the window branch;
- *  - per (batch, head): a w-row ring of the last keys and values, P + W +
+ *    reads it), then theta_i / pi (fp64) for the rotations;
+ *  - per (batch, head): a w-row ring of the last keys (fp32, rotated by
+ *    their absolute position, so that a step rotates only its query) and
+ *    values (bf16), P + W +
  *    Bq/s + 1 cell slots (raw keys and values of one cell, its mean key and
  *    largest key norm), and the lists that place the slots: the W recent
  *    cells, the running top-P older cells (a_c desc, c asc), the closed cells
  *    not yet available, the open cell, the free slots.
  * A cell stays in its slot from its first token until it leaves the pool; a
  * cell dropped from the top P is never needed again (the threshold only
- * rises), so its slot is reused.  Decoding supports w <= 512 (the window is
- * staged in shared memory), FS-L mode only, P + W <= 72, K <= 8. */
+ * rises), so its slot is reused.  Decoding supports w <= 512 (the window's
+ * values are staged in shared memory), FS-L mode only, P + W <= 72, K <= 8. */
 size_t fs_decode_state_bytes(int batch, int H, int d, const fs_params *p);
 
 /* Layout of a decode state, for inspection: offs receives 7 values --

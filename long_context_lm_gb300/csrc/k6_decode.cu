@@ -65,13 +65,13 @@ DecodeLayout decode_layout(int w, int P, int W, int K) {
   off = up(off + (size_t)L.nslots * kS * kD * 2);
   L.slot_v = off;
   off = up(off + (size_t)L.nslots * kS * kD * 2);
-  L.ring_k = off;
-  off = up(off + (size_t)w * kD * 2);
+  L.ring_k = off;  // rotated by absolute position, fp32
+  off = up(off + (size_t)w * kD * 4);
   L.ring_v = off;
   off = up(off + (size_t)w * kD * 2);
   L.head_bytes = off;
-  L.tab = 256;  // after the error word's 256-byte header
-  L.global_bytes = up(L.tab + (size_t)kDecodeTabRows * (kD / 2) * 8);
+  L.tab = 256;  // after the error word's 256-byte header: theta_i / pi (fp64)
+  L.global_bytes = up(L.tab + (size_t)(kD / 2) * 8);
   return L;
 }
 
@@ -99,6 +99,23 @@ struct StepParams {
 };
 
 __device__ __forceinline__ float bf16f(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+// (cos, sin) of pos * theta_i, th_pi = theta_i / pi: the product and its
+// reduction modulo 2 in fp64 (exact to about 2^-29 at pos < 2^24), then the
+// fp32 sine and cosine of pi times the reduced value
+__device__ __forceinline__ float2 angle_cs(double th_pi, int pos) {
+  const double x = (double)pos * th_pi;
+  const double red = x - 2.0 * floor(0.5 * x);
+  float sn, cs;
+  sincospif((float)red, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+// R(angles) on the pairs (i, i + d/2) of x, i < d/2: (x cos - y sin, x sin + y cos)
+__device__ __forceinline__ void rotate_pair(float x0, float x1, float2 cs, float &y0, float &y1) {
+  y0 = fmaf(x0, cs.x, -x1 * cs.y);
+  y1 = fmaf(x0, cs.y, x1 * cs.x);
+}
 
 __device__ __forceinline__ bool ranks_before(float a, int c, float a2, int c2) {
   return a > a2 || (a == a2 && c < c2);
@@ -158,32 +175,35 @@ __device__ __forceinline__ float sum_parts(const float2 (*part)[kD / 2], int dim
 __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p) {
   extern __shared__ __align__(1024) unsigned char dsm[];
   const DecodeLayout &L = p.L;
-  // dynamic shared memory: ring keys, ring values, slot summaries, the
-  // selected cells' keys and values
-  unsigned char *s_rk = dsm;
-  unsigned char *s_rv = s_rk + (size_t)L.w * kD * 2;
+  // dynamic shared memory: ring values, slot summaries, the selected cells'
+  // keys and values (the window's keys are read from the state directly)
+  unsigned char *s_rv = dsm;
   float *s_kbar = reinterpret_cast<float *>(s_rv + (size_t)L.w * kD * 2);
   float *s_amax = s_kbar + (size_t)L.nslots * kD;
   int *s_cell = reinterpret_cast<int *>(s_amax + (L.nslots + 3) / 4 * 4);
   unsigned char *s_ck = reinterpret_cast<unsigned char *>(s_cell + (L.nslots + 3) / 4 * 4);
   unsigned char *s_cv = s_ck + (size_t)L.K * kS * kD * 2;
 
-  __shared__ __align__(8) uint64_t barA, barB;
+  __shared__ __align__(8) uint64_t barA, barB, barC;
   __shared__ int s_hdr[kDecodeHeaderInts];
-  __shared__ float s_q[kD], s_k[kD], s_v[kD];
+  __shared__ float s_q[kD], s_k[kD];
+  __shared__ float s_qr[kD], s_kr[kD];  // R(t) q_t, R(t) k_t
   __shared__ int s_pool[kMaxP + 8];
   __shared__ float s_u[kMaxP + 8];
+  __shared__ int s_rank[3][kMaxP + 8];
+  __shared__ int s_pc[kMaxP + 8];
   __shared__ int s_sel[kMaxK], s_selc[kMaxK];
   __shared__ float s_w[1024];
   __shared__ float2 s_part[kThreads / 32][kD / 2];
   __shared__ float s_olong[kD];
+  __shared__ float s_wm[kThreads / 32], s_wl[kThreads / 32];  // per warp: window max, sum
   __shared__ float s_red[8];
   __shared__ int s_ok;
 
   const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = bh % p.H, t = p.t;
   int *err = reinterpret_cast<int *>(p.state);
-  const float2 *tab = reinterpret_cast<const float2 *>(p.state + L.tab);
+  const double *th_pi = reinterpret_cast<const double *>(p.state + L.tab);
   unsigned char *hs = p.state + L.global_bytes + (size_t)bh * L.head_bytes;
   int *g_hdr = reinterpret_cast<int *>(hs + L.hdr);
   int *g_cell = reinterpret_cast<int *>(hs + L.slot_cell);
@@ -191,25 +211,27 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
   float *g_kbar = reinterpret_cast<float *>(hs + L.slot_kbar);
   uint16_t *g_sk = reinterpret_cast<uint16_t *>(hs + L.slot_k);
   uint16_t *g_sv = reinterpret_cast<uint16_t *>(hs + L.slot_v);
-  uint16_t *g_rk = reinterpret_cast<uint16_t *>(hs + L.ring_k);
+  float *g_rk = reinterpret_cast<float *>(hs + L.ring_k);
   uint16_t *g_rv = reinterpret_cast<uint16_t *>(hs + L.ring_v);
   const size_t cell_bytes = (size_t)kS * kD * 2;
 
-  // ---- stage the ring and the slot summaries (bulk copies, one barrier)
+  // ---- stage the slot summaries (barA, needed first) and the ring's values
+  // (barC, needed only by the window's P.V): bulk copies
   if (tid == 0) {
     tc::mbar_init(&barA, 1);
     tc::mbar_init(&barB, 1);
+    tc::mbar_init(&barC, 1);
     tc::mbar_fence_init();
     const uint32_t ring = (uint32_t)L.w * kD * 2;
     const uint32_t sums = (uint32_t)L.nslots * kD * 4;
     const uint32_t small = (uint32_t)(L.nslots + 3) / 4 * 16;
-    tc::mbar_arrive_expect_tx(&barA, 2 * ring + sums + 2 * small);
+    tc::mbar_arrive_expect_tx(&barA, sums + 2 * small);
+    tc::mbar_arrive_expect_tx(&barC, ring);
+    tc::bulk_load(s_kbar, g_kbar, sums, &barA);
     for (uint32_t o = 0; o < ring; o += 32768) {
       const uint32_t n = ring - o < 32768 ? ring - o : 32768;
-      tc::bulk_load(s_rk + o, reinterpret_cast<const unsigned char *>(g_rk) + o, n, &barA);
-      tc::bulk_load(s_rv + o, reinterpret_cast<const unsigned char *>(g_rv) + o, n, &barA);
+      tc::bulk_load(s_rv + o, reinterpret_cast<const unsigned char *>(g_rv) + o, n, &barC);
     }
-    tc::bulk_load(s_kbar, g_kbar, sums, &barA);
     tc::bulk_load(s_amax, g_amax, small, &barA);
     tc::bulk_load(s_cell, g_cell, small, &barA);
   }
@@ -217,14 +239,21 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
   if (tid < kD) {
     s_q[tid] = bf16f(p.q_t[(size_t)bh * kD + tid]);
     s_k[tid] = bf16f(p.k_t[(size_t)bh * kD + tid]);
-    s_v[tid] = bf16f(p.v_t[(size_t)bh * kD + tid]);
   }
   __syncthreads();
+  // the query and the new key rotated by the absolute position t: the window
+  // score R(t) q . R(j) k equals q . R(j - t) k
+  if (tid < kD / 2) {
+    const float2 cs = angle_cs(th_pi[tid], t);
+    rotate_pair(s_q[tid], s_q[tid + kD / 2], cs, s_qr[tid], s_qr[tid + kD / 2]);
+    rotate_pair(s_k[tid], s_k[tid + kD / 2], cs, s_kr[tid], s_kr[tid + kD / 2]);
+  }
   // the state must be at position t (every copy is awaited before an exit)
   const bool in_step = s_hdr[kHT] == t;
   const bool staged = tc::mbar_wait(&barA, 0, err);
   if (!in_step || !staged) {
     if (tid == 0 && !in_step) tc::report_error(err, FS_ERR_STATE);
+    tc::mbar_wait(&barC, 0, nullptr);  // no copy in flight at exit (bounded by time)
     return;
   }
 
@@ -269,44 +298,73 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
     s_ok = s_hdr[kHOpen] >= 0;
   }
   __syncthreads();
-  if (!s_ok) return;  // a state that lost track of its slots is left as it was
+  if (!s_ok) {  // a state that lost track of its slots is left as it was
+    tc::mbar_wait(&barC, 0, nullptr);
+    return;
+  }
   const int open = s_hdr[kHOpen];
   // ---- 2. the new token: ring row t mod w and the open slot's row t mod s
   if (tid < 8) {
     const uint4 kv = reinterpret_cast<const uint4 *>(p.k_t + (size_t)bh * kD)[tid];
-    reinterpret_cast<uint4 *>(g_rk + (size_t)(t % L.w) * kD)[tid] = kv;
     reinterpret_cast<uint4 *>(g_sk + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[tid] = kv;
-    reinterpret_cast<uint4 *>(s_rk + (size_t)(t % L.w) * kD * 2)[tid] = kv;
+  } else if (tid >= 32 && tid < 48) {  // the rotated key, fp32, to ring row t mod w
+    const int c = tid - 32;
+    reinterpret_cast<float4 *>(g_rk + (size_t)(t % L.w) * kD)[c] =
+        make_float4(s_kr[4 * c], s_kr[4 * c + 1], s_kr[4 * c + 2], s_kr[4 * c + 3]);
   } else if (tid < 16) {
     const int c = tid - 8;
     const uint4 vv = reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[c];
     reinterpret_cast<uint4 *>(g_rv + (size_t)(t % L.w) * kD)[c] = vv;
     reinterpret_cast<uint4 *>(g_sv + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[c] = vv;
-    reinterpret_cast<uint4 *>(s_rv + (size_t)(t % L.w) * kD * 2)[c] = vv;
   }
 
   // ---- 3a. score the pool: u = q . kbar_c + lambda * a_c * erf(sigma (t - p_c) / s)
   const int nrec = s_hdr[kHRecent], nc = nrec + s_hdr[kHTop];
-  if (tid < nc) s_pool[tid] = tid < nrec ? s_hdr[kLRecent + tid] : s_hdr[kLTop + tid - nrec];
+  if (tid < nc) {
+    s_pool[tid] = tid < nrec ? s_hdr[kLRecent + tid] : s_hdr[kLTop + tid - nrec];
+    s_pc[tid] = s_cell[s_pool[tid]];  // the candidate's cell id
+  }
   __syncthreads();
   const float lam = p.lambda[h], sig = p.sigma[h];
-  for (int i = warp; i < nc; i += kThreads / 32) {
-    const int slot = s_pool[i];
-    const float2 kb = reinterpret_cast<const float2 *>(s_kbar + (size_t)slot * kD)[lane];
-    const float dot = warp_sum(fmaf(s_q[2 * lane], kb.x, s_q[2 * lane + 1] * kb.y));
-    if (lane == 0) {
+  // four lanes per candidate (16 dimensions each), eight candidates per warp
+  for (int i0 = warp * 8; i0 < nc; i0 += kThreads / 4) {
+    const int i = i0 + (lane >> 2), sub = lane & 3;
+    float dot = 0.f;
+    int slot = 0;
+    if (i < nc) {
+      slot = s_pool[i];
+      const float4 *kb = reinterpret_cast<const float4 *>(s_kbar + (size_t)slot * kD + 16 * sub);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 x = kb[c];
+        const float *qq = s_q + 16 * sub + 4 * c;
+        dot = fmaf(qq[0], x.x, fmaf(qq[1], x.y, fmaf(qq[2], x.z, fmaf(qq[3], x.w, dot))));
+      }
+    }
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    if (i < nc && sub == 0) {
       const float pc = (float)(s_cell[slot] * kS) + 0.5f * kS;
       s_u[i] = dot + lam * s_amax[slot] * erff(sig * ((float)t - pc) / kS);
     }
   }
   if (tid < kMaxK) s_sel[tid] = -1;
   __syncthreads();
-  // top K by (u desc, c asc): rank of each candidate by counting
-  if (tid < nc) {
-    const float u = s_u[tid];
-    const int c = s_cell[s_pool[tid]];
+  // top K by (u desc, c asc): rank of each candidate by counting, the
+  // comparisons split in three ranges of j
+  const int third = (nc + 2) / 3;
+  if (tid < 3 * nc) {
+    const int i = tid % nc, part = tid / nc;
+    const float u = s_u[i];
+    const int c = s_pc[i];
     int rank = 0;
-    for (int j = 0; j < nc; ++j) rank += ranks_before(s_u[j], s_cell[s_pool[j]], u, c);
+    for (int j = part * third; j < min(nc, (part + 1) * third); ++j)
+      rank += ranks_before(s_u[j], s_pc[j], u, c);
+    s_rank[part][i] = rank;
+  }
+  __syncthreads();
+  if (tid < nc) {
+    const int rank = s_rank[0][tid] + s_rank[1][tid] + s_rank[2][tid];
     if (rank < L.K) s_sel[rank] = s_pool[tid];
   }
   __syncthreads();
@@ -327,51 +385,100 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
     }
   }
 
-  // ---- 3c. RoPE window over rows [t - w + 1, t] (a5), while the cells land
+  // ---- 3c. RoPE window over rows [t - w + 1, t] (a5), while the cells land.
+  // Warp w takes keys i in [64w, 64w + 64): R(j) k_j from the ring (fp32)
+  // against R(t) q_t, four lanes per key (a contiguous 64-byte slice each),
+  // then its own softmax and P.V; the eight partials meet once.
   const int j0 = max(0, t - L.w + 1), nwin = t - j0 + 1;
-  float mloc = -INFINITY;
-  for (int i = tid; i < nwin; i += kThreads) {
-    const int j = j0 + i, o = t - j;  // R(j - t) = R(-o)
-    const uint4 *kr = reinterpret_cast<const uint4 *>(s_rk + (size_t)(j % L.w) * kD * 2);
-    float kx[kD];
+  const int r0 = j0 % L.w;  // ring row of key i: r0 + i, less w past the end
+  const auto ring_row = [&](int i) { const int rr = r0 + i; return rr >= L.w ? rr - L.w : rr; };
+  float dots[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 x = kr[c];
-      const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+  for (int h2 = 0; h2 < 2; ++h2) {
+    float4 xs[4][4];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        kx[8 * c + 2 * jj] = bf16_lo(wv[jj]);
-        kx[8 * c + 2 * jj + 1] = bf16_hi(wv[jj]);
+    for (int it = 0; it < 4; ++it) {  // every load of four key groups in flight at once
+      const int i = warp * 64 + (4 * h2 + it) * 8 + (lane >> 2);
+      if (i < nwin) {
+        const float4 *kr = reinterpret_cast<const float4 *>(
+            g_rk + (size_t)ring_row(i) * kD + 16 * (lane & 3));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) xs[it][c] = kr[c];
       }
     }
-    const float2 *tr = tab + (size_t)(o & 63) * (kD / 2);
-    const float2 *ta = tab + (size_t)(64 + (o >> 6)) * (kD / 2);
-    float dot = 0.f;
 #pragma unroll
-    for (int k = 0; k < kD / 2; ++k) {
-      // cos / sin of o*theta by the angle sum, then of -o*theta
-      const float2 a = __ldg(tr + k), b = __ldg(ta + k);
-      const float c = fmaf(a.x, b.x, -a.y * b.y), s = -fmaf(a.y, b.x, a.x * b.y);
-      const float y0 = fmaf(kx[k], c, -kx[k + kD / 2] * s);
-      const float y1 = fmaf(kx[k], s, kx[k + kD / 2] * c);
-      dot = fmaf(s_q[k], y0, fmaf(s_q[k + kD / 2], y1, dot));
+    for (int it = 0; it < 4; ++it) {
+      const int i = warp * 64 + (4 * h2 + it) * 8 + (lane >> 2);
+      float dot = 0.f;
+      if (i < nwin) {
+        const float *qq = s_qr + 16 * (lane & 3);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          dot = fmaf(qq[4 * c], xs[it][c].x, fmaf(qq[4 * c + 1], xs[it][c].y,
+                fmaf(qq[4 * c + 2], xs[it][c].z, fmaf(qq[4 * c + 3], xs[it][c].w, dot))));
+      }
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      dots[4 * h2 + it] = i < nwin ? dot * 0.125f : -INFINITY;
     }
-    s_w[i] = dot * 0.125f;
-    mloc = fmaxf(mloc, dot * 0.125f);
   }
-  const float mwin = block_max(mloc, s_red);  // its barriers also order the s_w writes
-  float lsum = 0.f;
-  for (int i = tid; i < nwin; i += kThreads) {
-    const float e = __expf(s_w[i] - mwin);
-    s_w[i] = e;
-    lsum += e;
+  // the warp's maximum and sum (the four lanes of a key hold the same values:
+  // reduce over the key groups only)
+  float mw = dots[0];
+#pragma unroll
+  for (int it = 1; it < 8; ++it) mw = fmaxf(mw, dots[it]);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+  float lw = 0.f;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    dots[it] = mw == -INFINITY ? 0.f : __expf(dots[it] - mw);  // now the weights
+    lw += dots[it];
+    if ((lane & 3) == 0) s_w[warp * 64 + it * 8 + (lane >> 2)] = dots[it];
   }
-  const float lwin = block_sum(lsum, s_red);
-  weighted_rows(s_w, nwin,
-                [&](int i) { return s_rv + (size_t)((j0 + i) % L.w) * kD * 2; }, s_part);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+  // the ring's values have landed; the new token's row joins them
+  const bool ring_ok = tc::mbar_wait(&barC, 0, err);
+  if (ring_ok && tid >= 8 && tid < 16)
+    reinterpret_cast<uint4 *>(s_rv + (size_t)(t % L.w) * kD * 2)[tid - 8] =
+        reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[tid - 8];
+  if (__syncthreads_or(!ring_ok)) {  // every thread leaves together, no copy in flight
+    if (nsel > 0) tc::mbar_wait(&barB, 0, nullptr);
+    return;
+  }
+  // P.V over the warp's keys (weights from shared memory, written above by
+  // the warp itself): lane l owns dimensions 2l, 2l + 1
+  float ax = 0.f, ay = 0.f;
+  const int iend = min(nwin, warp * 64 + 64);
+#pragma unroll 4
+  for (int i = warp * 64; i < iend; ++i) {
+    const uint32_t x = reinterpret_cast<const uint32_t *>(s_rv + (size_t)ring_row(i) * kD * 2)[lane];
+    const float wv = s_w[i];
+    ax = fmaf(wv, bf16_lo(x), ax);
+    ay = fmaf(wv, bf16_hi(x), ay);
+  }
+  s_part[warp][lane] = make_float2(ax, ay);
+  if (lane == 0) {
+    s_wm[warp] = mw;
+    s_wl[warp] = lw;
+  }
   __syncthreads();
   float owin = 0.f;
-  if (tid < kD) owin = sum_parts(s_part, tid) / lwin;
+  if (tid < kD) {
+    float mm = s_wm[0];
+#pragma unroll
+    for (int w8 = 1; w8 < kThreads / 32; ++w8) mm = fmaxf(mm, s_wm[w8]);
+    float ll = 0.f, oo = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < kThreads / 32; ++w8) {
+      const float sc = s_wm[w8] == -INFINITY ? 0.f : __expf(s_wm[w8] - mm);
+      const float2 pp = s_part[w8][tid >> 1];
+      ll = fmaf(s_wl[w8], sc, ll);
+      oo = fmaf((tid & 1) ? pp.y : pp.x, sc, oo);
+    }
+    owin = oo / ll;
+  }
   __syncthreads();  // s_part and s_w are reused below
 
   // ---- 3b. NoPE readout over the selected cells' tokens (a4), then RMSNorm
@@ -444,18 +551,10 @@ __global__ void __launch_bounds__(kThreads) k6_init_kernel(
   const int C = N / kS, nblk = N / kBq, cap = L.P + L.W;
   unsigned char *hs = state + L.global_bytes + (size_t)bh * L.head_bytes;
   if (bh == 0) {
-    // angle tables: rows o = r (r < 64) and o = 64a (a < 16) of (cos, sin)(o theta_i)
+    // theta_i / pi, fp64, for the steps' rotations
     if (tid == 0) *reinterpret_cast<int *>(state) = 0;
-    float2 *tab = reinterpret_cast<float2 *>(state + L.tab);
-    for (int idx = tid; idx < kDecodeTabRows * (kD / 2); idx += kThreads) {
-      const int row = idx / (kD / 2), i = idx % (kD / 2);
-      const double o = row < 64 ? (double)row : 64.0 * (double)(row - 64);
-      const double x = o * (pow(rope_base, -2.0 * i / kD) / 3.14159265358979323846);
-      const double red = x - 2.0 * floor(0.5 * x);
-      float sn, cs;
-      sincospif((float)red, &sn, &cs);
-      tab[idx] = make_float2(cs, sn);
-    }
+    double *th = reinterpret_cast<double *>(state + L.tab);
+    if (tid < kD / 2) th[tid] = pow(rope_base, -2.0 * tid / kD) / 3.14159265358979323846;
   }
   if (tid == 0) {
     for (int i = 0; i < kDecodeHeaderInts; ++i) s_hdr[i] = 0;
@@ -517,21 +616,33 @@ __global__ void __launch_bounds__(kThreads) k6_init_kernel(
     }
   }
   // the ring: rows [max(0, N0 - w), N0) at j mod w
-  uint4 *g_rk = reinterpret_cast<uint4 *>(hs + L.ring_k);
+  float *g_rk = reinterpret_cast<float *>(hs + L.ring_k);
   uint4 *g_rv = reinterpret_cast<uint4 *>(hs + L.ring_v);
   const int r0 = max(0, N0 - L.w);
   for (int e = tid; e < (N0 - r0) * 8; e += kThreads) {
     const int j = r0 + e / 8;
-    const size_t dst = (size_t)(j % L.w) * 8 + e % 8;
-    g_rk[dst] = reinterpret_cast<const uint4 *>(k)[(head + j) * 8 + e % 8];
-    g_rv[dst] = reinterpret_cast<const uint4 *>(v)[(head + j) * 8 + e % 8];
+    g_rv[(size_t)(j % L.w) * 8 + e % 8] = reinterpret_cast<const uint4 *>(v)[(head + j) * 8 + e % 8];
+  }
+  // keys rotated by their absolute position, fp32
+  for (int e = tid; e < (N0 - r0) * (kD / 2); e += kThreads) {
+    const int j = r0 + e / (kD / 2), i = e % (kD / 2);
+    const double thp = pow(rope_base, -2.0 * i / kD) / 3.14159265358979323846;
+    const double x = (double)j * thp;
+    const double red = x - 2.0 * floor(0.5 * x);
+    float sn, cs;
+    sincospif((float)red, &sn, &cs);
+    const float x0 = __uint_as_float((uint32_t)k[(head + j) * kD + i] << 16);
+    const float x1 = __uint_as_float((uint32_t)k[(head + j) * kD + i + kD / 2] << 16);
+    float *dst = g_rk + (size_t)(j % L.w) * kD;
+    dst[i] = fmaf(x0, cs, -x1 * sn);
+    dst[i + kD / 2] = fmaf(x0, sn, x1 * cs);
   }
 }
 
 }  // namespace
 
 size_t decode_smem_bytes(const DecodeLayout &L) {
-  return 2 * (size_t)L.w * kD * 2 + (size_t)L.nslots * kD * 4 + 2 * (size_t)(L.nslots + 3) / 4 * 16 +
+  return (size_t)L.w * kD * 2 + (size_t)L.nslots * kD * 4 + 2 * (size_t)(L.nslots + 3) / 4 * 16 +
          2 * (size_t)L.K * kS * kD * 2;
 }
 

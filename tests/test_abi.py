@@ -110,18 +110,19 @@ def test_attention_fwd_rejects_bad_arguments_before_launch(kw, status):
 def test_decode_state_is_bounded():
     # The decode state holds ((P+W)s + w + Bq + s) key and value rows per
     # (batch, head) plus the cells' summaries and its lists, whatever the
-    # position: the size takes no sequence length at all.
+    # position: the size takes no sequence length at all.  Rows are bf16,
+    # except the window's keys: fp32, kept rotated by their position.
     p = fs.fs_default_params()
     one = fs.fs_decode_state_bytes(1, 1)
     sixteen = fs.fs_decode_state_bytes(1, 16)
     per_head = (sixteen - one) // 15
     assert fs.fs_decode_state_bytes(2, 8) == sixteen
     rows = (p.P + p.W) * p.s + p.w + p.Bq + p.s
-    kv_bytes = rows * 64 * 2 * 2
+    kv_bytes = rows * 64 * 2 * 2 + p.w * 64 * 2
     nslots = p.P + p.W + p.Bq // p.s + 1
     summaries = nslots * (64 + 2) * 4
     assert kv_bytes <= per_head <= kv_bytes + summaries + 4096
-    assert per_head < 800 * 1024  # about 0.77 MB per head at the page values
+    assert per_head < 850 * 1024  # about 0.83 MB per head at the page values
     # shapes the decode kernel is not built for
     assert fs.fs_decode_state_bytes(1, 1, params=dict(w=1024)) == 0
     assert fs.fs_decode_state_bytes(1, 1, params=dict(mode=1)) == 0
