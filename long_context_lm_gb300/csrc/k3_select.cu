@@ -213,18 +213,21 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
           } else {
             u = __uint_as_float(d[jj]) + la;  // g = 1 exactly
           }
-          if (!ranks_before(u, c, wu, wc)) continue;
-          int cu = c;
+          // one warp-uniform test; the insertion itself is predicated (no
+          // per-lane branches)
+          const bool ins = ranks_before(u, c, wu, wc);
+          if (!__any_sync(0xffffffffu, ins)) continue;
+          int cu = ins ? c : kInvalid;
+          if (!ins) u = -INFINITY;
 #pragma unroll
           for (int k = 0; k < K; ++k) {
-            if (ranks_before(u, cu, bu[k], bc[k])) {
-              const float tu = bu[k];
-              const int tcc = bc[k];
-              bu[k] = u;
-              bc[k] = cu;
-              u = tu;
-              cu = tcc;
-            }
+            const bool sw = ranks_before(u, cu, bu[k], bc[k]);
+            const float tu = bu[k];
+            const int tcc = bc[k];
+            bu[k] = sw ? u : tu;
+            bc[k] = sw ? cu : tcc;
+            u = sw ? tu : u;
+            cu = sw ? tcc : cu;
           }
           wu = bu[K - 1];
           wc = bc[K - 1];
