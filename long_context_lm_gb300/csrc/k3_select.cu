@@ -199,38 +199,54 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
         tc::tmem_ld32(taddr + j0, d);  // columns past np are read, never used
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          if (jj == 16 && j0 + 16 >= np) break;  // np is a multiple of 16
-          const int2 ca = s_ca[j0 + jj];
-          const float la = __int_as_float(ca.y);
-          int c = ca.x;
-          float u;
-          if (c < 0) {  // kNeedsErf (the same for every lane of the warp)
-            c &= ~kNeedsErf;
-            const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
-            const float g = x < 4.0f ? erf_bias(x) : 1.0f;
-            u = __uint_as_float(d[jj]) + la * g;
-          } else {
-            u = __uint_as_float(d[jj]) + la;  // g = 1 exactly
-          }
-          // one warp-uniform test; the insertion itself is predicated (no
-          // per-lane branches)
-          const bool ins = ranks_before(u, c, wu, wc);
-          if (!__any_sync(0xffffffffu, ins)) continue;
-          int cu = ins ? c : kInvalid;
-          if (!ins) u = -INFINITY;
+        // eight candidates at a time: their scores, then one warp vote on
+        // whether any lane's row ranks one of them before its K-th entry
 #pragma unroll
-          for (int k = 0; k < K; ++k) {
-            const bool sw = ranks_before(u, cu, bu[k], bc[k]);
-            const float tu = bu[k];
-            const int tcc = bc[k];
-            bu[k] = sw ? u : tu;
-            bc[k] = sw ? cu : tcc;
-            u = sw ? tu : u;
-            cu = sw ? tcc : cu;
+        for (int j8 = 0; j8 < 32; j8 += 8) {
+          if (j8 == 16 && j0 + 16 >= np) break;  // np is a multiple of 16
+          float u8[8];
+          int c8[8];
+          bool any8 = false;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int2 ca = s_ca[j0 + j8 + e];
+            const float la = __int_as_float(ca.y);
+            int c = ca.x;
+            float u;
+            if (c < 0) {  // kNeedsErf (the same for every lane of the warp)
+              c &= ~kNeedsErf;
+              const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
+              const float g = x < 4.0f ? erf_bias(x) : 1.0f;
+              u = __uint_as_float(d[j8 + e]) + la * g;
+            } else {
+              u = __uint_as_float(d[j8 + e]) + la;  // g = 1 exactly
+            }
+            u8[e] = u;
+            c8[e] = c;
+            any8 |= ranks_before(u, c, wu, wc);
           }
-          wu = bu[K - 1];
-          wc = bc[K - 1];
+          if (!__any_sync(0xffffffffu, any8)) continue;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            // one warp-uniform test; the insertion itself is predicated (no
+            // per-lane branches)
+            const bool ins = ranks_before(u8[e], c8[e], wu, wc);
+            if (!__any_sync(0xffffffffu, ins)) continue;
+            int cu = ins ? c8[e] : kInvalid;
+            float u = ins ? u8[e] : -INFINITY;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+              const bool sw = ranks_before(u, cu, bu[k], bc[k]);
+              const float tu = bu[k];
+              const int tcc = bc[k];
+              bu[k] = sw ? u : tu;
+              bc[k] = sw ? cu : tcc;
+              u = sw ? tu : u;
+              cu = sw ? tcc : cu;
+            }
+            wu = bu[K - 1];
+            wc = bc[K - 1];
+          }
         }
       }
     }
