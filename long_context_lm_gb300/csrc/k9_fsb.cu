@@ -162,23 +162,49 @@ struct SearchParams {
   int32_t *sel;                    // [BH, N, K]
 };
 
-// element e (< 64) of a two-per-lane array: lane e % 32, slot e / 32
-__device__ __forceinline__ int lane_get(const int (&a)[2], int e) {
-  return __shfl_sync(0xffffffffu, e < 32 ? a[0] : a[1], e & 31);
-}
-__device__ __forceinline__ float lane_getf(const float (&a)[2], int e) {
-  return __shfl_sync(0xffffffffu, e < 32 ? a[0] : a[1], e & 31);
-}
-
 __device__ __forceinline__ float bfv(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
 
-// ranks_before on (bound, first leaf) pairs: higher bound first, ties by the
-// lower first leaf
-__device__ __forceinline__ bool node_before(float u, int f, float u2, int f2) {
-  return u > u2 || (u == u2 && f < f2);
-}
 
-constexpr int kMaxCand = 64;
+// Sort key of a candidate node: higher bound first, then the lower first
+// leaf, then the level; an empty position sorts last.  The bound's bits are mapped so that unsigned order is float order,
+// then inverted for "higher first".
+__device__ __forceinline__ unsigned long long node_key(float u, int first, int j) {
+  const uint32_t b = __float_as_uint(u);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)(~ord) << 32) | ((unsigned long long)(uint32_t)first << 5) |
+         (unsigned long long)(uint32_t)j;
+}
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long x, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)x, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(x >> 32), m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+// Ascending bitonic sort of the warp's NS * 32 keys, key p in lane p % 32,
+// slot p / 32 (NS = 1 or 2).
+template <int NS>
+__device__ __forceinline__ void warp_sort(unsigned long long (&key)[2], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32 * NS; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 32) {  // partner in the other slot of the lane (k = 64: ascending)
+        const unsigned long long a = key[0], b = key[1];
+        key[0] = a < b ? a : b;
+        key[1] = a < b ? b : a;
+        continue;
+      }
+#pragma unroll
+      for (int e = 0; e < NS; ++e) {
+        const int pos = 32 * e + lane;
+        const unsigned long long other = shfl_xor_u64(key[e], j);
+        const bool up = (pos & k) == 0, lower = (pos & j) == 0;
+        const unsigned long long mn = key[e] < other ? key[e] : other;
+        const unsigned long long mx = key[e] < other ? other : key[e];
+        key[e] = (lower == up) ? mn : mx;
+      }
+    }
+  }
+}
 
 __global__ void __launch_bounds__(256) k9_search_kernel(const SearchParams p) {
   __shared__ float s_q[8][kD];
@@ -206,112 +232,74 @@ __global__ void __launch_bounds__(256) k9_search_kernel(const SearchParams p) {
     const int *list = reinterpret_cast<const int *>(hs + L.list) + (size_t)f * C;
     const float *mean = reinterpret_cast<const float *>(hs + L.mean) + (size_t)f * L.nodes * kD;
     const float4 *meta = reinterpret_cast<const float4 *>(hs + L.meta) + (size_t)f * L.nodes;
-    // the beam: up to kMaxCand (level, index) nodes, two per lane
-    int bj[2] = {-1, -1}, bi[2] = {0, 0};
+    // the beam: at most 32 (level, index) nodes, node b in lane b (the roots
+    // number at most 24, the kept beams at most `beam` <= 16)
+    int bj = -1, bi = 0;
     int nb = 0;
     {
       int start = 0;
       for (int j = 31 - __clz(m); j >= 0; --j)
         if (m & (1 << j)) {
-          if (nb % 32 == lane) {
-            if (nb < 32) {
-              bj[0] = j;
-              bi[0] = start >> j;
-            } else {
-              bj[1] = j;
-              bi[1] = start >> j;
-            }
+          if (nb == lane) {
+            bj = j;
+            bi = start >> j;
           }
           ++nb;
           start += 1 << j;
         }
     }
-    while (true) {
-      // any inner node left?
-      bool inner = (bj[0] > 0) || (bj[1] > 0);
-      if (!__any_sync(0xffffffffu, inner)) break;
-      // children of every beam node (a leaf stays): up to 2 nb <= kMaxCand
-      int cj[2] = {-1, -1}, ci[2] = {0, 0};
-      float cu[2] = {-INFINITY, -INFINITY};
-      int cf[2] = {0x7fffffff, 0x7fffffff};
-      int nc = 0;
-      for (int b = 0; b < nb; ++b) {
-        const int j = lane_get(bj, b);
-        const int i = lane_get(bi, b);
-        const int kids = j == 0 ? 1 : 2;
-        for (int c = 0; c < kids; ++c) {
-          if (nc % 32 == lane) {
-            const int cjj = j == 0 ? 0 : j - 1, cii = j == 0 ? i : 2 * i + c;
-            if (nc < 32) {
-              cj[0] = cjj;
-              ci[0] = cii;
-            } else {
-              cj[1] = cjj;
-              ci[1] = cii;
-            }
-          }
-          ++nc;
-        }
-      }
-      // bounds, a lane per candidate
+    while (__any_sync(0xffffffffu, bj > 0)) {  // an inner node is left
+      // candidates at fixed positions: beam node b gives position 2b (its
+      // first child, or itself for a leaf) and 2b + 1 (its second child);
+      // position pos sits in lane pos % 32, slot pos / 32
+      unsigned long long key[2];
+      bool valid[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        if (cj[e] < 0) continue;
-        const int node = L.level_off[cj[e]] + ci[e];
+        const int pos = 32 * e + lane, b = pos >> 1, child = pos & 1;
+        const int pj = __shfl_sync(0xffffffffu, bj, b & 31);
+        const int pi = __shfl_sync(0xffffffffu, bi, b & 31);
+        valid[e] = b < nb && pj >= 0 && (pj > 0 || child == 0);
+        key[e] = ~0ull;
+        if (!valid[e]) continue;
+        const int cj = pj == 0 ? 0 : pj - 1, ci = pj == 0 ? pi : 2 * pi + child;
+        // the bound: a 64-dim dot with the node mean, radius, norm and erf terms
+        const int node = L.level_off[cj] + ci;
         const float4 *mu = reinterpret_cast<const float4 *>(mean + (size_t)node * kD);
         float d0 = 0.f, d1 = 0.f;
 #pragma unroll
         for (int v = 0; v < kD / 4; v += 2) {
-          const float4 a = __ldg(mu + v), b4 = __ldg(mu + v + 1);
-          d0 = fmaf(s_q[warp][4 * v], a.x, d0);
-          d0 = fmaf(s_q[warp][4 * v + 1], a.y, d0);
-          d0 = fmaf(s_q[warp][4 * v + 2], a.z, d0);
-          d0 = fmaf(s_q[warp][4 * v + 3], a.w, d0);
-          d1 = fmaf(s_q[warp][4 * v + 4], b4.x, d1);
-          d1 = fmaf(s_q[warp][4 * v + 5], b4.y, d1);
-          d1 = fmaf(s_q[warp][4 * v + 6], b4.z, d1);
-          d1 = fmaf(s_q[warp][4 * v + 7], b4.w, d1);
+          const float4 x = __ldg(mu + v), y = __ldg(mu + v + 1);
+          d0 = fmaf(s_q[warp][4 * v], x.x, d0);
+          d0 = fmaf(s_q[warp][4 * v + 1], x.y, d0);
+          d0 = fmaf(s_q[warp][4 * v + 2], x.z, d0);
+          d0 = fmaf(s_q[warp][4 * v + 3], x.w, d0);
+          d1 = fmaf(s_q[warp][4 * v + 4], y.x, d1);
+          d1 = fmaf(s_q[warp][4 * v + 5], y.y, d1);
+          d1 = fmaf(s_q[warp][4 * v + 6], y.z, d1);
+          d1 = fmaf(s_q[warp][4 * v + 7], y.w, d1);
         }
         const float4 mt = __ldg(meta + node);
         const int first = __float_as_int(mt.z);
         const float pf = (float)(first * kS) + 0.5f * kS;
-        cu[e] = (d0 + d1) + qnorm * mt.x + lam * mt.y * erff(sig * ((float)n - pf) / kS);
-        cf[e] = ci[e] << cj[e];  // first leaf of the node
+        const float u = (d0 + d1) + qnorm * mt.x + lam * mt.y * erff(sig * ((float)n - pf) / kS);
+        key[e] = node_key(u, ci << cj, cj);
       }
-      // keep the best `beam` by (bound desc, first leaf asc): rank by counting
-      int rank[2] = {0, 0};
-      for (int b = 0; b < nc; ++b) {
-        const float u = lane_getf(cu, b);
-        const int f2 = lane_get(cf, b);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) rank[e] += node_before(u, f2, cu[e], cf[e]);
-      }
-      // the kept nodes, in rank order, two per lane again
-      nb = min(nc, p.beam);
-      int nj[2] = {-1, -1}, ni[2] = {0, 0};
-      for (int b = 0; b < nc; ++b) {
-        const int r = lane_get(rank, b);
-        const int j = lane_get(cj, b);
-        const int i = lane_get(ci, b);
-        if (r < nb && r % 32 == lane) {
-          if (r < 32) {
-            nj[0] = j;
-            ni[0] = i;
-          } else {
-            nj[1] = j;
-            ni[1] = i;
-          }
-        }
-      }
-      bj[0] = nj[0];
-      bj[1] = nj[1];
-      bi[0] = ni[0];
-      bi[1] = ni[1];
+      const int nvalid = __popc(__ballot_sync(0xffffffffu, valid[0])) +
+                         __popc(__ballot_sync(0xffffffffu, valid[1]));
+      // rank order by one sort; the best `beam` form the next beam
+      if (__any_sync(0xffffffffu, valid[1]))
+        warp_sort<2>(key, lane);
+      else
+        warp_sort<1>(key, lane);
+      nb = min(nvalid, p.beam);
+      bj = lane < nb ? (int)(key[0] & 31u) : -1;
+      bi = lane < nb ? (int)((uint32_t)(key[0] >> 5) & 0xffffffu) >> bj : 0;
     }
     // the beam's leaves join the union (cells, deduplicated; two beams of at
     // most 16 fit a lane each)
     for (int b = 0; b < nb; ++b) {
-      const int i = lane_get(bi, b);
+      const int i = __shfl_sync(0xffffffffu, bi, b);
       const int c = list[i];
       const bool dup = __any_sync(0xffffffffu, lane < ncand && cand == c);
       if (!dup) {
