@@ -249,46 +249,50 @@ __global__ void __launch_bounds__(256) k9_search_kernel(const SearchParams p) {
         }
     }
     while (__any_sync(0xffffffffu, bj > 0)) {  // an inner node is left
-      // candidates at fixed positions: beam node b gives position 2b (its
-      // first child, or itself for a leaf) and 2b + 1 (its second child);
-      // position pos sits in lane pos % 32, slot pos / 32
-      unsigned long long key[2];
-      bool valid[2];
+      // candidates at fixed indices: beam node b gives index 2b (its first
+      // child, or itself for a leaf) and 2b + 1 (its second child).  Eight
+      // candidates per pass, four lanes each (16 contiguous dimensions of the
+      // node mean); candidate (pass, g) keeps its key in lane 4g + pass % 4,
+      // slot pass / 4 (the sort reorders all positions anyway).
+      unsigned long long key[2] = {~0ull, ~0ull};
+      const int npass = (2 * nb + 7) >> 3;
+      const int g = lane >> 2, sub = lane & 3;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int pos = 32 * e + lane, b = pos >> 1, child = pos & 1;
+      for (int pass = 0; pass < 6; ++pass) {
+        if (pass >= npass) break;  // the same for the whole warp
+        const int c = pass * 8 + g, b = c >> 1, child = c & 1;
         const int pj = __shfl_sync(0xffffffffu, bj, b & 31);
         const int pi = __shfl_sync(0xffffffffu, bi, b & 31);
-        valid[e] = b < nb && pj >= 0 && (pj > 0 || child == 0);
-        key[e] = ~0ull;
-        if (!valid[e]) continue;
-        const int cj = pj == 0 ? 0 : pj - 1, ci = pj == 0 ? pi : 2 * pi + child;
-        // the bound: a 64-dim dot with the node mean, radius, norm and erf terms
+        const bool valid = b < nb && pj >= 0 && (pj > 0 || child == 0);
+        const int cj = pj <= 0 ? 0 : pj - 1, ci = pj <= 0 ? pi : 2 * pi + child;
         const int node = L.level_off[cj] + ci;
-        const float4 *mu = reinterpret_cast<const float4 *>(mean + (size_t)node * kD);
-        float d0 = 0.f, d1 = 0.f;
+        float dot = 0.f;
+        if (valid) {
+          const float4 *mu = reinterpret_cast<const float4 *>(mean + (size_t)node * kD) + 4 * sub;
+          const float *qq = s_q[warp] + 16 * sub;
 #pragma unroll
-        for (int v = 0; v < kD / 4; v += 2) {
-          const float4 x = __ldg(mu + v), y = __ldg(mu + v + 1);
-          d0 = fmaf(s_q[warp][4 * v], x.x, d0);
-          d0 = fmaf(s_q[warp][4 * v + 1], x.y, d0);
-          d0 = fmaf(s_q[warp][4 * v + 2], x.z, d0);
-          d0 = fmaf(s_q[warp][4 * v + 3], x.w, d0);
-          d1 = fmaf(s_q[warp][4 * v + 4], y.x, d1);
-          d1 = fmaf(s_q[warp][4 * v + 5], y.y, d1);
-          d1 = fmaf(s_q[warp][4 * v + 6], y.z, d1);
-          d1 = fmaf(s_q[warp][4 * v + 7], y.w, d1);
+          for (int v = 0; v < 4; ++v) {
+            const float4 x = __ldg(mu + v);
+            dot = fmaf(qq[4 * v], x.x, fmaf(qq[4 * v + 1], x.y,
+                  fmaf(qq[4 * v + 2], x.z, fmaf(qq[4 * v + 3], x.w, dot))));
+          }
         }
-        const float4 mt = __ldg(meta + node);
-        const int first = __float_as_int(mt.z);
-        const float pf = (float)(first * kS) + 0.5f * kS;
-        const float u = (d0 + d1) + qnorm * mt.x + lam * mt.y * erff(sig * ((float)n - pf) / kS);
-        key[e] = node_key(u, ci << cj, cj);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        if (valid && sub == (pass & 3)) {
+          // the bound: the dot, then the radius, norm and erf terms
+          const float4 mt = __ldg(meta + node);
+          const int first = __float_as_int(mt.z);
+          const float pf = (float)(first * kS) + 0.5f * kS;
+          const float u = dot + qnorm * mt.x + lam * mt.y * erff(sig * ((float)n - pf) / kS);
+          key[pass >> 2] = node_key(u, ci << cj, cj);
+        }
       }
-      const int nvalid = __popc(__ballot_sync(0xffffffffu, valid[0])) +
-                         __popc(__ballot_sync(0xffffffffu, valid[1]));
+      // an inner node gives two candidates, a leaf one
+      const int nvalid = __popc(__ballot_sync(0xffffffffu, lane < nb)) +
+                         __popc(__ballot_sync(0xffffffffu, lane < nb && bj > 0));
       // rank order by one sort; the best `beam` form the next beam
-      if (__any_sync(0xffffffffu, valid[1]))
+      if (npass > 4)
         warp_sort<2>(key, lane);
       else
         warp_sort<1>(key, lane);
