@@ -312,27 +312,46 @@ __global__ void __launch_bounds__(256) k9_search_kernel(const SearchParams p) {
       }
     }
   }
-  // rerank: LSE of the 32 token logits of each union cell (a lane per token)
+  // rerank: LSE of the 32 token logits of each union cell.  Eight lanes per
+  // token row (one 16-byte chunk each), four rows per load: lane l takes
+  // chunk l % 8 of rows 4v + l / 8, v < 8, then the eight lanes of a row add
+  // up its partial dots.
   float lse_mine = -INFINITY;
+  const int tg = lane >> 3, chk = lane & 7;
+  float qv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) qv[e] = s_q[warp][8 * chk + e];
   for (int u = 0; u < ncand; ++u) {
     const int c = __shfl_sync(0xffffffffu, cand, u);
-    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k + ((size_t)bh * p.N + (size_t)c * kS + lane) * kD);
-    float dot = 0.f;
+    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k + ((size_t)bh * p.N + (size_t)c * kS) * kD);
+    float part[8];
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
-      const uint4 x = __ldg(kr + v);
+      const uint4 x = __ldg(kr + (4 * v + tg) * (kD / 8) + chk);
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        dot = fmaf(s_q[warp][8 * v + 2 * e], bf16_lo(w[e]), dot);
-        dot = fmaf(s_q[warp][8 * v + 2 * e + 1], bf16_hi(w[e]), dot);
+        dot = fmaf(qv[2 * e], bf16_lo(w[e]), dot);
+        dot = fmaf(qv[2 * e + 1], bf16_hi(w[e]), dot);
       }
+      part[v] = dot;
     }
-    const float lg = dot * 0.125f;
-    float mx = lg;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float sum = warp_sum(__expf(lg - mx));
+    for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) part[v] += __shfl_xor_sync(0xffffffffu, part[v], o);
+    // the lanes of row group tg now hold the logits of rows 4v + tg
+    float mx = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) mx = fmaxf(mx, part[v] * 0.125f);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    float sum = 0.f;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) sum += __expf(part[v] * 0.125f - mx);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 16);
     if (lane == u) lse_mine = mx + __logf(sum);
   }
   // top K by (LSE desc, c asc)
