@@ -616,6 +616,38 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------
 
+def probe_calls():
+    """One call of each entry point family on small shapes (the fsl_16k_b2
+    workload; the projection at B=1, N=16384, D=1024, H=16; four decode steps
+    from a state built at N0 = N - 64; FS-B with tau = the median cell norm),
+    for profiler captures of every kernel.  Prints nothing but 'ok'."""
+    from long_context_lm_gb300 import fs
+    from long_context_lm_gb300.inputs import make_prologue_inputs
+    wl = WORKLOADS["fsl_16k_b2"]
+    inp = make_inputs(wl.batch, wl.heads, wl.seq_len, wl.head_dim, wl.seed, wl.sigma_ln, wl.dtype,
+                      wl.needles, wl.n_needles, wl.params)
+    d = {k: getattr(inp, k).cuda() for k in ("q", "k", "v", "lam", "sigma", "mix")}
+    params = fs.fs_default_params(**wl.params)
+    B, H, N, _ = inp.q.shape
+    fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], params)
+    pi = make_prologue_inputs(1, 16384, 1024, 16, seed=1)
+    fs.fs_qkv_prologue(pi.x.cuda(), pi.w_qkv.cuda(), 16, gain=pi.gain.cuda())
+    kbar, amax = fs.fs_cell_summarize(d["k"])
+    pool, cnt = fs.fs_prune_cells(amax, N, params)
+    st = fs.fs_decode_state_init(B, H, params, k=d["k"], v=d["v"], kbar=kbar, amax=amax, pool=pool,
+                                 pool_count=cnt, N0=N - 64)
+    for t in range(N - 64, N - 60):
+        fs.fs_decode_step(*(d[x][:, :, t].contiguous() for x in ("q", "k", "v")), t, st, d["lam"],
+                          d["sigma"], d["mix"], params)
+    g = torch.randn(inp.q.shape, device="cuda")
+    fs.fs_attention_bwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], g, params)
+    pb = fs.fs_default_params(**dict(wl.params, mode=fs.FS_MODE_FSB, tau=float(amax.median().item())))
+    fs.fs_fsb_select(d["q"], d["k"], kbar, amax, d["lam"], d["sigma"], pb)
+    torch.cuda.synchronize()
+    fs.fs_check_status(st)
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -629,7 +661,12 @@ def main():
                     help="skip the decode-step and base-FS timings")
     ap.add_argument("--extra-lengths", default="fsl_16k_b2,fsl_256k",
                     help="other workloads timed briefly for the per-length figures ('none' = skip)")
+    ap.add_argument("--probe-calls", action="store_true",
+                    help="one call of each entry point on small shapes (for profiler captures), no timing")
     args = ap.parse_args()
+    if args.probe_calls:
+        probe_calls()
+        return
     if args.warmup < 3:
         args.warmup = 3
 
