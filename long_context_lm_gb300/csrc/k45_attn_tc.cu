@@ -76,7 +76,10 @@ constexpr uint32_t kOffV = kOffK + kRing * 32768;      // kRing x 16 KB
 constexpr uint32_t kOffT64 = kOffV + kRing * 16384;    // 64 rows x 272 B
 constexpr uint32_t kOffUL = kOffT64 + 64 * kT64Stride; // union list: kMaxSel int32
 constexpr uint32_t kOffRS = kOffUL + kMaxSel * 4;      // per row / pick: union slot, uint16
-constexpr uint32_t kSmemBytes = kOffRS + kMaxSel * 2 + 1024;  // + alignment slack
+constexpr int kBW = 256;                               // union bitmap words (8192 cells per pass)
+constexpr uint32_t kOffBM = kOffRS + kMaxSel * 2;      // union bitmap: kBW uint32
+constexpr uint32_t kOffPW = kOffBM + kBW * 4;          // cells before each bitmap word: kBW uint16
+constexpr uint32_t kSmemBytes = kOffPW + kBW * 2 + 1024;  // + alignment slack
 
 // TMEM columns: S / P buffers at 0 and 128; accumulator sets at 256 and 384
 // (O_win at +0, O_long at +64).  Inside a score buffer, key chunk c (32 keys)
@@ -393,46 +396,141 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
   drain_tma(bar, T);
 }
 
-// Union of the q-tile's selected cells, sorted ascending, by repeated
-// extraction of the smallest remaining id (cheap: the union is small); each
-// selection's slot in the union is recorded for the softmax masks.
+// Union of the q-tile's selected cells, sorted ascending, and each
+// selection's slot in it (for the softmax masks).  The warp marks the
+// selections in a shared bitmap over a window of 32 * kBW cell ids, then one
+// prefix sum of the words' bit counts gives every cell its rank: the union
+// is the set bits in order (ul), and a selection's slot is its word's prefix
+// plus the set bits below it.
+//
+// Ranking the words of one window, from word 0: the set bits in order go to
+// ul[nu...], each word's first rank to pw.  Returns the new union size.
+__device__ __forceinline__ int union_scan(const uint32_t *bm, uint16_t *pw, int *ul, int nwd,
+                                          int base, int nu, int lane) {
+  for (int w0 = 0; w0 < nwd; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t bits = w < nwd ? bm[w] : 0u;
+    const int cnt = __popc(bits);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int k = nu + incl - cnt;
+    if (w < nwd) pw[w] = (uint16_t)k;
+    while (bits) {
+      ul[k++] = base + 32 * w + (__ffs(bits) - 1);
+      bits &= bits - 1;
+    }
+    nu += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return nu;
+}
+
+// Cells are placed window by window (32 * kBW ids each, from the smallest
+// cell not yet placed; one window while N / s <= 8192): mark, rank, then
+// look up each selection's slot, reading the selections again for each step.
+// They are brought into L1 before the wait for the previous union's readers
+// (one line per lane: 128 K int32, 4 KB at most).  The fused kernel has
+// time to spare for this (the union is needed only after the window tiles)
+// and gains from the small code.  Alone, the long branch waits for each
+// union, so its kernel takes a register path when K <= 4 and every cell id is
+// below 8192: the selections (16 per lane at most) are loaded before the
+// wait, marked from the registers, and their slot lookups go out together.
+constexpr int kFastSel = 16;
 template <int M>
 __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) {
   const int lane = threadIdx.x & 31;
   int *ul = reinterpret_cast<int *>(smem + kOffUL);
   uint16_t *rs = reinterpret_cast<uint16_t *>(smem + kOffRS);
+  uint32_t *bm = reinterpret_cast<uint32_t *>(smem + kOffBM);
+  uint16_t *pw = reinterpret_cast<uint16_t *>(smem + kOffPW);
+  const int ne = p.K * (kBq / 32);  // selections per lane (a multiple of 4)
   uint32_t i = 0;
   for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
     const Item it = item_of<M>(p, g);
+    const int A = it.b0 / kS;  // cells ending at or before the block start
+    const int32_t *blk = p.sel + ((size_t)it.bh * p.N + it.b0) * p.K;
+    const int32_t *src = blk + lane;
+    const bool fast = M == kLongOnly && ne <= kFastSel && A <= 32 * kBW;
+    int c[kFastSel];
+    if (fast) {
+#pragma unroll
+      for (int e = 0; e < kFastSel; ++e) c[e] = e < ne ? __ldg(src + 32 * e) : -1;
+    } else if (Flags<M>::lng && 128 * lane < 4 * kBq * p.K + 127) {
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char *>(blk) + 128 * lane));
+    }
     if (i > 0 && !wait_nth(&bar.u_free, i - 1, p.err)) return;
     int nu = 0;
-    if (Flags<M>::lng) {
-      const int A = it.b0 / kS;  // cells ending at or before the block start
-      const int nsel = kBq * p.K;
-      const int32_t *src = p.sel + ((size_t)it.bh * p.N + it.b0) * p.K;
-      int v[kMaxSel / 32];
+    if (fast) {
+      for (int w = lane; w < (A + 31) >> 5; w += 32) bm[w] = 0u;
+      __syncwarp();
+      int hi = -1;
 #pragma unroll
-      for (int e = 0; e < kMaxSel / 32; ++e) {
-        const int idx = e * 32 + lane;
-        int c = idx < nsel ? src[idx] : -1;
-        v[e] = (c >= 0 && c < A) ? c : 0x7fffffff;
-        if (idx < nsel) rs[idx] = 0xffff;
+      for (int e = 0; e < kFastSel; ++e) {
+        if (c[e] >= A) c[e] = -1;  // not yet complete
+        hi = max(hi, c[e]);
+        if (c[e] >= 0) atomicOr(&bm[c[e] >> 5], 1u << (c[e] & 31));
+        else if (e < ne) rs[32 * e + lane] = 0xffff;
       }
-      while (true) {
-        int mn = 0x7fffffff;
 #pragma unroll
-        for (int e = 0; e < kMaxSel / 32; ++e) mn = min(mn, v[e]);
+      for (int o = 16; o > 0; o >>= 1) hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      __syncwarp();
+      nu = union_scan(bm, pw, ul, (hi >> 5) + 1, 0, 0, lane);
+      __syncwarp();
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        if (mn == 0x7fffffff) break;
+      for (int e = 0; e < kFastSel; ++e)
+        if (c[e] >= 0)
+          rs[32 * e + lane] =
+              (uint16_t)(pw[c[e] >> 5] + __popc(bm[c[e] >> 5] & ((1u << (c[e] & 31)) - 1u)));
+    } else if (Flags<M>::lng) {
+      // a selection's cell, or -1 for none / not yet complete
+      auto cell_of = [&](int e) {
+        const int v = __ldg(src + 32 * e);
+        return (v >= 0 && v < A) ? v : -1;
+      };
+      int lo = 0x7fffffff, hi = -1;
+#pragma unroll 4
+      for (int e = 0; e < ne; ++e) {
+        const int v = cell_of(e);
+        if (v < 0) rs[32 * e + lane] = 0xffff;
+        else lo = min(lo, v);
+        hi = max(hi, v);
+      }
 #pragma unroll
-        for (int e = 0; e < kMaxSel / 32; ++e)
-          if (v[e] == mn) {
-            rs[e * 32 + lane] = (uint16_t)nu;
-            v[e] = 0x7fffffff;
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      while (lo <= hi) {  // one pass per window of cells (warp-uniform)
+        const int base = lo & ~31, end = base + 32 * kBW;
+        const int nwd = min(kBW, ((hi - base) >> 5) + 1);
+        for (int w = lane; w < nwd; w += 32) bm[w] = 0u;
+        __syncwarp();
+#pragma unroll 4
+        for (int e = 0; e < ne; ++e) {
+          const int v = cell_of(e);
+          if (v >= base && v < end) atomicOr(&bm[(v - base) >> 5], 1u << (v & 31));
+        }
+        __syncwarp();
+        nu = union_scan(bm, pw, ul, nwd, base, nu, lane);
+        __syncwarp();
+        int next = 0x7fffffff;
+#pragma unroll 4
+        for (int e = 0; e < ne; ++e) {
+          const int v = cell_of(e);
+          if (v >= base && v < end) {
+            const int w = (v - base) >> 5;
+            rs[32 * e + lane] = (uint16_t)(pw[w] + __popc(bm[w] & ((1u << (v & 31)) - 1u)));
+          } else if (v >= end) {
+            next = min(next, v);
           }
-        if (lane == 0) ul[nu] = mn;
-        ++nu;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) next = min(next, __shfl_xor_sync(0xffffffffu, next, o));
+        lo = next;
+        __syncwarp();  // the bitmap is read before the next pass clears it
       }
     }
     if (lane == 0) bar.nu = nu;

@@ -144,6 +144,35 @@ def test_readout_adversarial_union():
         np.testing.assert_allclose(ol[n], ref, atol=2e-4, rtol=0)
 
 
+@pytest.mark.parametrize("K", [4, 8])
+def test_readout_union_wider_than_8192_cells(K):
+    # Past N = 8192 * s a block's selections can span more than 8192 cell ids,
+    # and the kernel's union is then built window by window.  Each row picks
+    # K cells spread over the whole history; half the rows of a block share
+    # their first cell (duplicates across rows, across the window edges too).
+    N = 262144 + 16384
+    inp = make_inputs(1, 1, N, seed=91 + K)
+    d = to_device(inp)
+    rng = np.random.default_rng(K)
+    n = np.arange(N)
+    A = (n // 128) * 4
+    c0 = np.floor(rng.random(N) * np.maximum(A, 1)).astype(np.int64)
+    shared = np.floor(rng.random(N // 128) * np.maximum(A[::128], 1)).astype(np.int64)
+    c0 = np.where(n % 2 == 0, shared[n // 128], c0)
+    step = np.maximum(A // K, 1)
+    sel = np.stack([(c0 + j * step) % np.maximum(A, 1) for j in range(K)], axis=1)
+    sel = np.where(A[:, None] >= K, sel, -1).astype(np.int32)
+    o_long = fs.fs_sparse_readout(d["q"], d["k"], d["v"],
+                                  torch.from_numpy(sel).view(1, 1, N, K).cuda(), dict(PAGE, K=K))
+    ol = o_long.cpu().numpy()[0, 0]
+    q, k, v = head_slices(inp)
+    rows = np.unique(np.concatenate([sample_rows(N, 10, 8, seed=K),
+                                     N - 128 + np.arange(0, 128, 9), [N - 1]]))
+    for r in rows:
+        ref = O.readout(q[0], k[0], v[0], int(r), sel[r].tolist())
+        np.testing.assert_allclose(ol[r], ref, atol=2e-4, rtol=0)
+
+
 # --------------------------------------------------------------------------- K5
 @pytest.mark.parametrize("N,w", [(128, 512), (1024, 512), (4096, 512), (2048, 1), (2048, 64),
                                  (2048, 100), (4096, 1000)])
