@@ -37,8 +37,8 @@ UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 E2E_HEADS = 4  # heads per group of the host-buffer pipeline (2.43 ms vs 2.50 for 2, 2.46 for 8)
 # dram__bytes_read.sum + dram__bytes_write.sum of fs_attn_tc_kernel in one ncu
-# capture (fsl_16k_b2: 281.89 + 101.99 MB over 2*16*16384 token-heads)
-ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (281.888256e6 + 101.994496e6) / (2 * 16 * 16384)
+# capture (fsl_16k_b2: 281.88 + 102.66 MB over 2*16*16384 token-heads)
+ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (281.875968e6 + 102.657792e6) / (2 * 16 * 16384)
 
 
 # ---------------------------------------------------------------------------
