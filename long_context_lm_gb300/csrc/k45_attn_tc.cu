@@ -871,7 +871,9 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
         const bool resc = !first && m != -INFINITY && mnew != m;
         const float alpha = resc ? tc::ex2(m - mnew) : 1.f;
         const float muse = mnew == -INFINITY ? 0.f : mnew;
-        l = l * alpha;
+        // rounded products and sums, never contracted into an FMA: every
+        // instantiation of this kernel gives the window branch the same bits
+        l = __fmul_rn(l, alpha);
         if (any) {
           // chunk 0 from xa, then chunk 1 moved into xa (one copy of the code)
 #pragma unroll 1
@@ -880,8 +882,8 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
             if (ch ? live1 : live0) {
               // an unpicked cell gets reference +inf: 2^(x - inf) = 0 exactly
               const float mref = (is_long && !(ch ? cell[1] : cell[0])) ? INFINITY : muse;
-              l += split ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
-                         : exp_chunk<false>(xa, pa, pa + 16, sl2, mref);
+              l = __fadd_rn(l, split ? exp_chunk<true>(xa, pa, pa + 16, sl2, mref)
+                                     : exp_chunk<false>(xa, pa, pa + 16, sl2, mref));
             } else {
               uint32_t z[16];
 #pragma unroll
