@@ -618,7 +618,7 @@ def run_reference(args):
 
 def probe_calls():
     """One call of each entry point family on small shapes (the fsl_16k_b2
-    workload; the projection at B=1, N=16384, D=1024, H=16; four decode steps
+    workload, also each attention branch alone; the projection at B=1, N=16384, D=1024, H=16; four decode steps
     from a state built at N0 = N - 64; FS-B with tau = the median cell norm),
     for profiler captures of every kernel.  Prints nothing but 'ok'."""
     from long_context_lm_gb300 import fs
@@ -629,7 +629,13 @@ def probe_calls():
     d = {k: getattr(inp, k).cuda() for k in ("q", "k", "v", "lam", "sigma", "mix")}
     params = fs.fs_default_params(**wl.params)
     B, H, N, _ = inp.q.shape
-    fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], params)
+    ws = torch.empty(fs.fs_workspace_bytes(B, H, N, 64, params), device="cuda", dtype=torch.uint8)
+    fs.fs_attention_fwd(d["q"], d["k"], d["v"], d["lam"], d["sigma"], d["mix"], params, ws=ws)
+    # each attention branch alone: the window branch (its operand pass and
+    # kernel), and the long branch on the forward's own selection
+    sel = fs.fs_workspace_view(ws, B, H, N, 64, params)["sel"].clone()
+    fs.fs_window_attn(d["q"], d["k"], d["v"], params=params)
+    fs.fs_sparse_readout(d["q"], d["k"], d["v"], sel, params)
     pi = make_prologue_inputs(1, 16384, 1024, 16, seed=1)
     fs.fs_qkv_prologue(pi.x.cuda(), pi.w_qkv.cuda(), 16, gain=pi.gain.cuda())
     kbar, amax = fs.fs_cell_summarize(d["k"])
