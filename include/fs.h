@@ -176,7 +176,8 @@ int fs_decode_state_init(const void *k, const void *v, int dtype,
  *   sel_t           [batch,H,K] int32 (nullable): the selected cells
  * The state must be at position t (after t tokens); otherwise the step
  * changes nothing and records FS_ERR_STATE in the state's error word.
- * One CTA per (batch, head); the state stays the same size at any t. */
+ * A cluster of 8 CTAs per (batch, head); the state stays the same size at
+ * any t. */
 int fs_decode_step(const void *q_t, const void *k_t, const void *v_t, int dtype,
                    int batch, int H, int d, int t, const float *lambda,
                    const float *sigma, const float *mix, const fs_params *p,

@@ -29,9 +29,12 @@
 //      with RMSNorm (a4), attends over the ring with RoPE and mixes (a5);
 //   4. when row t closes its cell ((t+1) % s == 0), writes the cell's kbar
 //      and a_c, bit-identical to the prefill's cell summaries, and queues it.
-// The step stages the ring and the pool's summaries in shared memory with
-// bulk asynchronous copies, then the selected cells' rows while the window
-// branch computes.  One CTA of 256 threads per (batch, head).
+// A step runs on a cluster of 8 CTAs of 256 threads per (batch, head), so
+// that a head's window and cells are read through 8 SMs: each CTA stages the
+// pool's summaries (a bulk asynchronous copy) and takes the same list, score
+// and top-K decisions; CTA c reads the window's keys 64c .. 64c + 63 and the
+// c-th selected cell, and the partial softmax results meet in CTA 0's shared
+// memory, which writes the output and the state.
 //
 // Angles: RoPE enters the window as q_t . R(j - t) k_j.  cos / sin of o*theta_i
 // for o = 64a + r (r < 64, a < 16) are two tables built once with the state
@@ -40,6 +43,10 @@
 #include "fs_common.cuh"
 #include "fs_internal.h"
 #include "tc05.cuh"
+
+#include <cooperative_groups.h>
+
+namespace cg = cooperative_groups;
 
 namespace fs {
 
@@ -78,6 +85,11 @@ DecodeLayout decode_layout(int w, int P, int W, int K) {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCluster = 8;                    // CTAs per (batch, head)
+constexpr int kWinPerCta = 512 / kCluster;     // window keys per CTA (w <= 512): 8 per warp
+static_assert(kWinPerCta == 8 * (kThreads / 32), "eight window keys per warp");
+static_assert(kS * kD * 2 == 16 * kThreads, "one 16-byte piece of a cell per thread");
+static_assert(kMaxK <= kCluster, "one selected cell per CTA");
 constexpr int kMaxSlots = kMaxP + 8 + kBq / kS + 1;
 // header ints of one head: counts, then the lists
 enum { kHT = 0, kHRecent = 1, kHTop = 2, kHPend = 3, kHOpen = 4, kHFree = 5 };
@@ -121,29 +133,6 @@ __device__ __forceinline__ bool ranks_before(float a, int c, float a2, int c2) {
   return a > a2 || (a == a2 && c < c2);
 }
 
-// block-wide max / sum over 256 threads (red: 8 floats of shared scratch)
-__device__ __forceinline__ float block_max(float v, float *red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float m = red[0];
-#pragma unroll
-  for (int i = 1; i < kThreads / 32; ++i) m = fmaxf(m, red[i]);
-  return m;
-}
-__device__ __forceinline__ float block_sum(float v, float *red) {
-  v = warp_sum(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < kThreads / 32; ++i) s += red[i];
-  return s;
-}
-
 // sum_i wgt[i] * v(row_of(i)) for i < n, rows in shared memory (64 bf16 each):
 // warp w takes i = w, w+8, ...; lane l owns dims 2l, 2l+1; the eight warp
 // partials go to part[w] for the caller to add up.
@@ -172,36 +161,46 @@ __device__ __forceinline__ float sum_parts(const float2 (*part)[kD / 2], int dim
   return o;
 }
 
+// One step, run by a cluster of kCluster CTAs per (batch, head).  Every CTA
+// takes the same decisions from the same state (the lists at a block start,
+// the pool's scores and the top K), so they need not talk until the end;
+// CTA c then attends over its 64 of the window's keys and over the c-th
+// selected cell, and hands its partial softmax (maximum, sum, weighted
+// values) of each branch to CTA 0, which adds them up, writes the output and
+// alone writes the state.
 __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p) {
   extern __shared__ __align__(1024) unsigned char dsm[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
   const DecodeLayout &L = p.L;
-  // dynamic shared memory: ring values, slot summaries, the selected cells'
-  // keys and values (the window's keys are read from the state directly)
-  unsigned char *s_rv = dsm;
-  float *s_kbar = reinterpret_cast<float *>(s_rv + (size_t)L.w * kD * 2);
+  // dynamic shared memory: slot summaries, then this CTA's cell rows
+  float *s_kbar = reinterpret_cast<float *>(dsm);
   float *s_amax = s_kbar + (size_t)L.nslots * kD;
   int *s_cell = reinterpret_cast<int *>(s_amax + (L.nslots + 3) / 4 * 4);
   unsigned char *s_ck = reinterpret_cast<unsigned char *>(s_cell + (L.nslots + 3) / 4 * 4);
-  unsigned char *s_cv = s_ck + (size_t)L.K * kS * kD * 2;
+  unsigned char *s_cv = s_ck + (size_t)kS * kD * 2;
 
-  __shared__ __align__(8) uint64_t barA, barB, barC;
+  __shared__ __align__(8) uint64_t barA;
   __shared__ int s_hdr[kDecodeHeaderInts];
   __shared__ float s_q[kD], s_k[kD];
-  __shared__ float s_qr[kD], s_kr[kD];  // R(t) q_t, R(t) k_t
+  // R(t) q_t, R(t) k_t (the new key is read as float4: 16-byte aligned)
+  __shared__ __align__(16) float s_qr[kD], s_kr[kD];
   __shared__ int s_pool[kMaxP + 8];
   __shared__ float s_u[kMaxP + 8];
   __shared__ int s_rank[3][kMaxP + 8];
   __shared__ int s_pc[kMaxP + 8];
-  __shared__ int s_sel[kMaxK], s_selc[kMaxK];
-  __shared__ float s_w[1024];
+  __shared__ int s_sel[kMaxK];
+  __shared__ float s_w[kWinPerCta];
   __shared__ float2 s_part[kThreads / 32][kD / 2];
-  __shared__ float s_olong[kD];
   __shared__ float s_wm[kThreads / 32], s_wl[kThreads / 32];  // per warp: window max, sum
-  __shared__ float s_red[8];
   __shared__ int s_ok;
+  // CTA 0 only: every CTA's partials, written there by the CTA itself
+  __shared__ float s_cm[2][kCluster], s_cl[2][kCluster];  // [branch][CTA]: max, sum
+  __shared__ float s_co[2][kCluster][kD];                  // weighted values
+  __shared__ int s_cok[kCluster];
 
-  const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = bh % p.H, t = p.t;
+  const int bh = blockIdx.x / kCluster, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = bh % p.H;
   int *err = reinterpret_cast<int *>(p.state);
   const double *th_pi = reinterpret_cast<const double *>(p.state + L.tab);
   unsigned char *hs = p.state + L.global_bytes + (size_t)bh * L.head_bytes;
@@ -213,25 +212,46 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
   uint16_t *g_sv = reinterpret_cast<uint16_t *>(hs + L.slot_v);
   float *g_rk = reinterpret_cast<float *>(hs + L.ring_k);
   uint16_t *g_rv = reinterpret_cast<uint16_t *>(hs + L.ring_v);
-  const size_t cell_bytes = (size_t)kS * kD * 2;
 
-  // ---- stage the slot summaries (barA, needed first) and the ring's values
-  // (barC, needed only by the window's P.V): bulk copies
+  // ---- the window's ring rows for this warp (they do not depend on the
+  // selection): loads issued now, used after the pool is scored.  Keys i in
+  // [kWinPerCta * rank + 8 * warp, + 8), four lanes per key (a contiguous
+  // 64-byte slice of R(j) k_j, fp32), and lane l's two dimensions of each
+  // key's value.  The newest key and value (j = t) come from the step's
+  // inputs: CTA 0 writes them into the ring only at the end.
+  const int t = p.t;
+  const int j0 = max(0, t - L.w + 1), nwin_all = t - j0 + 1;
+  const int r0 = j0 % L.w;  // ring row of key i: r0 + i, less w past the end
+  const auto ring_row = [&](int i) { const int rr = r0 + i; return rr >= L.w ? rr - L.w : rr; };
+  const int ibase = kWinPerCta * (int)rank + 8 * warp;  // the warp's first key
+  float4 xs[4];
+  uint32_t xv[8];
+  {
+    const int i = ibase + (lane >> 2);
+    if (i < nwin_all - 1) {
+      const float4 *kr =
+          reinterpret_cast<const float4 *>(g_rk + (size_t)ring_row(i) * kD + 16 * (lane & 3));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) xs[c] = kr[c];
+    }
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8) {
+      const int ik = ibase + k8;
+      xv[k8] = ik < nwin_all - 1
+          ? reinterpret_cast<const uint32_t *>(g_rv + (size_t)ring_row(ik) * kD)[lane]
+          : ik == nwin_all - 1 ? reinterpret_cast<const uint32_t *>(p.v_t + (size_t)bh * kD)[lane]
+                               : 0u;
+    }
+  }
+
+  // ---- stage the slot summaries: one bulk copy
   if (tid == 0) {
     tc::mbar_init(&barA, 1);
-    tc::mbar_init(&barB, 1);
-    tc::mbar_init(&barC, 1);
     tc::mbar_fence_init();
-    const uint32_t ring = (uint32_t)L.w * kD * 2;
     const uint32_t sums = (uint32_t)L.nslots * kD * 4;
     const uint32_t small = (uint32_t)(L.nslots + 3) / 4 * 16;
     tc::mbar_arrive_expect_tx(&barA, sums + 2 * small);
-    tc::mbar_arrive_expect_tx(&barC, ring);
     tc::bulk_load(s_kbar, g_kbar, sums, &barA);
-    for (uint32_t o = 0; o < ring; o += 32768) {
-      const uint32_t n = ring - o < 32768 ? ring - o : 32768;
-      tc::bulk_load(s_rv + o, reinterpret_cast<const unsigned char *>(g_rv) + o, n, &barC);
-    }
     tc::bulk_load(s_amax, g_amax, small, &barA);
     tc::bulk_load(s_cell, g_cell, small, &barA);
   }
@@ -248,17 +268,26 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
     rotate_pair(s_q[tid], s_q[tid + kD / 2], cs, s_qr[tid], s_qr[tid + kD / 2]);
     rotate_pair(s_k[tid], s_k[tid + kD / 2], cs, s_kr[tid], s_kr[tid + kD / 2]);
   }
-  // the state must be at position t (every copy is awaited before an exit)
+  // the state must be at position t: the same answer in every CTA, so they
+  // all leave here together (the copy is awaited first)
   const bool in_step = s_hdr[kHT] == t;
   const bool staged = tc::mbar_wait(&barA, 0, err);
-  if (!in_step || !staged) {
-    if (tid == 0 && !in_step) tc::report_error(err, FS_ERR_STATE);
-    tc::mbar_wait(&barC, 0, nullptr);  // no copy in flight at exit (bounded by time)
+  if (!in_step) {
+    if (tid == 0 && rank == 0) tc::report_error(err, FS_ERR_STATE);
+    if (!staged) tc::mbar_wait(&barA, 0, nullptr);  // no copy in flight at exit
     return;
   }
+  // every CTA of the cluster has started once all have arrived here: awaited
+  // before the first write into CTA 0's shared memory
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // a copy that did not land is this CTA's alone: it goes on to the meeting
+  // with the others and flags its partials as missing
+  if (tid == 0) s_ok = staged;
+  __syncthreads();
+  const bool ok = s_ok;
 
   // ---- 1. block start: pending cells become recent, leavers join the top list
-  if (tid == 0) {
+  if (tid == 0 && ok) {
     int *recent = s_hdr + kLRecent, *top = s_hdr + kLTop, *pend = s_hdr + kLPend;
     int *freel = s_hdr + kLFree;
     if (t > 0 && t % kBq == 0) {
@@ -292,34 +321,19 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
         s_hdr[kHOpen] = freel[--s_hdr[kHFree]];
       } else {
         s_hdr[kHOpen] = -1;
-        tc::report_error(err, FS_ERR_STATE);
+        if (rank == 0) tc::report_error(err, FS_ERR_STATE);
       }
     }
     s_ok = s_hdr[kHOpen] >= 0;
   }
   __syncthreads();
-  if (!s_ok) {  // a state that lost track of its slots is left as it was
-    tc::mbar_wait(&barC, 0, nullptr);
-    return;
-  }
+  // a state that lost track of its slots is left as it was (the same answer
+  // in every CTA whose copy landed)
+  const bool go = ok && s_ok;
   const int open = s_hdr[kHOpen];
-  // ---- 2. the new token: ring row t mod w and the open slot's row t mod s
-  if (tid < 8) {
-    const uint4 kv = reinterpret_cast<const uint4 *>(p.k_t + (size_t)bh * kD)[tid];
-    reinterpret_cast<uint4 *>(g_sk + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[tid] = kv;
-  } else if (tid >= 32 && tid < 48) {  // the rotated key, fp32, to ring row t mod w
-    const int c = tid - 32;
-    reinterpret_cast<float4 *>(g_rk + (size_t)(t % L.w) * kD)[c] =
-        make_float4(s_kr[4 * c], s_kr[4 * c + 1], s_kr[4 * c + 2], s_kr[4 * c + 3]);
-  } else if (tid < 16) {
-    const int c = tid - 8;
-    const uint4 vv = reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[c];
-    reinterpret_cast<uint4 *>(g_rv + (size_t)(t % L.w) * kD)[c] = vv;
-    reinterpret_cast<uint4 *>(g_sv + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[c] = vv;
-  }
 
   // ---- 3a. score the pool: u = q . kbar_c + lambda * a_c * erf(sigma (t - p_c) / s)
-  const int nrec = s_hdr[kHRecent], nc = nrec + s_hdr[kHTop];
+  const int nrec = go ? s_hdr[kHRecent] : 0, nc = go ? nrec + s_hdr[kHTop] : 0;
   if (tid < nc) {
     s_pool[tid] = tid < nrec ? s_hdr[kLRecent + tid] : s_hdr[kLTop + tid - nrec];
     s_pc[tid] = s_cell[s_pool[tid]];  // the candidate's cell id
@@ -357,165 +371,216 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
     const int i = tid % nc, part = tid / nc;
     const float u = s_u[i];
     const int c = s_pc[i];
-    int rank = 0;
+    int rank_i = 0;
     for (int j = part * third; j < min(nc, (part + 1) * third); ++j)
-      rank += ranks_before(s_u[j], s_pc[j], u, c);
-    s_rank[part][i] = rank;
+      rank_i += ranks_before(s_u[j], s_pc[j], u, c);
+    s_rank[part][i] = rank_i;
   }
   __syncthreads();
   if (tid < nc) {
-    const int rank = s_rank[0][tid] + s_rank[1][tid] + s_rank[2][tid];
-    if (rank < L.K) s_sel[rank] = s_pool[tid];
+    const int rank_i = s_rank[0][tid] + s_rank[1][tid] + s_rank[2][tid];
+    if (rank_i < L.K) s_sel[rank_i] = s_pool[tid];
   }
   __syncthreads();
   int nsel = 0;
   for (int k = 0; k < L.K; ++k) nsel += s_sel[k] >= 0;
-  if (tid < L.K) {
-    s_selc[tid] = s_sel[tid] >= 0 ? s_cell[s_sel[tid]] : -1;
-    if (p.sel_out) p.sel_out[(size_t)bh * L.K + tid] = s_selc[tid];
-  }
-  // the selected cells' rows, in rank order
-  if (tid == 0 && nsel > 0) {
-    tc::mbar_arrive_expect_tx(&barB, (uint32_t)(2 * nsel * cell_bytes));
-    for (int k = 0; k < nsel; ++k) {
-      tc::bulk_load(s_ck + k * cell_bytes, g_sk + (size_t)s_sel[k] * kS * kD, (uint32_t)cell_bytes,
-                    &barB);
-      tc::bulk_load(s_cv + k * cell_bytes, g_sv + (size_t)s_sel[k] * kS * kD, (uint32_t)cell_bytes,
-                    &barB);
-    }
+  if (rank == 0 && go && tid < L.K && p.sel_out)
+    p.sel_out[(size_t)bh * L.K + tid] = s_sel[tid] >= 0 ? s_cell[s_sel[tid]] : -1;
+  // this CTA's selected cell (the rank-th of the K best, if any): its rows,
+  // loaded now and stored after the window branch
+  const int my_slot = (int)rank < nsel ? s_sel[rank] : -1;
+  uint4 ck_row = make_uint4(0, 0, 0, 0), cv_row = ck_row;
+  if (my_slot >= 0) {
+    ck_row = reinterpret_cast<const uint4 *>(g_sk + (size_t)my_slot * kS * kD)[tid];
+    cv_row = reinterpret_cast<const uint4 *>(g_sv + (size_t)my_slot * kS * kD)[tid];
   }
 
-  // ---- 3c. RoPE window over rows [t - w + 1, t] (a5), while the cells land.
-  // Warp w takes keys i in [64w, 64w + 64): R(j) k_j from the ring (fp32)
-  // against R(t) q_t, four lanes per key (a contiguous 64-byte slice each),
-  // then its own softmax and P.V; the eight partials meet once.
-  const int j0 = max(0, t - L.w + 1), nwin = t - j0 + 1;
-  const int r0 = j0 % L.w;  // ring row of key i: r0 + i, less w past the end
-  const auto ring_row = [&](int i) { const int rr = r0 + i; return rr >= L.w ? rr - L.w : rr; };
-  float dots[8];
+  // ---- 3c. RoPE window over rows [t - w + 1, t] (a5): the warp's eight keys
+  // (loaded at the start) against R(t) q_t
+  const int nwin = go ? nwin_all : 0;
+  float dot = -INFINITY;
+  {
+    const int i = ibase + (lane >> 2);
+    if (i < nwin) {
+      if (i == nwin - 1) {
 #pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    float4 xs[4][4];
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {  // every load of four key groups in flight at once
-      const int i = warp * 64 + (4 * h2 + it) * 8 + (lane >> 2);
-      if (i < nwin) {
-        const float4 *kr = reinterpret_cast<const float4 *>(
-            g_rk + (size_t)ring_row(i) * kD + 16 * (lane & 3));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) xs[it][c] = kr[c];
+        for (int c = 0; c < 4; ++c) xs[c] = reinterpret_cast<const float4 *>(s_kr + 16 * (lane & 3))[c];
       }
-    }
+      const float *qq = s_qr + 16 * (lane & 3);
+      float d = 0.f;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int i = warp * 64 + (4 * h2 + it) * 8 + (lane >> 2);
-      float dot = 0.f;
-      if (i < nwin) {
-        const float *qq = s_qr + 16 * (lane & 3);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          dot = fmaf(qq[4 * c], xs[it][c].x, fmaf(qq[4 * c + 1], xs[it][c].y,
-                fmaf(qq[4 * c + 2], xs[it][c].z, fmaf(qq[4 * c + 3], xs[it][c].w, dot))));
-      }
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      dots[4 * h2 + it] = i < nwin ? dot * 0.125f : -INFINITY;
+      for (int c = 0; c < 4; ++c)
+        d = fmaf(qq[4 * c], xs[c].x, fmaf(qq[4 * c + 1], xs[c].y,
+            fmaf(qq[4 * c + 2], xs[c].z, fmaf(qq[4 * c + 3], xs[c].w, d))));
+      dot = d;
     }
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    dot = i < nwin ? dot * 0.125f : -INFINITY;
   }
-  // the warp's maximum and sum (the four lanes of a key hold the same values:
-  // reduce over the key groups only)
-  float mw = dots[0];
-#pragma unroll
-  for (int it = 1; it < 8; ++it) mw = fmaxf(mw, dots[it]);
+  // the warp's maximum and sum (the four lanes of a key hold the same value:
+  // reduce over the keys only)
+  float mw = dot;
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-  float lw = 0.f;
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    dots[it] = mw == -INFINITY ? 0.f : __expf(dots[it] - mw);  // now the weights
-    lw += dots[it];
-    if ((lane & 3) == 0) s_w[warp * 64 + it * 8 + (lane >> 2)] = dots[it];
-  }
+  const float wgt = mw == -INFINITY ? 0.f : __expf(dot - mw);
+  float lw = (lane & 3) == 0 ? wgt : 0.f;
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-  // the ring's values have landed; the new token's row joins them
-  const bool ring_ok = tc::mbar_wait(&barC, 0, err);
-  if (ring_ok && tid >= 8 && tid < 16)
-    reinterpret_cast<uint4 *>(s_rv + (size_t)(t % L.w) * kD * 2)[tid - 8] =
-        reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[tid - 8];
-  if (__syncthreads_or(!ring_ok)) {  // every thread leaves together, no copy in flight
-    if (nsel > 0) tc::mbar_wait(&barB, 0, nullptr);
-    return;
-  }
-  // P.V over the warp's keys (weights from shared memory, written above by
-  // the warp itself): lane l owns dimensions 2l, 2l + 1
+  // P.V over the warp's eight keys (key k8's weight sits in lane 4 * k8):
+  // lane l owns dimensions 2l, 2l + 1
   float ax = 0.f, ay = 0.f;
-  const int iend = min(nwin, warp * 64 + 64);
-#pragma unroll 4
-  for (int i = warp * 64; i < iend; ++i) {
-    const uint32_t x = reinterpret_cast<const uint32_t *>(s_rv + (size_t)ring_row(i) * kD * 2)[lane];
-    const float wv = s_w[i];
-    ax = fmaf(wv, bf16_lo(x), ax);
-    ay = fmaf(wv, bf16_hi(x), ay);
+#pragma unroll
+  for (int k8 = 0; k8 < 8; ++k8) {
+    const float wv = __shfl_sync(0xffffffffu, wgt, 4 * k8);
+    if (ibase + k8 < nwin) {
+      ax = fmaf(wv, bf16_lo(xv[k8]), ax);
+      ay = fmaf(wv, bf16_hi(xv[k8]), ay);
+    }
   }
   s_part[warp][lane] = make_float2(ax, ay);
   if (lane == 0) {
     s_wm[warp] = mw;
     s_wl[warp] = lw;
   }
+  // this CTA's cell rows into shared memory
+  if (my_slot >= 0) {
+    reinterpret_cast<uint4 *>(s_ck)[tid] = ck_row;
+    reinterpret_cast<uint4 *>(s_cv)[tid] = cv_row;
+  }
   __syncthreads();
-  float owin = 0.f;
-  if (tid < kD) {
-    float mm = s_wm[0];
+  // the CTA's window partial: maximum, sum and weighted values over its keys
+  float cm_w = s_wm[0];
 #pragma unroll
-    for (int w8 = 1; w8 < kThreads / 32; ++w8) mm = fmaxf(mm, s_wm[w8]);
-    float ll = 0.f, oo = 0.f;
+  for (int w8 = 1; w8 < kThreads / 32; ++w8) cm_w = fmaxf(cm_w, s_wm[w8]);
+  float cl_w = 0.f, co_w = 0.f;
+  if (tid < kD) {
 #pragma unroll
     for (int w8 = 0; w8 < kThreads / 32; ++w8) {
-      const float sc = s_wm[w8] == -INFINITY ? 0.f : __expf(s_wm[w8] - mm);
+      const float sc = s_wm[w8] == -INFINITY ? 0.f : __expf(s_wm[w8] - cm_w);
       const float2 pp = s_part[w8][tid >> 1];
-      ll = fmaf(s_wl[w8], sc, ll);
-      oo = fmaf((tid & 1) ? pp.y : pp.x, sc, oo);
+      cl_w = fmaf(s_wl[w8], sc, cl_w);
+      co_w = fmaf((tid & 1) ? pp.y : pp.x, sc, co_w);
     }
-    owin = oo / ll;
   }
-  __syncthreads();  // s_part and s_w are reused below
+  __syncthreads();  // s_part is reused below
 
-  // ---- 3b. NoPE readout over the selected cells' tokens (a4), then RMSNorm
-  const int ntok = nsel * kS;
-  bool cells_ok = true;
-  if (nsel > 0) cells_ok = tc::mbar_wait(&barB, 0, err);
-  if (tid == 0) s_ok = cells_ok;
-  __syncthreads();
-  if (!s_ok) return;
-  float lg = -INFINITY;
-  if (tid < ntok) {
-    const uint4 *kr = reinterpret_cast<const uint4 *>(s_ck + (size_t)tid * kD * 2);
-    float dot = 0.f;
+  // ---- 3b. NoPE readout over this CTA's cell (a4): warp 0, one lane per
+  // token, takes the logits, their maximum and sum; every warp then adds up
+  // weighted value rows
+  float cm_l = -INFINITY, cl_l = 0.f;
+  if (warp == 0) {
+    float lg = -INFINITY;
+    if (my_slot >= 0) {
+      const uint4 *kr = reinterpret_cast<const uint4 *>(s_ck + (size_t)lane * kD * 2);
+      float d = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 x = kr[c];
-      const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = kr[c];
+        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        dot = fmaf(s_q[8 * c + 2 * j], bf16_lo(wv[j]), dot);
-        dot = fmaf(s_q[8 * c + 2 * j + 1], bf16_hi(wv[j]), dot);
+        for (int j = 0; j < 4; ++j) {
+          d = fmaf(s_q[8 * c + 2 * j], bf16_lo(wv[j]), d);
+          d = fmaf(s_q[8 * c + 2 * j + 1], bf16_hi(wv[j]), d);
+        }
       }
+      lg = d * 0.125f;
     }
-    lg = dot * 0.125f;
+    cm_l = lg;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cm_l = fmaxf(cm_l, __shfl_xor_sync(0xffffffffu, cm_l, o));
+    const float pl = my_slot >= 0 ? __expf(lg - cm_l) : 0.f;
+    s_w[lane] = pl;
+    cl_l = warp_sum(pl);
   }
-  const float mlong = block_max(lg, s_red);
-  const float pl = tid < ntok ? __expf(lg - mlong) : 0.f;
-  if (tid < kMaxK * kS) s_w[tid] = pl;
-  const float llong = block_sum(pl, s_red);  // also orders the s_w writes
-  weighted_rows(s_w, ntok, [&](int i) { return s_cv + (size_t)i * kD * 2; }, s_part);
   __syncthreads();
-  if (tid < kD) s_olong[tid] = ntok > 0 ? sum_parts(s_part, tid) / llong : 0.f;
+  weighted_rows(s_w, my_slot >= 0 ? kS : 0, [&](int i) { return s_cv + (size_t)i * kD * 2; }, s_part);
   __syncthreads();
-  float ss = tid < kD ? s_olong[tid] * s_olong[tid] : 0.f;
-  ss = block_sum(ss, s_red);
-  const float rms_scale = ntok > 0 ? rsqrtf(ss / kD + p.rms_eps) : 0.f;
-  if (tid < kD) p.out[(size_t)bh * kD + tid] = owin + p.mix[h] * s_olong[tid] * rms_scale;
+  const float co_l = tid < kD ? sum_parts(s_part, tid) : 0.f;
+
+  // ---- partials to CTA 0, one meeting of the cluster
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  {
+    float(*r_cm)[kCluster] = cluster.map_shared_rank(s_cm, 0);
+    float(*r_cl)[kCluster] = cluster.map_shared_rank(s_cl, 0);
+    float(*r_co)[kCluster][kD] = cluster.map_shared_rank(s_co, 0);
+    int *r_cok = cluster.map_shared_rank(s_cok, 0);
+    if (tid == 0) {
+      r_cm[0][rank] = cm_w;
+      r_cl[0][rank] = cl_w;
+      r_cm[1][rank] = my_slot >= 0 ? cm_l : -INFINITY;
+      r_cl[1][rank] = my_slot >= 0 ? cl_l : 0.f;
+      r_cok[rank] = go ? 1 : (ok ? 2 : 0);  // 2: a state that lost its slots
+    }
+    if (tid < kD) {
+      r_co[0][rank][tid] = co_w;
+      r_co[1][rank][tid] = my_slot >= 0 ? co_l : 0.f;
+    }
+  }
+  cluster.sync();
+  if (!ok) tc::mbar_wait(&barA, 0, nullptr);  // no copy in flight at exit
+  if (rank != 0) return;
+
+  // ---- CTA 0: the totals, the output, then the state (only if every CTA
+  // worked from a staged state; otherwise the state is left as it was)
+  bool all_go = true;
+#pragma unroll
+  for (int c = 0; c < kCluster; ++c) all_go = all_go && s_cok[c] == 1;
+  if (!all_go) return;
+  // warp 0: lane l takes dimensions 2l, 2l + 1 of both branches; the CTAs'
+  // partials are added in CTA order
+  if (warp == 0) {
+    float mt[2], lt[2];
+#pragma unroll
+    for (int br = 0; br < 2; ++br) {
+      float m = s_cm[br][0];
+#pragma unroll
+      for (int c = 1; c < kCluster; ++c) m = fmaxf(m, s_cm[br][c]);
+      mt[br] = m;
+      float l = 0.f;
+#pragma unroll
+      for (int c = 0; c < kCluster; ++c)
+        l = fmaf(s_cl[br][c], s_cm[br][c] == -INFINITY ? 0.f : __expf(s_cm[br][c] - m), l);
+      lt[br] = l;
+    }
+    float owin[2], olong[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int dim = 2 * lane + e;
+      float ow = 0.f, ol = 0.f;
+#pragma unroll
+      for (int c = 0; c < kCluster; ++c) {
+        const float sw = s_cm[0][c] == -INFINITY ? 0.f : __expf(s_cm[0][c] - mt[0]);
+        const float sl = s_cm[1][c] == -INFINITY ? 0.f : __expf(s_cm[1][c] - mt[1]);
+        ow = fmaf(s_co[0][c][dim], sw, ow);
+        ol = fmaf(s_co[1][c][dim], sl, ol);
+      }
+      owin[e] = ow / lt[0];
+      olong[e] = nsel > 0 ? ol / lt[1] : 0.f;
+    }
+    const float ss = warp_sum(olong[0] * olong[0] + olong[1] * olong[1]);
+    const float rms_scale = nsel > 0 ? rsqrtf(ss / kD + p.rms_eps) : 0.f;
+    const float mh = p.mix[h];
+    *reinterpret_cast<float2 *>(p.out + (size_t)bh * kD + 2 * lane) =
+        make_float2(owin[0] + mh * olong[0] * rms_scale, owin[1] + mh * olong[1] * rms_scale);
+  }
+
+  // ---- 2. the new token: ring row t mod w (the rotated key, fp32, and the
+  // value) and the open slot's row t mod s
+  if (tid < 8) {
+    const uint4 kv = reinterpret_cast<const uint4 *>(p.k_t + (size_t)bh * kD)[tid];
+    reinterpret_cast<uint4 *>(g_sk + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[tid] = kv;
+  } else if (tid < 16) {
+    const int c = tid - 8;
+    const uint4 vv = reinterpret_cast<const uint4 *>(p.v_t + (size_t)bh * kD)[c];
+    reinterpret_cast<uint4 *>(g_rv + (size_t)(t % L.w) * kD)[c] = vv;
+    reinterpret_cast<uint4 *>(g_sv + (size_t)open * kS * kD + (size_t)(t % kS) * kD)[c] = vv;
+  } else if (tid >= 32 && tid < 48) {
+    const int c = tid - 32;
+    reinterpret_cast<float4 *>(g_rk + (size_t)(t % L.w) * kD)[c] =
+        make_float4(s_kr[4 * c], s_kr[4 * c + 1], s_kr[4 * c + 2], s_kr[4 * c + 3]);
+  }
+  __syncthreads();  // the open slot's new row is read back below
 
   // ---- 4. row t closes its cell: summary, as the prefill computes it; the
   // cell waits in the pending list for the next block start
@@ -642,8 +707,7 @@ __global__ void __launch_bounds__(kThreads) k6_init_kernel(
 }  // namespace
 
 size_t decode_smem_bytes(const DecodeLayout &L) {
-  return (size_t)L.w * kD * 2 + (size_t)L.nslots * kD * 4 + 2 * (size_t)(L.nslots + 3) / 4 * 16 +
-         2 * (size_t)L.K * kS * kD * 2;
+  return (size_t)L.nslots * kD * 4 + 2 * (size_t)(L.nslots + 3) / 4 * 16 + 2 * (size_t)kS * kD * 2;
 }
 
 cudaError_t launch_decode_init(const void *k, const void *v, const float *kbar, const float *amax,
@@ -675,8 +739,19 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(k6_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k6_decode_kernel<<<a.batch * a.H, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.batch * a.H * kCluster));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k6_decode_kernel, p);
 }
 
 }  // namespace fs
