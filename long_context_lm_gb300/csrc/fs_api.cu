@@ -270,7 +270,7 @@ int fs_select_cells(const void *q, int dtype, const float *kbar, const float *am
   const bool fs_mode = p->mode == FS_MODE_FS;
   if (!fs_mode && (!pool || !pool_count)) return FS_ERR_INVALID_ARG;
   return status_of(launch_select(q, kbar, amax, pool, pool_count, lambda, sigma,
-                                 Shape{batch, H, N, d}, p->K, p->P + p->W, fs_mode, sel,
+                                 Shape{batch, H, N, d}, p->K, p->P + p->W, p->W, fs_mode, sel,
                                  sel_score, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
@@ -420,7 +420,7 @@ int forward(const void *q, const void *k, const void *v, int dtype, const Shape 
                                 base + L.fsb, sel, st)));
   else
     FS_TRY(status_of(launch_select(qb, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
-                                   p->P + p->W, fs_mode, sel, nullptr, err, st)));
+                                   p->P + p->W, p->W, fs_mode, sel, nullptr, err, st)));
   FS_TRY(mark(3));
   AttnArgs a{};
   a.sh = sh;
@@ -674,7 +674,7 @@ extern "C" int fs_attention_bwd(const void *q, const void *k, const void *v, int
   if (!fs_mode)
     FS_TRY(status_of(launch_prune(amax, sh, p->P, p->W, pool, pool_count, base + L.prune, st)));
   FS_TRY(status_of(launch_select(q, kbar, amax, pool, pool_count, lambda, sigma, sh, p->K,
-                                 p->P + p->W, fs_mode, sel, nullptr, err, st)));
+                                 p->P + p->W, p->W, fs_mode, sel, nullptr, err, st)));
   BwdArgs a{};
   a.sh = sh;
   a.q = q;

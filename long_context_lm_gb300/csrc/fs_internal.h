@@ -22,8 +22,9 @@ cudaError_t launch_prune(const float *amax, const Shape &sh, int P, int W, int32
                          int32_t *pool_count, void *ws, cudaStream_t st);
 cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const int32_t *pool, const int32_t *pool_count, const float *lambda,
-                          const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
-                          int32_t *sel, float *sel_score, int *err, cudaStream_t st);
+                          const float *sigma, const Shape &sh, int K, int cap, int W,
+                          bool fs_mode, int32_t *sel, float *sel_score, int *err,
+                          cudaStream_t st);
 // RoPE angle table (rope_table_bytes(N) of device memory, written by
 // launch_rope_table) and the window operands prepared from it: kt = rotated
 // keys [rows, 128] bf16 (hi | lo), v16 = values [rows, 64] fp16.

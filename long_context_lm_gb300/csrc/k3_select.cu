@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
     const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
     const float *__restrict__ amax, const int32_t *__restrict__ pool,
     const int32_t *__restrict__ pool_count, const float *__restrict__ lambda,
-    const float *__restrict__ sigma, int H, int N, int cap, int fs_mode,
+    const float *__restrict__ sigma, int H, int N, int cap, int W, int fs_mode,
     int32_t *__restrict__ sel, float *__restrict__ sel_score, int *err) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem =
@@ -124,7 +124,12 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
         const int j = (p0 + tid + it * kThreads) >> 3;
         int c = -1;
         if (j < nc) {
-          c = fs_mode ? base + j : __ldg(pl + base + j);
+          // FS-L: the ranked older cells (a_c desc) first, the W recent
+          // ones last: the rows' K-th scores rise sooner, so the warp vote
+          // turns more groups of candidates away (the result does not depend
+          // on the order)
+          const int nrec = min(min(W, A), count), jj = j < count - nrec ? nrec + j : j - (count - nrec);
+          c = fs_mode ? base + j : __ldg(pl + jj);
           if (c < 0 || c >= A) c = -1;  // not a cell this block may read: skipped
         }
         cj[it] = c;
@@ -272,8 +277,9 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
 
 cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
                           const int32_t *pool, const int32_t *pool_count, const float *lambda,
-                          const float *sigma, const Shape &sh, int K, int cap, bool fs_mode,
-                          int32_t *sel, float *sel_score, int *err, cudaStream_t st) {
+                          const float *sigma, const Shape &sh, int K, int cap, int W,
+                          bool fs_mode, int32_t *sel, float *sel_score, int *err,
+                          cudaStream_t st) {
   const int smem = 16384 + 3 * chunk_rows(fs_mode ? 1 : 0, cap) * 128 + 1024;
   dim3 grid(sh.nblk(), sh.BH());
   const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(q);
@@ -282,7 +288,7 @@ cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, st>>>(qb, kbar, amax, pool, pool_count, lambda, sigma, sh.H,
-                                       sh.N, cap, fsm, sel, sel_score, err);
+                                       sh.N, cap, W, fsm, sel, sel_score, err);
     return cudaSuccess;
   };
   cudaError_t e;
