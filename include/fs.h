@@ -369,7 +369,9 @@ size_t fs_host_workspace_bytes(int batch, int H, int N, int d,
  * entry point has no counterpart on the pages: it serves callers whose
  * activations live in host memory.  The op is independent per (batch,
  * head), so the call walks groups of `heads_per_chunk` heads of one batch
- * row through two device staging slots.  The load of the next group, the
+ * row through two device staging slots; the first group of the first and of
+ * the last batch row takes half as many heads, since the call's first load
+ * and last store overlap no compute.  The load of the next group, the
  * forward of this one and the store of the previous one overlap: loads on
  * one copy stream, forwards on `stream`, stores on a second copy stream,
  * ordered by events.  Results are bit-identical to fs_attention_fwd.

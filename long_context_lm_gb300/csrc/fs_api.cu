@@ -540,9 +540,15 @@ int fs_attention_fwd_host(const void *q, const void *k, const void *v, int dtype
   const size_t elem = dtype == FS_FP32 ? 4 : 2;
   int rc = FS_OK;
   int chunk = 0;
+  // Groups of hc heads, except the first group of the call's first and last
+  // (batch) rows, which takes half as many: the call's first load and its
+  // last store overlap no compute, so both are kept short (with H a multiple
+  // of hc the last group then has half the heads as well).
+  const int hhalf = (hc + 1) / 2;
   for (int b = 0; b < batch && rc == FS_OK; ++b) {
-    for (int h0 = 0; h0 < H && rc == FS_OK; h0 += hc, ++chunk) {
-      const int hn = H - h0 < hc ? H - h0 : hc;
+    for (int h0 = 0, hn = 0; h0 < H && rc == FS_OK; h0 += hn, ++chunk) {
+      const int hg = (h0 == 0 && (b == 0 || b == batch - 1)) ? hhalf : hc;
+      hn = H - h0 < hg ? H - h0 : hg;
       const int s = chunk & 1;
       char *slot = base + kHeader + s * HL.slot_bytes;
       char *qd = slot, *kd = qd + HL.qkv_bytes, *vd = kd + HL.qkv_bytes;
