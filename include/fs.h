@@ -89,6 +89,17 @@ const char *fs_status_string(int status);
  * FS_ERR_CUDA (static string; "no error" if there was none). */
 const char *fs_last_cuda_error(void);
 
+/* Diagnostics (no counterpart on the pages): each CTA of the attention
+ * kernel launches that the calling host thread makes next (inside
+ * fs_attention_fwd, fs_window_attn and fs_sparse_readout) writes the device's
+ * global timer, in ns, at its start and at its end into timeline[2 * cta] and
+ * timeline[2 * cta + 1]: the spread of the CTAs' finish times shows how well
+ * the q-tiles were balanced.  timeline is device memory of `entries` int64,
+ * owned by the caller; a launch of more than entries / 2 CTAs records
+ * nothing.  (NULL, 0) turns it off.  FS_ERR_INVALID_ARG when exactly one of
+ * timeline and entries is zero, or entries < 0. */
+int fs_set_attention_timeline(long long *timeline, int entries);
+
 /* Device workspace bytes fs_attention_fwd needs for this shape (includes the
  * bf16 staging copies of q, k, v when dtype is FS_FP32).  0 on bad args. */
 size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p,
@@ -396,7 +407,8 @@ int fs_attention_fwd_host(const void *q, const void *k, const void *v,
                           void *stream);
 
 /* Every workspace begins with a 256-byte header whose first int is a device
- * error word, cleared at the start of each call.  Kernels that wait on
+ * error word, cleared at the start of each call (the next two ints are the
+ * attention kernel's q-tile tickets, cleared with it and left clear).  Kernels that wait on
  * mbarriers give up after a bounded number of polls (seconds) and record
  * FS_ERR_TIMEOUT there instead of hanging; the window branch records
  * FS_ERR_RANGE there when a value of v is outside the fp16 range (its

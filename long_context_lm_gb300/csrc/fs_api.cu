@@ -193,6 +193,12 @@ const char *fs_status_string(int status) {
 
 const char *fs_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
 
+int fs_set_attention_timeline(long long *timeline, int entries) {
+  if ((timeline == nullptr) != (entries == 0) || entries < 0) return FS_ERR_INVALID_ARG;
+  fs::set_attention_timeline(timeline, entries);
+  return FS_OK;
+}
+
 size_t fs_workspace_bytes(int batch, int H, int N, int d, const fs_params *p, int dtype) {
   if (check_params(p) || check_shape(batch, H, N, d) || check_dtype(dtype)) return 0;
   return make_layout(Shape{batch, H, N, d}, *p, dtype).total;
@@ -323,7 +329,7 @@ int fs_window_attn_traced(const void *q, const void *k, const void *v, int dtype
     if (!stage_events || !stage_events[i]) return FS_OK;
     return status_of(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st));
   };
-  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, 4 * sizeof(int), st)));
   FS_TRY(mark(0));
   FS_TRY(prepare_window(sh, k, v, p->rope_base, base, W, err, st));
   FS_TRY(mark(1));
@@ -343,6 +349,7 @@ int fs_window_attn_traced(const void *q, const void *k, const void *v, int dtype
   a.window = true;
   a.out = out;
   a.err = err;
+  a.sched = err + 1;  // the header's second and third ints
   FS_TRY(status_of(launch_attn_tc(a, st)));
   return mark(2);
 }
@@ -366,7 +373,7 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   const Layout L = make_layout(sh, *p, dtype);
   if (ws_bytes < L.total) return FS_ERR_INVALID_ARG;
   int *err = reinterpret_cast<int *>(ws);
-  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), static_cast<cudaStream_t>(stream))));
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, 4 * sizeof(int), static_cast<cudaStream_t>(stream))));
   return forward(q, k, v, dtype, sh, p, lambda, sigma, mix, out, static_cast<char *>(ws), L, err,
                  static_cast<cudaStream_t>(stream), stage_events);
 }
@@ -438,6 +445,7 @@ int forward(const void *q, const void *k, const void *v, int dtype, const Shape 
   a.window = true;
   a.out = out;
   a.err = err;
+  a.sched = err + 1;  // the header's second and third ints
   FS_TRY(status_of(launch_attn_tc(a, st)));
   return mark(4);
 }
@@ -531,7 +539,7 @@ int fs_attention_fwd_host(const void *q, const void *k, const void *v, int dtype
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *base = static_cast<char *>(ws);
   int *err = reinterpret_cast<int *>(base);
-  FS_TRY(status_of(cudaMemsetAsync(err, 0, sizeof(int), st)));
+  FS_TRY(status_of(cudaMemsetAsync(err, 0, 4 * sizeof(int), st)));
   // The loads begin only after everything already on the caller's stream:
   // an earlier call's forwards and stores that still read the staging slots,
   // and any work that writes the host inputs.

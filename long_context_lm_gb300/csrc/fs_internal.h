@@ -54,8 +54,13 @@ struct AttnArgs {
   bool window, write_long;
   float *out;
   int *err;
+  int *sched;  // nullable: two ints, zero at launch, left zero (q-tile tickets)
+  long long *timeline;  // nullable: per CTA, global-timer ns at its start and end
 };
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
+// Per-CTA timeline of the calling host thread's next attention launches
+// (fs_set_attention_timeline): buffer and its length in int64 entries.
+void set_attention_timeline(long long *timeline, int entries);
 // Bounded decode state (see k6_decode.cu): a global part (256-byte header
 // whose first int is the error word, then the relative-angle tables), then
 // one fixed-size block per (batch, head).  Offsets inside a head's block.

@@ -112,6 +112,8 @@ struct Barriers {
   uint64_t stats_full[2], stat_free[2];  // per q-tile parity: row sums published / read
   uint64_t pair[4];               // the two softmax warps of a row block meet here
   uint64_t u_full, u_free;   // union of the q-tile's cells built / consumed
+  uint64_t g_full[4];        // the CTA's q-tile sequence: item i published in slot i % 4
+  int g_ring[4];
   uint64_t fin[2];
   uint32_t tmem;
   int nu;                    // cells in the current union
@@ -128,6 +130,8 @@ struct Params {
   const float *mix;
   const float2 *tab;       // (cos, sin) of r*theta_i (rows r < 64), 64*u*theta_i (row 64 + u)
   int H, N, w, K, nblk, nitems;
+  int *sched;              // nullable: [0] next item ticket, [1] CTAs finished (zero at launch)
+  long long *timeline;     // nullable: per CTA, global-timer ns at its start and at its end
   float rms_eps;
   size_t nrows;            // BH * N (first out-of-range key row: zero fill)
   float *out;
@@ -166,6 +170,22 @@ __device__ __forceinline__ Item item_of(const Params &p, int g) {
   it.kt0 = max(0, it.b0 - p.w + 1) / kKT * kKT;
   it.nw = Flags<M>::window ? (it.b0 + kBq - it.kt0) / kKT : 0;
   return it;
+}
+
+// The CTA's i-th q-tile.  Without a scheduler word the CTAs take q-tiles
+// round-robin; with one, each CTA starts with q-tile blockIdx.x and then
+// takes the next unclaimed one (one atomic ticket per q-tile, drawn by the
+// union warp one q-tile ahead and published to the CTA's roles in a ring of
+// four), so CTAs that drew cheap q-tiles take more of them and all finish
+// together.  A value >= nitems ends the sequence; -1 is a failed wait.
+__device__ __forceinline__ int next_item(const Params &p, Barriers &bar, uint32_t i) {
+  if (!p.sched) return blockIdx.x + (int)i * gridDim.x;
+  if (!wait_nth(&bar.g_full[i & 3], i >> 2, p.err)) return -1;
+  return *reinterpret_cast<volatile int *>(&bar.g_ring[i & 3]);
+}
+__device__ __forceinline__ void publish_item(Barriers &bar, uint32_t i, int g) {
+  bar.g_ring[i & 3] = g;
+  tc::mbar_arrive(&bar.g_full[i & 3]);  // release: the roles read the slot after their wait
 }
 template <int M>
 __device__ __forceinline__ int long_tiles(const Barriers &bar) {
@@ -245,7 +265,10 @@ __device__ void role_qk(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
   const uint64_t dqh = tc::desc_sw128(base + kOffQ), dql = tc::desc_sw128(base + kOffQ + 16384);
   const uint64_t dqr = tc::desc_sw128(base + kOffQR);
   uint32_t T = 0, i = 0;
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+  for (;; ++i) {
+    const int g = next_item(p, bar, i);
+    if (g < 0) return;
+    if (g >= p.nitems) break;
     const Item it = item_of<M>(p, g);
     if (!wait_nth(&bar.q_full, i, p.err)) return;
     int nl = 0;
@@ -293,7 +316,10 @@ __device__ void role_pv(const Params &p, Barriers &bar, uint32_t tmem, uint32_t 
   const uint32_t id_pv = tc::idesc_bf16(128, kD, 1);  // long: bf16 P hi / lo, bf16 V
   const uint32_t id_pv_h = tc::idesc_f16(128, kD, 1);  // window (and long16): fp16 P, V
   uint32_t T = 0, i = 0;
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+  for (;; ++i) {
+    const int g = next_item(p, bar, i);
+    if (g < 0) return;
+    if (g >= p.nitems) break;
     const Item it = item_of<M>(p, g);
     const uint32_t ob = tmem + kColO + 128 * (i & 1);
     // an accumulator set is reused once the epilogue two q-tiles back has read it
@@ -355,7 +381,10 @@ __device__ void role_tma(const Params &p, Barriers &bar, unsigned char *smem,
                          const CUtensorMap *cv) {
   uint32_t T = 0, i = 0;
   const int *ul = reinterpret_cast<const int *>(smem + kOffUL);
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+  for (;; ++i) {
+    const int g = next_item(p, bar, i);
+    if (g < 0) return drain_tma(bar, T);
+    if (g >= p.nitems) break;
     const Item it = item_of<M>(p, g);
     const int row0 = it.bh * p.N;
     int nl = 0;
@@ -448,7 +477,19 @@ __device__ void role_union(const Params &p, Barriers &bar, unsigned char *smem) 
   uint16_t *pw = reinterpret_cast<uint16_t *>(smem + kOffPW);
   const int ne = p.K * (kBq / 32);  // selections per lane (a multiple of 4)
   uint32_t i = 0;
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+  // the scheduler (see next_item): the CTA's first q-tile is its own index,
+  // each later one a ticket drawn one q-tile ahead
+  if (p.sched && lane == 0) publish_item(bar, 0, blockIdx.x < p.nitems ? blockIdx.x : p.nitems);
+  for (int g = blockIdx.x, g_next = 0; g < p.nitems; g = g_next, ++i) {
+    g_next = g + gridDim.x;
+    if (p.sched) {
+      int tk = 0;
+      if (lane == 0) {
+        tk = gridDim.x + atomicAdd(p.sched, 1);
+        publish_item(bar, i + 1, tk < p.nitems ? tk : p.nitems);
+      }
+      g_next = __shfl_sync(0xffffffffu, tk, 0);
+    }
     const Item it = item_of<M>(p, g);
     const int A = it.b0 / kS;  // cells ending at or before the block start
     const int32_t *blk = p.sel + ((size_t)it.bh * p.N + it.b0) * p.K;
@@ -552,7 +593,9 @@ __device__ void role_qprep(const Params &p, Barriers &bar, unsigned char *smem, 
                            int r) {
   uint32_t i = 0;
   int g_prev = -1;
-  for (int g = blockIdx.x;; g += gridDim.x, ++i) {
+  for (;; ++i) {
+    const int g = next_item(p, bar, i);
+    if (g < 0) return;
     const bool real = g < p.nitems;
     if (real) {
       const Item it = item_of<M>(p, g);
@@ -804,7 +847,10 @@ __device__ void role_softmax(const Params &p, Barriers &bar, uint32_t tmem, unsi
   const float sl2 = 1.4426950408889634f * 0.125f;  // log2(e) / sqrt(64)
   uint32_t T = 0, i = 0;
   Pair pr{&bar.pair[quarter], bar.xch, 0u};
-  for (int g = blockIdx.x; g < p.nitems; g += gridDim.x, ++i) {
+  for (;; ++i) {
+    const int g = next_item(p, bar, i);
+    if (g < 0) return;
+    if (g >= p.nitems) break;
     const Item it = item_of<M>(p, g);
     const int n = it.b0 + r;
     const uint32_t ow_addr = tmem + kColO + 128 * (i & 1) + 32 * half + lane_base;
@@ -948,6 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Barriers bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0 && p.timeline) p.timeline[2 * blockIdx.x] = tc::global_ns();
 
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar.q_full, kRotThreads);
@@ -970,6 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     for (int q4 = 0; q4 < 4; ++q4) tc::mbar_init(&bar.pair[q4], 2);
     tc::mbar_init(&bar.pv_done, 1);
     tc::mbar_init(&bar.u_full, 1);
+    for (int j = 0; j < 4; ++j) tc::mbar_init(&bar.g_full[j], 1);
     // the union may be rebuilt once every role has read it: 8 softmax warps,
     // the two issuers and the TMA thread
     tc::mbar_init(&bar.u_free, 11);
@@ -1031,6 +1079,12 @@ __global__ void __launch_bounds__(kThreads, 1) fs_attn_tc_kernel(
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0 && p.timeline) p.timeline[2 * blockIdx.x + 1] = tc::global_ns();
+  // the last CTA to finish clears the scheduler words for the next launch
+  if (threadIdx.x == 0 && p.sched && atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+    atomicExch(p.sched, 0);
+    atomicExch(p.sched + 1, 0);
+  }
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1077,6 +1131,16 @@ int sm_count() {
 
 }  // namespace
 
+namespace {
+thread_local long long *g_timeline = nullptr;
+thread_local int g_timeline_entries = 0;
+}  // namespace
+
+void set_attention_timeline(long long *timeline, int entries) {
+  g_timeline = timeline;
+  g_timeline_entries = entries;
+}
+
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   const Shape &sh = a.sh;
   if (!a.window && !a.sel) return cudaErrorInvalidValue;
@@ -1095,7 +1159,7 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   if (!make_rows_map(&ck, a.k, nrows, kD, kS, false) ||
       !make_rows_map(&cv, long16 ? a.v16 : a.v, nrows, kD, kS, long16))
     return cudaErrorInvalidValue;
-  Params p;
+  Params p{};
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.sel = a.sel;
   p.o_long_in = a.o_long_in;
@@ -1107,6 +1171,8 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
   p.K = a.K;
   p.nblk = sh.nblk();
   p.nitems = sh.BH() * sh.nblk();
+  p.sched = a.sched;
+  p.timeline = a.timeline;
   p.rms_eps = a.rms_eps;
   p.nrows = nrows;
   p.out = a.out;
@@ -1125,6 +1191,7 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.nitems < sm_count() ? p.nitems : sm_count();
+  if (!p.timeline && g_timeline && g_timeline_entries >= 2 * grid) p.timeline = g_timeline;
   kern<<<grid, kThreads, kSmemBytes, st>>>(mkt, mv16, ck, cv, p);
   return cudaGetLastError();
 }

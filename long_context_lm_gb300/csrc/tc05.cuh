@@ -37,6 +37,12 @@ __device__ __forceinline__ void report_error(int *err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+__device__ __forceinline__ long long global_ns() {
+  long long v;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

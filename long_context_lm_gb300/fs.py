@@ -26,6 +26,7 @@ FS_BF16, FS_FP32 = 0, 1
 FS_MODE_FSL, FS_MODE_FS, FS_MODE_FSB = 0, 1, 2
 
 SYMBOLS = ["fs_default_params", "fs_status_string", "fs_last_cuda_error", "fs_workspace_bytes",
+           "fs_set_attention_timeline",
            "fs_prune_workspace_bytes", "fs_window_workspace_bytes", "fs_cell_summarize",
            "fs_prune_cells", "fs_select_cells", "fs_sparse_readout", "fs_window_attn",
            "fs_attention_fwd", "fs_attention_fwd_traced", "fs_workspace_view", "fs_check_status",
@@ -105,6 +106,7 @@ def load(build_if_stale: bool = True):
         L.fs_attention_fwd_host.argtypes = [P, P, P, I, I, I, I, I, PP, P, P, P, P, I, P, Z, P]
         L.fs_workspace_view.argtypes = [I, I, I, I, PP, I] + [ctypes.POINTER(Z)] * 5
         L.fs_check_status.argtypes = [P, P]
+        L.fs_set_attention_timeline.argtypes = [P, I]
         L.fs_selftest_wait_timeout.argtypes = [P, P]
         L.fs_prune_static_scratch_bytes.argtypes = []
         L.fs_prune_static_scratch_bytes.restype = Z
@@ -607,6 +609,19 @@ def fs_workspace_view(ws, batch, H, N, d, params=None, dtype=FS_BF16):
         nbytes = n * torch.tensor([], dtype=dtype_).element_size()
         res[name] = ws[off.value: off.value + nbytes].view(dtype_).view(shape)
     return res
+
+
+def fs_set_attention_timeline(buf=None):
+    """Record each CTA's start and end (device global timer, ns) of the calling
+    thread's following attention launches into ``buf`` (a CUDA int64 tensor,
+    two entries per CTA); ``None`` turns it off."""
+    L = load()
+    if buf is None:
+        _check(L.fs_set_attention_timeline(None, 0), "fs_set_attention_timeline")
+        return
+    if not (buf.is_cuda and buf.dtype == torch.int64 and buf.is_contiguous()):
+        raise ValueError("timeline must be a contiguous CUDA int64 tensor")
+    _check(L.fs_set_attention_timeline(_ptr(buf), buf.numel()), "fs_set_attention_timeline")
 
 
 def fs_check_status(ws, stream=None):

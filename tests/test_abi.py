@@ -126,3 +126,12 @@ def test_decode_state_is_bounded():
     # shapes the decode kernel is not built for
     assert fs.fs_decode_state_bytes(1, 1, params=dict(w=1024)) == 0
     assert fs.fs_decode_state_bytes(1, 1, params=dict(mode=1)) == 0
+
+
+def test_attention_timeline_argument_checks():
+    # host-side only: the setter stores the pointer, nothing reaches the GPU
+    L = fs.load()
+    assert L.fs_set_attention_timeline(None, 5) == fs.FS_ERR_INVALID_ARG
+    assert L.fs_set_attention_timeline(ctypes.c_void_p(256), 0) == fs.FS_ERR_INVALID_ARG
+    assert L.fs_set_attention_timeline(ctypes.c_void_p(256), -2) == fs.FS_ERR_INVALID_ARG
+    assert L.fs_set_attention_timeline(None, 0) == fs.FS_OK
