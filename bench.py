@@ -37,8 +37,8 @@ UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 E2E_HEADS = 2  # heads per group of the host-buffer pipeline (2.60 ms per call vs 2.73 for 4, 3.15 for 8)
 # dram__bytes_read.sum + dram__bytes_write.sum of fs_attn_tc_kernel in one ncu
-# capture (fsl_16k_b2: 281.88 + 102.66 MB over 2*16*16384 token-heads)
-ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (281.875968e6 + 102.657792e6) / (2 * 16 * 16384)
+# capture (fsl_16k_b2: 281.92 + 106.35 MB over 2*16*16384 token-heads)
+ATTN_DRAM_BYTES_PER_TOKEN_HEAD = (281.918208e6 + 106.351104e6) / (2 * 16 * 16384)
 
 
 # ---------------------------------------------------------------------------
