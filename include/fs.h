@@ -95,8 +95,9 @@ const char *fs_last_cuda_error(void);
  * global timer, in ns, at its start and at its end into timeline[2 * cta] and
  * timeline[2 * cta + 1]: the spread of the CTAs' finish times shows how well
  * the q-tiles were balanced.  timeline is device memory of `entries` int64,
- * owned by the caller; a launch of more than entries / 2 CTAs records
- * nothing.  (NULL, 0) turns it off.  FS_ERR_INVALID_ARG when exactly one of
+ * owned by the caller, which must keep it allocated until it turns the
+ * timeline off again (the library keeps only the pointer); a launch of more
+ * than entries / 2 CTAs records nothing.  (NULL, 0) turns it off.  FS_ERR_INVALID_ARG when exactly one of
  * timeline and entries is zero, or entries < 0. */
 int fs_set_attention_timeline(long long *timeline, int entries);
 

@@ -615,13 +615,19 @@ def fs_set_attention_timeline(buf=None):
     """Record each CTA's start and end (device global timer, ns) of the calling
     thread's following attention launches into ``buf`` (a CUDA int64 tensor,
     two entries per CTA); ``None`` turns it off."""
+    global _timeline_buf
     L = load()
     if buf is None:
         _check(L.fs_set_attention_timeline(None, 0), "fs_set_attention_timeline")
+        _timeline_buf = None
         return
     if not (buf.is_cuda and buf.dtype == torch.int64 and buf.is_contiguous()):
         raise ValueError("timeline must be a contiguous CUDA int64 tensor")
     _check(L.fs_set_attention_timeline(_ptr(buf), buf.numel()), "fs_set_attention_timeline")
+    _timeline_buf = buf  # the library keeps only the pointer: keep the memory alive
+
+
+_timeline_buf = None
 
 
 def fs_check_status(ws, stream=None):
