@@ -530,17 +530,19 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
   // warp 0: lane l takes dimensions 2l, 2l + 1 of both branches; the CTAs'
   // partials are added in CTA order
   if (warp == 0) {
-    float mt[2], lt[2];
+    // each CTA's scale exp(m_c - M) per branch, once; then the sums
+    float sc[2][kCluster], lt[2];
 #pragma unroll
     for (int br = 0; br < 2; ++br) {
       float m = s_cm[br][0];
 #pragma unroll
       for (int c = 1; c < kCluster; ++c) m = fmaxf(m, s_cm[br][c]);
-      mt[br] = m;
       float l = 0.f;
 #pragma unroll
-      for (int c = 0; c < kCluster; ++c)
-        l = fmaf(s_cl[br][c], s_cm[br][c] == -INFINITY ? 0.f : __expf(s_cm[br][c] - m), l);
+      for (int c = 0; c < kCluster; ++c) {
+        sc[br][c] = s_cm[br][c] == -INFINITY ? 0.f : __expf(s_cm[br][c] - m);
+        l = fmaf(s_cl[br][c], sc[br][c], l);
+      }
       lt[br] = l;
     }
     float owin[2], olong[2];
@@ -550,10 +552,8 @@ __global__ void __launch_bounds__(kThreads) k6_decode_kernel(const StepParams p)
       float ow = 0.f, ol = 0.f;
 #pragma unroll
       for (int c = 0; c < kCluster; ++c) {
-        const float sw = s_cm[0][c] == -INFINITY ? 0.f : __expf(s_cm[0][c] - mt[0]);
-        const float sl = s_cm[1][c] == -INFINITY ? 0.f : __expf(s_cm[1][c] - mt[1]);
-        ow = fmaf(s_co[0][c][dim], sw, ow);
-        ol = fmaf(s_co[1][c][dim], sl, ol);
+        ow = fmaf(s_co[0][c][dim], sc[0][c], ow);
+        ol = fmaf(s_co[1][c][dim], sc[1][c], ol);
       }
       owin[e] = ow / lt[0];
       olong[e] = nsel > 0 ? ol / lt[1] : 0.f;
