@@ -342,7 +342,10 @@ int fs_attention_fwd(const void *q, const void *k, const void *v, int dtype,
  * The forward's selection stages run again inside the call (cell summaries,
  * pools, scores and top-K, bit-identical to the forward's).  dk and dv of the
  * long branch are accumulated with fp32 atomic additions, so their last bits
- * can differ between runs; everything else is deterministic. */
+ * can differ between runs; everything else is deterministic.  The window
+ * branch's kernels run on the tensor cores with bounded waits: a wait that
+ * gives up records FS_ERR_TIMEOUT in the workspace's status word
+ * (fs_check_status(ws)). */
 size_t fs_backward_workspace_bytes(int batch, int H, int N, int d,
                                    const fs_params *p);
 int fs_attention_bwd(const void *q, const void *k, const void *v, int dtype,

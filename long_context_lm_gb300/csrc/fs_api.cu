@@ -706,6 +706,7 @@ extern "C" int fs_attention_bwd(const void *q, const void *k, const void *v, int
   a.dv = dv;
   a.dmix = dmix;
   a.ws = base + L.total;
+  a.err = err;
   return status_of(launch_backward(a, st));
 }
 

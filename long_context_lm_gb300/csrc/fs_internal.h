@@ -129,6 +129,7 @@ struct BwdArgs {
   float rope_base, rms_eps;
   float *dq, *dk, *dv, *dmix;
   void *ws;                // backward_workspace_bytes
+  int *err;                // bounded-wait failures (FS_ERR_TIMEOUT)
 };
 size_t backward_workspace_bytes(const Shape &sh);
 cudaError_t launch_backward(const BwdArgs &a, cudaStream_t st);

@@ -19,6 +19,8 @@
 // fp64 and an fp32 sincospi; an absolute angle is composed from its two rows
 // by the angle-sum identity in fp32 (error of a few fp32 ulps, independent of
 // the position).
+#include <cmath>
+
 #include "cell_summary.cuh"
 #include "fs_common.cuh"
 #include "fs_internal.h"
@@ -27,23 +29,23 @@
 namespace fs {
 namespace {
 
-// theta_i / pi per block in fp64 (32 pow calls), then per entry one fp64
-// product reduced modulo 2 exactly and an fp32 sincospi of the remainder: the
-// fp64 work is a multiply and a floor, not a trigonometric evaluation (fp64
-// throughput is small on this chip).  Entry error: the fp32 rounding of the
-// reduced angle (<= 2^-24 * pi rad) plus sincospif's ulp, against the fp64
-// reference values.
+// theta_i / pi in fp64, formed once on the host
+struct Theta {
+  double over_pi[kD / 2];
+};
+
+// Per entry one fp64 product reduced modulo 2 exactly and an fp32 sincospi of
+// the remainder: the fp64 work is a multiply and a floor, not a trigonometric
+// evaluation (fp64 throughput is small on this chip).  Entry error: the fp32
+// rounding of the reduced angle (<= 2^-24 * pi rad) plus sincospif's ulp,
+// against the fp64 reference values.
 __global__ void __launch_bounds__(256) rope_table_kernel(float2 *__restrict__ tab, int rows,
-                                                         double base) {
-  __shared__ double s_th[kD / 2];
-  if (threadIdx.x < kD / 2)
-    s_th[threadIdx.x] = pow(base, -2.0 * (double)threadIdx.x / (double)kD) / 3.14159265358979323846;
-  __syncthreads();
+                                                         const Theta th) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * (kD / 2)) return;
   const int row = idx / (kD / 2), i = idx % (kD / 2);
   const double pos = row < 64 ? (double)row : 64.0 * (double)(row - 64);
-  const double x = pos * s_th[i];                // angle / pi
+  const double x = pos * th.over_pi[i];          // angle / pi
   const double r = x - 2.0 * floor(0.5 * x);     // in [0, 2), exact
   float sn, cs;
   sincospif((float)r, &sn, &cs);
@@ -206,8 +208,11 @@ size_t rope_table_bytes(int N) { return (size_t)(64 + (N + 63) / 64) * (kD / 2) 
 
 cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st) {
   const int rows = 64 + (N + 63) / 64;
+  Theta th;
+  for (int i = 0; i < kD / 2; ++i)
+    th.over_pi[i] = std::pow((double)rope_base, -2.0 * i / (double)kD) / 3.14159265358979323846;
   rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(static_cast<float2 *>(tab),
-                                                                  rows, (double)rope_base);
+                                                                  rows, th);
   return cudaGetLastError();
 }
 

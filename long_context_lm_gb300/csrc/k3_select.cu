@@ -97,8 +97,8 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
   const int r = tid;  // query row of a scoring thread
   const int n = b0 + r;
   const float lam = lambda[h], sig_s = sigma[h] * (1.0f / kS);
-  // ranked top-K (u desc, c asc) in registers; (wu, wc) mirrors the K-th
-  // entry so that most candidates are rejected by one comparison
+  // ranked top-K (u desc, c asc) in registers; wu mirrors the K-th score,
+  // so that a group of candidates that no row can take costs one comparison each
   float bu[K];
   int bc[K];
 #pragma unroll
@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
     bc[i] = kInvalid;
   }
   float wu = -INFINITY;
-  int wc = kInvalid;
   bool ok = true;
 
   for (int base = 0, chunk = 0; base < count; base += kChunk, ++chunk) {
@@ -203,10 +202,8 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
         uint32_t d[32];
         tc::tmem_ld32(taddr + j0, d);  // columns past np are read, never used
         tc::tmem_wait_ld();
-#pragma unroll
         // sixteen candidates at a time: their scores, then one warp vote on
-        // whether any lane's row ranks one of them before its K-th entry
-        // (one vote per 16: 163 us at 64k, against 169 per 8 and 168 per 4)
+        // whether any lane's row may take one of them (score >= its K-th)
 #pragma unroll
         for (int j16 = 0; j16 < 32; j16 += 16) {
           if (j16 == 16 && j0 + 16 >= np) break;  // np is a multiple of 16
@@ -229,29 +226,28 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
             }
             u16[e] = u;
             c16[e] = c;
-            any16 |= ranks_before(u, c, wu, wc);
+            any16 |= u >= wu;  // a superset of the candidates that rank before the K-th
           }
           if (!__any_sync(0xffffffffu, any16)) continue;
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            // one warp-uniform test; the insertion itself is predicated (no
-            // per-lane branches)
-            const bool ins = ranks_before(u16[e], c16[e], wu, wc);
-            if (!__any_sync(0xffffffffu, ins)) continue;
-            int cu = ins ? c16[e] : kInvalid;
-            float u = ins ? u16[e] : -INFINITY;
+            // where the candidate goes: its rank against each kept entry, all
+            // tests independent (the list is sorted, so they are monotone in
+            // k); then every entry moves in one step.  A lane whose row does
+            // not take it fails every test and keeps its list.
+            const float u = u16[e];
+            const int cu = c16[e];
+            bool s[K];
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
-              const bool sw = ranks_before(u, cu, bu[k], bc[k]);
-              const float tu = bu[k];
-              const int tcc = bc[k];
-              bu[k] = sw ? u : tu;
-              bc[k] = sw ? cu : tcc;
-              u = sw ? tu : u;
-              cu = sw ? tcc : cu;
+            for (int k = 0; k < K; ++k) s[k] = ranks_before(u, cu, bu[k], bc[k]);
+#pragma unroll
+            for (int k = K - 1; k > 0; --k) {
+              bu[k] = s[k] ? (s[k - 1] ? bu[k - 1] : u) : bu[k];
+              bc[k] = s[k] ? (s[k - 1] ? bc[k - 1] : cu) : bc[k];
             }
+            bu[0] = s[0] ? u : bu[0];
+            bc[0] = s[0] ? cu : bc[0];
             wu = bu[K - 1];
-            wc = bc[K - 1];
           }
         }
       }
