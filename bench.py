@@ -453,11 +453,12 @@ def time_prologue(B, N, H, stream, D=1024, iters=10):
 
 def time_backward(q, k, v, lam, sigma, mix, params, stream, counts, iters=3):
     """fs_attention_bwd on the benchmark's inputs with a random upstream
-    gradient (the forward's selection recomputed inside the call).  Its
-    kernels work in fp32 on the CUDA cores: the roofline is the fp32 FMA rate
-    (152 SMs x 128 FMA per clock x 2.07 GHz), the work the executed FMA of
-    the design: 576 per (query, window key) pair (query side 320, key side
-    256) and 576 per (query, selected token) pair of the long branch."""
+    gradient (the forward's selection recomputed inside the call).  Every
+    contraction runs on the tensor cores (bf16 operands split hi | lo where
+    fp32 inputs need it), so the roofline is the bf16 tensor peak and the
+    work the useful flops of the plain algorithm: 640 per (query, window key)
+    pair (S, dP, dv, dq, dk: 2 x 64 each) and 768 per (query, selected token)
+    pair of the long branch (the same plus the recomputed o)."""
     from long_context_lm_gb300 import fs
     B, H, N, d = q.shape
     g = torch.randn((B, H, N, d), device=q.device, dtype=torch.float32)
@@ -467,12 +468,13 @@ def time_backward(q, k, v, lam, sigma, mix, params, stream, counts, iters=3):
                 iters)
     n = np.arange(N, dtype=np.float64)
     win_pairs = B * H * float(np.minimum(n + 1, params.w).sum())
-    fma = 576.0 * win_pairs + 576.0 * float(counts["tokens_read"])
-    peak = 152 * 128 * 2 * 2.07e9 / 1e12  # TFLOP/s, fp32 FMA
-    ach = 2 * fma / (ms / 1e3) / 1e12
-    return {"ms": ms, "tokens_per_s": B * N / (ms / 1e3), "bound": "alu",
-            "achieved_TFLOP/s": ach, "peak_TFLOP/s": peak, "frac": ach / peak,
-            "note": "fp32 CUDA-core kernels; includes recomputing the forward's selection"}
+    flops = 640.0 * win_pairs + 768.0 * float(counts["tokens_read"])
+    pk = peaks()
+    ach = flops / (ms / 1e3) / 1e12
+    return {"ms": ms, "tokens_per_s": B * N / (ms / 1e3), "bound": "tensor",
+            "achieved_TFLOP/s": ach, "peak_TFLOP/s": pk["bf16"], "frac": ach / pk["bf16"],
+            "note": "tcgen05 kernels (window: query side and key side; long branch: union "
+                    "tiles); useful flops; includes recomputing the forward's selection"}
 
 
 def time_decode(q, k, v, lam, sigma, mix, params, stream, steps=256, warm=8):

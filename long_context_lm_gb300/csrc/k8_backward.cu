@@ -33,54 +33,6 @@
 namespace fs {
 namespace {
 
-constexpr int kQT = 128;  // query tile
-constexpr float kScale = 0.125f;  // 1 / sqrt(64)
-// shared-memory rows of 64 floats keep dims 32..63 four words further (column
-// c at c + 4 * (c / 32)): the two threads of a row read the same element
-// index of their halves at the same time, which then sit in different banks,
-// and both halves stay 16-byte aligned for vector loads
-constexpr int kRow = kD + 4;
-constexpr int kH1 = 36;  // first column of the second half
-__device__ __forceinline__ int col(int c) { return c + 4 * (c >> 5); }
-
-// dot of 32 register values with 32 consecutive shared floats (16-byte
-// aligned), four independent partial sums
-__device__ __forceinline__ float dot32(const float (&a)[32], const float *s) {
-  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    const float4 b = *reinterpret_cast<const float4 *>(s + e);
-    p0 = fmaf(a[e], b.x, p0);
-    p1 = fmaf(a[e + 1], b.y, p1);
-    p2 = fmaf(a[e + 2], b.z, p2);
-    p3 = fmaf(a[e + 3], b.w, p3);
-  }
-  return (p0 + p1) + (p2 + p3);
-}
-// acc += f * s[0..32)
-__device__ __forceinline__ void axpy32(float (&acc)[32], float f, const float *s) {
-#pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    const float4 b = *reinterpret_cast<const float4 *>(s + e);
-    acc[e] = fmaf(f, b.x, acc[e]);
-    acc[e + 1] = fmaf(f, b.y, acc[e + 1]);
-    acc[e + 2] = fmaf(f, b.z, acc[e + 2]);
-    acc[e + 3] = fmaf(f, b.w, acc[e + 3]);
-  }
-}
-
-__device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
-
-struct BwdParams {
-  const uint16_t *q, *k, *v;       // [BH, N, 64] bf16
-  const float *g;                  // upstream gradient [BH, N, 64]
-  const int32_t *sel;              // [BH, N, K]
-  const float *mix;
-  float *dq, *dk, *dv, *dmix;      // outputs
-  int H, N, K;
-  float rms_eps;
-};
-
 // ---------------------------------------------------------------------------
 // window branch on the tensor cores (tcgen05, TMEM accumulators)
 // ---------------------------------------------------------------------------
@@ -550,204 +502,430 @@ __global__ void __launch_bounds__(kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
 }
 
 // ---------------------------------------------------------------------------
-// long branch
+// long branch on the tensor cores
 // ---------------------------------------------------------------------------
-constexpr int kMaxU = kBq * kMaxK;
+// One CTA per (head, 128-query tile), thread r = TMEM lane r = query row r.
+// The union of the tile's selected cells (ascending) is cut into long tiles
+// of four cells (128 tokens, raw bf16 k and v gathered into shared memory);
+// a row reads only the cells it picked, the other columns of a tile are
+// masked.  q and k are exact in bf16, so S = q k^T is one MMA chain; the
+// forward's P, the gradient do and dS are split hi | lo like the window's.
+//   pass A  S per tile: the row maximum;
+//   pass B  S again, P = 2^(s/8 - m), l, o += P v: o, RMSNorm, dm_h, do, lse;
+//   pass C  S and dP = do v^T: dS = P (dP - do.o) / 8, dq += dS k; then the
+//           tile transposed (tokens in the lanes): S^T, dP^T, P^T, dS^T from
+//           the rows' statistics, dv_t = P^T do and dk_t = dS^T q, added to
+//           the cells' rows with fp32 atomics (other query tiles read the
+//           same cells).
+constexpr uint32_t kLOffQ = 0;                  // q tile (bf16)
+constexpr uint32_t kLOffDo = kTileB;            // do hi, lo
+constexpr uint32_t kLOffK = 3 * kTileB;         // gathered keys
+constexpr uint32_t kLOffV = 4 * kTileB;         // gathered values
+constexpr uint32_t kLOffStat = 5 * kTileB;      // lse2[128], dodo[128], rmask[128]
+constexpr uint32_t kLOffUl = kLOffStat + 3 * kT * 4;  // union list (<= 128 K ids)
+constexpr uint32_t kLOffBm = kLOffUl + kT * kMaxK * 4;  // bitmap words, then word ranks
+constexpr uint32_t kColO = 256, kColDv = 320, kColDk = 384;
 
-__global__ void __launch_bounds__(256) k8_long_kernel(const BwdParams p) {
-  __shared__ __align__(16) float s_k[kS][kRow];
-  __shared__ __align__(16) float s_v[kS][kRow];
-  __shared__ int s_ul[kMaxU];
+__host__ __device__ inline uint32_t long_bwd_smem(int N) {
+  const uint32_t nwd = (uint32_t)((N / kS + 31) / 32);
+  return kLOffBm + nwd * 4 + (nwd * 2 + 15) / 16 * 16 + 1024;
+}
+
+struct LongBwd {
+  const unsigned char *q, *k, *v;  // bf16 rows, 128 B each
+  const float *g;
+  const int32_t *sel;
+  const float *mix;
+  float *dq, *dk, *dv, *dmix;
+  int H, N, K;
+  float rms_eps;
+  int *err;
+};
+
+// 128 token rows of a long tile: row i is token i % 32 of union cell
+// slot 4t + i / 32; rows past the union are zeros
+__device__ __forceinline__ void load_cells(unsigned char *dst, const unsigned char *x,
+                                           size_t head, const int *ul, int slot0, int nu) {
+  for (int e = threadIdx.x; e < kT * 8; e += kT) {
+    const int i = e >> 3, ch = e & 7, sl = slot0 + (i >> 5);
+    unsigned char *d = dst + swz128(i, ch);
+    if (sl < nu)
+      cp_async16(d, x + (head + (size_t)ul[sl] * kS + (i & 31)) * 128 + 16 * ch);
+    else
+      *reinterpret_cast<uint4 *>(d) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// D (+)= A(tmem, packed pairs; hi at +0, lo at +16 per chunk) . B over 128
+// rows, the A halves given by `parts` (1: hi; 2: hi, lo)
+__device__ __forceinline__ void mma_r128_parts(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                               bool acc, int parts) {
+  for (int part = 0; part < parts; ++part) mma_r128(d, a + 16u * part, b, id, acc || part > 0);
+}
+
+__global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ uint32_t s_tmem;
   __shared__ int s_nu;
-  __shared__ float s_red[8];
-  __shared__ int s_pick[kQT][kMaxK];  // the tile's rows' selected cells
-  extern __shared__ float dyn[];  // per row: q (64), do (64), lse, do.o
-  const int tid = threadIdx.x, half = tid & 1, r = tid >> 1;
-  const int nblk = p.N / kQT;
-  const int bh = blockIdx.x / nblk, b0 = (blockIdx.x % nblk) * kQT, h = bh % p.H;
-  const int n = b0 + r;
-  const size_t row = (size_t)bh * p.N + n;
-  const int A = b0 / kS;
-  // union of the tile's selected cells, ascending (repeated minimum, warp 0)
-  if (tid < 32) {
-    int cnt = 0, last = -1;
-    while (true) {
-      int mn = 0x7fffffff;
-      for (int e = tid; e < kQT * p.K; e += 32) {
-        const int c = p.sel[((size_t)bh * p.N + b0) * p.K + e];
-        if (c >= 0 && c < A && c > last) mn = min(mn, c);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      if (mn == 0x7fffffff) break;
-      if (tid == 0) s_ul[cnt] = mn;
-      ++cnt;
-      last = mn;
-    }
-    if (tid == 0) s_nu = cnt;
+  __shared__ float s_red[4];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nblk = p.N / kT;
+  const int bh = blockIdx.x / nblk, b0 = (blockIdx.x % nblk) * kT, h = bh % p.H;
+  const int n = b0 + tid;
+  const size_t head = (size_t)bh * p.N;
+  const int A = b0 / kS;  // cells available to the tile
+  if (A == 0) return;     // the first block has no long branch: nothing to add
+  const uint32_t sb = smem_u32(smem);
+  float *s_lse2 = reinterpret_cast<float *>(smem + kLOffStat);
+  float *s_dodo = s_lse2 + kT;
+  int *s_rmask = reinterpret_cast<int *>(s_dodo + kT);
+  int *ul = reinterpret_cast<int *>(smem + kLOffUl);
+  const int nwd = (A + 31) / 32;
+  uint32_t *bm = reinterpret_cast<uint32_t *>(smem + kLOffBm);
+  uint16_t *pw = reinterpret_cast<uint16_t *>(bm + nwd);
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, kBwdTmem);
+    tc::tmem_relinquish();
   }
-  for (int e = tid; e < kQT * kMaxK; e += 256) {
-    const int rr = e / kMaxK, k = e % kMaxK;
-    s_pick[rr][k] = k < p.K ? p.sel[((size_t)bh * p.N + b0 + rr) * p.K + k] : -1;
+  if (tid == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::mbar_fence_init();
   }
+  load_tile(smem + kLOffQ, p.q + (head + b0) * 128, 128, 0);
+  cp_async_commit();
+  for (int w = tid; w < nwd; w += kT) bm[w] = 0u;
   __syncthreads();
-  const int nu = s_nu;
+  // union: mark, rank the words (warp 0), then each pick's slot
   int pick[kMaxK];
 #pragma unroll
-  for (int k = 0; k < kMaxK; ++k) pick[k] = k < p.K ? p.sel[row * p.K + k] : -1;
-  float qh[32], acc[32];
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    qh[e] = bf(p.q[row * kD + 32 * half + e]) * kScale;
-    acc[e] = 0.f;
-  }
-  float m = -INFINITY, l = 0.f;
-  // pass 1: softmax over the row's selected tokens (union order) and o
-  for (int u = 0; u < nu; ++u) {
-    const int c = s_ul[u];
-    __syncthreads();
-    for (int e = tid; e < kS * kD; e += 256) {
-      const size_t src = ((size_t)bh * p.N + (size_t)c * kS + e / kD) * kD + e % kD;
-      s_k[e / kD][col(e % kD)] = bf(p.k[src]);
-      s_v[e / kD][col(e % kD)] = bf(p.v[src]);
-    }
-    __syncthreads();
-    bool mine = false;
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) mine |= pick[k] == c;
-    if (!mine) continue;  // both threads of the row agree
-    for (int t = 0; t < kS; ++t) {
-      const float part = dot32(qh, &s_k[t][kH1 * half]);
-      const float sc = part + __shfl_xor_sync(0x3u << (tid & 30), part, 1);
-      if (sc > m) {
-        const float f = __expf(m - sc);
-        l *= f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] *= f;
-        m = sc;
-      }
-      const float pe = __expf(sc - m);
-      l += pe;
-      axpy32(acc, pe, &s_v[t][kH1 * half]);
-    }
-  }
-  const bool has = l > 0.f;
-  // RMSNorm, mix weight, and do
-  float gh[32], doh[32];
-  float ss = 0.f, og = 0.f, dmx = 0.f;
-  const float mh = p.mix[h];
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    acc[e] = has ? acc[e] / l : 0.f;
-    gh[e] = p.g[row * kD + 32 * half + e];
-    ss = fmaf(acc[e], acc[e], ss);
-    og = fmaf(acc[e], mh * gh[e], og);
-  }
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  og += __shfl_xor_sync(0xffffffffu, og, 1);
-  const float rho = has ? rsqrtf(ss / kD + p.rms_eps) : 0.f;
-  float dodo = 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    dmx = fmaf(gh[e], acc[e] * rho, dmx);
-    doh[e] = rho * mh * gh[e] - rho * rho * rho * og * acc[e] / kD;
-    dodo = fmaf(doh[e], acc[e], dodo);
-  }
-  dodo += __shfl_xor_sync(0xffffffffu, dodo, 1);
-  const float lse = m + __logf(l);
-  // dm_h: the tile's sum, one atomic per CTA
-  const float dmx2 = dmx + __shfl_xor_sync(0xffffffffu, dmx, 1);
-  const float bs = warp_sum(half == 0 ? dmx2 : 0.f);
-  if ((tid & 31) == 0) s_red[tid >> 5] = bs;
-  // per-row values the scatter pass reads
-  float *rq = dyn + (size_t)r * (2 * kD + 2);
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    rq[32 * half + e] = qh[e];
-    rq[kD + 32 * half + e] = has ? doh[e] : 0.f;
-  }
-  if (half == 0) {
-    rq[2 * kD] = lse;
-    rq[2 * kD + 1] = dodo;
+  for (int k = 0; k < kMaxK; ++k) {
+    const int c = k < p.K ? p.sel[(head + n) * p.K + k] : -1;
+    pick[k] = (c >= 0 && c < A) ? c : -1;
+    if (pick[k] >= 0) atomicOr(bm + (pick[k] >> 5), 1u << (pick[k] & 31));
   }
   __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int i = 0; i < 8; ++i) t += s_red[i];
-    atomicAdd(p.dmix + h, t);
-  }
-  // pass 2: dq from the selected tokens
+  if (warp == 0) {
+    int nu = 0;
+    for (int w0 = 0; w0 < nwd; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t bits = w < nwd ? bm[w] : 0u;
+      const int cnt = __popc(bits);
+      int incl = cnt;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-  for (int u = 0; u < nu; ++u) {
-    const int c = s_ul[u];
-    __syncthreads();
-    for (int e = tid; e < kS * kD; e += 256) {
-      const size_t src = ((size_t)bh * p.N + (size_t)c * kS + e / kD) * kD + e % kD;
-      s_k[e / kD][col(e % kD)] = bf(p.k[src]);
-      s_v[e / kD][col(e % kD)] = bf(p.v[src]);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int kk = nu + incl - cnt;
+      if (w < nwd) pw[w] = (uint16_t)kk;
+      while (bits) {
+        ul[kk++] = 32 * w + (__ffs(bits) - 1);
+        bits &= bits - 1;
+      }
+      nu += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncthreads();
-    bool mine = false;
+    if (lane == 0) s_nu = nu;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const int nu = s_nu, nt = (nu + 3) / 4;
+  int slot[kMaxK];
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) mine |= pick[k] == c;
-    if (mine) {
-      for (int t = 0; t < kS; ++t) {
-        const float ps = dot32(qh, &s_k[t][kH1 * half]);
-        const float pd = dot32(doh, &s_v[t][kH1 * half]);
-        const float sc = ps + __shfl_xor_sync(0x3u << (tid & 30), ps, 1);
-        const float dp = pd + __shfl_xor_sync(0x3u << (tid & 30), pd, 1);
-        const float ds = __expf(sc - lse) * (dp - dodo) * kScale;
-        axpy32(acc, ds, &s_k[t][kH1 * half]);
+  for (int k = 0; k < kMaxK; ++k) {
+    const int c = pick[k];
+    slot[k] = c < 0 ? -1 : pw[c >> 5] + __popc(bm[c >> 5] & ((1u << (c & 31)) - 1u));
+  }
+  const uint32_t tmem = s_tmem, lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t id_s = tc::idesc_bf16(kT, kT, 0), id_o = tc::idesc_bf16(kT, kD, 1);
+  const uint64_t dq_ = tc::desc_sw128(sb + kLOffQ);
+  const uint64_t ddh = tc::desc_sw128(sb + kLOffDo), ddl = tc::desc_sw128(sb + kLOffDo + kTileB);
+  const uint64_t dk_ = tc::desc_sw128(sb + kLOffK), dv_ = tc::desc_sw128(sb + kLOffV);
+  const float sl2 = 1.4426950408889634f * 0.125f;
+  uint32_t ph0 = 0, ph1 = 0;
+  bool ok = true;
+  float m = -INFINITY, l = 0.f;
+  // which of tile t's four cells this row reads (bit c)
+  auto row_mask = [&](int t) {
+    int mk = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k)
+      if (slot[k] >= 4 * t && slot[k] < 4 * t + 4) mk |= 1 << (slot[k] - 4 * t);
+    return mk;
+  };
+  // ---- pass A: row maxima
+  for (int t = 0; t < nt; ++t) {
+    load_cells(smem + kLOffK, p.k, head, ul, 4 * t, nu);
+    cp_async_commit();
+    cp_async_wait<0>();
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == 0) {
+      mma_d64(tmem + kColSt, dq_, dk_, id_s, false);
+      tc::mma_commit(&bar[0]);
+    }
+    ok = tc::mbar_wait(&bar[0], ph0, p.err) && ok;
+    ph0 ^= 1;
+    tc::fence_after_sync();
+    const int mk = row_mask(t);
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      if (!__any_sync(0xffffffffu, (mk >> ch) & 1)) continue;  // warp-uniform
+      uint32_t xs[32];
+      tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
+      tc::tmem_wait_ld();
+      if ((mk >> ch) & 1) {
+        float cm = __uint_as_float(xs[0]);
+#pragma unroll
+        for (int e = 1; e < 32; ++e) cm = fmaxf(cm, __uint_as_float(xs[e]));
+        m = fmaxf(m, cm * sl2);
       }
     }
-    // scatter: dk, dv of cell c from the tile's rows that picked it; thread
-    // (token t = tid / 8, dims 8*(tid % 8) ..) sums over those rows
-    const int t = tid >> 3, d0 = 8 * (tid & 7);
-    float kt[8], vt[8], dk8[8], dv8[8];
+  }
+  // ---- pass B: P, l and o += P v
+  ok = cta_sync_ok(ok);
+  for (int t = 0; t < nt; ++t) {
+    load_cells(smem + kLOffK, p.k, head, ul, 4 * t, nu);
+    load_cells(smem + kLOffV, p.v, head, ul, 4 * t, nu);
+    cp_async_commit();
+    cp_async_wait<0>();
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == 0) {
+      mma_d64(tmem + kColSt, dq_, dk_, id_s, false);
+      tc::mma_commit(&bar[0]);
+    }
+    ok = tc::mbar_wait(&bar[0], ph0, p.err) && ok;
+    ph0 ^= 1;
+    tc::fence_after_sync();
+    const int mk = row_mask(t);
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t xs[32];
+      tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
+      tc::tmem_wait_ld();
+      const bool vis = (mk >> ch) & 1;
+      float x[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        x[e] = vis ? tc::ex2(fmaf(__uint_as_float(xs[e]), sl2, -m)) : 0.f;
+        l += x[e];
+      }
+      store_split(tmem + kColSt + 32 * ch + lane_base, x);
+    }
+    tc::tmem_wait_st();
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == 0) {
+      mma_r128_parts(tmem + kColO, tmem + kColSt, dv_, id_o, t > 0, 2);
+      tc::mma_commit(&bar[1]);
+    }
+    ok = tc::mbar_wait(&bar[1], ph1, p.err) && ok;
+    ph1 ^= 1;
+    tc::fence_after_sync();
+  }
+  ok = cta_sync_ok(ok);
+  // ---- the row's RMSNorm, dm_h, do, lse
+  const bool has = l > 0.f;
+  float lse2 = 0.f, dodo = 0.f, dmx = 0.f;
+  if (ok) {
+    float o[64];
+    {
+      uint32_t r0[32], r1[32];
+      tc::tmem_ld32(tmem + kColO + lane_base, r0);
+      tc::tmem_ld32(tmem + kColO + 32 + lane_base, r1);
+      tc::tmem_wait_ld();
+      const float il = has ? 1.f / l : 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        // (selects, not products: with no long tile the columns were never written)
+        o[e] = has ? __uint_as_float(r0[e]) * il : 0.f;
+        o[32 + e] = has ? __uint_as_float(r1[e]) * il : 0.f;
+      }
+    }
+    const float mh = p.mix[h];
+    const float4 *gr = reinterpret_cast<const float4 *>(p.g + (head + n) * kD);
+    float ss = 0.f, og = 0.f;
+#pragma unroll
+    for (int e4 = 0; e4 < 16; ++e4) {
+      const float4 g4 = __ldg(gr + e4);
+      const float ge[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float oe = o[4 * e4 + u];
+        ss = fmaf(oe, oe, ss);
+        og = fmaf(oe, mh * ge[u], og);
+        dmx = fmaf(ge[u], oe, dmx);
+      }
+    }
+    const float rho = has ? rsqrtf(ss / kD + p.rms_eps) : 0.f;
+    dmx *= rho;
+    const float c3 = rho * rho * rho * og / kD;
+    // do = rho m_h g - rho^3 (o . m_h g) o / d, written split into shared memory
+    unsigned char *dh = smem + kLOffDo, *dl = smem + kLOffDo + kTileB;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      const float4 ga = __ldg(gr + 2 * ch), gb = __ldg(gr + 2 * ch + 1);
+      const float ge[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+      float dv8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        dv8[u] = has ? rho * mh * ge[u] - c3 * o[8 * ch + u] : 0.f;
+        dodo = fmaf(dv8[u], o[8 * ch + u], dodo);
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        hi[u] = pack_bf16(dv8[2 * u], dv8[2 * u + 1]);
+        lo[u] = pack_bf16(dv8[2 * u] - bf16_lo(hi[u]), dv8[2 * u + 1] - bf16_hi(hi[u]));
+      }
+      *reinterpret_cast<uint4 *>(dh + swz128(tid, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>(dl + swz128(tid, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    lse2 = has ? m + __log2f(l) : 0.f;
+  }
+  s_lse2[tid] = lse2;
+  s_dodo[tid] = dodo;
+  dmx = warp_sum(dmx);
+  if (lane == 0) s_red[warp] = dmx;
+  ok = cta_sync_ok(ok);
+  if (tid == 0 && ok) atomicAdd(p.dmix + h, (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]));
+  // ---- pass C: dq from the rows' side, then dk, dv from the tokens' side
+  for (int t = 0; t < nt; ++t) {
+    load_cells(smem + kLOffK, p.k, head, ul, 4 * t, nu);
+    load_cells(smem + kLOffV, p.v, head, ul, 4 * t, nu);
+    cp_async_commit();
+    cp_async_wait<0>();
+    ok = cta_sync_ok(ok);  // also publishes do (generic stores) to the tensor core
+    if (!ok) break;
+    if (tid == 0) {
+      mma_d64(tmem + kColSt, dq_, dk_, id_s, false);
+      mma_d64(tmem + kColDp, ddh, dv_, id_s, false);
+      mma_d64(tmem + kColDp, ddl, dv_, id_s, true);
+      tc::mma_commit(&bar[0]);
+    }
+    ok = tc::mbar_wait(&bar[0], ph0, p.err) && ok;
+    ph0 ^= 1;
+    tc::fence_after_sync();
+    const int mk = row_mask(t);
+    s_rmask[tid] = mk;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t xs[32], xd[32];
+      tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
+      tc::tmem_ld32(tmem + kColDp + 32 * ch + lane_base, xd);
+      tc::tmem_wait_ld();
+      const bool vis = (mk >> ch) & 1;
+      float x[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float pe = vis ? tc::ex2(fmaf(__uint_as_float(xs[e]), sl2, -lse2)) : 0.f;
+        x[e] = pe * (__uint_as_float(xd[e]) - dodo) * 0.125f;
+      }
+      store_split(tmem + kColSt + 32 * ch + lane_base, x);
+    }
+    tc::tmem_wait_st();
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == 0) {
+      mma_r128_parts(tmem + kColO, tmem + kColSt, dk_, id_o, t > 0, 2);  // dq += dS k
+      tc::mma_commit(&bar[1]);
+    }
+    ok = tc::mbar_wait(&bar[1], ph1, p.err) && ok;
+    ph1 ^= 1;
+    tc::fence_after_sync();
+    if (tid == 0 && ok) {  // the tile transposed: S^T = k q^T, dP^T = v do^T
+      mma_d64(tmem + kColSt, dk_, dq_, id_s, false);
+      mma_d64(tmem + kColDp, dv_, ddh, id_s, false);
+      mma_d64(tmem + kColDp, dv_, ddl, id_s, true);
+      tc::mma_commit(&bar[0]);
+    }
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    ok = tc::mbar_wait(&bar[0], ph0, p.err) && ok;
+    ph0 ^= 1;
+    tc::fence_after_sync();
+    const int cell = tid >> 5;  // this thread's token is token tid % 32 of cell slot 4t + cell
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t xs[32], xd[32];
+      tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
+      tc::tmem_ld32(tmem + kColDp + 32 * ch + lane_base, xd);
+      tc::tmem_wait_ld();
+      float pe[32], ds[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int r = 32 * ch + e;
+        const bool vis = (s_rmask[r] >> cell) & 1;
+        pe[e] = vis ? tc::ex2(fmaf(__uint_as_float(xs[e]), sl2, -s_lse2[r])) : 0.f;
+        ds[e] = pe[e] * (__uint_as_float(xd[e]) - s_dodo[r]) * 0.125f;
+      }
+      store_split(tmem + kColSt + 32 * ch + lane_base, pe);
+      store_split(tmem + kColDp + 32 * ch + lane_base, ds);
+    }
+    tc::tmem_wait_st();
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == 0) {
+      mma_r128_split(tmem + kColDv, tmem + kColSt, ddh, ddl, id_o, false);  // dv = P^T do
+      mma_r128_parts(tmem + kColDk, tmem + kColDp, dq_, id_o, false, 2);   // dk = dS^T q
+      tc::mma_commit(&bar[1]);
+    }
+    ok = tc::mbar_wait(&bar[1], ph1, p.err) && ok;
+    ph1 ^= 1;
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    const int sl = 4 * t + cell;
+    if (sl < nu) {  // (the loads below are whole-warp: sl is warp-uniform)
+      const size_t trow = head + (size_t)ul[sl] * kS + (tid & 31);
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        uint32_t r0[32], r1[32];
+        const uint32_t col = part ? kColDk : kColDv;
+        float *dst = (part ? p.dk : p.dv) + trow * kD;
+        tc::tmem_ld32(tmem + col + lane_base, r0);
+        tc::tmem_ld32(tmem + col + 32 + lane_base, r1);
+        tc::tmem_wait_ld();
+        float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          atomicAdd(d4 + e, make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
+                                        __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3])));
+          atomicAdd(d4 + 8 + e,
+                    make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
+                                __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3])));
+        }
+      }
+    }
+  }
+  ok = cta_sync_ok(ok);
+  if (ok && nt > 0) {  // dq of the long branch, added to the window's
+    uint32_t r0[32], r1[32];
+    tc::tmem_ld32(tmem + kColO + lane_base, r0);
+    tc::tmem_ld32(tmem + kColO + 32 + lane_base, r1);
+    tc::tmem_wait_ld();
+    float4 *o = reinterpret_cast<float4 *>(p.dq + (head + n) * kD);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      kt[e] = s_k[t][col(d0 + e)];
-      vt[e] = s_v[t][col(d0 + e)];
-      dk8[e] = 0.f;
-      dv8[e] = 0.f;
-    }
-    for (int rr = 0; rr < kQT; ++rr) {
-      bool picked = false;
-#pragma unroll
-      for (int k = 0; k < kMaxK; ++k) picked |= s_pick[rr][k] == c;
-      if (!picked) continue;  // the same for every thread
-      const float *rq2 = dyn + (size_t)rr * (2 * kD + 2);
-      float ps = 0.f, pd = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ps = fmaf(rq2[d0 + e], kt[e], ps);
-        pd = fmaf(rq2[kD + d0 + e], vt[e], pd);
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        pd += __shfl_xor_sync(0xffffffffu, pd, o);
-      }
-      const float pr = __expf(ps - rq2[2 * kD]);
-      const float ds = pr * (pd - rq2[2 * kD + 1]);  // the 1/8 is in the stored q
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        dv8[e] = fmaf(pr, rq2[kD + d0 + e], dv8[e]);
-        dk8[e] = fmaf(ds, rq2[d0 + e], dk8[e]);
-      }
-    }
-    const size_t trow = (size_t)bh * p.N + (size_t)c * kS + t;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      atomicAdd(p.dk + trow * kD + d0 + e, dk8[e]);
-      atomicAdd(p.dv + trow * kD + d0 + e, dv8[e]);
+      float4 a = o[e], b = o[8 + e];
+      a.x += __uint_as_float(r0[4 * e]); a.y += __uint_as_float(r0[4 * e + 1]);
+      a.z += __uint_as_float(r0[4 * e + 2]); a.w += __uint_as_float(r0[4 * e + 3]);
+      b.x += __uint_as_float(r1[4 * e]); b.y += __uint_as_float(r1[4 * e + 1]);
+      b.z += __uint_as_float(r1[4 * e + 2]); b.w += __uint_as_float(r1[4 * e + 3]);
+      o[e] = a;
+      o[8 + e] = b;
     }
   }
-  // dq of the long branch added to the window's (scale 1/8 applied here: the
-  // stored q was prescaled, k was not)
-#pragma unroll
-  for (int e = 0; e < 32; ++e) p.dq[row * kD + 32 * half + e] += acc[e];
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kBwdTmem);
+  }
 }
 
 }  // namespace
@@ -798,27 +976,27 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t st) {
       return e;
   k8_win_q_tc_kernel<<<ntile, kT, kBwdSmem, st>>>(w);
   k8_win_kv_tc_kernel<<<ntile, kT, kBwdSmem, st>>>(w);
-  BwdParams p;
-  p.q = static_cast<const uint16_t *>(a.q);
-  p.k = static_cast<const uint16_t *>(a.k);
-  p.v = static_cast<const uint16_t *>(a.v);
-  p.g = a.g;
-  p.sel = a.sel;
-  p.mix = a.mix;
-  p.dq = a.dq;
-  p.dk = a.dk;
-  p.dv = a.dv;
-  p.dmix = a.dmix;
-  p.H = sh.H;
-  p.N = sh.N;
-  p.K = a.K;
-  p.rms_eps = a.rms_eps;
-  const unsigned nq = (unsigned)(sh.BH() * (sh.N / kQT));
-  const int dyn = kQT * (2 * kD + 2) * 4;
-  if ((e = cudaFuncSetAttribute(k8_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                dyn)) != cudaSuccess)
+  LongBwd lp;
+  lp.q = static_cast<const unsigned char *>(a.q);
+  lp.k = static_cast<const unsigned char *>(a.k);
+  lp.v = static_cast<const unsigned char *>(a.v);
+  lp.g = a.g;
+  lp.sel = a.sel;
+  lp.mix = a.mix;
+  lp.dq = a.dq;
+  lp.dk = a.dk;
+  lp.dv = a.dv;
+  lp.dmix = a.dmix;
+  lp.H = sh.H;
+  lp.N = sh.N;
+  lp.K = a.K;
+  lp.rms_eps = a.rms_eps;
+  lp.err = a.err;
+  const uint32_t lsm = long_bwd_smem(sh.N);
+  if ((e = cudaFuncSetAttribute(k8_long_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)lsm)) != cudaSuccess)
     return e;
-  k8_long_kernel<<<nq, 256, dyn, st>>>(p);
+  k8_long_tc_kernel<<<ntile, kT, lsm, st>>>(lp);
   return cudaGetLastError();
 }
 
