@@ -5,11 +5,13 @@ test_oracle_backward.py), GPU only.
 Both sides hold the pools and selections at the forward's; the test first
 checks that the GPU forward selects the oracle's cells on every row (so
 both differentiate the same function).  Tolerance from the arithmetic: the
-GPU works in fp32 (bf16 inputs exact), accumulating up to w + K*s products
-per row and about (w + 128) per key, with fast exponentials (relative error
-about 2^-21); the errors stay near 1e-6 relative to the gradients' scale.  The
-test allows max-abs 2e-4 and mean-abs 2e-5 relative to each gradient's
-largest magnitude."""
+GPU takes every product on the tensor cores with fp32 accumulation, its
+fp32 operands (rotated q and k, g, P, dS, do) split into bf16 hi + lo and
+multiplied as hi.hi + hi.lo + lo.hi (about 2^-16 relative per product; bf16
+q, k, v are exact), over up to w + K*s products per row and about w + 128
+per key, with fast exponentials (relative error about 2^-21).  The test
+allows max-abs 2e-4 and mean-abs 2e-5 relative to each gradient's largest
+magnitude."""
 import numpy as np
 import pytest
 import torch
@@ -64,6 +66,10 @@ def _run(B, H, N, params, seed, sigma_ln=0.8):
     (1, 2, 640, dict(PAGE, mode=1), 2),                # base FS (every available cell)
     (1, 1, 2560, PAGE, 3),                             # the pool is pruned (A > 72)
     (1, 2, 256, dict(PAGE, K=8), 4),                   # K = 8
+    # unions of several long tiles; a seed whose selections have no near tie
+    # (smallest deciding gap 6.8e-5 relative), so both sides pick the same cells
+    (1, 2, 4096, PAGE, 19),
+    (1, 1, 1024, dict(PAGE, w=200), 6),                # window edge inside a tile
 ])
 def test_backward_matches_oracle(B, H, N, params, seed):
     print(_run(B, H, N, params, seed))
