@@ -523,7 +523,8 @@ def time_decode(q, k, v, lam, sigma, mix, params, stream, steps=256, warm=8):
     gbs = B * H * step_bytes / (us / 1e6) / 1e9
     roof = {"bound": "hbm", "bytes_per_head_step": step_bytes, "GB/s": gbs,
             "hbm_frac": gbs / pk["hbm"],
-            "note": "one CTA per (batch, head): latency-bound, not bandwidth-bound"}
+            "note": "a cluster of 8 CTAs per (batch, head): latency-bound, not "
+                    "bandwidth-bound; bytes counted in bf16 (the ring keeps fp32 rotated keys)"}
     return {"t0": N + warm, "us_per_token": us, "heads": B * H, "steps": steps, "roofline": roof,
             "state_bytes": state.numel(), "state_bytes_per_head": state.numel() / (B * H),
             "note": "bounded state from the prefill; graph of consecutive steps, all (batch, head)"}
