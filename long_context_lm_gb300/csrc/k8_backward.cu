@@ -21,11 +21,11 @@
 //   k8_win_kv_tc one CTA per 128-key tile, tcgen05: every query tile that
 //                sees the tile, from the saved row statistics; writes dk
 //                (rotated back) and dv;
-//   k8_long      one CTA per 128-query tile (CUDA cores, fp32): the union of
-//                the tile's selected cells is staged cell by cell; each row's
-//                softmax, RMSNorm and their backward give dq (added), dm_h,
-//                and per cell the dk, dv contributions of the tile's rows,
-//                added into dk, dv.
+//   k8_long_tc   one CTA per 128-query tile, tcgen05: the union of the
+//                tile's selected cells in long tiles of four cells; each
+//                row's softmax, RMSNorm and their backward give dq (added to
+//                the window's), dm_h, and per long tile the dk, dv
+//                contributions of the tile's rows, added into dk, dv.
 #include "fs_common.cuh"
 #include "fs_internal.h"
 #include "tc05.cuh"
