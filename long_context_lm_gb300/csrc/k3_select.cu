@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
   // ranks), and carries kNeedsErf when the bias factor can fall below 1 for
   // some row of the block.
   __shared__ int2 s_ca[kChunk];
+  __shared__ uint32_t s_gerf;  // bit g: a candidate of group g (16) needs the erf
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t s_tmem;
 
@@ -110,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
   bool ok = true;
 
   for (int base = 0, chunk = 0; base < count; base += kChunk, ++chunk) {
+    if (tid == 0) s_gerf = 0u;
+    __syncthreads();
     const int nc = min(kChunk, count - base);
     const int np = (nc + 15) / 16 * 16;
     // candidate ids, norms and mean keys in one pass: eight threads share a
@@ -157,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
             cf = x0 < 4.0f ? (c | kNeedsErf) : c;
           }
           s_ca[j] = make_int2(cf, __float_as_int(la));
+          if (cf < 0) atomicOr(&s_gerf, 1u << (j >> 4));
         }
       }
 #pragma unroll
@@ -210,23 +214,34 @@ __global__ void __launch_bounds__(kThreads, K <= 5 ? 4 : 3) k3_select_tc_kernel(
           float u16[16];
           int c16[16];
           bool any16 = false;
+          if ((s_gerf >> ((j0 + j16) >> 4)) & 1u) {  // some candidate of the group needs the erf
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int2 ca = s_ca[j0 + j16 + e];
-            const float la = __int_as_float(ca.y);
-            int c = ca.x;
-            float u;
-            if (c < 0) {  // kNeedsErf (the same for every lane of the warp)
-              c &= ~kNeedsErf;
-              const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
-              const float g = x < 4.0f ? erf_bias(x) : 1.0f;
-              u = __uint_as_float(d[j16 + e]) + la * g;
-            } else {
-              u = __uint_as_float(d[j16 + e]) + la;  // g = 1 exactly
+            for (int e = 0; e < 16; ++e) {
+              const int2 ca = s_ca[j0 + j16 + e];
+              const float la = __int_as_float(ca.y);
+              int c = ca.x;
+              float u;
+              if (c < 0) {  // kNeedsErf (the same for every lane of the warp)
+                c &= ~kNeedsErf;
+                const float x = sig_s * ((float)(n - c * kS) - 0.5f * kS);
+                const float g = x < 4.0f ? erf_bias(x) : 1.0f;
+                u = __uint_as_float(d[j16 + e]) + la * g;
+              } else {
+                u = __uint_as_float(d[j16 + e]) + la;  // g = 1 exactly
+              }
+              u16[e] = u;
+              c16[e] = c;
+              any16 |= u >= wu;  // a superset of the candidates that rank before the K-th
             }
-            u16[e] = u;
-            c16[e] = c;
-            any16 |= u >= wu;  // a superset of the candidates that rank before the K-th
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int2 ca = s_ca[j0 + j16 + e];
+              const float u = __uint_as_float(d[j16 + e]) + __int_as_float(ca.y);
+              u16[e] = u;
+              c16[e] = ca.x;
+              any16 |= u >= wu;
+            }
           }
           if (!__any_sync(0xffffffffu, any16)) continue;
 #pragma unroll
