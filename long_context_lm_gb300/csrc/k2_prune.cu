@@ -17,6 +17,9 @@
 //   3. k2_emit: every block independently merges the prefix list of the
 //      chunks below L with the sorted partial chunk [64*floor(L/64), L) and
 //      writes the recent cells plus the first min(P, L) ranked cells.
+// Steps 1 and 2 run as one kernel per head (k2_sort_scan) with the lists in
+// shared memory while a head has at most kScanSmemChunks chunks (N up to
+// 393216 at s = 32); longer heads take the two global-memory kernels.
 // Keys are (float bits of a_c << 32) | (0xffffffff - c): larger key = higher
 // rank, so the order is exact and equal norms rank the older cell first.
 // Key 0 is padding and ranks below every real cell.
@@ -127,6 +130,46 @@ __global__ void __launch_bounds__(1024) k2_chunk_scan_kernel(uint64_t *buf0, uin
   }
 }
 
+// Steps 1 and 2 for one head in shared memory: every warp sorts chunks
+// (warp w: chunks w, w + 32, ...), then the same inclusive prefix as
+// k2_chunk_scan between two shared buffers; the result goes to `prefix`.
+constexpr int kScanSmemChunks = 192;
+
+__global__ void __launch_bounds__(1024) k2_sort_scan_kernel(const float *__restrict__ amax,
+                                                            int C, int nchunks,
+                                                            uint64_t *__restrict__ prefix) {
+  extern __shared__ uint64_t lists[];  // two buffers of nchunks x 64 keys
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int bh = blockIdx.x;
+  const float *a = amax + (size_t)bh * C;
+  uint64_t *in = lists, *out = lists + (size_t)nchunks * 64;
+  for (int ch = warp; ch < nchunks; ch += nw) {
+    const int c0 = ch * 64 + 2 * lane;
+    uint64_t x0 = c0 < C ? cell_key(a[c0], c0) : 0ull;
+    uint64_t x1 = c0 + 1 < C ? cell_key(a[c0 + 1], c0 + 1) : 0ull;
+    warp_sort64_desc(x0, x1, lane);
+    in[ch * 64 + 2 * lane] = x0;
+    in[ch * 64 + 2 * lane + 1] = x1;
+  }
+  __syncthreads();
+  for (int off = 1; off < nchunks; off <<= 1) {
+    for (int i = warp; i < nchunks; i += nw) {
+      uint64_t a0 = in[i * 64 + 2 * lane], a1 = in[i * 64 + 2 * lane + 1];
+      if (i >= off)
+        warp_merge64_desc(a0, a1, in[(i - off) * 64 + 2 * lane], in[(i - off) * 64 + 2 * lane + 1],
+                          lane);
+      out[i * 64 + 2 * lane] = a0;
+      out[i * 64 + 2 * lane + 1] = a1;
+    }
+    __syncthreads();
+    uint64_t *t = in;
+    in = out;
+    out = t;
+  }
+  uint64_t *dst = prefix + (size_t)bh * nchunks * 64;
+  for (int e = threadIdx.x; e < nchunks * 64; e += blockDim.x) dst[e] = in[e];
+}
+
 __global__ void __launch_bounds__(128) k2_emit_kernel(
     const float *__restrict__ amax, const uint64_t *__restrict__ prefix, int BH, int C,
     int nchunks, int nblk, int cells_per_blk, int P, int W, int32_t *__restrict__ pool,
@@ -173,12 +216,22 @@ cudaError_t launch_prune(const float *amax, const Shape &sh, int P, int W, int32
   const int BH = sh.BH();
   uint64_t *buf0 = static_cast<uint64_t *>(ws);
   uint64_t *buf1 = buf0 + (size_t)BH * nchunks * 64;
-  const long long nlists = (long long)BH * nchunks;
-  k2_chunk_sort_kernel<<<(unsigned)((nlists + 3) / 4), 128, 0, st>>>(amax, BH, C, nchunks, buf0);
-  int levels = 0;
-  for (int off = 1; off < nchunks; off <<= 1) ++levels;
-  if (levels > 0) k2_chunk_scan_kernel<<<BH, 1024, 0, st>>>(buf0, buf1, nchunks);
-  const uint64_t *prefix = (levels % 2 == 0) ? buf0 : buf1;
+  const uint64_t *prefix = buf0;
+  if (nchunks <= kScanSmemChunks) {
+    const int smem = 2 * nchunks * 64 * (int)sizeof(uint64_t);
+    cudaError_t e = cudaFuncSetAttribute(k2_sort_scan_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k2_sort_scan_kernel<<<BH, 1024, smem, st>>>(amax, C, nchunks, buf0);
+  } else {
+    const long long nlists = (long long)BH * nchunks;
+    k2_chunk_sort_kernel<<<(unsigned)((nlists + 3) / 4), 128, 0, st>>>(amax, BH, C, nchunks,
+                                                                       buf0);
+    int levels = 0;
+    for (int off = 1; off < nchunks; off <<= 1) ++levels;
+    if (levels > 0) k2_chunk_scan_kernel<<<BH, 1024, 0, st>>>(buf0, buf1, nchunks);
+    prefix = (levels % 2 == 0) ? buf0 : buf1;
+  }
   const long long nwarps = (long long)BH * sh.nblk();
   k2_emit_kernel<<<(unsigned)((nwarps + 3) / 4), 128, 0, st>>>(
       amax, prefix, BH, C, nchunks, sh.nblk(), kBq / kS, P, W, pool, pool_count);

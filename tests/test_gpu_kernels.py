@@ -38,7 +38,9 @@ def _gpu_pools(amax_np, N, P, W):
     return pool[0].cpu().numpy(), count[0].cpu().numpy()
 
 
-@pytest.mark.parametrize("N", [128, 256, 2304, 2432, 8192, 65536, 262144 + 128])
+# 393216: 192 chunks of 64 cells, the most the per-head shared-memory scan takes;
+# 401408: past it, the two global-memory kernels
+@pytest.mark.parametrize("N", [128, 256, 2304, 2432, 8192, 65536, 262144 + 128, 393216, 401408])
 @pytest.mark.parametrize("P,W,quant", [(64, 8, 0), (64, 8, 4), (3, 2, 0), (64, 0, 2), (1, 8, 0)])
 def test_prune_is_bit_exact(N, P, W, quant):
     # Integer/index work: identical to the oracle's definition (sort per
