@@ -286,9 +286,12 @@ def run_ours(args, rank, world, local_rank):
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s",
                 "frac": ach / pk["hbm"], "traffic": None, "peak_source": pk["source"]}
     # our kernels per step: RoPE angle table 1, one pass for the window operands
-    # and the cell summaries 1, prune (sort, scan when >1 chunk, emit), select 1,
-    # attention 1 (+3 roundings for fp32 inputs)
-    prune_launches = 0 if params.mode == fs.FS_MODE_FS else 2 + (1 if N // 32 > 64 else 0)
+    # and the cell summaries 1, prune (sort + scan in one kernel per head up to
+    # 192 chunks of 64 cells, else sort and, for more than one chunk, scan;
+    # then emit), select 1, attention 1 (+3 roundings for fp32 inputs)
+    nch = (N // 32 + 63) // 64
+    prune_launches = 0 if params.mode == fs.FS_MODE_FS else (
+        2 if nch <= 192 else 3)
     launches_per_step = 2 + prune_launches + 1 + 1 + (3 if code == fs.FS_FP32 else 0)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
