@@ -137,7 +137,8 @@ constexpr int kScanSmemChunks = 192;
 
 __global__ void __launch_bounds__(1024) k2_sort_scan_kernel(const float *__restrict__ amax,
                                                             int C, int nchunks,
-                                                            uint64_t *__restrict__ prefix) {
+                                                            uint64_t *__restrict__ prefix,
+                                                            uint64_t *__restrict__ sorted) {
   extern __shared__ uint64_t lists[];  // two buffers of nchunks x 64 keys
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int bh = blockIdx.x;
@@ -150,6 +151,9 @@ __global__ void __launch_bounds__(1024) k2_sort_scan_kernel(const float *__restr
     warp_sort64_desc(x0, x1, lane);
     in[ch * 64 + 2 * lane] = x0;
     in[ch * 64 + 2 * lane + 1] = x1;
+    uint64_t *sd = sorted + ((size_t)bh * nchunks + ch) * 64;  // for the emit's partial chunks
+    sd[2 * lane] = x0;
+    sd[2 * lane + 1] = x1;
   }
   __syncthreads();
   for (int off = 1; off < nchunks; off <<= 1) {
@@ -170,10 +174,16 @@ __global__ void __launch_bounds__(1024) k2_sort_scan_kernel(const float *__restr
   for (int e = threadIdx.x; e < nchunks * 64; e += blockDim.x) dst[e] = in[e];
 }
 
+// The partial chunk [64 ci, L) in descending order: sorted here from the
+// norms, or (kSorted) taken from the chunk's sorted list by keeping the cells
+// below L in their order (the same keys in the same order as sorting them).
+template <bool kSorted>
 __global__ void __launch_bounds__(128) k2_emit_kernel(
-    const float *__restrict__ amax, const uint64_t *__restrict__ prefix, int BH, int C,
-    int nchunks, int nblk, int cells_per_blk, int P, int W, int32_t *__restrict__ pool,
+    const float *__restrict__ amax, const uint64_t *__restrict__ prefix,
+    const uint64_t *__restrict__ sorted, int BH, int C, int nchunks, int nblk,
+    int cells_per_blk, int P, int W, int32_t *__restrict__ pool,
     int32_t *__restrict__ pool_count) {
+  __shared__ uint64_t s_part[4][64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long gid = (long long)blockIdx.x * 4 + warp;
   if (gid >= (long long)BH * nblk) return;
@@ -186,13 +196,31 @@ __global__ void __launch_bounds__(128) k2_emit_kernel(
   for (int r = lane; r < nrec; r += 32) pl[r] = L + r;
   const int keep = L < P ? L : P;
   if (L > 0) {
-    const float *a = amax + (size_t)bh * C;
     const int ci = L / 64, rem = L % 64;
     uint64_t x0 = 0ull, x1 = 0ull;
-    const int c0 = ci * 64 + 2 * lane;
-    if (2 * lane < rem) x0 = cell_key(a[c0], c0);
-    if (2 * lane + 1 < rem) x1 = cell_key(a[c0 + 1], c0 + 1);
-    warp_sort64_desc(x0, x1, lane);
+    if (kSorted) {
+      if (rem > 0) {
+        // compact the chunk's sorted keys of cells below L, order kept
+        const uint64_t *sd = sorted + ((size_t)bh * nchunks + ci) * 64;
+        const uint64_t y0 = sd[2 * lane], y1 = sd[2 * lane + 1];
+        const bool k0 = y0 != 0ull && key_cell(y0) < L, k1 = y1 != 0ull && key_cell(y1) < L;
+        const uint32_t b0 = __ballot_sync(0xffffffffu, k0), b1 = __ballot_sync(0xffffffffu, k1);
+        const uint32_t below = (1u << lane) - 1u;
+        const int pos = __popc(b0 & below) + __popc(b1 & below);
+        __syncwarp();
+        if (k0) s_part[warp][pos] = y0;
+        if (k1) s_part[warp][pos + (k0 ? 1 : 0)] = y1;
+        __syncwarp();
+        x0 = 2 * lane < rem ? s_part[warp][2 * lane] : 0ull;
+        x1 = 2 * lane + 1 < rem ? s_part[warp][2 * lane + 1] : 0ull;
+      }
+    } else {
+      const float *a = amax + (size_t)bh * C;
+      const int c0 = ci * 64 + 2 * lane;
+      if (2 * lane < rem) x0 = cell_key(a[c0], c0);
+      if (2 * lane + 1 < rem) x1 = cell_key(a[c0 + 1], c0 + 1);
+      warp_sort64_desc(x0, x1, lane);
+    }
     if (ci > 0) {
       const uint64_t *pf = prefix + ((size_t)bh * nchunks + (ci - 1)) * 64;
       warp_merge64_desc(x0, x1, pf[2 * lane], pf[2 * lane + 1], lane);
@@ -217,12 +245,16 @@ cudaError_t launch_prune(const float *amax, const Shape &sh, int P, int W, int32
   uint64_t *buf0 = static_cast<uint64_t *>(ws);
   uint64_t *buf1 = buf0 + (size_t)BH * nchunks * 64;
   const uint64_t *prefix = buf0;
+  const long long nwarps = (long long)BH * sh.nblk();
+  const unsigned egrid = (unsigned)((nwarps + 3) / 4);
   if (nchunks <= kScanSmemChunks) {
     const int smem = 2 * nchunks * 64 * (int)sizeof(uint64_t);
     cudaError_t e = cudaFuncSetAttribute(k2_sort_scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k2_sort_scan_kernel<<<BH, 1024, smem, st>>>(amax, C, nchunks, buf0);
+    k2_sort_scan_kernel<<<BH, 1024, smem, st>>>(amax, C, nchunks, buf0, buf1);
+    k2_emit_kernel<true><<<egrid, 128, 0, st>>>(amax, buf0, buf1, BH, C, nchunks, sh.nblk(),
+                                                kBq / kS, P, W, pool, pool_count);
   } else {
     const long long nlists = (long long)BH * nchunks;
     k2_chunk_sort_kernel<<<(unsigned)((nlists + 3) / 4), 128, 0, st>>>(amax, BH, C, nchunks,
@@ -231,10 +263,9 @@ cudaError_t launch_prune(const float *amax, const Shape &sh, int P, int W, int32
     for (int off = 1; off < nchunks; off <<= 1) ++levels;
     if (levels > 0) k2_chunk_scan_kernel<<<BH, 1024, 0, st>>>(buf0, buf1, nchunks);
     prefix = (levels % 2 == 0) ? buf0 : buf1;
+    k2_emit_kernel<false><<<egrid, 128, 0, st>>>(amax, prefix, nullptr, BH, C, nchunks,
+                                                 sh.nblk(), kBq / kS, P, W, pool, pool_count);
   }
-  const long long nwarps = (long long)BH * sh.nblk();
-  k2_emit_kernel<<<(unsigned)((nwarps + 3) / 4), 128, 0, st>>>(
-      amax, prefix, BH, C, nchunks, sh.nblk(), kBq / kS, P, W, pool, pool_count);
   return cudaGetLastError();
 }
 
