@@ -284,7 +284,10 @@ __global__ void __launch_bounds__(256) k9_search_kernel(const SearchParams p) {
           const float4 mt = __ldg(meta + node);
           const int first = __float_as_int(mt.z);
           const float pf = (float)(first * kS) + 0.5f * kS;
-          const float u = dot + qnorm * mt.x + lam * mt.y * erff(sig * ((float)n - pf) / kS);
+          // erf(x) rounds to 1 in fp32 once x >= 4 (erfc(4) = 1.5e-8): only
+          // nodes that reach the newest cells need the special function
+          const float x = sig * ((float)n - pf) / kS;
+          const float u = dot + qnorm * mt.x + lam * mt.y * (x < 4.0f ? erff(x) : 1.0f);
           key[pass >> 2] = node_key(u, ci << cj, cj);
         }
       }
