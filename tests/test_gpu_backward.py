@@ -70,6 +70,8 @@ def _run(B, H, N, params, seed, sigma_ln=0.8):
     # (smallest deciding gap 6.8e-5 relative), so both sides pick the same cells
     (1, 2, 4096, PAGE, 19),
     (1, 1, 1024, dict(PAGE, w=200), 6),                # window edge inside a tile
+    (1, 1, 512, dict(PAGE, w=1), 7),                   # the window is the token itself
+    (1, 2, 1024, dict(PAGE, K=1), 8),                  # one cell per row
 ])
 def test_backward_matches_oracle(B, H, N, params, seed):
     print(_run(B, H, N, params, seed))
