@@ -317,7 +317,40 @@ def run_ours(args, rank, world, local_rank):
         res["fsb_mode"] = time_fsb_mode(q, k, v, lam, sigma, mix, params, stream, B * N)
         res["prologue"] = time_prologue(B, N, H, stream)
         res["backward"] = time_backward(q, k, v, lam, sigma, mix, params, stream, counts)
+        res["graph"] = time_graph(q, k, v, lam, sigma, mix, params, stream, out, ws,
+                                  min(args.steps, 100))
     return res
+
+
+def time_graph(q, k, v, lam, sigma, mix, params, stream, out, ws, steps):
+    """The same forward captured once in a CUDA graph and replayed back to
+    back on the benchmark's inputs: one graph launch a step instead of the
+    call's kernel launches and its memset (a warm-up call on the capturing
+    stream precedes the capture, as the graph test does)."""
+    from long_context_lm_gb300 import fs
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fs.fs_attention_fwd(q, k, v, lam, sigma, mix, params, out=out, ws=ws)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fs.fs_attention_fwd(q, k, v, lam, sigma, mix, params, out=out, ws=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    B, _, N, _ = q.shape
+    return {"ms_per_step": ms, "tokens_per_s": B * N / (ms / 1e3), "steps": steps,
+            "note": "fs_attention_fwd captured once in a CUDA graph, replayed back to back"}
 
 
 def _timed(fn, stream, iters):
