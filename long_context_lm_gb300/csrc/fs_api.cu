@@ -151,7 +151,7 @@ int prepare_window(const Shape &sh, const void *k, const void *v, float rope_bas
 int forward(const void *q, const void *k, const void *v, int dtype, const Shape &sh,
             const fs_params *p, const float *lambda, const float *sigma, const float *mix,
             float *out, char *base, const Layout &L, int *err, cudaStream_t st,
-            void *const *stage_events);
+            void *const *stage_events, bool clear_status);
 
 }  // namespace
 }  // namespace fs
@@ -373,9 +373,10 @@ int fs_attention_fwd_traced(const void *q, const void *k, const void *v, int dty
   const Layout L = make_layout(sh, *p, dtype);
   if (ws_bytes < L.total) return FS_ERR_INVALID_ARG;
   int *err = reinterpret_cast<int *>(ws);
-  FS_TRY(status_of(cudaMemsetAsync(err, 0, 4 * sizeof(int), static_cast<cudaStream_t>(stream))));
+  // the status word and the q-tile tickets are zeroed by the forward's first
+  // kernel (no separate memset)
   return forward(q, k, v, dtype, sh, p, lambda, sigma, mix, out, static_cast<char *>(ws), L, err,
-                 static_cast<cudaStream_t>(stream), stage_events);
+                 static_cast<cudaStream_t>(stream), stage_events, true);
 }
 
 }  // extern "C"
@@ -384,11 +385,12 @@ namespace fs {
 namespace {
 
 // The forward on validated arguments: workspace `base` laid out as `L`;
-// device errors are recorded in `err` (not cleared here).
+// device errors are recorded in `err`, whose four ints the first kernel zeroes
+// when `clear_status` (else the caller has).
 int forward(const void *q, const void *k, const void *v, int dtype, const Shape &sh,
             const fs_params *p, const float *lambda, const float *sigma, const float *mix,
             float *out, char *base, const Layout &L, int *err, cudaStream_t st,
-            void *const *stage_events) {
+            void *const *stage_events, bool clear_status) {
   const int N = sh.N, d = sh.d;
   const void *qb = q, *kb = k, *vb = v;
   if (dtype == FS_FP32) {
@@ -414,7 +416,8 @@ int forward(const void *q, const void *k, const void *v, int dtype, const Shape 
   FS_TRY(mark(0));
   // angle table, then rotated keys, fp16 values and cell summaries in one
   // pass over k and v
-  FS_TRY(status_of(launch_rope_table(base + L.win.tab, sh.N, p->rope_base, st)));
+  FS_TRY(status_of(launch_rope_table(base + L.win.tab, sh.N, p->rope_base, st,
+                                     clear_status ? err : nullptr)));
   FS_TRY(status_of(launch_prep_summary(kb, vb, base + L.win.tab, sh, base + L.win.kt,
                                        base + L.win.v16, kbar, amax, err, st)));
   FS_TRY(mark(1));
@@ -580,7 +583,7 @@ int fs_attention_fwd_host(const void *q, const void *k, const void *v, int dtype
       if (rc == FS_OK) {
         const Shape sh{1, hn, N, d};
         rc = forward(qd, kd, vd, dtype, sh, p, lambda + h0, sigma + h0, mix + h0, od, fws,
-                     make_layout(sh, *p, dtype), err, st, nullptr);
+                     make_layout(sh, *p, dtype), err, st, nullptr, false);
       }
       if (rc == FS_OK) rc = status_of(cudaEventRecord(cp->computed[s], st));
       // store

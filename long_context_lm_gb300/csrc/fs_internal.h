@@ -29,7 +29,8 @@ cudaError_t launch_select(const void *q, const float *kbar, const float *amax,
 // launch_rope_table) and the window operands prepared from it: kt = rotated
 // keys [rows, 128] bf16 (hi | lo), v16 = values [rows, 64] fp16.
 size_t rope_table_bytes(int N);
-cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st);
+cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st,
+                              int *clear = nullptr);
 // k0_prep with the cell summaries of the same keys (one read of k).
 cudaError_t launch_prep_summary(const void *k, const void *v, const void *tab, const Shape &sh,
                                 void *kt, void *v16, float *kbar, float *amax, int *err,

@@ -39,9 +39,12 @@ struct Theta {
 // evaluation (fp64 throughput is small on this chip).  Entry error: the fp32
 // rounding of the reduced angle (<= 2^-24 * pi rad) plus sincospif's ulp,
 // against the fp64 reference values.
+// `clear` (nullable): four status ints the caller's first kernel zeroes in
+// place of a memset (the kernels that use them run after this one).
 __global__ void __launch_bounds__(256) rope_table_kernel(float2 *__restrict__ tab, int rows,
-                                                         const Theta th) {
+                                                         const Theta th, int *clear) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (clear && idx < 4) clear[idx] = 0;
   if (idx >= rows * (kD / 2)) return;
   const int row = idx / (kD / 2), i = idx % (kD / 2);
   const double pos = row < 64 ? (double)row : 64.0 * (double)(row - 64);
@@ -206,13 +209,13 @@ __global__ void __launch_bounds__(256, 3) k0_prep_summary_kernel(
 
 size_t rope_table_bytes(int N) { return (size_t)(64 + (N + 63) / 64) * (kD / 2) * sizeof(float2); }
 
-cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st) {
+cudaError_t launch_rope_table(void *tab, int N, float rope_base, cudaStream_t st, int *clear) {
   const int rows = 64 + (N + 63) / 64;
   Theta th;
   for (int i = 0; i < kD / 2; ++i)
     th.over_pi[i] = std::pow((double)rope_base, -2.0 * i / (double)kD) / 3.14159265358979323846;
   rope_table_kernel<<<(rows * (kD / 2) + 255) / 256, 256, 0, st>>>(static_cast<float2 *>(tab),
-                                                                  rows, th);
+                                                                  rows, th, clear);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,6 @@
 """fs_attention_fwd inside a CUDA graph (GPU only).
 
-The forward is six launches and one memset on the caller's stream, with no
+The forward is six kernel launches on the caller's stream, with no
 host synchronisation, so stream capture records it whole.  A captured
 forward must replay to the eager result bit for bit, and recompute when the
 inputs in its buffers change.  A warm-up call precedes the capture: the
