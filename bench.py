@@ -325,8 +325,8 @@ def run_ours(args, rank, world, local_rank):
 def time_graph(q, k, v, lam, sigma, mix, params, stream, out, ws, steps):
     """The same forward captured once in a CUDA graph and replayed back to
     back on the benchmark's inputs: one graph launch a step instead of the
-    call's kernel launches and its memset (a warm-up call on the capturing
-    stream precedes the capture, as the graph test does)."""
+    call's six kernel launches (a warm-up call on the capturing stream
+    precedes the capture, as the graph test does)."""
     from long_context_lm_gb300 import fs
     side = torch.cuda.Stream()
     side.wait_stream(stream)
