@@ -44,8 +44,9 @@ namespace {
 // v is exact in bf16 (one term).  P and dS are split the same way when they
 // are written back to TMEM as the A operand of the second products.
 //
-// Both kernels take one 128-row tile per CTA, 4 warps, thread t = TMEM lane
-// t = the tile's row t.  Tiles sit in shared memory as 128-byte rows with the
+// Both kernels take one 128-row tile per CTA with 8 warps: thread t and
+// t + 128 own TMEM lane t = the tile's row t, and the tile's columns 0..63
+// and 64..127 (two warps per SM sub-partition for the element-wise work).  Tiles sit in shared memory as 128-byte rows with the
 // hardware's 128-byte swizzle; the same bytes serve as a K-major operand
 // (contraction over d) and as an MN-major B operand (contraction over rows).
 // TMEM: S (128 columns), dP (128), then the accumulators; P (dS) is written
@@ -72,7 +73,7 @@ __device__ __forceinline__ uint32_t p_chunk_col(int ks) {  // A operand, K step 
 // into a swizzled tile, by 16-byte asynchronous copies of all 128 threads
 __device__ __forceinline__ void load_tile(unsigned char *dst, const unsigned char *src,
                                           size_t ld, int off) {
-  for (int e = threadIdx.x; e < kT * 8; e += kT) {
+  for (int e = threadIdx.x; e < kT * 8; e += blockDim.x) {
     const int r = e >> 3, ch = e & 7;
     cp_async16(dst + swz128(r, ch), src + (size_t)r * ld + off + 16 * ch);
   }
@@ -226,16 +227,20 @@ __device__ __forceinline__ bool cta_sync_ok(bool ok) {
 // key tiles: S = q~ k~^T and dP = g v^T, the row's online log-sum-exp and
 // gdo = sum_j p_j dP_j (= g . o_win).  Pass 2: S and dP again, dS = P (dP -
 // gdo) / 8, dq~ += dS k~.  Writes lse2 and gdo (for the key side) and dq.
-__global__ void __launch_bounds__(kT, 1) k8_win_q_tc_kernel(const WinBwd p) {
+__global__ void __launch_bounds__(2 * kT, 1) k8_win_q_tc_kernel(const WinBwd p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar[2];
   __shared__ uint32_t s_tmem;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ float s_mla[3][kT];  // the second half's pass-0 partials
+  __shared__ float s_st[2][kT];   // the merged row statistics
+  // 8 warps: warps w and w + 4 share TMEM lanes 32 (w % 4).. (query rows) and
+  // take each key tile's columns 0..63 and 64..127
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & (kT - 1), half = tid >> 7;
   const int nblk = p.N / kT;
   const int bh = blockIdx.x / nblk, b0 = (blockIdx.x % nblk) * kT;
-  const int n = b0 + tid;
+  const int n = b0 + row;
   const size_t head = (size_t)bh * p.N;
   const uint32_t sb = smem_u32(smem);
   if (warp == 0) {
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kT, 1) k8_win_q_tc_kernel(const WinBwd p) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = s_tmem, lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tmem = s_tmem, lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t id_s = tc::idesc_bf16(kT, kT, 0), id_dq = tc::idesc_bf16(kT, kD, 1);
   const uint64_t dqh = tc::desc_sw128(sb + kOffA), dql = tc::desc_sw128(sb + kOffA + kTileB);
   const uint64_t dgh = tc::desc_sw128(sb + kOffB), dgl = tc::desc_sw128(sb + kOffB + kTileB);
@@ -286,7 +291,7 @@ __global__ void __launch_bounds__(kT, 1) k8_win_q_tc_kernel(const WinBwd p) {
       ph0 ^= 1;
       tc::fence_after_sync();
 #pragma unroll 1
-      for (int c0 = 0; c0 < kT; c0 += 32) {
+      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
         uint32_t xs[32], xd[32];
         tc::tmem_ld32(tmem + kColSt + c0 + lane_base, xs);
         tc::tmem_ld32(tmem + kColDp + c0 + lane_base, xd);
@@ -341,15 +346,31 @@ __global__ void __launch_bounds__(kT, 1) k8_win_q_tc_kernel(const WinBwd p) {
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
-    if (pass == 0) {
-      lse2 = m + __log2f(l);  // l >= 1: the row sees itself
-      gdo = a / l;
-      p.lse2[head + n] = lse2;
-      p.gdo[head + n] = gdo;
+    if (pass == 0) {  // merge the halves' partials (a half may have seen no key: m = -inf)
+      if (half) {
+        s_mla[0][row] = m;
+        s_mla[1][row] = l;
+        s_mla[2][row] = a;
+      }
+      __syncthreads();
+      if (!half) {
+        const float m1 = s_mla[0][row], mm = fmaxf(m, m1);
+        const float f0 = tc::ex2(m - mm), f1 = tc::ex2(m1 - mm);
+        const float lt = l * f0 + s_mla[1][row] * f1, at = a * f0 + s_mla[2][row] * f1;
+        lse2 = mm + __log2f(lt);  // lt >= 1: the row sees itself
+        gdo = at / lt;
+        p.lse2[head + n] = lse2;
+        p.gdo[head + n] = gdo;
+        s_st[0][row] = lse2;
+        s_st[1][row] = gdo;
+      }
+      __syncthreads();
+      lse2 = s_st[0][row];
+      gdo = s_st[1][row];
     }
   }
   ok = cta_sync_ok(ok);
-  if (ok) {
+  if (ok && !half) {  // warps 0-3 (warp-uniform)
     uint32_t r0[32], r1[32];
     tc::tmem_ld32(tmem + kColA0 + lane_base, r0);
     tc::tmem_ld32(tmem + kColA0 + 32 + lane_base, r1);
@@ -376,16 +397,18 @@ __global__ void __launch_bounds__(kT, 1) k8_win_q_tc_kernel(const WinBwd p) {
 // Key side: one CTA per (head, 128-key tile), over the query tiles whose
 // windows reach it.  S^T = k~ q~^T and dP^T = v g^T, P^T and dS^T from the
 // query side's row statistics, then dv += P^T g and dk~ += dS^T q~.
-__global__ void __launch_bounds__(kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
+__global__ void __launch_bounds__(2 * kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar[2];
   __shared__ uint32_t s_tmem;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  // 8 warps: warps w and w + 4 share TMEM lanes 32 (w % 4).. (key rows) and
+  // take the tile's columns 0..63 and 64..127
+  const int tid = threadIdx.x, warp = tid >> 5, row = tid & (kT - 1), half = tid >> 7;
   const int nblk = p.N / kT;
   const int bh = blockIdx.x / nblk, j0 = (blockIdx.x % nblk) * kT;
-  const int j = j0 + tid;
+  const int j = j0 + row;
   const size_t head = (size_t)bh * p.N;
   const uint32_t sb = smem_u32(smem);
   float *s_lse2 = reinterpret_cast<float *>(smem + kOffStat);
@@ -405,7 +428,7 @@ __global__ void __launch_bounds__(kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = s_tmem, lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tmem = s_tmem, lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t id_s = tc::idesc_bf16(kT, kT, 0), id_kv = tc::idesc_bf16(kT, kD, 1);
   const uint64_t dkh = tc::desc_sw128(sb + kOffA), dkl = tc::desc_sw128(sb + kOffA + kTileB);
   const uint64_t dvv = tc::desc_sw128(sb + kOffB);
@@ -419,8 +442,8 @@ __global__ void __launch_bounds__(kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
   for (int n0 = j0; n0 <= nlast; n0 += kT) {
     load_split(smem + kOffC, p.qs + (head + n0) * 256);
     load_split(smem + kOffD, p.gs + (head + n0) * 256);
-    s_lse2[tid] = p.lse2[head + n0 + tid];
-    s_gdo[tid] = p.gdo[head + n0 + tid];
+    if (half == 0) s_lse2[row] = p.lse2[head + n0 + row];
+    else s_gdo[row] = p.gdo[head + n0 + row];
     cp_async_commit();
     cp_async_wait<0>();
     ok = cta_sync_ok(ok);
@@ -437,7 +460,7 @@ __global__ void __launch_bounds__(kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
     ph0 ^= 1;
     tc::fence_after_sync();
 #pragma unroll 1
-    for (int c0 = 0; c0 < kT; c0 += 32) {
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
       uint32_t xs[32], xd[32];
       tc::tmem_ld32(tmem + kColSt + c0 + lane_base, xs);
       tc::tmem_ld32(tmem + kColDp + c0 + lane_base, xd);
@@ -466,30 +489,20 @@ __global__ void __launch_bounds__(kT, 1) k8_win_kv_tc_kernel(const WinBwd p) {
     tc::fence_after_sync();
   }
   ok = cta_sync_ok(ok);
-  if (ok) {
+  if (ok) {  // warps 0-3: dv; warps 4-7: dk~, rotated back
     uint32_t r0[32], r1[32];
+    const uint32_t col = half ? kColA1 : kColA0;
+    tc::tmem_ld32(tmem + col + lane_base, r0);
+    tc::tmem_ld32(tmem + col + 32 + lane_base, r1);
+    tc::tmem_wait_ld();
     float y[64];
-    tc::tmem_ld32(tmem + kColA0 + lane_base, r0);  // dv
-    tc::tmem_ld32(tmem + kColA0 + 32 + lane_base, r1);
-    tc::tmem_wait_ld();
-    float4 *o = reinterpret_cast<float4 *>(p.dv + (head + j) * kD);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      o[e] = make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
-                         __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3]));
-      o[8 + e] = make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
-                             __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
-    }
-    tc::tmem_ld32(tmem + kColA1 + lane_base, r0);  // dk~
-    tc::tmem_ld32(tmem + kColA1 + 32 + lane_base, r1);
-    tc::tmem_wait_ld();
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       y[e] = __uint_as_float(r0[e]);
       y[32 + e] = __uint_as_float(r1[e]);
     }
-    rotate_back_row(y, j, p.tab);
-    o = reinterpret_cast<float4 *>(p.dk + (head + j) * kD);
+    if (half) rotate_back_row(y, j, p.tab);
+    float4 *o = reinterpret_cast<float4 *>((half ? p.dk : p.dv) + (head + j) * kD);
 #pragma unroll
     for (int e = 0; e < 16; ++e) o[e] = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
   }
@@ -974,8 +987,8 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t st) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kBwdSmem)) != cudaSuccess)
       return e;
-  k8_win_q_tc_kernel<<<ntile, kT, kBwdSmem, st>>>(w);
-  k8_win_kv_tc_kernel<<<ntile, kT, kBwdSmem, st>>>(w);
+  k8_win_q_tc_kernel<<<ntile, 2 * kT, kBwdSmem, st>>>(w);
+  k8_win_kv_tc_kernel<<<ntile, 2 * kT, kBwdSmem, st>>>(w);
   LongBwd lp;
   lp.q = static_cast<const unsigned char *>(a.q);
   lp.k = static_cast<const unsigned char *>(a.k);
