@@ -517,7 +517,9 @@ __global__ void __launch_bounds__(2 * kT, 1) k8_win_kv_tc_kernel(const WinBwd p)
 // ---------------------------------------------------------------------------
 // long branch on the tensor cores
 // ---------------------------------------------------------------------------
-// One CTA per (head, 128-query tile), thread r = TMEM lane r = query row r.
+// One CTA per (head, 128-query tile), 8 warps: threads r and r + 128 own TMEM
+// lane r = query row r (token r of the transposed tile) and a tile's columns
+// 0..63 and 64..127; the rows' maxima and sums are merged across the halves.
 // The union of the tile's selected cells (ascending) is cut into long tiles
 // of four cells (128 tokens, raw bf16 k and v gathered into shared memory);
 // a row reads only the cells it picked, the other columns of a tile are
@@ -559,7 +561,7 @@ struct LongBwd {
 // slot 4t + i / 32; rows past the union are zeros
 __device__ __forceinline__ void load_cells(unsigned char *dst, const unsigned char *x,
                                            size_t head, const int *ul, int slot0, int nu) {
-  for (int e = threadIdx.x; e < kT * 8; e += kT) {
+  for (int e = threadIdx.x; e < kT * 8; e += blockDim.x) {
     const int i = e >> 3, ch = e & 7, sl = slot0 + (i >> 5);
     unsigned char *d = dst + swz128(i, ch);
     if (sl < nu)
@@ -576,7 +578,7 @@ __device__ __forceinline__ void mma_r128_parts(uint32_t d, uint32_t a, uint64_t 
   for (int part = 0; part < parts; ++part) mma_r128(d, a + 16u * part, b, id, acc || part > 0);
 }
 
-__global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
+__global__ void __launch_bounds__(2 * kT, 1) k8_long_tc_kernel(const LongBwd p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -584,10 +586,14 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
   __shared__ uint32_t s_tmem;
   __shared__ int s_nu;
   __shared__ float s_red[4];
+  __shared__ float s_half[2][kT];  // the halves' partial row maxima, then row sums
+  // 8 warps: warps w and w + 4 share TMEM lanes 32 (w % 4).. (rows, or tokens
+  // in the transposed tile) and take columns 0..63 and 64..127 of a tile
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & (kT - 1), half = tid >> 7;
   const int nblk = p.N / kT;
   const int bh = blockIdx.x / nblk, b0 = (blockIdx.x % nblk) * kT, h = bh % p.H;
-  const int n = b0 + tid;
+  const int n = b0 + row;
   const size_t head = (size_t)bh * p.N;
   const int A = b0 / kS;  // cells available to the tile
   if (A == 0) return;     // the first block has no long branch: nothing to add
@@ -610,7 +616,7 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
   }
   load_tile(smem + kLOffQ, p.q + (head + b0) * 128, 128, 0);
   cp_async_commit();
-  for (int w = tid; w < nwd; w += kT) bm[w] = 0u;
+  for (int w = tid; w < nwd; w += blockDim.x) bm[w] = 0u;
   __syncthreads();
   // union: mark, rank the words (warp 0), then each pick's slot
   int pick[kMaxK];
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
   for (int k = 0; k < kMaxK; ++k) {
     const int c = k < p.K ? p.sel[(head + n) * p.K + k] : -1;
     pick[k] = (c >= 0 && c < A) ? c : -1;
-    if (pick[k] >= 0) atomicOr(bm + (pick[k] >> 5), 1u << (pick[k] & 31));
+    if (!half && pick[k] >= 0) atomicOr(bm + (pick[k] >> 5), 1u << (pick[k] & 31));
   }
   __syncthreads();
   if (warp == 0) {
@@ -653,7 +659,7 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     const int c = pick[k];
     slot[k] = c < 0 ? -1 : pw[c >> 5] + __popc(bm[c >> 5] & ((1u << (c & 31)) - 1u));
   }
-  const uint32_t tmem = s_tmem, lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tmem = s_tmem, lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t id_s = tc::idesc_bf16(kT, kT, 0), id_o = tc::idesc_bf16(kT, kD, 1);
   const uint64_t dq_ = tc::desc_sw128(sb + kLOffQ);
   const uint64_t ddh = tc::desc_sw128(sb + kLOffDo), ddl = tc::desc_sw128(sb + kLOffDo + kTileB);
@@ -686,7 +692,7 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     tc::fence_after_sync();
     const int mk = row_mask(t);
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
       if (!__any_sync(0xffffffffu, (mk >> ch) & 1)) continue;  // warp-uniform
       uint32_t xs[32];
       tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
@@ -700,7 +706,9 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     }
   }
   // ---- pass B: P, l and o += P v
+  s_half[half][row] = m;  // the row maximum over both halves
   ok = cta_sync_ok(ok);
+  m = fmaxf(s_half[0][row], s_half[1][row]);
   for (int t = 0; t < nt; ++t) {
     load_cells(smem + kLOffK, p.k, head, ul, 4 * t, nu);
     load_cells(smem + kLOffV, p.v, head, ul, 4 * t, nu);
@@ -717,7 +725,7 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     tc::fence_after_sync();
     const int mk = row_mask(t);
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
       uint32_t xs[32];
       tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
       tc::tmem_wait_ld();
@@ -741,11 +749,13 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     ph1 ^= 1;
     tc::fence_after_sync();
   }
+  s_half[half][row] = l;  // the row sum over both halves
   ok = cta_sync_ok(ok);
-  // ---- the row's RMSNorm, dm_h, do, lse
+  l = s_half[0][row] + s_half[1][row];
+  // ---- the row's RMSNorm, dm_h, do, lse (warps 0-3)
   const bool has = l > 0.f;
   float lse2 = 0.f, dodo = 0.f, dmx = 0.f;
-  if (ok) {
+  if (ok && !half) {
     float o[64];
     {
       uint32_t r0[32], r1[32];
@@ -796,16 +806,20 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
         hi[u] = pack_bf16(dv8[2 * u], dv8[2 * u + 1]);
         lo[u] = pack_bf16(dv8[2 * u] - bf16_lo(hi[u]), dv8[2 * u + 1] - bf16_hi(hi[u]));
       }
-      *reinterpret_cast<uint4 *>(dh + swz128(tid, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4 *>(dl + swz128(tid, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4 *>(dh + swz128(row, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>(dl + swz128(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     lse2 = has ? m + __log2f(l) : 0.f;
   }
-  s_lse2[tid] = lse2;
-  s_dodo[tid] = dodo;
+  if (!half) {
+    s_lse2[row] = lse2;
+    s_dodo[row] = dodo;
+  }
   dmx = warp_sum(dmx);
-  if (lane == 0) s_red[warp] = dmx;
+  if (lane == 0 && !half) s_red[warp] = dmx;
   ok = cta_sync_ok(ok);
+  lse2 = s_lse2[row];  // the row's statistics, for both halves
+  dodo = s_dodo[row];
   if (tid == 0 && ok) atomicAdd(p.dmix + h, (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]));
   // ---- pass C: dq from the rows' side, then dk, dv from the tokens' side
   for (int t = 0; t < nt; ++t) {
@@ -825,9 +839,9 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     ph0 ^= 1;
     tc::fence_after_sync();
     const int mk = row_mask(t);
-    s_rmask[tid] = mk;
+    s_rmask[row] = mk;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
       uint32_t xs[32], xd[32];
       tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
       tc::tmem_ld32(tmem + kColDp + 32 * ch + lane_base, xd);
@@ -862,9 +876,9 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     ok = tc::mbar_wait(&bar[0], ph0, p.err) && ok;
     ph0 ^= 1;
     tc::fence_after_sync();
-    const int cell = tid >> 5;  // this thread's token is token tid % 32 of cell slot 4t + cell
+    const int cell = row >> 5;  // this thread's token is token row % 32 of cell slot 4t + cell
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
       uint32_t xs[32], xd[32];
       tc::tmem_ld32(tmem + kColSt + 32 * ch + lane_base, xs);
       tc::tmem_ld32(tmem + kColDp + 32 * ch + lane_base, xd);
@@ -893,30 +907,26 @@ __global__ void __launch_bounds__(kT, 1) k8_long_tc_kernel(const LongBwd p) {
     ok = cta_sync_ok(ok);
     if (!ok) break;
     const int sl = 4 * t + cell;
-    if (sl < nu) {  // (the loads below are whole-warp: sl is warp-uniform)
-      const size_t trow = head + (size_t)ul[sl] * kS + (tid & 31);
-#pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
-        uint32_t r0[32], r1[32];
-        const uint32_t col = part ? kColDk : kColDv;
-        float *dst = (part ? p.dk : p.dv) + trow * kD;
-        tc::tmem_ld32(tmem + col + lane_base, r0);
-        tc::tmem_ld32(tmem + col + 32 + lane_base, r1);
-        tc::tmem_wait_ld();
-        float4 *d4 = reinterpret_cast<float4 *>(dst);
+    if (sl < nu) {  // warps 0-3: dv, warps 4-7: dk (sl is warp-uniform)
+      const size_t trow = head + (size_t)ul[sl] * kS + (row & 31);
+      uint32_t r0[32], r1[32];
+      const uint32_t col = half ? kColDk : kColDv;
+      float4 *d4 = reinterpret_cast<float4 *>((half ? p.dk : p.dv) + trow * kD);
+      tc::tmem_ld32(tmem + col + lane_base, r0);
+      tc::tmem_ld32(tmem + col + 32 + lane_base, r1);
+      tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          atomicAdd(d4 + e, make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
-                                        __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3])));
-          atomicAdd(d4 + 8 + e,
-                    make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
-                                __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3])));
-        }
+      for (int e = 0; e < 8; ++e) {
+        atomicAdd(d4 + e, make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
+                                      __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3])));
+        atomicAdd(d4 + 8 + e,
+                  make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
+                              __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3])));
       }
     }
   }
   ok = cta_sync_ok(ok);
-  if (ok && nt > 0) {  // dq of the long branch, added to the window's
+  if (ok && nt > 0 && !half) {  // dq of the long branch, added to the window's
     uint32_t r0[32], r1[32];
     tc::tmem_ld32(tmem + kColO + lane_base, r0);
     tc::tmem_ld32(tmem + kColO + 32 + lane_base, r1);
@@ -1009,7 +1019,7 @@ cudaError_t launch_backward(const BwdArgs &a, cudaStream_t st) {
   if ((e = cudaFuncSetAttribute(k8_long_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)lsm)) != cudaSuccess)
     return e;
-  k8_long_tc_kernel<<<ntile, kT, lsm, st>>>(lp);
+  k8_long_tc_kernel<<<ntile, 2 * kT, lsm, st>>>(lp);
   return cudaGetLastError();
 }
 
